@@ -1,0 +1,257 @@
+/*
+ * pf.h — C ABI of libpf: batched / chunked prefill through a dense Qwen3/Llama-style
+ * decoder stack whose linear weights are 1-bit sign + f16 group scale ("Q1") or
+ * INT4-affine, on one sm_103a GPU.
+ *
+ * The operation follows three pages:
+ *   [P1] oxibonsai-kernels 0.1.1, src/gpu_backend/metal_prefill.rs
+ *        (encode_layer_prefill: sections 1-7; encode_full_forward_prefill: tail)
+ *   [P2] oxibonsai-kernels 0.1.0, src/gpu_backend/metal_full_layer.rs
+ *        (GpuKvCache layout; encode_layer_into: the per-token twin)
+ *   [P3] turbospark-runtime 0.3.0, src/families/llama/prefill.rs
+ *        (prefill_chunk_real_llama_dense: chunk contract, micro-batching, checks)
+ *
+ * Conventions for every entry point:
+ *  - Memory. The caller owns every buffer (packed weights, norm weights, KV cache,
+ *    workspace, inputs, outputs); libpf keeps non-owning pointers only and performs
+ *    no device allocation. "_dev" pointers are device memory of the current CUDA
+ *    device, "_host" pointers host memory.
+ *  - Errors. Arguments are validated before anything is launched; on failure the
+ *    call returns a pf_status other than PF_OK, pf_last_error() describes it, and no
+ *    state (KV position, buffers) has changed. CUDA launch errors return PF_ERR_CUDA.
+ *  - Asynchrony. GPU work is enqueued on the given stream (a cudaStream_t passed as
+ *    void*, NULL = legacy default stream) and is not waited for, except where a call
+ *    says it synchronises. Kernels whose internal waits time out (a bounded wait on
+ *    a barrier that never completed) record PF_ERR_DEVICE_TIMEOUT in a device status
+ *    word; pf_session_sync() / pf_status_read() report it.
+ *  - Thread safety. Calls on distinct sessions may run concurrently; one session is
+ *    used by one host thread at a time. pf_last_error() is thread-local.
+ */
+#ifndef PF_H_
+#define PF_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ------------------------------------------------------------------ status codes */
+/* Mirrors the error cases of [P1] encode_full_forward_prefill (short buffers, layer
+ * count) and [P3] prefill_chunk_real_llama_dense (empty chunk, non-sequential start,
+ * token outside vocab, logits length). */
+typedef enum {
+  PF_OK = 0,
+  PF_ERR_INVALID_ARG = 1,        /* NULL pointer, negative size, bad enum value */
+  PF_ERR_SHAPE = 2,              /* dimensions the kernels do not support */
+  PF_ERR_EMPTY_CHUNK = 3,        /* M == 0 ([P3] "empty chunk") */
+  PF_ERR_NONSEQUENTIAL_START = 4,/* start_pos != KV position ([P3]) */
+  PF_ERR_TOKEN_OUT_OF_VOCAB = 5, /* token < 0 or >= vocab ([P3]) */
+  PF_ERR_KV_CAPACITY = 6,        /* start_pos + M > max_seq */
+  PF_ERR_LOGITS = 7,             /* logits requested but no LM head / buffer */
+  PF_ERR_UNSUPPORTED = 8,        /* a mode this build refuses by name */
+  PF_ERR_CUDA = 9,               /* a CUDA runtime call failed */
+  PF_ERR_DEVICE_TIMEOUT = 10,    /* a kernel's bounded wait expired (see status word) */
+  PF_ERR_WORKSPACE = 11          /* workspace too small / not initialised */
+} pf_status;
+
+typedef enum { PF_W_Q1_G128 = 0, PF_W_INT4_AFFINE_G128 = 1 } pf_wformat;
+typedef enum { PF_KV_F32 = 0, PF_KV_BF16 = 1, PF_KV_F16 = 2 } pf_kvdtype;
+
+/* Model configuration ([P1] LayerConfig + the tail's final_norm_eps / vocab). */
+typedef struct {
+  int32_t hidden;        /* H; multiple of 128 */
+  int32_t intermediate;  /* I; multiple of 128 */
+  int32_t n_q_heads;     /* nq */
+  int32_t n_kv_heads;    /* nkv; divides nq */
+  int32_t head_dim;      /* hd; 64 or 128 */
+  int32_t n_layers;
+  int32_t vocab;         /* 0 when the model has no embedding / LM head */
+  float rope_theta;
+  float eps;             /* RMSNorm eps of the layers (also the QK-norm eps) */
+  float final_eps;       /* eps of the final norm */
+  int32_t qk_norm;       /* 1: per-head RMSNorm of Q and K before RoPE */
+  int32_t wfmt;          /* pf_wformat */
+  int32_t kv_dtype;      /* pf_kvdtype */
+  int32_t max_seq;       /* KV capacity (positions) */
+  int32_t max_chunk;     /* largest micro-batch the workspace is sized for (<= 8192) */
+} pf_config;
+
+/* One layer's weights ([P1] LayerWeightRefs), all device pointers. Packed tensors
+ * come from pf_pack_weights_host (gate_up with interleave_gate_up = 1). */
+typedef struct {
+  const float* attn_norm; /* [H] f32 */
+  const void* qkv;        /* packed, N = (nq + 2 nkv) hd rows (Q|K|V, head-major), K = H */
+  const float* q_norm;    /* [hd] f32, NULL when qk_norm == 0 */
+  const float* k_norm;    /* [hd] f32, NULL when qk_norm == 0 */
+  const void* o_proj;     /* packed, N = H, K = nq hd */
+  const float* ffn_norm;  /* [H] f32 */
+  const void* gate_up;    /* packed + interleaved, N = 2 I (gate rows then up rows), K = H */
+  const void* down;       /* packed, N = H, K = I */
+} pf_layer_weights;
+
+/* Whole model. `layers` is a HOST array of n_layers entries. */
+typedef struct {
+  pf_config cfg;
+  const pf_layer_weights* layers;
+  const float* embed;      /* [vocab, H] f32 device, or NULL (hidden-input use only) */
+  const float* final_norm; /* [H] f32 device, or NULL */
+  const void* lm_head;     /* packed, N = vocab, K = H, or NULL */
+} pf_model;
+
+typedef struct pf_session pf_session; /* opaque */
+
+/* ------------------------------------------------------------------ misc */
+const char* pf_last_error(void);      /* thread-local, never NULL */
+const char* pf_status_name(int status);
+int32_t pf_abi_version(void);         /* bumps on any ABI change */
+
+/* ------------------------------------------------------------------ packing
+ * Canonical host formats (the pages name "Q1 block bytes" and an "AoS -> SoA"
+ * conversion at upload, [P2] build_cached_weights, without the block layout):
+ *  Q1:   codes = sign bits uint8 [N, K/8]; bit j (LSB first) of byte b of row n is
+ *        weight k = 8b + j; a set bit means +scale. scales = f16 bits [N, K/128].
+ *  INT4: codes uint8 [N, K/2]; low nibble of byte b is k = 2b, high nibble k = 2b+1;
+ *        w = scale * (q - zero); scales, zeros = f16 bits [N, K/128].
+ * The device layout (tiles of 256 rows x 128 weights, scales beside their bits, sign
+ * bits / nibbles permuted for the dequantiser) is private to libpf; only its size
+ * is public. With interleave_gate_up = 1 (N = 2I, I % 128 == 0), each 256-row tile
+ * holds 128 gate rows followed by the 128 matching up rows, so one GEMM tile sees
+ * both inputs of SwiGLU. Rows are padded to a multiple of 256 with zero scale.
+ * Pure host code; safe without a GPU.
+ */
+size_t pf_packed_bytes(int32_t wfmt, int64_t N, int64_t K);
+pf_status pf_pack_weights_host(int32_t wfmt, const uint8_t* codes_host,
+                               const uint16_t* scales_f16_host,
+                               const uint16_t* zeros_f16_host /* NULL for Q1 */,
+                               int64_t N, int64_t K, int32_t interleave_gate_up,
+                               void* dst_host, size_t dst_bytes);
+
+/* ------------------------------------------------------------------ sizes */
+size_t pf_kv_bytes(const pf_config* cfg);        /* bytes of ONE of K / V:
+                                                    n_layers*nkv*max_seq*hd*elem */
+size_t pf_workspace_bytes(const pf_config* cfg); /* activations for max_chunk rows,
+                                                    RoPE table, status words */
+/* Validates a configuration; PF_OK or the reason it is not supported. Host only. */
+pf_status pf_config_check(const pf_config* cfg);
+/* The argument checks pf_prefill_chunk / pf_prefill_hidden run before any launch, in
+ * the order of [P3] prefill_chunk_real_llama_dense (empty chunk, sequential start,
+ * vocabulary), then KV capacity and the head: tokens_host may be NULL (hidden input);
+ * kv_position is the session's current position; want_logits / has_head say whether
+ * logits are requested and whether the model has a final norm + LM head. Host only. */
+pf_status pf_validate_chunk(const pf_config* cfg, int32_t kv_position,
+                            const int32_t* tokens_host, int32_t M, int32_t start_pos,
+                            int32_t want_logits, int32_t has_head);
+
+/* ------------------------------------------------------------------ sessions
+ * A session binds a model, a KV cache (K and V buffers of pf_kv_bytes each, layout
+ * [n_layers][nkv][max_seq][hd] of the cache element type, [P2] GpuKvCache) and a
+ * workspace. Creation computes the RoPE table cos/sin(p * theta^(-2i/hd)) on the
+ * host in double precision ([P1] PrefillBuffers cos_buf/sin_buf are host-made too),
+ * copies it into the workspace and clears the status words; it synchronises the
+ * stream. The KV position starts at 0. The model struct and its layer array are
+ * copied; the device buffers they point to must outlive the session.
+ */
+pf_status pf_session_create(const pf_model* model, void* k_cache_dev, void* v_cache_dev,
+                            void* workspace_dev, size_t workspace_bytes, void* stream,
+                            pf_session** out);
+pf_status pf_session_destroy(pf_session* s);
+int32_t pf_session_position(const pf_session* s); /* -1 for NULL */
+/* Sets the KV position (e.g. 0 to reuse the cache for a new prompt, or the length of a
+ * cache the caller filled itself). Slots at or beyond the new position are stale. */
+pf_status pf_session_set_position(pf_session* s, int32_t position);
+/* 1: record each chunk's launches once per (M, buffers) as a CUDA graph and replay it
+ * (default); 0: launch kernels directly. */
+pf_status pf_session_set_graphs(pf_session* s, int32_t enable);
+/* Synchronises the stream, then reads and clears the session's device status word. */
+pf_status pf_session_sync(pf_session* s, void* stream);
+
+/* ------------------------------------------------------------------ the path
+ * pf_prefill_chunk — [P3] prefill_chunk(tokens, start_position, logits): embeds M
+ * token ids (HOST array, checked against vocab on the host before any launch), runs
+ * them through every layer at positions start_pos .. start_pos+M-1 in micro-batches
+ * of at most max_chunk rows ([P3] MAX_PREFILL_BATCH), and, if logits_dev != NULL,
+ * writes the f32 logits [vocab] of the LAST position ([P1] tail: final RMSNorm of the
+ * last row + LM head). Requires start_pos == pf_session_position ([P3] sequential
+ * start) and start_pos + M <= max_seq. On success the KV position advances by M.
+ */
+pf_status pf_prefill_chunk(pf_session* s, const int32_t* tokens_host, int32_t M,
+                           int32_t start_pos, float* logits_dev, void* stream);
+
+/* Same, from f32 hidden rows x_dev [M, H] (updated in place to the last layer's
+ * output, [P1] hidden_buf is updated in place by the residual GEMMs). M may exceed
+ * max_chunk; rows are processed in micro-batches. */
+pf_status pf_prefill_hidden(pf_session* s, float* x_dev, int32_t M, int32_t start_pos,
+                            float* logits_dev, void* stream);
+
+/* One layer ([P1] encode_layer_prefill, sections 1-7) on x_dev [M, H] (in place),
+ * writing the layer's KV slots start_pos .. start_pos+M-1. Does NOT check or move the
+ * session's KV position (the caller sequences layers); M <= max_chunk. */
+pf_status pf_layer_forward(pf_session* s, int32_t layer, float* x_dev, int32_t M,
+                           int32_t start_pos, void* stream);
+
+/* End to end from host memory: copies tokens_host to the device, runs
+ * pf_prefill_chunk, copies the last position's logits into logits_host [vocab]
+ * (may be NULL) and synchronises the stream. */
+pf_status pf_prefill_tokens_host(pf_session* s, const int32_t* tokens_host, int32_t M,
+                                 int32_t start_pos, float* logits_host, void* stream);
+
+/* ------------------------------------------------------------------ single steps
+ * Each step of the path as its own call, for step-level parity checks. They launch
+ * the same kernels the session uses. status_dev (int32, device) receives
+ * PF_ERR_DEVICE_TIMEOUT if a bounded wait expires; it may be NULL for kernels
+ * without waits. None of them synchronises.
+ */
+/* RMSNorm rows ([P1] dispatch_batched_rmsnorm): y = x * w / sqrt(mean(x^2) + eps),
+ * x f32 [M, H] -> y f16 [M, H] (the GEMM operand type). */
+pf_status pf_op_rmsnorm(const float* x_dev, const float* w_dev, float eps, int32_t M,
+                        int32_t H, uint16_t* y_f16_dev, void* stream);
+/* Dequantise a packed tensor to f16 [N, K] row-major (bit-exact check of unpacking):
+ * Q1 -> +-scale; INT4 -> f16(f16(q - z) * s) evaluated in f16 arithmetic. */
+pf_status pf_op_dequant(int32_t wfmt, const void* packed_dev, int64_t N, int64_t K,
+                        uint16_t* w_f16_dev, void* stream);
+/* Quantised GEMM out[m, n] (+)= sum_k a[m, k] w[n, k] on the tensor cores.
+ * a: f16 [M, K] row-major; epilogue: 0 = store f32 out[M, N] (ld = N),
+ * 1 = residual add into f32 out[M, N] (out += a W^T), 2 = SwiGLU of an interleaved
+ * gate_up weight: out f16 [M, N/2] = silu(gate) * up. split_k >= 1 (0 = automatic;
+ * epilogue 0 with split_k > 1 requires out zeroed beforehand; epilogue 2 forces 1). */
+pf_status pf_op_gemm(int32_t wfmt, int32_t epilogue, const uint16_t* a_f16_dev,
+                     const void* packed_dev, int32_t M, int32_t N, int32_t K, void* out_dev,
+                     int32_t split_k, int32_t* status_dev, void* stream);
+/* Fused per-head QK RMSNorm + RoPE + KV store ([P1] section 3 fused_qk_norm /
+ * fused_qk_rope / fused_kv_store; [P2] dispatch_fused_qk_norm_rope): from qkv f32
+ * [M, (nq+2nkv) hd], writes q_dev [M, nq, hd] (bf16 when kv_dtype is bf16, else f16)
+ * and the K (post-RoPE) / V slots of `layer` at positions start_pos.. in the caches.
+ * rope_dev: table from pf_rope_table_host ([max_seq][hd/2] of (cos, sin) f32). */
+pf_status pf_op_qk_norm_rope_kv(const pf_config* cfg, const float* qkv_dev,
+                                const float* q_norm_dev, const float* k_norm_dev,
+                                const float* rope_dev, int32_t layer, int32_t start_pos,
+                                int32_t M, void* q_dev, void* k_cache_dev,
+                                void* v_cache_dev, void* stream);
+/* Causal GQA attention ([P1] section 3 scores/softmax/weighted sum, batched; [P3]
+ * encode_attention_decode_batch): query rows at positions start_pos.., keys 0..pos of
+ * `layer`'s cache; out f16 [M, nq hd]. */
+pf_status pf_op_attention(const pf_config* cfg, const void* q_dev, const void* k_cache_dev,
+                          const void* v_cache_dev, int32_t layer, int32_t start_pos,
+                          int32_t M, uint16_t* out_f16_dev, void* stream);
+/* Embedding rows ([P3] encode_embed_any, scale 1.0): x[t] = E[tokens[t]] (device ids,
+ * assumed in range). */
+pf_status pf_op_embed(const float* embed_dev, const int32_t* tokens_dev, int32_t M,
+                      int32_t H, float* x_dev, void* stream);
+/* Tail ([P1] rmsnorm_weighted_v2 + dispatch_gemv_q1): logits[v] = W_lm . rmsnorm(x_row)
+ * for one f32 row x_row_dev [H]; logits f32 [vocab]. */
+pf_status pf_op_lm_head(int32_t wfmt, const float* x_row_dev, const float* norm_w_dev,
+                        float eps, const void* packed_dev, int32_t vocab, int32_t H,
+                        float* logits_dev, void* stream);
+/* Host RoPE table [max_seq][hd/2][2] = (cos, sin)(p * theta^(-2i/hd)), computed in
+ * double and rounded to f32. */
+pf_status pf_rope_table_host(float theta, int32_t head_dim, int32_t max_seq, float* dst_host);
+/* Reads (and clears) a device status word written by the single-step kernels;
+ * synchronises the stream. */
+pf_status pf_status_read(int32_t* status_dev, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* PF_H_ */

@@ -1,0 +1,738 @@
+// pf_host.cu — libpf's C ABI: argument validation, the host-side weight packer, the
+// RoPE table, workspace layout, sessions, and the layer / chunk driver that enqueues the
+// kernels on one stream (optionally recorded once per shape as a CUDA graph and
+// replayed).
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <string>
+#include <tuple>
+#include <vector>
+
+#include "pf_internal.h"
+
+namespace pf {
+namespace {
+
+thread_local std::string g_err = "";
+
+pf_status fail(pf_status st, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_err = buf;
+  return st;
+}
+
+pf_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(PF_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+#define PF_CUDA(call, what)                        \
+  do {                                             \
+    cudaError_t e_ = (call);                       \
+    if (e_ != cudaSuccess) return cuda_fail(e_, what); \
+  } while (0)
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+size_t kv_elem_bytes(int kv_dtype) { return kv_dtype == PF_KV_F32 ? 4 : 2; }
+
+// ------------------------------------------------------------------ workspace layout
+struct WsLayout {
+  size_t status, params, tokens, x, y, qkv, q, attn, act, gu, rope, total;
+};
+
+WsLayout ws_layout(const pf_config& c) {
+  WsLayout L{};
+  const size_t C = static_cast<size_t>(c.max_chunk);
+  const size_t H = c.hidden, I = c.intermediate, hd = c.head_dim;
+  const size_t qkv_rows = static_cast<size_t>(c.n_q_heads + 2 * c.n_kv_heads) * hd;
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = o;
+    o = align_up(o + bytes, 256);
+    return at;
+  };
+  L.status = take(STATUS_WORDS * sizeof(int));
+  L.params = take(4 * sizeof(int));
+  L.tokens = take(C * sizeof(int));
+  L.x = take(C * H * 4);
+  L.y = take(C * H * 2);
+  L.qkv = take(C * qkv_rows * 4);
+  L.q = take(C * c.n_q_heads * hd * 2);
+  L.attn = take(C * c.n_q_heads * hd * 2);
+  L.act = take(C * I * 2);
+  L.gu = take(C * 2 * I * 4);
+  L.rope = take(static_cast<size_t>(c.max_seq) * (hd / 2) * 2 * 4);
+  L.total = o;
+  return L;
+}
+
+// ------------------------------------------------------------------ tensor maps
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn get_encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+}  // namespace
+
+bool encode_tmap_f16_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
+                        uint32_t box_inner, uint32_t box_outer) {
+  EncodeTiledFn fn = get_encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {inner * 2};
+  const cuuint32_t box[2] = {box_inner, box_outer};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int device_sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 148;
+  return n;
+}
+
+}  // namespace pf
+
+using namespace pf;
+
+// ====================================================================== sessions
+struct GraphKey {
+  int M;
+  const void* x;
+  const void* logits;
+  int from_tokens;
+  int layer;  // -1: whole stack
+  bool operator<(const GraphKey& o) const {
+    return std::tie(M, x, logits, from_tokens, layer) <
+           std::tie(o.M, o.x, o.logits, o.from_tokens, o.layer);
+  }
+};
+
+struct pf_session {
+  pf_model model;
+  std::vector<pf_layer_weights> layers;
+  void* k = nullptr;
+  void* v = nullptr;
+  uint8_t* ws = nullptr;
+  size_t ws_bytes = 0;
+  WsLayout L{};
+  int position = 0;
+  bool graphs = true;
+  int sms = 148;
+  std::map<GraphKey, cudaGraphExec_t> execs;
+};
+
+namespace {
+
+template <typename T>
+T* wsp(pf_session* s, size_t off) {
+  return reinterpret_cast<T*>(s->ws + off);
+}
+
+pf_status check_cfg(const pf_config* c) {
+  if (!c) return fail(PF_ERR_INVALID_ARG, "config is NULL");
+  if (c->hidden <= 0 || c->hidden % 128) return fail(PF_ERR_SHAPE, "hidden %d: need a positive multiple of 128", c->hidden);
+  if (c->intermediate <= 0 || c->intermediate % 128)
+    return fail(PF_ERR_SHAPE, "intermediate %d: need a positive multiple of 128", c->intermediate);
+  if (c->head_dim != 64 && c->head_dim != 128) return fail(PF_ERR_SHAPE, "head_dim %d: 64 or 128", c->head_dim);
+  if (c->n_q_heads <= 0 || c->n_kv_heads <= 0 || c->n_q_heads % c->n_kv_heads)
+    return fail(PF_ERR_SHAPE, "heads %d/%d: nkv must divide nq", c->n_q_heads, c->n_kv_heads);
+  const int G = c->n_q_heads / c->n_kv_heads;
+  if (64 % G) return fail(PF_ERR_SHAPE, "GQA group %d must divide 64", G);
+  if ((c->n_q_heads * c->head_dim) % 128)
+    return fail(PF_ERR_SHAPE, "nq*hd %d: need a multiple of 128", c->n_q_heads * c->head_dim);
+  if (c->n_layers <= 0) return fail(PF_ERR_SHAPE, "n_layers %d", c->n_layers);
+  if (c->vocab < 0) return fail(PF_ERR_SHAPE, "vocab %d", c->vocab);
+  if (c->wfmt != PF_W_Q1_G128 && c->wfmt != PF_W_INT4_AFFINE_G128)
+    return fail(PF_ERR_INVALID_ARG, "weight format %d", c->wfmt);
+  if (c->kv_dtype != PF_KV_F32 && c->kv_dtype != PF_KV_BF16 && c->kv_dtype != PF_KV_F16)
+    return fail(PF_ERR_INVALID_ARG, "kv dtype %d", c->kv_dtype);
+  if (c->max_seq <= 0) return fail(PF_ERR_SHAPE, "max_seq %d", c->max_seq);
+  if (c->max_chunk <= 0 || c->max_chunk > 8192) return fail(PF_ERR_SHAPE, "max_chunk %d: 1..8192", c->max_chunk);
+  if (!(c->eps >= 0.f) || !(c->final_eps >= 0.f) || !(c->rope_theta > 0.f))
+    return fail(PF_ERR_INVALID_ARG, "eps / rope_theta");
+  return PF_OK;
+}
+
+pf_status enqueue_gemm(pf_session* s, int wfmt, int epi, const void* a, const void* w, int M, int N,
+                       int K, void* out, cudaStream_t st) {
+  GemmArgs g{};
+  g.wfmt = wfmt;
+  g.epilogue = epi;
+  g.a = a;
+  g.w = reinterpret_cast<const uint8_t*>(w);
+  g.M = M;
+  g.N = N;
+  g.K = K;
+  g.out = out;
+  g.split_k = choose_split_k(M, N, K, epi, s->sms);
+  g.status = wsp<int>(s, s->L.status);
+  if (epi == EPI_STORE_F32 && g.split_k > 1)
+    PF_CUDA(cudaMemsetAsync(out, 0, static_cast<size_t>(M) * N * 4, st), "memset gemm output");
+  PF_CUDA(launch_gemm(g, st), "gemm launch");
+  return PF_OK;
+}
+
+// metal_prefill.rs encode_layer_prefill, sections 1-7, on x [M, H] (in place).
+pf_status enqueue_layer(pf_session* s, int l, float* x, int M, cudaStream_t st) {
+  const pf_config& c = s->model.cfg;
+  const pf_layer_weights& w = s->layers[l];
+  const int H = c.hidden, I = c.intermediate, hd = c.head_dim;
+  const int qkv_rows = (c.n_q_heads + 2 * c.n_kv_heads) * hd;
+  const int* start_dev = wsp<int>(s, s->L.params);
+  void* y = wsp<void>(s, s->L.y);
+  float* qkv = wsp<float>(s, s->L.qkv);
+  void* q = wsp<void>(s, s->L.q);
+  void* attn = wsp<void>(s, s->L.attn);
+  void* act = wsp<void>(s, s->L.act);
+  pf_status r;
+  // 1. pre-attention RMSNorm
+  PF_CUDA(launch_rmsnorm(x, w.attn_norm, c.eps, M, H, y, st), "rmsnorm");
+  // 2. fused QKV projection
+  if ((r = enqueue_gemm(s, c.wfmt, EPI_STORE_F32, y, w.qkv, M, qkv_rows, H, qkv, st)) != PF_OK) return r;
+  // 3. QK-norm + RoPE + KV store, then causal GQA attention over cache + chunk
+  PF_CUDA(launch_qk_norm_rope_kv(c, qkv, w.q_norm, w.k_norm, wsp<float>(s, s->L.rope), l, start_dev,
+                                 0, M, q, s->k, s->v, st),
+          "qk_norm_rope_kv");
+  PF_CUDA(launch_attention(c, q, s->k, s->v, l, start_dev, 0, M, attn, st), "attention");
+  // 4. O projection + residual
+  if ((r = enqueue_gemm(s, c.wfmt, EPI_RESID_ADD, attn, w.o_proj, M, H, c.n_q_heads * hd, x, st)) != PF_OK)
+    return r;
+  // 5. FFN RMSNorm
+  PF_CUDA(launch_rmsnorm(x, w.ffn_norm, c.eps, M, H, y, st), "rmsnorm");
+  // 6. gate_up + SwiGLU (split along K through an f32 scratch when that fills the GPU better)
+  const int split_gu = choose_split_k(M, 2 * I, H, EPI_STORE_F32, s->sms);
+  if (split_gu > 1) {
+    float* gu = wsp<float>(s, s->L.gu);
+    if ((r = enqueue_gemm(s, c.wfmt, EPI_STORE_F32, y, w.gate_up, M, 2 * I, H, gu, st)) != PF_OK) return r;
+    PF_CUDA(launch_swiglu_f32(gu, M, I, act, st), "swiglu");
+  } else {
+    if ((r = enqueue_gemm(s, c.wfmt, EPI_SWIGLU, y, w.gate_up, M, 2 * I, H, act, st)) != PF_OK) return r;
+  }
+  // 7. down projection + residual
+  if ((r = enqueue_gemm(s, c.wfmt, EPI_RESID_ADD, act, w.down, M, H, I, x, st)) != PF_OK) return r;
+  return PF_OK;
+}
+
+// One micro-batch: [embed] -> every layer -> [final norm + LM head on the last row].
+pf_status enqueue_chunk(pf_session* s, float* x, int M, bool from_tokens, float* logits,
+                        cudaStream_t st) {
+  const pf_config& c = s->model.cfg;
+  if (from_tokens)
+    PF_CUDA(launch_embed(s->model.embed, wsp<int>(s, s->L.tokens), M, c.hidden, x, st), "embed");
+  for (int l = 0; l < c.n_layers; ++l) {
+    pf_status r = enqueue_layer(s, l, x, M, st);
+    if (r != PF_OK) return r;
+  }
+  if (logits)
+    PF_CUDA(launch_lm_head(c.wfmt, x + static_cast<size_t>(M - 1) * c.hidden, s->model.final_norm,
+                           c.final_eps, reinterpret_cast<const uint8_t*>(s->model.lm_head), c.vocab,
+                           c.hidden, logits, st),
+            "lm_head");
+  return PF_OK;
+}
+
+// Runs `body` directly, or as a CUDA graph recorded on first use for `key`.
+template <typename Body>
+pf_status run_maybe_graph(pf_session* s, const GraphKey& key, cudaStream_t st, Body body) {
+  if (!s->graphs) return body();
+  auto it = s->execs.find(key);
+  if (it == s->execs.end()) {
+    PF_CUDA(cudaStreamBeginCapture(st, cudaStreamCaptureModeThreadLocal), "begin capture");
+    pf_status r = body();
+    cudaGraph_t graph = nullptr;
+    cudaError_t e = cudaStreamEndCapture(st, &graph);
+    if (r != PF_OK) {
+      if (graph) cudaGraphDestroy(graph);
+      return r;
+    }
+    if (e != cudaSuccess) return cuda_fail(e, "end capture");
+    cudaGraphExec_t exec = nullptr;
+    e = cudaGraphInstantiate(&exec, graph, 0);
+    cudaGraphDestroy(graph);
+    if (e != cudaSuccess) return cuda_fail(e, "graph instantiate");
+    if (s->execs.size() >= 64) {
+      cudaGraphExecDestroy(s->execs.begin()->second);
+      s->execs.erase(s->execs.begin());
+    }
+    it = s->execs.emplace(key, exec).first;
+  }
+  PF_CUDA(cudaGraphLaunch(it->second, st), "graph launch");
+  return PF_OK;
+}
+
+pf_status set_start(pf_session* s, int start, cudaStream_t st) {
+  PF_CUDA(launch_set_int(wsp<int>(s, s->L.params), start, st), "set start");
+  return PF_OK;
+}
+
+// Raises the dynamic shared-memory limit of the big kernels once, outside any capture.
+void prepare_all() {
+  static std::once_flag once;
+  std::call_once(once, [] {
+    prepare_gemm_kernels();
+    prepare_attention_kernels();
+  });
+}
+
+}  // namespace
+
+// ====================================================================== C ABI
+extern "C" {
+
+const char* pf_last_error(void) { return g_err.c_str(); }
+
+const char* pf_status_name(int st) {
+  switch (st) {
+    case PF_OK: return "PF_OK";
+    case PF_ERR_INVALID_ARG: return "PF_ERR_INVALID_ARG";
+    case PF_ERR_SHAPE: return "PF_ERR_SHAPE";
+    case PF_ERR_EMPTY_CHUNK: return "PF_ERR_EMPTY_CHUNK";
+    case PF_ERR_NONSEQUENTIAL_START: return "PF_ERR_NONSEQUENTIAL_START";
+    case PF_ERR_TOKEN_OUT_OF_VOCAB: return "PF_ERR_TOKEN_OUT_OF_VOCAB";
+    case PF_ERR_KV_CAPACITY: return "PF_ERR_KV_CAPACITY";
+    case PF_ERR_LOGITS: return "PF_ERR_LOGITS";
+    case PF_ERR_UNSUPPORTED: return "PF_ERR_UNSUPPORTED";
+    case PF_ERR_CUDA: return "PF_ERR_CUDA";
+    case PF_ERR_DEVICE_TIMEOUT: return "PF_ERR_DEVICE_TIMEOUT";
+    case PF_ERR_WORKSPACE: return "PF_ERR_WORKSPACE";
+    default: return "PF_ERR_UNKNOWN";
+  }
+}
+
+int32_t pf_abi_version(void) { return 1; }
+
+size_t pf_packed_bytes(int32_t wfmt, int64_t N, int64_t K) {
+  if ((wfmt != PF_W_Q1_G128 && wfmt != PF_W_INT4_AFFINE_G128) || N <= 0 || K <= 0 || K % GROUP)
+    return 0;
+  return static_cast<size_t>(padded_rows(N) / TILE_N) * static_cast<size_t>(K / GROUP) *
+         chunk_bytes(wfmt);
+}
+
+pf_status pf_pack_weights_host(int32_t wfmt, const uint8_t* codes, const uint16_t* scales,
+                               const uint16_t* zeros, int64_t N, int64_t K,
+                               int32_t interleave_gate_up, void* dst, size_t dst_bytes) {
+  const size_t need = pf_packed_bytes(wfmt, N, K);
+  if (need == 0) return fail(PF_ERR_SHAPE, "pack: format %d, N %lld, K %lld (K %% 128 == 0)", wfmt, (long long)N, (long long)K);
+  if (!codes || !scales || !dst) return fail(PF_ERR_INVALID_ARG, "pack: NULL pointer");
+  if (wfmt == PF_W_INT4_AFFINE_G128 && !zeros) return fail(PF_ERR_INVALID_ARG, "pack: INT4 needs zeros");
+  if (dst_bytes < need) return fail(PF_ERR_INVALID_ARG, "pack: dst holds %zu bytes, need %zu", dst_bytes, need);
+  if (interleave_gate_up && (N % 256)) return fail(PF_ERR_SHAPE, "pack: interleaved gate_up needs N = 2I, I %% 128 == 0");
+  uint8_t* out = static_cast<uint8_t*>(dst);
+  std::memset(out, 0, need);
+  const int64_t G = K / GROUP, Np = padded_rows(N), I = N / 2;
+  const size_t cb = chunk_bytes(wfmt);
+  // even / odd bit compaction of one byte: low nibble = bits 0,2,4,6; high = bits 1,3,5,7
+  static uint8_t eo[256];
+  static std::once_flag once;
+  std::call_once(once, [] {
+    for (int b = 0; b < 256; ++b) {
+      int e = 0, o = 0;
+      for (int i = 0; i < 4; ++i) {
+        e |= ((b >> (2 * i)) & 1) << i;
+        o |= ((b >> (2 * i + 1)) & 1) << i;
+      }
+      eo[b] = static_cast<uint8_t>(e | (o << 4));
+    }
+  });
+  auto rev16 = [](uint32_t v) {
+    v = ((v & 0x5555u) << 1) | ((v >> 1) & 0x5555u);
+    v = ((v & 0x3333u) << 2) | ((v >> 2) & 0x3333u);
+    v = ((v & 0x0F0Fu) << 4) | ((v >> 4) & 0x0F0Fu);
+    v = ((v & 0x00FFu) << 8) | ((v >> 8) & 0x00FFu);
+    return v & 0xFFFFu;
+  };
+  for (int64_t p = 0; p < Np; ++p) {
+    int64_t src;
+    if (interleave_gate_up) {
+      const int64_t t = p / 256, r = p % 256;
+      src = r < 128 ? t * 128 + r : I + t * 128 + (r - 128);
+    } else {
+      src = p < N ? p : -1;
+    }
+    if (src < 0) continue;  // padding row: zero scale (and zero codes)
+    const int64_t t = p / TILE_N, r = p % TILE_N;
+    for (int64_t g = 0; g < G; ++g) {
+      uint8_t* ch = out + (t * G + g) * cb;
+      const uint16_t sc = scales[src * G + g];
+      if (wfmt == PF_W_Q1_G128) {
+        const uint8_t* row = codes + src * (K / 8) + g * 16;
+        for (int h = 0; h < 2; ++h)
+          for (int b = 0; b < 2; ++b) {
+            const uint8_t* w4 = row + h * 8 + b * 4;  // 32 weights, LSB-first
+            uint32_t E = 0, O = 0;
+            for (int j = 0; j < 4; ++j) {
+              E |= static_cast<uint32_t>(eo[w4[j]] & 15) << (4 * j);
+              O |= static_cast<uint32_t>(eo[w4[j]] >> 4) << (4 * j);
+            }
+            // bit i of E/O = sign bit of element 2i / 2i+1; store NEGATIVE flags at 15-i / 31-i
+            const uint32_t Z = rev16(~E & 0xFFFFu) | (rev16(~O & 0xFFFFu) << 16);
+            std::memcpy(ch + h * Q1_HALF_BYTES + r * 8 + b * 4, &Z, 4);
+          }
+        std::memcpy(ch + Q1_SCALE_OFF + r * 2, &sc, 2);
+      } else {
+        const uint8_t* row = codes + src * (K / 2) + g * 64;
+        for (int h = 0; h < 2; ++h)
+          for (int w = 0; w < 8; ++w) {
+            const uint8_t* b = row + h * 32 + w * 4;  // 8 weights: byte j = (k 2j, k 2j+1)
+            uint32_t lo = 0, hi = 0;
+            for (int j = 0; j < 4; ++j) {
+              lo |= static_cast<uint32_t>(b[j] & 15) << (4 * j);
+              hi |= static_cast<uint32_t>(b[j] >> 4) << (4 * j);
+            }
+            const uint32_t word = lo | (hi << 16);
+            std::memcpy(ch + h * I4_HALF_BYTES + r * 32 + w * 4, &word, 4);
+          }
+        const uint16_t z = zeros[src * G + g];
+        std::memcpy(ch + I4_SCALE_OFF + r * 2, &sc, 2);
+        std::memcpy(ch + I4_ZERO_OFF + r * 2, &z, 2);
+      }
+    }
+  }
+  return PF_OK;
+}
+
+size_t pf_kv_bytes(const pf_config* c) {
+  if (check_cfg(c) != PF_OK) return 0;
+  return static_cast<size_t>(c->n_layers) * c->n_kv_heads * c->max_seq * c->head_dim *
+         kv_elem_bytes(c->kv_dtype);
+}
+
+size_t pf_workspace_bytes(const pf_config* c) {
+  if (check_cfg(c) != PF_OK) return 0;
+  return ws_layout(*c).total;
+}
+
+pf_status pf_config_check(const pf_config* c) { return check_cfg(c); }
+
+pf_status pf_validate_chunk(const pf_config* c, int32_t kv_position, const int32_t* tokens,
+                            int32_t M, int32_t start, int32_t want_logits, int32_t has_head) {
+  pf_status r = check_cfg(c);
+  if (r != PF_OK) return r;
+  if (M <= 0) return fail(PF_ERR_EMPTY_CHUNK, "prefill called with an empty chunk (M = %d)", M);
+  if (start != kv_position)
+    return fail(PF_ERR_NONSEQUENTIAL_START, "non-sequential chunk start %d; KV cache is at %d", start, kv_position);
+  if (tokens) {
+    for (int i = 0; i < M; ++i)
+      if (tokens[i] < 0 || tokens[i] >= c->vocab)
+        return fail(PF_ERR_TOKEN_OUT_OF_VOCAB, "token id %d outside vocab %d", tokens[i], c->vocab);
+  }
+  if (static_cast<int64_t>(start) + M > c->max_seq)
+    return fail(PF_ERR_KV_CAPACITY, "chunk [%d, %d) exceeds KV capacity %d", start, start + M, c->max_seq);
+  if (want_logits && !has_head)
+    return fail(PF_ERR_LOGITS, "logits requested but the model has no final norm / LM head");
+  return PF_OK;
+}
+
+pf_status pf_rope_table_host(float theta, int32_t hd, int32_t max_seq, float* dst) {
+  if (!dst || hd <= 0 || hd % 2 || max_seq <= 0 || !(theta > 0.f))
+    return fail(PF_ERR_INVALID_ARG, "rope table arguments");
+  const int half = hd / 2;
+  for (int i = 0; i < half; ++i) {
+    const double inv = std::pow(static_cast<double>(theta), -2.0 * i / hd);
+    for (int p = 0; p < max_seq; ++p) {
+      const double a = p * inv;
+      dst[(static_cast<size_t>(p) * half + i) * 2 + 0] = static_cast<float>(std::cos(a));
+      dst[(static_cast<size_t>(p) * half + i) * 2 + 1] = static_cast<float>(std::sin(a));
+    }
+  }
+  return PF_OK;
+}
+
+pf_status pf_session_create(const pf_model* model, void* k, void* v, void* ws, size_t ws_bytes,
+                            void* stream, pf_session** out) {
+  if (!out) return fail(PF_ERR_INVALID_ARG, "out is NULL");
+  *out = nullptr;
+  if (!model) return fail(PF_ERR_INVALID_ARG, "model is NULL");
+  pf_status r = check_cfg(&model->cfg);
+  if (r != PF_OK) return r;
+  const pf_config& c = model->cfg;
+  if (!model->layers || !k || !v || !ws) return fail(PF_ERR_INVALID_ARG, "layers / k / v / workspace is NULL");
+  for (int l = 0; l < c.n_layers; ++l) {
+    const pf_layer_weights& w = model->layers[l];
+    if (!w.attn_norm || !w.qkv || !w.o_proj || !w.ffn_norm || !w.gate_up || !w.down)
+      return fail(PF_ERR_INVALID_ARG, "layer %d: a weight pointer is NULL", l);
+    if (c.qk_norm && (!w.q_norm || !w.k_norm))
+      return fail(PF_ERR_INVALID_ARG, "layer %d: qk_norm set but q_norm / k_norm NULL", l);
+  }
+  const WsLayout L = ws_layout(c);
+  if (ws_bytes < L.total) return fail(PF_ERR_WORKSPACE, "workspace %zu bytes, need %zu", ws_bytes, L.total);
+  if ((reinterpret_cast<uintptr_t>(ws) & 255) || (reinterpret_cast<uintptr_t>(k) & 15) ||
+      (reinterpret_cast<uintptr_t>(v) & 15))
+    return fail(PF_ERR_INVALID_ARG, "workspace must be 256-B aligned, caches 16-B aligned");
+  auto* s = new pf_session();
+  s->model = *model;
+  s->layers.assign(model->layers, model->layers + c.n_layers);
+  s->model.layers = s->layers.data();
+  s->k = k;
+  s->v = v;
+  s->ws = static_cast<uint8_t*>(ws);
+  s->ws_bytes = ws_bytes;
+  s->L = L;
+  s->sms = device_sm_count();
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  std::vector<float> rope(static_cast<size_t>(c.max_seq) * (c.head_dim / 2) * 2);
+  pf_rope_table_host(c.rope_theta, c.head_dim, c.max_seq, rope.data());
+  cudaError_t e = cudaMemcpyAsync(s->ws + L.rope, rope.data(), rope.size() * 4, cudaMemcpyHostToDevice, st);
+  if (e == cudaSuccess) e = cudaMemsetAsync(s->ws + L.status, 0, STATUS_WORDS * 4, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) {
+    delete s;
+    return cuda_fail(e, "session init");
+  }
+  prepare_all();
+  *out = s;
+  return PF_OK;
+}
+
+pf_status pf_session_destroy(pf_session* s) {
+  if (!s) return fail(PF_ERR_INVALID_ARG, "session is NULL");
+  for (auto& kv : s->execs) cudaGraphExecDestroy(kv.second);
+  delete s;
+  return PF_OK;
+}
+
+int32_t pf_session_position(const pf_session* s) { return s ? s->position : -1; }
+
+pf_status pf_session_set_position(pf_session* s, int32_t position) {
+  if (!s) return fail(PF_ERR_INVALID_ARG, "session is NULL");
+  if (position < 0 || position > s->model.cfg.max_seq)
+    return fail(PF_ERR_KV_CAPACITY, "position %d outside [0, %d]", position, s->model.cfg.max_seq);
+  s->position = position;
+  return PF_OK;
+}
+
+pf_status pf_session_set_graphs(pf_session* s, int32_t enable) {
+  if (!s) return fail(PF_ERR_INVALID_ARG, "session is NULL");
+  s->graphs = enable != 0;
+  return PF_OK;
+}
+
+pf_status pf_session_sync(pf_session* s, void* stream) {
+  if (!s) return fail(PF_ERR_INVALID_ARG, "session is NULL");
+  return pf_status_read(wsp<int>(s, s->L.status), stream);
+}
+
+pf_status pf_status_read(int32_t* status_dev, void* stream) {
+  if (!status_dev) return fail(PF_ERR_INVALID_ARG, "status pointer is NULL");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int32_t h = 0;
+  PF_CUDA(cudaStreamSynchronize(st), "stream sync");
+  PF_CUDA(cudaMemcpy(&h, status_dev, 4, cudaMemcpyDeviceToHost), "status read");
+  if (h != 0) {
+    PF_CUDA(cudaMemset(status_dev, 0, 4), "status clear");
+    return fail(static_cast<pf_status>(h), "device status %d (%s) recorded by a kernel", h, pf_status_name(h));
+  }
+  return PF_OK;
+}
+
+static pf_status prefill_common(pf_session* s, const int32_t* tokens, float* x, int32_t M,
+                                int32_t start, float* logits, void* stream) {
+  if (!s) return fail(PF_ERR_INVALID_ARG, "session is NULL");
+  const pf_config& c = s->model.cfg;
+  if (M > 0 && tokens == nullptr && x == nullptr) return fail(PF_ERR_INVALID_ARG, "input is NULL");
+  if (tokens && (!s->model.embed || c.vocab <= 0)) return fail(PF_ERR_INVALID_ARG, "model has no embedding table");
+  const int has_head = s->model.lm_head && s->model.final_norm && c.vocab > 0;
+  pf_status v = pf_validate_chunk(&c, s->position, tokens, M, start, logits != nullptr, has_head);
+  if (v != PF_OK) return v;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int off = 0;
+  while (off < M) {  // micro-batches of at most max_chunk rows; head on the last only
+    const int m = std::min(M - off, c.max_chunk);
+    const bool last = off + m == M;
+    float* xc;
+    if (tokens) {
+      xc = wsp<float>(s, s->L.x);
+      PF_CUDA(cudaMemcpyAsync(wsp<int>(s, s->L.tokens), tokens + off, static_cast<size_t>(m) * 4,
+                              cudaMemcpyHostToDevice, st),
+              "tokens upload");
+    } else {
+      xc = x + static_cast<size_t>(off) * c.hidden;
+    }
+    pf_status r = set_start(s, start + off, st);
+    if (r != PF_OK) return r;
+    float* lg = last ? logits : nullptr;
+    GraphKey key{m, xc, lg, tokens != nullptr, -1};
+    r = run_maybe_graph(s, key, st, [&] { return enqueue_chunk(s, xc, m, tokens != nullptr, lg, st); });
+    if (r != PF_OK) return r;
+    s->position = start + off + m;  // turbospark prefill.rs kv.advance_by(m)
+    off += m;
+  }
+  return PF_OK;
+}
+
+pf_status pf_prefill_chunk(pf_session* s, const int32_t* tokens_host, int32_t M, int32_t start_pos,
+                           float* logits_dev, void* stream) {
+  if (s && M > 0 && !tokens_host) return fail(PF_ERR_INVALID_ARG, "tokens is NULL");
+  return prefill_common(s, tokens_host, nullptr, M, start_pos, logits_dev, stream);
+}
+
+pf_status pf_prefill_hidden(pf_session* s, float* x_dev, int32_t M, int32_t start_pos,
+                            float* logits_dev, void* stream) {
+  if (s && M > 0 && !x_dev) return fail(PF_ERR_INVALID_ARG, "x is NULL");
+  return prefill_common(s, nullptr, x_dev, M, start_pos, logits_dev, stream);
+}
+
+pf_status pf_layer_forward(pf_session* s, int32_t layer, float* x_dev, int32_t M, int32_t start_pos,
+                           void* stream) {
+  if (!s) return fail(PF_ERR_INVALID_ARG, "session is NULL");
+  const pf_config& c = s->model.cfg;
+  if (layer < 0 || layer >= c.n_layers) return fail(PF_ERR_INVALID_ARG, "layer %d of %d", layer, c.n_layers);
+  if (M <= 0) return fail(PF_ERR_EMPTY_CHUNK, "empty chunk (M = %d)", M);
+  if (M > c.max_chunk) return fail(PF_ERR_SHAPE, "M %d exceeds max_chunk %d", M, c.max_chunk);
+  if (!x_dev) return fail(PF_ERR_INVALID_ARG, "x is NULL");
+  if (start_pos < 0 || static_cast<int64_t>(start_pos) + M > c.max_seq)
+    return fail(PF_ERR_KV_CAPACITY, "chunk [%d, %d) exceeds KV capacity %d", start_pos, start_pos + M, c.max_seq);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  pf_status r = set_start(s, start_pos, st);
+  if (r != PF_OK) return r;
+  GraphKey key{M, x_dev, nullptr, 0, layer};
+  return run_maybe_graph(s, key, st, [&] { return enqueue_layer(s, layer, x_dev, M, st); });
+}
+
+pf_status pf_prefill_tokens_host(pf_session* s, const int32_t* tokens_host, int32_t M, int32_t start_pos,
+                                 float* logits_host, void* stream) {
+  if (!s) return fail(PF_ERR_INVALID_ARG, "session is NULL");
+  const pf_config& c = s->model.cfg;
+  float* lg_dev = nullptr;
+  if (logits_host) {
+    if (!s->model.lm_head || c.vocab <= 0) return fail(PF_ERR_LOGITS, "no LM head");
+    // logits land in the f32 gate_up scratch (>= vocab floats is checked) before the copy out
+    const size_t room = static_cast<size_t>(c.max_chunk) * 2 * c.intermediate;
+    if (room < static_cast<size_t>(c.vocab)) return fail(PF_ERR_WORKSPACE, "workspace too small for logits");
+    lg_dev = wsp<float>(s, s->L.gu);
+  }
+  pf_status r = pf_prefill_chunk(s, tokens_host, M, start_pos, lg_dev, stream);
+  if (r != PF_OK) return r;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (logits_host)
+    PF_CUDA(cudaMemcpyAsync(logits_host, lg_dev, static_cast<size_t>(c.vocab) * 4,
+                            cudaMemcpyDeviceToHost, st),
+            "logits download");
+  PF_CUDA(cudaStreamSynchronize(st), "sync");
+  return PF_OK;
+}
+
+// ---------------------------------------------------------------------- single steps
+pf_status pf_op_rmsnorm(const float* x, const float* w, float eps, int32_t M, int32_t H,
+                        uint16_t* y, void* stream) {
+  if (!x || !w || !y) return fail(PF_ERR_INVALID_ARG, "NULL pointer");
+  if (M <= 0 || H <= 0 || H % 4) return fail(PF_ERR_SHAPE, "M %d, H %d", M, H);
+  PF_CUDA(launch_rmsnorm(x, w, eps, M, H, y, static_cast<cudaStream_t>(stream)), "rmsnorm");
+  return PF_OK;
+}
+
+pf_status pf_op_dequant(int32_t wfmt, const void* packed, int64_t N, int64_t K, uint16_t* w,
+                        void* stream) {
+  if (pf_packed_bytes(wfmt, N, K) == 0) return fail(PF_ERR_SHAPE, "dequant shape");
+  if (!packed || !w) return fail(PF_ERR_INVALID_ARG, "NULL pointer");
+  PF_CUDA(launch_dequant(wfmt, static_cast<const uint8_t*>(packed), N, K, w,
+                         static_cast<cudaStream_t>(stream)),
+          "dequant");
+  return PF_OK;
+}
+
+pf_status pf_op_gemm(int32_t wfmt, int32_t epi, const uint16_t* a, const void* packed, int32_t M,
+                     int32_t N, int32_t K, void* out, int32_t split_k, int32_t* status,
+                     void* stream) {
+  if (!a || !packed || !out) return fail(PF_ERR_INVALID_ARG, "NULL pointer");
+  if (wfmt != PF_W_Q1_G128 && wfmt != PF_W_INT4_AFFINE_G128) return fail(PF_ERR_INVALID_ARG, "format");
+  if (epi < EPI_STORE_F32 || epi > EPI_SWIGLU) return fail(PF_ERR_INVALID_ARG, "epilogue %d", epi);
+  if (M <= 0 || N <= 0 || K <= 0 || K % 128 || N % 8) return fail(PF_ERR_SHAPE, "M %d N %d K %d", M, N, K);
+  if (epi == EPI_SWIGLU && N % 256) return fail(PF_ERR_SHAPE, "SwiGLU needs N = 2I with I %% 128 == 0");
+  if (reinterpret_cast<uintptr_t>(a) & 15) return fail(PF_ERR_INVALID_ARG, "a must be 16-B aligned");
+  prepare_all();
+  GemmArgs g{};
+  g.wfmt = wfmt;
+  g.epilogue = epi;
+  g.a = a;
+  g.w = static_cast<const uint8_t*>(packed);
+  g.M = M;
+  g.N = N;
+  g.K = K;
+  g.out = out;
+  g.split_k = split_k > 0 ? split_k : choose_split_k(M, N, K, epi, device_sm_count());
+  g.status = status;
+  PF_CUDA(launch_gemm(g, static_cast<cudaStream_t>(stream)), "gemm");
+  return PF_OK;
+}
+
+pf_status pf_op_qk_norm_rope_kv(const pf_config* cfg, const float* qkv, const float* qn,
+                                const float* kn, const float* rope, int32_t layer, int32_t start,
+                                int32_t M, void* q, void* kc, void* vc, void* stream) {
+  pf_status r = check_cfg(cfg);
+  if (r != PF_OK) return r;
+  if (!qkv || !rope || !q || !kc || !vc || (cfg->qk_norm && (!qn || !kn)))
+    return fail(PF_ERR_INVALID_ARG, "NULL pointer");
+  if (M <= 0 || layer < 0 || layer >= cfg->n_layers || start < 0 ||
+      static_cast<int64_t>(start) + M > cfg->max_seq)
+    return fail(PF_ERR_SHAPE, "M %d layer %d start %d", M, layer, start);
+  PF_CUDA(launch_qk_norm_rope_kv(*cfg, qkv, qn, kn, rope, layer, nullptr, start, M, q, kc, vc,
+                                 static_cast<cudaStream_t>(stream)),
+          "qk_norm_rope_kv");
+  return PF_OK;
+}
+
+pf_status pf_op_attention(const pf_config* cfg, const void* q, const void* kc, const void* vc,
+                          int32_t layer, int32_t start, int32_t M, uint16_t* out, void* stream) {
+  pf_status r = check_cfg(cfg);
+  if (r != PF_OK) return r;
+  if (!q || !kc || !vc || !out) return fail(PF_ERR_INVALID_ARG, "NULL pointer");
+  if (M <= 0 || layer < 0 || layer >= cfg->n_layers || start < 0 ||
+      static_cast<int64_t>(start) + M > cfg->max_seq)
+    return fail(PF_ERR_SHAPE, "M %d layer %d start %d", M, layer, start);
+  prepare_all();
+  PF_CUDA(launch_attention(*cfg, q, kc, vc, layer, nullptr, start, M, out,
+                           static_cast<cudaStream_t>(stream)),
+          "attention");
+  return PF_OK;
+}
+
+pf_status pf_op_embed(const float* E, const int32_t* tokens, int32_t M, int32_t H, float* x,
+                      void* stream) {
+  if (!E || !tokens || !x) return fail(PF_ERR_INVALID_ARG, "NULL pointer");
+  if (M <= 0 || H <= 0 || H % 4) return fail(PF_ERR_SHAPE, "M %d H %d", M, H);
+  PF_CUDA(launch_embed(E, tokens, M, H, x, static_cast<cudaStream_t>(stream)), "embed");
+  return PF_OK;
+}
+
+pf_status pf_op_lm_head(int32_t wfmt, const float* x_row, const float* nw, float eps,
+                        const void* packed, int32_t vocab, int32_t H, float* logits, void* stream) {
+  if (!x_row || !nw || !packed || !logits) return fail(PF_ERR_INVALID_ARG, "NULL pointer");
+  if (pf_packed_bytes(wfmt, vocab, H) == 0) return fail(PF_ERR_SHAPE, "vocab %d H %d", vocab, H);
+  PF_CUDA(launch_lm_head(wfmt, x_row, nw, eps, static_cast<const uint8_t*>(packed), vocab, H,
+                         logits, static_cast<cudaStream_t>(stream)),
+          "lm_head");
+  return PF_OK;
+}
+
+}  // extern "C"

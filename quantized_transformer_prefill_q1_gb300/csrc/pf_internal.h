@@ -1,0 +1,89 @@
+// pf_internal.h — definitions shared by libpf's translation units (not installed).
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/pf.h"
+
+// A bounded device-side wait gives up after this long (ns) and reports
+// PF_ERR_DEVICE_TIMEOUT; healthy waits last microseconds.
+#ifndef PF_WAIT_LIMIT_NS
+#define PF_WAIT_LIMIT_NS 1000000000ull
+#endif
+
+namespace pf {
+
+// ------------------------------------------------------------------ packed weight layout
+// Tiles of TILE_N = 256 rows x GROUP = 128 weights ("chunks"), chunk (t, g) at byte
+// offset (t * K/128 + g) * chunk_bytes. Inside a chunk, each half h (k in
+// [128g + 64h, 128g + 64h + 64)) of every row is contiguous so that one GEMM stage
+// (64 k x 256 rows) is one contiguous block, followed by the 256 scales (and zeros).
+//
+// Q1 half-row (8 B): two 32-bit words Z0 (k 0..31 of the half), Z1 (k 32..63). In a
+// word, element pair i (elements 2i, 2i+1) keeps the NEGATIVE flag of element 2i at
+// bit 15-i and of element 2i+1 at bit 31-i, so ((Z << i) & 0x80008000) is directly the
+// f16x2 sign mask of pair i.
+// INT4 half-row (32 B): eight 32-bit words, word w = k 8w..8w+7; pair p of the word
+// (elements 8w+2p, 8w+2p+1) keeps the even code at bits [4p, 4p+4) and the odd code at
+// bits [16+4p, 16+4p+4), so ((word >> 4p) & 0x000F000F) are both codes of pair p.
+constexpr int TILE_N = 256;
+constexpr int GROUP = 128;
+constexpr int Q1_HALF_BYTES = TILE_N * 8;            // 2048
+constexpr int Q1_SCALE_OFF = 2 * Q1_HALF_BYTES;       // 4096
+constexpr int Q1_CHUNK_BYTES = Q1_SCALE_OFF + TILE_N * 2;  // 4608
+constexpr int I4_HALF_BYTES = TILE_N * 32;           // 8192
+constexpr int I4_SCALE_OFF = 2 * I4_HALF_BYTES;       // 16384
+constexpr int I4_ZERO_OFF = I4_SCALE_OFF + TILE_N * 2; // 16896
+constexpr int I4_CHUNK_BYTES = I4_ZERO_OFF + TILE_N * 2;  // 17408
+
+__host__ __device__ inline int64_t padded_rows(int64_t N) { return (N + TILE_N - 1) / TILE_N * TILE_N; }
+__host__ __device__ inline size_t chunk_bytes(int wfmt) {
+  return wfmt == PF_W_Q1_G128 ? Q1_CHUNK_BYTES : I4_CHUNK_BYTES;
+}
+
+enum Epilogue : int { EPI_STORE_F32 = 0, EPI_RESID_ADD = 1, EPI_SWIGLU = 2 };
+
+// ------------------------------------------------------------------ status words
+// int32 [4] in device memory: [0] = first error code recorded by a kernel.
+constexpr int STATUS_WORDS = 4;
+
+// ------------------------------------------------------------------ launchers
+// Each returns cudaGetLastError() after enqueueing on `stream`.
+struct GemmArgs {
+  int wfmt;
+  int epilogue;
+  const void* a;        // f16 [M, K] row-major
+  const uint8_t* w;     // packed
+  int M, N, K;
+  void* out;            // f32 [M, N] or f16 [M, N/2]
+  int split_k;          // >= 1
+  int* status;          // may be NULL
+};
+cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t stream);
+int choose_split_k(int M, int N, int K, int epilogue, int num_sms);
+
+cudaError_t launch_rmsnorm(const float* x, const float* w, float eps, int M, int H, void* y_f16,
+                           cudaStream_t stream);
+cudaError_t launch_dequant(int wfmt, const uint8_t* packed, int64_t N, int64_t K, void* w_f16,
+                           cudaStream_t stream);
+cudaError_t launch_qk_norm_rope_kv(const pf_config& c, const float* qkv, const float* q_norm,
+                                   const float* k_norm, const float* rope, int layer,
+                                   const int* start_dev, int start_host, int M, void* q_out,
+                                   void* k_cache, void* v_cache, cudaStream_t stream);
+cudaError_t launch_attention(const pf_config& c, const void* q, const void* k_cache,
+                             const void* v_cache, int layer, const int* start_dev, int start_host,
+                             int M, void* out_f16, cudaStream_t stream);
+cudaError_t launch_embed(const float* E, const int* tokens, int M, int H, float* x,
+                         cudaStream_t stream);
+cudaError_t launch_lm_head(int wfmt, const float* x_row, const float* norm_w, float eps,
+                           const uint8_t* packed, int vocab, int H, float* logits,
+                           cudaStream_t stream);
+cudaError_t launch_swiglu_f32(const float* gu, int M, int I, void* out_f16, cudaStream_t stream);
+cudaError_t launch_set_int(int* dst, int value, cudaStream_t stream);
+
+int device_sm_count();
+cudaError_t prepare_gemm_kernels();
+cudaError_t prepare_attention_kernels();
+
+}  // namespace pf

@@ -1,0 +1,330 @@
+"""ctypes binding of libpf (include/pf.h): the same entry-point names, argument
+marshalling only. Every step of the path runs in libpf's CUDA kernels; torch is used
+for device memory and streams. If libpf.so is missing, importing the library raises —
+there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Dict, List, Optional, Sequence
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libpf.so")
+
+PF_OK = 0
+STATUS = {
+    0: "PF_OK", 1: "PF_ERR_INVALID_ARG", 2: "PF_ERR_SHAPE", 3: "PF_ERR_EMPTY_CHUNK",
+    4: "PF_ERR_NONSEQUENTIAL_START", 5: "PF_ERR_TOKEN_OUT_OF_VOCAB", 6: "PF_ERR_KV_CAPACITY",
+    7: "PF_ERR_LOGITS", 8: "PF_ERR_UNSUPPORTED", 9: "PF_ERR_CUDA", 10: "PF_ERR_DEVICE_TIMEOUT",
+    11: "PF_ERR_WORKSPACE",
+}
+W_Q1, W_INT4 = 0, 1
+KV_F32, KV_BF16, KV_F16 = 0, 1, 2
+EPI_STORE_F32, EPI_RESID_ADD, EPI_SWIGLU = 0, 1, 2
+_WFMT = {"q1": W_Q1, "int4": W_INT4}
+_KVDT = {"f32": KV_F32, "bf16": KV_BF16, "f16": KV_F16}
+
+
+class PfError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"{STATUS.get(status, status)}: {msg}")
+        self.status = status
+
+
+class pf_config(ctypes.Structure):
+    _fields_ = [("hidden", ctypes.c_int32), ("intermediate", ctypes.c_int32),
+                ("n_q_heads", ctypes.c_int32), ("n_kv_heads", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32), ("n_layers", ctypes.c_int32),
+                ("vocab", ctypes.c_int32), ("rope_theta", ctypes.c_float),
+                ("eps", ctypes.c_float), ("final_eps", ctypes.c_float),
+                ("qk_norm", ctypes.c_int32), ("wfmt", ctypes.c_int32),
+                ("kv_dtype", ctypes.c_int32), ("max_seq", ctypes.c_int32),
+                ("max_chunk", ctypes.c_int32)]
+
+
+class pf_layer_weights(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in
+                ("attn_norm", "qkv", "q_norm", "k_norm", "o_proj", "ffn_norm", "gate_up", "down")]
+
+
+class pf_model(ctypes.Structure):
+    _fields_ = [("cfg", pf_config), ("layers", ctypes.POINTER(pf_layer_weights)),
+                ("embed", ctypes.c_void_p), ("final_norm", ctypes.c_void_p),
+                ("lm_head", ctypes.c_void_p)]
+
+
+_VP, _I32, _I64, _SZ, _F = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t, ctypes.c_float
+_SIGS = {
+    "pf_last_error": ([], ctypes.c_char_p),
+    "pf_status_name": ([ctypes.c_int], ctypes.c_char_p),
+    "pf_abi_version": ([], _I32),
+    "pf_packed_bytes": ([_I32, _I64, _I64], _SZ),
+    "pf_pack_weights_host": ([_I32, _VP, _VP, _VP, _I64, _I64, _I32, _VP, _SZ], _I32),
+    "pf_kv_bytes": ([ctypes.POINTER(pf_config)], _SZ),
+    "pf_workspace_bytes": ([ctypes.POINTER(pf_config)], _SZ),
+    "pf_config_check": ([ctypes.POINTER(pf_config)], _I32),
+    "pf_validate_chunk": ([ctypes.POINTER(pf_config), _I32, _VP, _I32, _I32, _I32, _I32], _I32),
+    "pf_session_create": ([ctypes.POINTER(pf_model), _VP, _VP, _VP, _SZ, _VP,
+                           ctypes.POINTER(_VP)], _I32),
+    "pf_session_destroy": ([_VP], _I32),
+    "pf_session_position": ([_VP], _I32),
+    "pf_session_set_position": ([_VP, _I32], _I32),
+    "pf_session_set_graphs": ([_VP, _I32], _I32),
+    "pf_session_sync": ([_VP, _VP], _I32),
+    "pf_prefill_chunk": ([_VP, _VP, _I32, _I32, _VP, _VP], _I32),
+    "pf_prefill_hidden": ([_VP, _VP, _I32, _I32, _VP, _VP], _I32),
+    "pf_layer_forward": ([_VP, _I32, _VP, _I32, _I32, _VP], _I32),
+    "pf_prefill_tokens_host": ([_VP, _VP, _I32, _I32, _VP, _VP], _I32),
+    "pf_op_rmsnorm": ([_VP, _VP, _F, _I32, _I32, _VP, _VP], _I32),
+    "pf_op_dequant": ([_I32, _VP, _I64, _I64, _VP, _VP], _I32),
+    "pf_op_gemm": ([_I32, _I32, _VP, _VP, _I32, _I32, _I32, _VP, _I32, _VP, _VP], _I32),
+    "pf_op_qk_norm_rope_kv": ([ctypes.POINTER(pf_config), _VP, _VP, _VP, _VP, _I32, _I32, _I32,
+                               _VP, _VP, _VP, _VP], _I32),
+    "pf_op_attention": ([ctypes.POINTER(pf_config), _VP, _VP, _VP, _I32, _I32, _I32, _VP, _VP], _I32),
+    "pf_op_embed": ([_VP, _VP, _I32, _I32, _VP, _VP], _I32),
+    "pf_op_lm_head": ([_I32, _VP, _VP, _F, _VP, _I32, _I32, _VP, _VP], _I32),
+    "pf_rope_table_host": ([_F, _I32, _I32, _VP], _I32),
+    "pf_status_read": ([_VP, _VP], _I32),
+}
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """Loads libpf.so (built by ``build.py``); raises if it is missing."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"libpf.so not built ({LIB_PATH}); run __graft_entry__.build()")
+        l = ctypes.CDLL(LIB_PATH)
+        for name, (args, res) in _SIGS.items():
+            f = getattr(l, name)
+            f.argtypes = args
+            f.restype = res
+        _lib = l
+    return _lib
+
+
+def header_symbols() -> List[str]:
+    return list(_SIGS)
+
+
+def check(status: int) -> None:
+    if status != PF_OK:
+        raise PfError(status, lib().pf_last_error().decode())
+
+
+def _ptr(t) -> Optional[int]:
+    """Device / host address of a torch tensor or numpy array (None passes NULL)."""
+    if t is None:
+        return None
+    if isinstance(t, np.ndarray):
+        assert t.flags["C_CONTIGUOUS"]
+        return t.ctypes.data
+    return t.data_ptr()
+
+
+def _stream(stream=None) -> Optional[int]:
+    if stream is not None:
+        return stream
+    import torch
+    return torch.cuda.current_stream().cuda_stream
+
+
+# ------------------------------------------------------------------ host-side calls
+def make_config(shape, max_chunk: int, n_layers: Optional[int] = None, max_seq: Optional[int] = None,
+                vocab: Optional[int] = None) -> pf_config:
+    return pf_config(hidden=shape.hidden, intermediate=shape.intermediate,
+                     n_q_heads=shape.n_q_heads, n_kv_heads=shape.n_kv_heads,
+                     head_dim=shape.head_dim,
+                     n_layers=shape.n_layers if n_layers is None else n_layers,
+                     vocab=shape.vocab if vocab is None else vocab,
+                     rope_theta=shape.rope_theta, eps=shape.eps, final_eps=shape.final_eps,
+                     qk_norm=int(shape.qk_norm), wfmt=_WFMT[shape.wfmt],
+                     kv_dtype=_KVDT[shape.kv_dtype],
+                     max_seq=shape.max_seq if max_seq is None else max_seq, max_chunk=max_chunk)
+
+
+def pf_packed_bytes(wfmt: int, n: int, k: int) -> int:
+    return lib().pf_packed_bytes(wfmt, n, k)
+
+
+def pf_pack_weights_host(w: Dict, interleave_gate_up: bool = False) -> np.ndarray:
+    """Packs one canonical quantised tensor (see ``synth``) into libpf's device layout."""
+    wfmt = _WFMT[w["fmt"]]
+    n, k = w["n"], w["k"]
+    nbytes = pf_packed_bytes(wfmt, n, k)
+    out = np.empty(nbytes, np.uint8)
+    codes = np.ascontiguousarray(w["bits"] if wfmt == W_Q1 else w["codes"])
+    scales = np.ascontiguousarray(w["scales"]).view(np.uint16)
+    zeros = None if wfmt == W_Q1 else np.ascontiguousarray(w["zeros"]).view(np.uint16)
+    check(lib().pf_pack_weights_host(wfmt, _ptr(codes), _ptr(scales), _ptr(zeros), n, k,
+                                     int(interleave_gate_up), _ptr(out), nbytes))
+    return out
+
+
+def pf_validate_chunk(cfg: pf_config, kv_position: int, tokens: Optional[np.ndarray], m: int,
+                      start: int, want_logits: bool, has_head: bool) -> int:
+    t = None if tokens is None else np.ascontiguousarray(tokens, dtype=np.int32)
+    return lib().pf_validate_chunk(ctypes.byref(cfg), kv_position, _ptr(t), m, start,
+                                   int(want_logits), int(has_head))
+
+
+def pf_rope_table_host(theta: float, head_dim: int, max_seq: int) -> np.ndarray:
+    out = np.empty((max_seq, head_dim // 2, 2), np.float32)
+    check(lib().pf_rope_table_host(theta, head_dim, max_seq, _ptr(out)))
+    return out
+
+
+# ------------------------------------------------------------------ single steps (GPU)
+def pf_op_rmsnorm(x, w, eps, y, stream=None):
+    m, h = x.shape
+    check(lib().pf_op_rmsnorm(_ptr(x), _ptr(w), eps, m, h, _ptr(y), _stream(stream)))
+
+
+def pf_op_dequant(wfmt, packed, n, k, out, stream=None):
+    check(lib().pf_op_dequant(wfmt, _ptr(packed), n, k, _ptr(out), _stream(stream)))
+
+
+def pf_op_gemm(wfmt, epilogue, a, packed, m, n, k, out, split_k=0, status=None, stream=None):
+    check(lib().pf_op_gemm(wfmt, epilogue, _ptr(a), _ptr(packed), m, n, k, _ptr(out), split_k,
+                           _ptr(status), _stream(stream)))
+
+
+def pf_op_qk_norm_rope_kv(cfg, qkv, qn, kn, rope, layer, start, m, q, kc, vc, stream=None):
+    check(lib().pf_op_qk_norm_rope_kv(ctypes.byref(cfg), _ptr(qkv), _ptr(qn), _ptr(kn), _ptr(rope),
+                                      layer, start, m, _ptr(q), _ptr(kc), _ptr(vc), _stream(stream)))
+
+
+def pf_op_attention(cfg, q, kc, vc, layer, start, m, out, stream=None):
+    check(lib().pf_op_attention(ctypes.byref(cfg), _ptr(q), _ptr(kc), _ptr(vc), layer, start, m,
+                                _ptr(out), _stream(stream)))
+
+
+def pf_op_embed(e, tokens, m, h, x, stream=None):
+    check(lib().pf_op_embed(_ptr(e), _ptr(tokens), m, h, _ptr(x), _stream(stream)))
+
+
+def pf_op_lm_head(wfmt, x_row, norm_w, eps, packed, vocab, h, logits, stream=None):
+    check(lib().pf_op_lm_head(wfmt, _ptr(x_row), _ptr(norm_w), eps, _ptr(packed), vocab, h,
+                              _ptr(logits), _stream(stream)))
+
+
+def pf_status_read(status, stream=None):
+    check(lib().pf_status_read(_ptr(status), _stream(stream)))
+
+
+# ------------------------------------------------------------------ model + session
+class DeviceModel:
+    """Uploads a stack's weights (packed once, on the host) into device memory owned by
+    torch tensors and fills a ``pf_model`` pointing at them."""
+
+    def __init__(self, shape, layers: Sequence[Dict], extra: Optional[Dict] = None,
+                 max_chunk: int = 512, device: str = "cuda", max_seq: Optional[int] = None):
+        import torch
+        self.shape = shape
+        self.keep: List = []
+        extra = extra or {}
+
+        def dev(a: np.ndarray):
+            t = torch.from_numpy(np.ascontiguousarray(a)).to(device)
+            self.keep.append(t)
+            return t
+
+        def packed(w, inter=False):
+            return dev(pf_pack_weights_host(w, inter))
+
+        n = len(layers)
+        self.cfg = make_config(shape, max_chunk, n_layers=n, max_seq=max_seq,
+                               vocab=shape.vocab if "lm_head" in extra else 0)
+        self.layer_arr = (pf_layer_weights * n)()
+        for i, w in enumerate(layers):
+            lw = self.layer_arr[i]
+            lw.attn_norm = _ptr(dev(w["attn_norm"]))
+            lw.ffn_norm = _ptr(dev(w["ffn_norm"]))
+            lw.q_norm = _ptr(dev(w["q_norm"])) if w["q_norm"] is not None else None
+            lw.k_norm = _ptr(dev(w["k_norm"])) if w["k_norm"] is not None else None
+            lw.qkv = _ptr(packed(w["qkv"]))
+            lw.o_proj = _ptr(packed(w["o"]))
+            lw.gate_up = _ptr(packed(w["gate_up"], True))
+            lw.down = _ptr(packed(w["down"]))
+        self.model = pf_model(cfg=self.cfg, layers=self.layer_arr)
+        if "embed" in extra:
+            self.model.embed = _ptr(dev(extra["embed"]))
+        if "lm_head" in extra:
+            self.model.final_norm = _ptr(dev(extra["final_norm"]))
+            self.model.lm_head = _ptr(packed(extra["lm_head"]))
+
+
+_KV_TORCH = {KV_F32: "float32", KV_BF16: "bfloat16", KV_F16: "float16"}
+
+
+class Session:
+    """A pf_session with its KV cache and workspace allocated by torch (caller-owned)."""
+
+    def __init__(self, dm: DeviceModel, stream=None, kv_fill_bits: Optional[int] = None,
+                 graphs: bool = True):
+        import torch
+        self.dm = dm
+        c = dm.cfg
+        dt = getattr(torch, _KV_TORCH[c.kv_dtype])
+        shape = (c.n_layers, c.n_kv_heads, c.max_seq, c.head_dim)
+        self.k = torch.empty(shape, dtype=dt, device="cuda")
+        self.v = torch.empty(shape, dtype=dt, device="cuda")
+        if kv_fill_bits is not None:  # sentinel bit pattern in every slot
+            ib = torch.int32 if c.kv_dtype == KV_F32 else torch.int16
+            self.k.view(ib).fill_(kv_fill_bits)
+            self.v.view(ib).fill_(kv_fill_bits)
+        wsb = lib().pf_workspace_bytes(ctypes.byref(c))
+        if wsb == 0:
+            raise PfError(2, lib().pf_last_error().decode())
+        self.ws = torch.empty(wsb, dtype=torch.uint8, device="cuda")
+        h = ctypes.c_void_p()
+        check(lib().pf_session_create(ctypes.byref(dm.model), _ptr(self.k), _ptr(self.v),
+                                      _ptr(self.ws), wsb, _stream(stream), ctypes.byref(h)))
+        self.h = h
+        check(lib().pf_session_set_graphs(self.h, int(graphs)))
+
+    @property
+    def position(self) -> int:
+        return lib().pf_session_position(self.h)
+
+    def set_position(self, p: int) -> None:
+        check(lib().pf_session_set_position(self.h, p))
+
+    def set_graphs(self, on: bool) -> None:
+        check(lib().pf_session_set_graphs(self.h, int(on)))
+
+    def prefill_chunk(self, tokens: np.ndarray, start: int, logits=None, stream=None) -> None:
+        t = np.ascontiguousarray(tokens, dtype=np.int32)
+        check(lib().pf_prefill_chunk(self.h, _ptr(t), len(t), start, _ptr(logits), _stream(stream)))
+
+    def prefill_hidden(self, x, start: int, logits=None, stream=None) -> None:
+        check(lib().pf_prefill_hidden(self.h, _ptr(x), x.shape[0], start, _ptr(logits),
+                                      _stream(stream)))
+
+    def layer_forward(self, layer: int, x, start: int, stream=None) -> None:
+        check(lib().pf_layer_forward(self.h, layer, _ptr(x), x.shape[0], start, _stream(stream)))
+
+    def prefill_tokens_host(self, tokens: np.ndarray, start: int, logits_host: Optional[np.ndarray],
+                            stream=None) -> None:
+        t = np.ascontiguousarray(tokens, dtype=np.int32)
+        check(lib().pf_prefill_tokens_host(self.h, _ptr(t), len(t), start, _ptr(logits_host),
+                                           _stream(stream)))
+
+    def sync(self, stream=None) -> None:
+        check(lib().pf_session_sync(self.h, _stream(stream)))
+
+    def close(self) -> None:
+        if getattr(self, "h", None):
+            lib().pf_session_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
