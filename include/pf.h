@@ -167,6 +167,24 @@ pf_status pf_session_set_graphs(pf_session* s, int32_t enable);
 /* Synchronises the stream, then reads and clears the session's device status word. */
 pf_status pf_session_sync(pf_session* s, void* stream);
 
+/* Per-kernel timing, the CUDA analogue of the pages' per-layer / per-phase profiling
+ * ([P2] OXIBONSAI_PROFILE, [P3] phase counters). While enabled, chunks run without graph
+ * replay and every kernel launch is bracketed by CUDA events on its stream;
+ * pf_session_profile_read synchronises the stream and returns, per kernel class, the
+ * summed device milliseconds and the launch count since the previous read (arrays of
+ * PF_K_COUNT entries), then clears them. */
+typedef enum {
+  PF_K_RMSNORM = 0, PF_K_GEMM_QKV = 1, PF_K_QK_ROPE_KV = 2, PF_K_ATTENTION = 3,
+  PF_K_GEMM_O = 4, PF_K_GEMM_GATE_UP = 5, PF_K_GEMM_DOWN = 6, PF_K_EMBED = 7,
+  PF_K_LM_HEAD = 8, PF_K_OTHER = 9, PF_K_COUNT = 10
+} pf_kernel_class;
+pf_status pf_session_set_profile(pf_session* s, int32_t enable);
+pf_status pf_session_profile_read(pf_session* s, void* stream, double* ms_out,
+                                  int64_t* launches_out);
+/* Number of libpf kernels enqueued by this session so far (graph replays count every
+ * kernel node they run). */
+int64_t pf_session_kernel_launches(const pf_session* s);
+
 /* ------------------------------------------------------------------ the path
  * pf_prefill_chunk — [P3] prefill_chunk(tokens, start_position, logits): embeds M
  * token ids (HOST array, checked against vocab on the host before any launch), runs
@@ -190,6 +208,14 @@ pf_status pf_prefill_hidden(pf_session* s, float* x_dev, int32_t M, int32_t star
  * session's KV position (the caller sequences layers); M <= max_chunk. */
 pf_status pf_layer_forward(pf_session* s, int32_t layer, float* x_dev, int32_t M,
                            int32_t start_pos, void* stream);
+
+/* Same as pf_prefill_chunk with the token ids already in device memory (int32 [M]).
+ * Every host-side check runs except the vocabulary check, which the embedding kernel
+ * performs instead: an id outside [0, vocab) gets a zero row and records
+ * PF_ERR_TOKEN_OUT_OF_VOCAB in the session status word (read by pf_session_sync); the
+ * KV position still advances by M in that case. */
+pf_status pf_prefill_chunk_dev(pf_session* s, const int32_t* tokens_dev, int32_t M,
+                               int32_t start_pos, float* logits_dev, void* stream);
 
 /* End to end from host memory: copies tokens_host to the device, runs
  * pf_prefill_chunk, copies the last position's logits into logits_host [vocab]
@@ -235,10 +261,12 @@ pf_status pf_op_qk_norm_rope_kv(const pf_config* cfg, const float* qkv_dev,
 pf_status pf_op_attention(const pf_config* cfg, const void* q_dev, const void* k_cache_dev,
                           const void* v_cache_dev, int32_t layer, int32_t start_pos,
                           int32_t M, uint16_t* out_f16_dev, void* stream);
-/* Embedding rows ([P3] encode_embed_any, scale 1.0): x[t] = E[tokens[t]] (device ids,
- * assumed in range). */
+/* Embedding rows ([P3] encode_embed_any, scale 1.0): x[t] = E[tokens[t]] (device ids).
+ * An id outside [0, vocab) yields a zero row and PF_ERR_TOKEN_OUT_OF_VOCAB in
+ * *status_dev (if not NULL). */
 pf_status pf_op_embed(const float* embed_dev, const int32_t* tokens_dev, int32_t M,
-                      int32_t H, float* x_dev, void* stream);
+                      int32_t H, int32_t vocab, float* x_dev, int32_t* status_dev,
+                      void* stream);
 /* Tail ([P1] rmsnorm_weighted_v2 + dispatch_gemv_q1): logits[v] = W_lm . rmsnorm(x_row)
  * for one f32 row x_row_dev [H]; logits f32 [vocab]. */
 pf_status pf_op_lm_head(int32_t wfmt, const float* x_row_dev, const float* norm_w_dev,

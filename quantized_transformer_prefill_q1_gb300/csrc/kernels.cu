@@ -151,12 +151,20 @@ __global__ void __launch_bounds__(256) qk_norm_rope_kv_kernel(
 
 // ------------------------------------------------------------------ embedding
 // turbospark-runtime prefill.rs (`encode_embed_any` per token, scale 1.0): x[t] = E[id].
+// An id outside [0, vocab) gets a zero row and records PF_ERR_TOKEN_OUT_OF_VOCAB.
 __global__ void __launch_bounds__(256) embed_kernel(const float* __restrict__ E,
                                                     const int* __restrict__ tokens, int H,
-                                                    float* __restrict__ x) {
+                                                    int vocab, float* __restrict__ x,
+                                                    int* __restrict__ status) {
   const int t = blockIdx.x;
-  const float4* src = reinterpret_cast<const float4*>(E + static_cast<size_t>(tokens[t]) * H);
+  const int id = tokens[t];
   float4* dst = reinterpret_cast<float4*>(x + static_cast<size_t>(t) * H);
+  if (id < 0 || id >= vocab) {
+    for (int i = threadIdx.x; i < (H >> 2); i += blockDim.x) dst[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (threadIdx.x == 0 && status) atomicCAS(status, 0, PF_ERR_TOKEN_OUT_OF_VOCAB);
+    return;
+  }
+  const float4* src = reinterpret_cast<const float4*>(E + static_cast<size_t>(id) * H);
   for (int i = threadIdx.x; i < (H >> 2); i += blockDim.x) dst[i] = src[i];
 }
 
@@ -358,9 +366,9 @@ cudaError_t launch_qk_norm_rope_kv(const pf_config& c, const float* qkv, const f
   return cudaGetLastError();
 }
 
-cudaError_t launch_embed(const float* E, const int* tokens, int M, int H, float* x,
-                         cudaStream_t stream) {
-  embed_kernel<<<M, 256, 0, stream>>>(E, tokens, H, x);
+cudaError_t launch_embed(const float* E, const int* tokens, int M, int H, int vocab, float* x,
+                         int* status, cudaStream_t stream) {
+  embed_kernel<<<M, 256, 0, stream>>>(E, tokens, H, vocab, x, status);
   return cudaGetLastError();
 }
 

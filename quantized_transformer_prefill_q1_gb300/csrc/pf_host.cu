@@ -128,13 +128,22 @@ using namespace pf;
 struct GraphKey {
   int M;
   const void* x;
+  const void* tokens;
   const void* logits;
-  int from_tokens;
   int layer;  // -1: whole stack
   bool operator<(const GraphKey& o) const {
-    return std::tie(M, x, logits, from_tokens, layer) <
-           std::tie(o.M, o.x, o.logits, o.from_tokens, o.layer);
+    return std::tie(M, x, tokens, logits, layer) < std::tie(o.M, o.x, o.tokens, o.logits, o.layer);
   }
+};
+
+struct GraphExec {
+  cudaGraphExec_t exec;
+  int64_t kernels;  // libpf kernels recorded in it
+};
+
+struct ProfRecord {
+  int cls;
+  cudaEvent_t e0, e1;
 };
 
 struct pf_session {
@@ -147,8 +156,12 @@ struct pf_session {
   WsLayout L{};
   int position = 0;
   bool graphs = true;
+  bool profile = false;
   int sms = 148;
-  std::map<GraphKey, cudaGraphExec_t> execs;
+  int64_t launches = 0;
+  std::map<GraphKey, GraphExec> execs;
+  std::vector<ProfRecord> prof;
+  std::vector<cudaEvent_t> event_pool;
 };
 
 namespace {
@@ -183,8 +196,44 @@ pf_status check_cfg(const pf_config* c) {
   return PF_OK;
 }
 
-pf_status enqueue_gemm(pf_session* s, int wfmt, int epi, const void* a, const void* w, int M, int N,
-                       int K, void* out, cudaStream_t st) {
+cudaEvent_t take_event(pf_session* s) {
+  if (!s->event_pool.empty()) {
+    cudaEvent_t e = s->event_pool.back();
+    s->event_pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  cudaEventCreate(&e);
+  return e;
+}
+
+// Enqueues one libpf kernel through `call`, counting it and, in profile mode, bracketing
+// it with CUDA events on its stream.
+template <typename Call>
+pf_status launch_k(pf_session* s, int cls, cudaStream_t st, const char* what, Call call) {
+  cudaEvent_t e0 = nullptr;
+  if (s->profile) {
+    e0 = take_event(s);
+    PF_CUDA(cudaEventRecord(e0, st), "event record");
+  }
+  PF_CUDA(call(), what);
+  if (s->profile) {
+    cudaEvent_t e1 = take_event(s);
+    PF_CUDA(cudaEventRecord(e1, st), "event record");
+    s->prof.push_back({cls, e0, e1});
+  }
+  ++s->launches;
+  return PF_OK;
+}
+
+#define PF_TRY(expr)                \
+  do {                              \
+    pf_status r_ = (expr);          \
+    if (r_ != PF_OK) return r_;     \
+  } while (0)
+
+pf_status enqueue_gemm(pf_session* s, int cls, int wfmt, int epi, const void* a, const void* w,
+                       int M, int N, int K, void* out, cudaStream_t st) {
   GemmArgs g{};
   g.wfmt = wfmt;
   g.epilogue = epi;
@@ -198,8 +247,7 @@ pf_status enqueue_gemm(pf_session* s, int wfmt, int epi, const void* a, const vo
   g.status = wsp<int>(s, s->L.status);
   if (epi == EPI_STORE_F32 && g.split_k > 1)
     PF_CUDA(cudaMemsetAsync(out, 0, static_cast<size_t>(M) * N * 4, st), "memset gemm output");
-  PF_CUDA(launch_gemm(g, st), "gemm launch");
-  return PF_OK;
+  return launch_k(s, cls, st, "gemm launch", [&] { return launch_gemm(g, st); });
 }
 
 // metal_prefill.rs encode_layer_prefill, sections 1-7, on x [M, H] (in place).
@@ -214,63 +262,72 @@ pf_status enqueue_layer(pf_session* s, int l, float* x, int M, cudaStream_t st) 
   void* q = wsp<void>(s, s->L.q);
   void* attn = wsp<void>(s, s->L.attn);
   void* act = wsp<void>(s, s->L.act);
-  pf_status r;
   // 1. pre-attention RMSNorm
-  PF_CUDA(launch_rmsnorm(x, w.attn_norm, c.eps, M, H, y, st), "rmsnorm");
+  PF_TRY(launch_k(s, PF_K_RMSNORM, st, "rmsnorm",
+                  [&] { return launch_rmsnorm(x, w.attn_norm, c.eps, M, H, y, st); }));
   // 2. fused QKV projection
-  if ((r = enqueue_gemm(s, c.wfmt, EPI_STORE_F32, y, w.qkv, M, qkv_rows, H, qkv, st)) != PF_OK) return r;
+  PF_TRY(enqueue_gemm(s, PF_K_GEMM_QKV, c.wfmt, EPI_STORE_F32, y, w.qkv, M, qkv_rows, H, qkv, st));
   // 3. QK-norm + RoPE + KV store, then causal GQA attention over cache + chunk
-  PF_CUDA(launch_qk_norm_rope_kv(c, qkv, w.q_norm, w.k_norm, wsp<float>(s, s->L.rope), l, start_dev,
-                                 0, M, q, s->k, s->v, st),
-          "qk_norm_rope_kv");
-  PF_CUDA(launch_attention(c, q, s->k, s->v, l, start_dev, 0, M, attn, st), "attention");
+  PF_TRY(launch_k(s, PF_K_QK_ROPE_KV, st, "qk_norm_rope_kv", [&] {
+    return launch_qk_norm_rope_kv(c, qkv, w.q_norm, w.k_norm, wsp<float>(s, s->L.rope), l,
+                                  start_dev, 0, M, q, s->k, s->v, st);
+  }));
+  PF_TRY(launch_k(s, PF_K_ATTENTION, st, "attention", [&] {
+    return launch_attention(c, q, s->k, s->v, l, start_dev, 0, M, attn, st);
+  }));
   // 4. O projection + residual
-  if ((r = enqueue_gemm(s, c.wfmt, EPI_RESID_ADD, attn, w.o_proj, M, H, c.n_q_heads * hd, x, st)) != PF_OK)
-    return r;
+  PF_TRY(enqueue_gemm(s, PF_K_GEMM_O, c.wfmt, EPI_RESID_ADD, attn, w.o_proj, M, H,
+                      c.n_q_heads * hd, x, st));
   // 5. FFN RMSNorm
-  PF_CUDA(launch_rmsnorm(x, w.ffn_norm, c.eps, M, H, y, st), "rmsnorm");
+  PF_TRY(launch_k(s, PF_K_RMSNORM, st, "rmsnorm",
+                  [&] { return launch_rmsnorm(x, w.ffn_norm, c.eps, M, H, y, st); }));
   // 6. gate_up + SwiGLU (split along K through an f32 scratch when that fills the GPU better)
   const int split_gu = choose_split_k(M, 2 * I, H, EPI_STORE_F32, s->sms);
   if (split_gu > 1) {
     float* gu = wsp<float>(s, s->L.gu);
-    if ((r = enqueue_gemm(s, c.wfmt, EPI_STORE_F32, y, w.gate_up, M, 2 * I, H, gu, st)) != PF_OK) return r;
-    PF_CUDA(launch_swiglu_f32(gu, M, I, act, st), "swiglu");
+    PF_TRY(enqueue_gemm(s, PF_K_GEMM_GATE_UP, c.wfmt, EPI_STORE_F32, y, w.gate_up, M, 2 * I, H, gu, st));
+    PF_TRY(launch_k(s, PF_K_OTHER, st, "swiglu", [&] { return launch_swiglu_f32(gu, M, I, act, st); }));
   } else {
-    if ((r = enqueue_gemm(s, c.wfmt, EPI_SWIGLU, y, w.gate_up, M, 2 * I, H, act, st)) != PF_OK) return r;
+    PF_TRY(enqueue_gemm(s, PF_K_GEMM_GATE_UP, c.wfmt, EPI_SWIGLU, y, w.gate_up, M, 2 * I, H, act, st));
   }
   // 7. down projection + residual
-  if ((r = enqueue_gemm(s, c.wfmt, EPI_RESID_ADD, act, w.down, M, H, I, x, st)) != PF_OK) return r;
+  PF_TRY(enqueue_gemm(s, PF_K_GEMM_DOWN, c.wfmt, EPI_RESID_ADD, act, w.down, M, H, I, x, st));
   return PF_OK;
 }
 
 // One micro-batch: [embed] -> every layer -> [final norm + LM head on the last row].
-pf_status enqueue_chunk(pf_session* s, float* x, int M, bool from_tokens, float* logits,
+pf_status enqueue_chunk(pf_session* s, float* x, int M, const int* tokens_dev, float* logits,
                         cudaStream_t st) {
   const pf_config& c = s->model.cfg;
-  if (from_tokens)
-    PF_CUDA(launch_embed(s->model.embed, wsp<int>(s, s->L.tokens), M, c.hidden, x, st), "embed");
-  for (int l = 0; l < c.n_layers; ++l) {
-    pf_status r = enqueue_layer(s, l, x, M, st);
-    if (r != PF_OK) return r;
-  }
+  if (tokens_dev)
+    PF_TRY(launch_k(s, PF_K_EMBED, st, "embed", [&] {
+      return launch_embed(s->model.embed, tokens_dev, M, c.hidden, c.vocab, x,
+                          wsp<int>(s, s->L.status), st);
+    }));
+  for (int l = 0; l < c.n_layers; ++l) PF_TRY(enqueue_layer(s, l, x, M, st));
   if (logits)
-    PF_CUDA(launch_lm_head(c.wfmt, x + static_cast<size_t>(M - 1) * c.hidden, s->model.final_norm,
-                           c.final_eps, reinterpret_cast<const uint8_t*>(s->model.lm_head), c.vocab,
-                           c.hidden, logits, st),
-            "lm_head");
+    PF_TRY(launch_k(s, PF_K_LM_HEAD, st, "lm_head", [&] {
+      return launch_lm_head(c.wfmt, x + static_cast<size_t>(M - 1) * c.hidden, s->model.final_norm,
+                            c.final_eps, reinterpret_cast<const uint8_t*>(s->model.lm_head), c.vocab,
+                            c.hidden, logits, st);
+    }));
   return PF_OK;
 }
 
-// Runs `body` directly, or as a CUDA graph recorded on first use for `key`.
+// Runs `body` directly, or as a CUDA graph recorded on first use for `key` (never while
+// profiling: the per-launch events need the launches themselves).
 template <typename Body>
 pf_status run_maybe_graph(pf_session* s, const GraphKey& key, cudaStream_t st, Body body) {
-  if (!s->graphs) return body();
+  if (!s->graphs || s->profile) return body();
   auto it = s->execs.find(key);
   if (it == s->execs.end()) {
+    const int64_t before = s->launches;
     PF_CUDA(cudaStreamBeginCapture(st, cudaStreamCaptureModeThreadLocal), "begin capture");
     pf_status r = body();
     cudaGraph_t graph = nullptr;
     cudaError_t e = cudaStreamEndCapture(st, &graph);
+    const int64_t recorded = s->launches - before;
+    s->launches = before;  // counted when the graph runs
     if (r != PF_OK) {
       if (graph) cudaGraphDestroy(graph);
       return r;
@@ -281,18 +338,19 @@ pf_status run_maybe_graph(pf_session* s, const GraphKey& key, cudaStream_t st, B
     cudaGraphDestroy(graph);
     if (e != cudaSuccess) return cuda_fail(e, "graph instantiate");
     if (s->execs.size() >= 64) {
-      cudaGraphExecDestroy(s->execs.begin()->second);
+      cudaGraphExecDestroy(s->execs.begin()->second.exec);
       s->execs.erase(s->execs.begin());
     }
-    it = s->execs.emplace(key, exec).first;
+    it = s->execs.emplace(key, GraphExec{exec, recorded}).first;
   }
-  PF_CUDA(cudaGraphLaunch(it->second, st), "graph launch");
+  PF_CUDA(cudaGraphLaunch(it->second.exec, st), "graph launch");
+  s->launches += it->second.kernels;
   return PF_OK;
 }
 
 pf_status set_start(pf_session* s, int start, cudaStream_t st) {
-  PF_CUDA(launch_set_int(wsp<int>(s, s->L.params), start, st), "set start");
-  return PF_OK;
+  return launch_k(s, PF_K_OTHER, st, "set start",
+                  [&] { return launch_set_int(wsp<int>(s, s->L.params), start, st); });
 }
 
 // Raises the dynamic shared-memory limit of the big kernels once, outside any capture.
@@ -516,7 +574,12 @@ pf_status pf_session_create(const pf_model* model, void* k, void* v, void* ws, s
 
 pf_status pf_session_destroy(pf_session* s) {
   if (!s) return fail(PF_ERR_INVALID_ARG, "session is NULL");
-  for (auto& kv : s->execs) cudaGraphExecDestroy(kv.second);
+  for (auto& kv : s->execs) cudaGraphExecDestroy(kv.second.exec);
+  for (auto& r : s->prof) {
+    cudaEventDestroy(r.e0);
+    cudaEventDestroy(r.e1);
+  }
+  for (auto e : s->event_pool) cudaEventDestroy(e);
   delete s;
   return PF_OK;
 }
@@ -537,6 +600,33 @@ pf_status pf_session_set_graphs(pf_session* s, int32_t enable) {
   return PF_OK;
 }
 
+pf_status pf_session_set_profile(pf_session* s, int32_t enable) {
+  if (!s) return fail(PF_ERR_INVALID_ARG, "session is NULL");
+  s->profile = enable != 0;
+  return PF_OK;
+}
+
+pf_status pf_session_profile_read(pf_session* s, void* stream, double* ms_out, int64_t* launches_out) {
+  if (!s || !ms_out || !launches_out) return fail(PF_ERR_INVALID_ARG, "NULL pointer");
+  PF_CUDA(cudaStreamSynchronize(static_cast<cudaStream_t>(stream)), "stream sync");
+  for (int i = 0; i < PF_K_COUNT; ++i) {
+    ms_out[i] = 0.0;
+    launches_out[i] = 0;
+  }
+  for (auto& r : s->prof) {
+    float ms = 0.f;
+    PF_CUDA(cudaEventElapsedTime(&ms, r.e0, r.e1), "event elapsed");
+    ms_out[r.cls] += ms;
+    launches_out[r.cls] += 1;
+    s->event_pool.push_back(r.e0);
+    s->event_pool.push_back(r.e1);
+  }
+  s->prof.clear();
+  return PF_OK;
+}
+
+int64_t pf_session_kernel_launches(const pf_session* s) { return s ? s->launches : -1; }
+
 pf_status pf_session_sync(pf_session* s, void* stream) {
   if (!s) return fail(PF_ERR_INVALID_ARG, "session is NULL");
   return pf_status_read(wsp<int>(s, s->L.status), stream);
@@ -555,14 +645,17 @@ pf_status pf_status_read(int32_t* status_dev, void* stream) {
   return PF_OK;
 }
 
-static pf_status prefill_common(pf_session* s, const int32_t* tokens, float* x, int32_t M,
-                                int32_t start, float* logits, void* stream) {
+// tokens: host ids (checked here, copied per micro-batch) or, with tokens_on_device, device
+// ids (checked by the embedding kernel); x: hidden rows when tokens is NULL.
+static pf_status prefill_common(pf_session* s, const int32_t* tokens, bool tokens_on_device,
+                                float* x, int32_t M, int32_t start, float* logits, void* stream) {
   if (!s) return fail(PF_ERR_INVALID_ARG, "session is NULL");
   const pf_config& c = s->model.cfg;
   if (M > 0 && tokens == nullptr && x == nullptr) return fail(PF_ERR_INVALID_ARG, "input is NULL");
   if (tokens && (!s->model.embed || c.vocab <= 0)) return fail(PF_ERR_INVALID_ARG, "model has no embedding table");
   const int has_head = s->model.lm_head && s->model.final_norm && c.vocab > 0;
-  pf_status v = pf_validate_chunk(&c, s->position, tokens, M, start, logits != nullptr, has_head);
+  pf_status v = pf_validate_chunk(&c, s->position, tokens_on_device ? nullptr : tokens, M, start,
+                                  logits != nullptr, has_head);
   if (v != PF_OK) return v;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   int off = 0;
@@ -570,21 +663,25 @@ static pf_status prefill_common(pf_session* s, const int32_t* tokens, float* x, 
     const int m = std::min(M - off, c.max_chunk);
     const bool last = off + m == M;
     float* xc;
+    const int* tok_dev = nullptr;
     if (tokens) {
       xc = wsp<float>(s, s->L.x);
-      PF_CUDA(cudaMemcpyAsync(wsp<int>(s, s->L.tokens), tokens + off, static_cast<size_t>(m) * 4,
-                              cudaMemcpyHostToDevice, st),
-              "tokens upload");
+      if (tokens_on_device) {
+        tok_dev = tokens + off;
+      } else {
+        tok_dev = wsp<int>(s, s->L.tokens);
+        PF_CUDA(cudaMemcpyAsync(wsp<int>(s, s->L.tokens), tokens + off, static_cast<size_t>(m) * 4,
+                                cudaMemcpyHostToDevice, st),
+                "tokens upload");
+      }
     } else {
       xc = x + static_cast<size_t>(off) * c.hidden;
     }
-    pf_status r = set_start(s, start + off, st);
-    if (r != PF_OK) return r;
+    PF_TRY(set_start(s, start + off, st));
     float* lg = last ? logits : nullptr;
-    GraphKey key{m, xc, lg, tokens != nullptr, -1};
-    r = run_maybe_graph(s, key, st, [&] { return enqueue_chunk(s, xc, m, tokens != nullptr, lg, st); });
-    if (r != PF_OK) return r;
-    s->position = start + off + m;  // turbospark prefill.rs kv.advance_by(m)
+    GraphKey key{m, xc, tok_dev, lg, -1};
+    PF_TRY(run_maybe_graph(s, key, st, [&] { return enqueue_chunk(s, xc, m, tok_dev, lg, st); }));
+    s->position = start + off + m;  // turbospark prefill.rs: kv.advance_by(m)
     off += m;
   }
   return PF_OK;
@@ -593,13 +690,19 @@ static pf_status prefill_common(pf_session* s, const int32_t* tokens, float* x, 
 pf_status pf_prefill_chunk(pf_session* s, const int32_t* tokens_host, int32_t M, int32_t start_pos,
                            float* logits_dev, void* stream) {
   if (s && M > 0 && !tokens_host) return fail(PF_ERR_INVALID_ARG, "tokens is NULL");
-  return prefill_common(s, tokens_host, nullptr, M, start_pos, logits_dev, stream);
+  return prefill_common(s, tokens_host, false, nullptr, M, start_pos, logits_dev, stream);
+}
+
+pf_status pf_prefill_chunk_dev(pf_session* s, const int32_t* tokens_dev, int32_t M, int32_t start_pos,
+                               float* logits_dev, void* stream) {
+  if (s && M > 0 && !tokens_dev) return fail(PF_ERR_INVALID_ARG, "tokens is NULL");
+  return prefill_common(s, tokens_dev, true, nullptr, M, start_pos, logits_dev, stream);
 }
 
 pf_status pf_prefill_hidden(pf_session* s, float* x_dev, int32_t M, int32_t start_pos,
                             float* logits_dev, void* stream) {
   if (s && M > 0 && !x_dev) return fail(PF_ERR_INVALID_ARG, "x is NULL");
-  return prefill_common(s, nullptr, x_dev, M, start_pos, logits_dev, stream);
+  return prefill_common(s, nullptr, false, x_dev, M, start_pos, logits_dev, stream);
 }
 
 pf_status pf_layer_forward(pf_session* s, int32_t layer, float* x_dev, int32_t M, int32_t start_pos,
@@ -615,7 +718,7 @@ pf_status pf_layer_forward(pf_session* s, int32_t layer, float* x_dev, int32_t M
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   pf_status r = set_start(s, start_pos, st);
   if (r != PF_OK) return r;
-  GraphKey key{M, x_dev, nullptr, 0, layer};
+  GraphKey key{M, x_dev, nullptr, nullptr, layer};
   return run_maybe_graph(s, key, st, [&] { return enqueue_layer(s, layer, x_dev, M, st); });
 }
 
@@ -717,11 +820,11 @@ pf_status pf_op_attention(const pf_config* cfg, const void* q, const void* kc, c
   return PF_OK;
 }
 
-pf_status pf_op_embed(const float* E, const int32_t* tokens, int32_t M, int32_t H, float* x,
-                      void* stream) {
+pf_status pf_op_embed(const float* E, const int32_t* tokens, int32_t M, int32_t H, int32_t vocab,
+                      float* x, int32_t* status, void* stream) {
   if (!E || !tokens || !x) return fail(PF_ERR_INVALID_ARG, "NULL pointer");
-  if (M <= 0 || H <= 0 || H % 4) return fail(PF_ERR_SHAPE, "M %d H %d", M, H);
-  PF_CUDA(launch_embed(E, tokens, M, H, x, static_cast<cudaStream_t>(stream)), "embed");
+  if (M <= 0 || H <= 0 || H % 4 || vocab <= 0) return fail(PF_ERR_SHAPE, "M %d H %d vocab %d", M, H, vocab);
+  PF_CUDA(launch_embed(E, tokens, M, H, vocab, x, status, static_cast<cudaStream_t>(stream)), "embed");
   return PF_OK;
 }
 

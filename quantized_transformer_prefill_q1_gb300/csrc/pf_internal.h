@@ -74,8 +74,8 @@ cudaError_t launch_qk_norm_rope_kv(const pf_config& c, const float* qkv, const f
 cudaError_t launch_attention(const pf_config& c, const void* q, const void* k_cache,
                              const void* v_cache, int layer, const int* start_dev, int start_host,
                              int M, void* out_f16, cudaStream_t stream);
-cudaError_t launch_embed(const float* E, const int* tokens, int M, int H, float* x,
-                         cudaStream_t stream);
+cudaError_t launch_embed(const float* E, const int* tokens, int M, int H, int vocab, float* x,
+                         int* status, cudaStream_t stream);
 cudaError_t launch_lm_head(int wfmt, const float* x_row, const float* norm_w, float eps,
                            const uint8_t* packed, int vocab, int H, float* logits,
                            cudaStream_t stream);

@@ -24,6 +24,8 @@ STATUS = {
 W_Q1, W_INT4 = 0, 1
 KV_F32, KV_BF16, KV_F16 = 0, 1, 2
 EPI_STORE_F32, EPI_RESID_ADD, EPI_SWIGLU = 0, 1, 2
+KERNEL_CLASSES = ("rmsnorm", "gemm_qkv", "qk_rope_kv", "attention", "gemm_o", "gemm_gate_up",
+                  "gemm_down", "embed", "lm_head", "other")
 _WFMT = {"q1": W_Q1, "int4": W_INT4}
 _KVDT = {"f32": KV_F32, "bf16": KV_BF16, "f16": KV_F16}
 
@@ -75,6 +77,11 @@ _SIGS = {
     "pf_session_set_graphs": ([_VP, _I32], _I32),
     "pf_session_sync": ([_VP, _VP], _I32),
     "pf_prefill_chunk": ([_VP, _VP, _I32, _I32, _VP, _VP], _I32),
+    "pf_prefill_chunk_dev": ([_VP, _VP, _I32, _I32, _VP, _VP], _I32),
+    "pf_session_set_profile": ([_VP, _I32], _I32),
+    "pf_session_profile_read": ([_VP, _VP, ctypes.POINTER(ctypes.c_double),
+                                 ctypes.POINTER(ctypes.c_int64)], _I32),
+    "pf_session_kernel_launches": ([_VP], ctypes.c_int64),
     "pf_prefill_hidden": ([_VP, _VP, _I32, _I32, _VP, _VP], _I32),
     "pf_layer_forward": ([_VP, _I32, _VP, _I32, _I32, _VP], _I32),
     "pf_prefill_tokens_host": ([_VP, _VP, _I32, _I32, _VP, _VP], _I32),
@@ -84,7 +91,7 @@ _SIGS = {
     "pf_op_qk_norm_rope_kv": ([ctypes.POINTER(pf_config), _VP, _VP, _VP, _VP, _I32, _I32, _I32,
                                _VP, _VP, _VP, _VP], _I32),
     "pf_op_attention": ([ctypes.POINTER(pf_config), _VP, _VP, _VP, _I32, _I32, _I32, _VP, _VP], _I32),
-    "pf_op_embed": ([_VP, _VP, _I32, _I32, _VP, _VP], _I32),
+    "pf_op_embed": ([_VP, _VP, _I32, _I32, _I32, _VP, _VP, _VP], _I32),
     "pf_op_lm_head": ([_I32, _VP, _VP, _F, _VP, _I32, _I32, _VP, _VP], _I32),
     "pf_rope_table_host": ([_F, _I32, _I32, _VP], _I32),
     "pf_status_read": ([_VP, _VP], _I32),
@@ -204,8 +211,9 @@ def pf_op_attention(cfg, q, kc, vc, layer, start, m, out, stream=None):
                                 _ptr(out), _stream(stream)))
 
 
-def pf_op_embed(e, tokens, m, h, x, stream=None):
-    check(lib().pf_op_embed(_ptr(e), _ptr(tokens), m, h, _ptr(x), _stream(stream)))
+def pf_op_embed(e, tokens, m, h, vocab, x, status=None, stream=None):
+    check(lib().pf_op_embed(_ptr(e), _ptr(tokens), m, h, vocab, _ptr(x), _ptr(status),
+                            _stream(stream)))
 
 
 def pf_op_lm_head(wfmt, x_row, norm_w, eps, packed, vocab, h, logits, stream=None):
@@ -301,6 +309,24 @@ class Session:
     def prefill_chunk(self, tokens: np.ndarray, start: int, logits=None, stream=None) -> None:
         t = np.ascontiguousarray(tokens, dtype=np.int32)
         check(lib().pf_prefill_chunk(self.h, _ptr(t), len(t), start, _ptr(logits), _stream(stream)))
+
+    def prefill_chunk_dev(self, tokens_dev, start: int, logits=None, stream=None) -> None:
+        check(lib().pf_prefill_chunk_dev(self.h, _ptr(tokens_dev), tokens_dev.shape[0], start,
+                                         _ptr(logits), _stream(stream)))
+
+    def set_profile(self, on: bool) -> None:
+        check(lib().pf_session_set_profile(self.h, int(on)))
+
+    def profile_read(self, stream=None) -> Dict[str, tuple]:
+        """{kernel class: (summed ms, launches)} since the previous read."""
+        ms = (ctypes.c_double * len(KERNEL_CLASSES))()
+        n = (ctypes.c_int64 * len(KERNEL_CLASSES))()
+        check(lib().pf_session_profile_read(self.h, _stream(stream), ms, n))
+        return {name: (ms[i], n[i]) for i, name in enumerate(KERNEL_CLASSES)}
+
+    @property
+    def kernel_launches(self) -> int:
+        return lib().pf_session_kernel_launches(self.h)
 
     def prefill_hidden(self, x, start: int, logits=None, stream=None) -> None:
         check(lib().pf_prefill_hidden(self.h, _ptr(x), x.shape[0], start, _ptr(logits),

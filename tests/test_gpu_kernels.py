@@ -233,9 +233,19 @@ def test_embed_bit_exact():
     E = synth.rng_for(17).standard_normal((1000, 256)).astype(np.float32)
     toks = synth.tokens(37, 1000, seed=3)
     x = torch.empty((37, 256), dtype=torch.float32, device="cuda")
-    pf.pf_op_embed(dev(E), dev(toks), 37, 256, x)
-    torch.cuda.synchronize()
+    status = torch.zeros(4, dtype=torch.int32, device="cuda")
+    pf.pf_op_embed(dev(E), dev(toks), 37, 256, 1000, x, status)
+    pf.pf_status_read(status)
     np.testing.assert_array_equal(x.cpu().numpy(), E[toks])
+    # an id outside the vocabulary: zero row and a recorded status, other rows intact
+    bad = toks.copy()
+    bad[5] = 1000
+    pf.pf_op_embed(dev(E), dev(bad), 37, 256, 1000, x, status)
+    with pytest.raises(pf.PfError) as e:
+        pf.pf_status_read(status)
+    assert e.value.status == 5
+    got = x.cpu().numpy()
+    assert np.all(got[5] == 0) and np.array_equal(np.delete(got, 5, 0), np.delete(E[bad], 5, 0))
 
 
 @pytest.mark.parametrize("fmt,vocab,h", [("q1", 1000, 256), ("int4", 1000, 256), ("q1", 151936, 4096)])
