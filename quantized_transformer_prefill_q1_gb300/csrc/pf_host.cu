@@ -162,6 +162,7 @@ struct pf_session {
   std::map<GraphKey, GraphExec> execs;
   std::vector<ProfRecord> prof;
   std::vector<cudaEvent_t> event_pool;
+  cudaStream_t capture_stream = nullptr;
 };
 
 namespace {
@@ -314,18 +315,24 @@ pf_status enqueue_chunk(pf_session* s, float* x, int M, const int* tokens_dev, f
   return PF_OK;
 }
 
-// Runs `body` directly, or as a CUDA graph recorded on first use for `key` (never while
-// profiling: the per-launch events need the launches themselves).
+// Runs body(stream) directly on `st`, or as a CUDA graph recorded on first use for `key`
+// and replayed on `st` (never while profiling: the per-launch events need the launches
+// themselves). Recording uses the session's own non-blocking stream, since the caller's
+// stream may be the legacy default stream, on which capture is not permitted; recording
+// executes nothing.
 template <typename Body>
 pf_status run_maybe_graph(pf_session* s, const GraphKey& key, cudaStream_t st, Body body) {
-  if (!s->graphs || s->profile) return body();
+  if (!s->graphs || s->profile) return body(st);
   auto it = s->execs.find(key);
   if (it == s->execs.end()) {
+    if (!s->capture_stream)
+      PF_CUDA(cudaStreamCreateWithFlags(&s->capture_stream, cudaStreamNonBlocking), "capture stream");
+    cudaStream_t cs = s->capture_stream;
     const int64_t before = s->launches;
-    PF_CUDA(cudaStreamBeginCapture(st, cudaStreamCaptureModeThreadLocal), "begin capture");
-    pf_status r = body();
+    PF_CUDA(cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal), "begin capture");
+    pf_status r = body(cs);
     cudaGraph_t graph = nullptr;
-    cudaError_t e = cudaStreamEndCapture(st, &graph);
+    cudaError_t e = cudaStreamEndCapture(cs, &graph);
     const int64_t recorded = s->launches - before;
     s->launches = before;  // counted when the graph runs
     if (r != PF_OK) {
@@ -580,6 +587,7 @@ pf_status pf_session_destroy(pf_session* s) {
     cudaEventDestroy(r.e1);
   }
   for (auto e : s->event_pool) cudaEventDestroy(e);
+  if (s->capture_stream) cudaStreamDestroy(s->capture_stream);
   delete s;
   return PF_OK;
 }
@@ -680,7 +688,8 @@ static pf_status prefill_common(pf_session* s, const int32_t* tokens, bool token
     PF_TRY(set_start(s, start + off, st));
     float* lg = last ? logits : nullptr;
     GraphKey key{m, xc, tok_dev, lg, -1};
-    PF_TRY(run_maybe_graph(s, key, st, [&] { return enqueue_chunk(s, xc, m, tok_dev, lg, st); }));
+    PF_TRY(run_maybe_graph(s, key, st,
+                           [&](cudaStream_t rs) { return enqueue_chunk(s, xc, m, tok_dev, lg, rs); }));
     s->position = start + off + m;  // turbospark prefill.rs: kv.advance_by(m)
     off += m;
   }
@@ -719,7 +728,8 @@ pf_status pf_layer_forward(pf_session* s, int32_t layer, float* x_dev, int32_t M
   pf_status r = set_start(s, start_pos, st);
   if (r != PF_OK) return r;
   GraphKey key{M, x_dev, nullptr, nullptr, layer};
-  return run_maybe_graph(s, key, st, [&] { return enqueue_layer(s, layer, x_dev, M, st); });
+  return run_maybe_graph(s, key, st,
+                         [&](cudaStream_t rs) { return enqueue_layer(s, layer, x_dev, M, rs); });
 }
 
 pf_status pf_prefill_tokens_host(pf_session* s, const int32_t* tokens_host, int32_t M, int32_t start_pos,

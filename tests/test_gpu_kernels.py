@@ -245,7 +245,7 @@ def test_embed_bit_exact():
         pf.pf_status_read(status)
     assert e.value.status == 5
     got = x.cpu().numpy()
-    assert np.all(got[5] == 0) and np.array_equal(np.delete(got, 5, 0), np.delete(E[bad], 5, 0))
+    assert np.all(got[5] == 0) and np.array_equal(np.delete(got, 5, 0), np.delete(E[toks], 5, 0))
 
 
 @pytest.mark.parametrize("fmt,vocab,h", [("q1", 1000, 256), ("int4", 1000, 256), ("q1", 151936, 4096)])
