@@ -278,6 +278,12 @@ pf_status pf_rope_table_host(float theta, int32_t head_dim, int32_t max_seq, flo
 /* Reads (and clears) a device status word written by the single-step kernels;
  * synchronises the stream. */
 pf_status pf_status_read(int32_t* status_dev, void* stream);
+/* Failure-detection self-test: one CTA waits, bounded by limit_ns (1 us .. 10 s), on an
+ * mbarrier that gets its single arrival only if `arrive` is non-zero. Without it the wait
+ * gives up and records PF_ERR_DEVICE_TIMEOUT in *status_dev — the path every pipelined
+ * kernel takes when a stage never completes. Nothing faults or hangs. */
+pf_status pf_selftest_bounded_wait(int32_t* status_dev, int64_t limit_ns, int32_t arrive,
+                                   void* stream);
 
 #ifdef __cplusplus
 }

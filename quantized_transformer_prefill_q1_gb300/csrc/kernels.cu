@@ -314,6 +314,26 @@ __global__ void __launch_bounds__(128) dequant_kernel(const uint8_t* __restrict_
 
 __global__ void set_int_kernel(int* dst, int v) { *dst = v; }
 
+// Exercises the bounded wait every pipelined kernel uses: one mbarrier expecting one
+// arrival; with `arrive` set a thread provides it, otherwise nothing ever does and the
+// wait must give up after limit_ns and record PF_ERR_DEVICE_TIMEOUT.
+__global__ void wait_selftest_kernel(int* status, long long limit_ns, int arrive) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  const uint32_t b = smem_u32(&bar);
+  if (threadIdx.x == 0) {
+    mbar_init(b, 1);
+    abort_flag = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 1 && arrive) mbar_arrive(b);
+  if (threadIdx.x == 0) {
+    const bool ok = mbar_wait(b, 0, &abort_flag, static_cast<uint64_t>(limit_ns));
+    if (!ok && status) atomicCAS(status, 0, PF_ERR_DEVICE_TIMEOUT);
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_rmsnorm(const float* x, const float* w, float eps, int M, int H, void* y,
@@ -414,6 +434,11 @@ cudaError_t launch_dequant(int wfmt, const uint8_t* packed, int64_t N, int64_t K
 
 cudaError_t launch_set_int(int* dst, int value, cudaStream_t stream) {
   set_int_kernel<<<1, 1, 0, stream>>>(dst, value);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_wait_selftest(int* status, long long limit_ns, int arrive, cudaStream_t stream) {
+  wait_selftest_kernel<<<1, 32, 0, stream>>>(status, limit_ns, arrive);
   return cudaGetLastError();
 }
 

@@ -640,6 +640,15 @@ pf_status pf_session_sync(pf_session* s, void* stream) {
   return pf_status_read(wsp<int>(s, s->L.status), stream);
 }
 
+pf_status pf_selftest_bounded_wait(int32_t* status_dev, int64_t limit_ns, int32_t arrive,
+                                   void* stream) {
+  if (!status_dev) return fail(PF_ERR_INVALID_ARG, "status pointer is NULL");
+  if (limit_ns < 1000 || limit_ns > 10000000000LL) return fail(PF_ERR_INVALID_ARG, "limit_ns %lld", (long long)limit_ns);
+  PF_CUDA(launch_wait_selftest(status_dev, limit_ns, arrive, static_cast<cudaStream_t>(stream)),
+          "wait selftest");
+  return PF_OK;
+}
+
 pf_status pf_status_read(int32_t* status_dev, void* stream) {
   if (!status_dev) return fail(PF_ERR_INVALID_ARG, "status pointer is NULL");
   cudaStream_t st = static_cast<cudaStream_t>(stream);

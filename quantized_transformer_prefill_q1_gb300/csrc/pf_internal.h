@@ -81,6 +81,7 @@ cudaError_t launch_lm_head(int wfmt, const float* x_row, const float* norm_w, fl
                            cudaStream_t stream);
 cudaError_t launch_swiglu_f32(const float* gu, int M, int I, void* out_f16, cudaStream_t stream);
 cudaError_t launch_set_int(int* dst, int value, cudaStream_t stream);
+cudaError_t launch_wait_selftest(int* status, long long limit_ns, int arrive, cudaStream_t stream);
 
 int device_sm_count();
 cudaError_t prepare_gemm_kernels();

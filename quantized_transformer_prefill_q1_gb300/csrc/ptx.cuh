@@ -53,13 +53,14 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 // which case it raises *abort itself. Every wait in the pipelined kernels goes through
 // here, so a barrier that never completes ends the CTA with an error status instead of
 // a hang.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort) {
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort,
+                                          uint64_t limit_ns = PF_WAIT_LIMIT_NS) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
     if (*abort) return false;
-    if (global_timer_ns() - t0 > PF_WAIT_LIMIT_NS) {
+    if (global_timer_ns() - t0 > limit_ns) {
       *abort = 1;
       return false;
     }

@@ -95,6 +95,7 @@ _SIGS = {
     "pf_op_lm_head": ([_I32, _VP, _VP, _F, _VP, _I32, _I32, _VP, _VP], _I32),
     "pf_rope_table_host": ([_F, _I32, _I32, _VP], _I32),
     "pf_status_read": ([_VP, _VP], _I32),
+    "pf_selftest_bounded_wait": ([_VP, _I64, _I32, _VP], _I32),
 }
 
 _lib = None
@@ -223,6 +224,10 @@ def pf_op_lm_head(wfmt, x_row, norm_w, eps, packed, vocab, h, logits, stream=Non
 
 def pf_status_read(status, stream=None):
     check(lib().pf_status_read(_ptr(status), _stream(stream)))
+
+
+def pf_selftest_bounded_wait(status, limit_ns: int, arrive: bool, stream=None):
+    check(lib().pf_selftest_bounded_wait(_ptr(status), limit_ns, int(arrive), _stream(stream)))
 
 
 # ------------------------------------------------------------------ model + session
