@@ -43,14 +43,87 @@ NCU_TRAFFIC = {}
 def parse():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=10)
+    p.add_argument("--steps", type=int, default=40)
     p.add_argument("--warmup", type=int, default=3)
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--layers", type=int, default=36, help="development only; 36 is the workload")
     p.add_argument("--profile-steps", type=int, default=2)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--seed", type=int, default=0)
+    p.add_argument("--case", default=None,
+                   choices=["gemm_gate_up", "gemm_qkv", "gemm_down", "attention", "rmsnorm",
+                            "qk_rope_kv", "lm_head"],
+                   help="small single-kernel case at the workload's shapes (for ncu captures)")
+    p.add_argument("--reps", type=int, default=3)
     return p.parse_args()
+
+
+def run_case(args):
+    """Runs one kernel of the workload `--reps` times at its production shape (chunk of
+    512 rows, last chunk's positions for attention) with a few hundred MB on the device;
+    prints the average CUDA-event time per launch."""
+    import numpy as np
+    import torch
+
+    from quantized_transformer_prefill_q1_gb300 import pf, synth
+    s = synth.QWEN3_8B_STACK
+    rng = synth.rng_for(99)
+    M, H, I = CHUNK, s.hidden, s.intermediate
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()  # noqa: E731
+    cfg = pf.make_config(s, CHUNK, n_layers=1)
+    if args.case.startswith("gemm"):
+        n, k, epi = {"gemm_gate_up": (2 * I, H, pf.EPI_SWIGLU), "gemm_qkv": (s.qkv_rows, H, pf.EPI_STORE_F32),
+                     "gemm_down": (H, I, pf.EPI_RESID_ADD)}[args.case]
+        a = dev(rng.standard_normal((M, k)).astype(np.float16))
+        w = dev(pf.pf_pack_weights_host(synth.q1_weight(rng, n, k), epi == pf.EPI_SWIGLU))
+        out = torch.zeros((M, n // 2 if epi == pf.EPI_SWIGLU else n),
+                          dtype=torch.float16 if epi == pf.EPI_SWIGLU else torch.float32, device="cuda")
+        split = 1 if epi != pf.EPI_STORE_F32 else 0
+        fn = lambda: pf.pf_op_gemm(pf.W_Q1, epi, a, w, M, n, k, out, split)  # noqa: E731
+        flops = 2 * M * n * k
+    elif args.case == "attention":
+        start = PROMPT - CHUNK
+        q = torch.randn((M, s.n_q_heads, s.head_dim), device="cuda").to(torch.bfloat16)
+        kc = torch.randn((1, s.n_kv_heads, s.max_seq, s.head_dim), device="cuda").to(torch.bfloat16)
+        vc = torch.randn_like(kc)
+        out = torch.empty((M, s.n_q_heads * s.head_dim), dtype=torch.float16, device="cuda")
+        fn = lambda: pf.pf_op_attention(cfg, q, kc, vc, 0, start, M, out)  # noqa: E731
+        flops = sum(4 * s.n_q_heads * s.head_dim * (p + 1) for p in range(start, start + M))
+    elif args.case == "rmsnorm":
+        x = torch.randn((M, H), device="cuda")
+        wv = torch.ones(H, device="cuda")
+        y = torch.empty((M, H), dtype=torch.float16, device="cuda")
+        fn = lambda: pf.pf_op_rmsnorm(x, wv, 1e-6, y)  # noqa: E731
+        flops = None
+    elif args.case == "qk_rope_kv":
+        qkv = torch.randn((M, s.qkv_rows), device="cuda")
+        qn = torch.ones(s.head_dim, device="cuda")
+        rope = dev(pf.pf_rope_table_host(s.rope_theta, s.head_dim, s.max_seq))
+        q = torch.empty((M, s.n_q_heads, s.head_dim), dtype=torch.bfloat16, device="cuda")
+        kc = torch.empty((1, s.n_kv_heads, s.max_seq, s.head_dim), dtype=torch.bfloat16, device="cuda")
+        vc = torch.empty_like(kc)
+        fn = lambda: pf.pf_op_qk_norm_rope_kv(cfg, qkv, qn, qn, rope, 0, 0, M, q, kc, vc)  # noqa: E731
+        flops = None
+    else:  # lm_head
+        w = dev(pf.pf_pack_weights_host(synth.q1_weight(rng, s.vocab, H)))
+        x = torch.randn(H, device="cuda")
+        nw = torch.ones(H, device="cuda")
+        logits = torch.empty(s.vocab, device="cuda")
+        fn = lambda: pf.pf_op_lm_head(pf.W_Q1, x, nw, 1e-6, w, s.vocab, H, logits)  # noqa: E731
+        flops = None
+    fn()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.reps):
+        fn()
+    e1.record()
+    e1.synchronize()
+    us = e0.elapsed_time(e1) / args.reps * 1e3
+    line = {"case": args.case, "us_per_launch": us}
+    if flops:
+        line["tflops"] = flops / us / 1e6
+    print(json.dumps(line), flush=True)
 
 
 def load_peaks():
@@ -343,7 +416,9 @@ def run_ours(args):
 
 def main():
     args = parse()
-    if args.impl == "reference":
+    if args.case:
+        run_case(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)
