@@ -8,10 +8,12 @@
 // fused, `dispatch_fused_gate_up_swiglu_gemm`).
 //
 // Persistent CTAs (one per SM) walk a list of work units = (128-token tile, 256-row
-// weight tile, K split). Warp roles:
-//   warp 0       TMA producer: activation tile (128 x 64 f16, 128-B swizzle) and the
-//                stage's packed weight block (bulk copy) into a ring of stages;
-//   warps 6..13  dequantise the packed block (one weight row per thread) into a 256 x 64
+// weight tile, K split). Three rings of 64-wide k stages decouple the streams: packed
+// weights (small, deep ring: hides the HBM latency of the weight stream), activation
+// tiles, and dequantised weight tiles. Warp roles:
+//   warp 0       TMA producer of the activation ring (128 x 64 f16, 128-B swizzle);
+//   warp 14      bulk-copy producer of the packed-weight ring;
+//   warps 6..13  dequantise a packed block (one weight row per thread) into a 256 x 64
 //                f16 K-major tile in the same swizzled layout: the UMMA B operand;
 //   warp 1       allocates 512 TMEM columns (two 128 x 256 f32 accumulators) and one lane
 //                issues tcgen05.mma (M=128, N=256, K=16) x 4 per stage, committing each
@@ -34,8 +36,9 @@ constexpr int NUM_EPI_WARPS = 4;
 constexpr int NUM_DQ_WARPS = 8;
 constexpr int DQ_THREADS = NUM_DQ_WARPS * 32;  // == BN: one weight row per thread
 constexpr int EPI_THREADS = NUM_EPI_WARPS * 32;
-constexpr int NUM_THREADS = 32 * (2 + NUM_EPI_WARPS + NUM_DQ_WARPS);  // 448
 constexpr int FIRST_DQ_WARP = 2 + NUM_EPI_WARPS;
+constexpr int PK_WARP = FIRST_DQ_WARP + NUM_DQ_WARPS;  // packed-weight producer
+constexpr int NUM_THREADS = 32 * (PK_WARP + 1);       // 480
 constexpr int A_STAGE = BM * BK * 2;  // 16 KB
 constexpr int B_STAGE = BN * BK * 2;  // 32 KB
 constexpr int TMEM_COLS = 512;        // two accumulators of 256 f32 columns
@@ -50,7 +53,7 @@ struct Fmt<PF_W_Q1_G128> {
   static constexpr int META_OFF = Q1_SCALE_OFF;
   static constexpr int META = TILE_N * 2;
   static constexpr int P_STAGE = HALF + META;  // 2560
-  static constexpr int STAGES = 4;
+  static constexpr int SA = 5, SB = 3, SP = 8;  // activation / dequantised / packed rings
 };
 template <>
 struct Fmt<PF_W_INT4_AFFINE_G128> {
@@ -59,13 +62,14 @@ struct Fmt<PF_W_INT4_AFFINE_G128> {
   static constexpr int META_OFF = I4_SCALE_OFF;
   static constexpr int META = TILE_N * 4;  // scales then zeros
   static constexpr int P_STAGE = HALF + META;  // 9216
-  static constexpr int STAGES = 3;
+  static constexpr int SA = 4, SB = 3, SP = 6;
 };
 
 template <int WFMT>
 constexpr int smem_bytes() {
-  return 1024 /*alignment slack*/ + Fmt<WFMT>::STAGES * (A_STAGE + B_STAGE + Fmt<WFMT>::P_STAGE) +
-         256 /*barriers and flags*/;
+  using F = Fmt<WFMT>;
+  return 1024 /*alignment slack*/ + F::SA * A_STAGE + F::SB * B_STAGE + F::SP * F::P_STAGE +
+         512 /*barriers and flags*/;
 }
 
 // Bounded wait that ignores the abort flag (used while draining after an abort).
@@ -97,23 +101,28 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                   int M, int N, int K, void* __restrict__ out, Units units, int n_units,
                   int atomic_out, int* __restrict__ status) {
   using F = Fmt<WFMT>;
-  constexpr int S = F::STAGES;
+  constexpr int SA = F::SA, SB = F::SB, SP = F::SP;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* gbase = smem_raw + (base - raw);
   const uint32_t a_st = base;
-  const uint32_t b_st = a_st + S * A_STAGE;
-  const uint32_t p_st = b_st + S * B_STAGE;
+  const uint32_t b_st = a_st + SA * A_STAGE;
+  const uint32_t p_st = b_st + SB * B_STAGE;
   const uint8_t* p_gen = gbase + (p_st - base);
-  const uint32_t bar0 = p_st + S * F::P_STAGE;
-  // barriers: full[S], bfull[S], empty[S], acc_full[2], acc_empty[2], drain; then flags
-  auto full = [&](int s) { return bar0 + 8u * s; };
-  auto bfull = [&](int s) { return bar0 + 8u * (S + s); };
-  auto empty = [&](int s) { return bar0 + 8u * (2 * S + s); };
-  auto acc_full = [&](int b) { return bar0 + 8u * (3 * S + b); };
-  auto acc_empty = [&](int b) { return bar0 + 8u * (3 * S + 2 + b); };
-  const uint32_t drain_bar = bar0 + 8u * (3 * S + 4);
+  const uint32_t bar0 = p_st + SP * F::P_STAGE;
+  // barriers: fullA/emptyA [SA], fullB/emptyB [SB], fullP/emptyP [SP], acc_full/acc_empty
+  // [2], drain; then the abort flag and the TMEM address slot
+  auto full_a = [&](int s) { return bar0 + 8u * s; };
+  auto empty_a = [&](int s) { return bar0 + 8u * (SA + s); };
+  auto full_b = [&](int s) { return bar0 + 8u * (2 * SA + s); };
+  auto empty_b = [&](int s) { return bar0 + 8u * (2 * SA + SB + s); };
+  auto full_p = [&](int s) { return bar0 + 8u * (2 * SA + 2 * SB + s); };
+  auto empty_p = [&](int s) { return bar0 + 8u * (2 * SA + 2 * SB + SP + s); };
+  const uint32_t acc0 = bar0 + 8u * (2 * SA + 2 * SB + 2 * SP);
+  auto acc_full = [&](int b) { return acc0 + 8u * b; };
+  auto acc_empty = [&](int b) { return acc0 + 8u * (2 + b); };
+  const uint32_t drain_bar = acc0 + 8u * 4;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + (drain_bar + 8u - base));
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + (drain_bar + 16u - base));
 
@@ -121,10 +130,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const int lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < S; ++s) {
-      mbar_init(full(s), 1);
-      mbar_init(bfull(s), DQ_THREADS);
-      mbar_init(empty(s), 1);
+    for (int s = 0; s < SA; ++s) {
+      mbar_init(full_a(s), 1);
+      mbar_init(empty_a(s), 1);
+    }
+    for (int s = 0; s < SB; ++s) {
+      mbar_init(full_b(s), DQ_THREADS);
+      mbar_init(empty_b(s), 1);
+    }
+    for (int s = 0; s < SP; ++s) {
+      mbar_init(full_p(s), 1);
+      mbar_init(empty_p(s), DQ_THREADS);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(acc_full(b), 1);
@@ -145,9 +161,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const uint32_t tmem_base = *tmem_slot;
   const int G = K / GROUP;
 
-  if (warp == 0) {
-    // ---------------------------------------------------------------- TMA producer
+  if (warp == 0 || warp == PK_WARP) {
+    // ---------------------------------------------------------------- producers
     if (lane == 0) {
+      const bool act = warp == 0;  // activation ring, else packed-weight ring
+      const int S = act ? SA : SP;
       int it = 0;
       bool ok = true;
       for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
@@ -156,21 +174,26 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         for (int i = 0; i < nkb; ++i, ++it) {
           const int s = it % S;
           const uint32_t ph = (it / S) & 1;
-          if (!mbar_wait(empty(s), ph ^ 1, abort_flag)) {
+          if (!mbar_wait(act ? empty_a(s) : empty_p(s), ph ^ 1, abort_flag)) {
             ok = false;
             break;
           }
           const int kb = kb0 + i;
-          const uint8_t* chunk =
-              wpk + (static_cast<size_t>(nt) * G + (kb >> 1)) * static_cast<size_t>(F::CHUNK);
-          mbar_arrive_expect_tx(full(s), A_STAGE + F::P_STAGE);
-          tma_load_2d(a_st + s * A_STAGE, &tmap_a, kb * BK, mt * BM, full(s));
-          bulk_load(p_st + s * F::P_STAGE, chunk + (kb & 1) * F::HALF, F::HALF, full(s));
-          bulk_load(p_st + s * F::P_STAGE + F::HALF, chunk + F::META_OFF, F::META, full(s));
+          if (act) {
+            mbar_arrive_expect_tx(full_a(s), A_STAGE);
+            tma_load_2d(a_st + s * A_STAGE, &tmap_a, kb * BK, mt * BM, full_a(s));
+          } else {
+            const uint8_t* chunk =
+                wpk + (static_cast<size_t>(nt) * G + (kb >> 1)) * static_cast<size_t>(F::CHUNK);
+            mbar_arrive_expect_tx(full_p(s), F::P_STAGE);
+            bulk_load(p_st + s * F::P_STAGE, chunk + (kb & 1) * F::HALF, F::HALF, full_p(s));
+            bulk_load(p_st + s * F::P_STAGE + F::HALF, chunk + F::META_OFF, F::META, full_p(s));
+          }
         }
       }
       if (!ok) {  // let copies already in flight land before shared memory is released
-        for (int j = max(0, it - S); j < it; ++j) mbar_wait_drain(full(j % S), (j / S) & 1);
+        for (int j = max(0, it - S); j < it; ++j)
+          mbar_wait_drain(act ? full_a(j % S) : full_p(j % S), (j / S) & 1);
       }
     }
   } else if (warp == 1) {
@@ -191,19 +214,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + b * BN;
         for (int i = 0; i < nkb; ++i, ++it) {
-          const int s = it % S;
-          const uint32_t ph = (it / S) & 1;
-          if (!(mbar_wait(bfull(s), ph, abort_flag) && mbar_wait(full(s), ph, abort_flag))) {
+          const int sa = it % SA, sb = it % SB;
+          if (!(mbar_wait(full_b(sb), (it / SB) & 1, abort_flag) &&
+                mbar_wait(full_a(sa), (it / SA) & 1, abort_flag))) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint64_t ad = sdesc_kmajor_sw128(a_st + s * A_STAGE);
-          const uint64_t bd = sdesc_kmajor_sw128(b_st + s * B_STAGE);
+          const uint64_t ad = sdesc_kmajor_sw128(a_st + sa * A_STAGE);
+          const uint64_t bd = sdesc_kmajor_sw128(b_st + sb * B_STAGE);
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk)
             umma_f16_ss(d_tmem, ad + 2 * kk, bd + 2 * kk, idesc, (i | kk) != 0);
-          umma_commit(empty(s));
+          umma_commit(empty_a(sa));
+          umma_commit(empty_b(sb));
         }
         if (ok) umma_commit(acc_full(b));
       }
@@ -221,20 +245,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       int mt, nt, kb0, nkb;
       units.decode(u, mt, nt, kb0, nkb);
       for (int i = 0; i < nkb; ++i, ++it) {
-        const int s = it % S;
-        const uint32_t ph = (it / S) & 1;
-        if (!mbar_wait(full(s), ph, abort_flag)) {
+        const int sp = it % SP, sb = it % SB;
+        if (!(mbar_wait(full_p(sp), (it / SP) & 1, abort_flag) &&
+              mbar_wait(empty_b(sb), ((it / SB) & 1) ^ 1, abort_flag))) {
           ok = false;
           break;
         }
-        const uint8_t* p = p_gen + s * F::P_STAGE;
-        const uint32_t bt = b_st + s * B_STAGE;
+        const uint8_t* p = p_gen + sp * F::P_STAGE;
+        const uint32_t bt = b_st + sb * B_STAGE;
         if (WFMT == PF_W_Q1_G128)
           dequant_row_q1(p, d, bt);
         else
           dequant_row_int4(p, d, bt);
         fence_proxy_async_smem();
-        mbar_arrive(bfull(s));
+        mbar_arrive(full_b(sb));
+        mbar_arrive(empty_p(sp));
       }
     }
   } else {
