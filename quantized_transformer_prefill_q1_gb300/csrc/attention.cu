@@ -330,9 +330,14 @@ cudaError_t prepare_attention_kernels() {
   return e;
 }
 
+// Routes 16-bit caches to the tcgen05 kernel (attention_tc.cu); f32 caches stage K/V
+// through registers into the m16n8k16 kernel above.
 cudaError_t launch_attention(const pf_config& c, const void* q, const void* k_cache,
                              const void* v_cache, int layer, const int* start_dev, int start_host,
-                             int M, void* out, cudaStream_t stream) {
+                             int M, void* out, int* status, cudaStream_t stream) {
+  if (attention_tc_supported(c))
+    return launch_attention_tc(c, q, k_cache, v_cache, layer, start_dev, start_host, M, out, status,
+                               stream);
   if (c.head_dim == 128)
     return dispatch_kv<128>(c, q, k_cache, v_cache, layer, start_dev, start_host, M, out, stream);
   return dispatch_kv<64>(c, q, k_cache, v_cache, layer, start_dev, start_host, M, out, stream);

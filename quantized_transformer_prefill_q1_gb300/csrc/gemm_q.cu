@@ -53,7 +53,7 @@ struct Fmt<PF_W_Q1_G128> {
   static constexpr int META_OFF = Q1_SCALE_OFF;
   static constexpr int META = TILE_N * 2;
   static constexpr int P_STAGE = HALF + META;  // 2560
-  static constexpr int SA = 5, SB = 3, SP = 8;  // activation / dequantised / packed rings
+  static constexpr int SA = 4, SB = 4, SP = 6;  // activation / dequantised / packed rings
 };
 template <>
 struct Fmt<PF_W_INT4_AFFINE_G128> {
@@ -62,7 +62,7 @@ struct Fmt<PF_W_INT4_AFFINE_G128> {
   static constexpr int META_OFF = I4_SCALE_OFF;
   static constexpr int META = TILE_N * 4;  // scales then zeros
   static constexpr int P_STAGE = HALF + META;  // 9216
-  static constexpr int SA = 4, SB = 3, SP = 6;
+  static constexpr int SA = 3, SB = 4, SP = 4;
 };
 
 template <int WFMT>

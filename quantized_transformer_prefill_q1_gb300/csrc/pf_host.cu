@@ -113,6 +113,24 @@ bool encode_tmap_f16_2d(CUtensorMap* map, const void* base, uint64_t inner, uint
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool encode_tmap_16(CUtensorMap* map, int bf16, int rank, const void* base, const uint64_t* dims,
+                    const uint64_t* strides_bytes, const uint32_t* box) {
+  EncodeTiledFn fn = get_encode_fn();
+  if (!fn || rank < 2 || rank > 5) return false;
+  cuuint64_t d[5], s[4];
+  cuuint32_t b[5], e[5];
+  for (int i = 0; i < rank; ++i) {
+    d[i] = dims[i];
+    b[i] = box[i];
+    e[i] = 1;
+    if (i + 1 < rank) s[i] = strides_bytes[i];
+  }
+  return fn(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+            static_cast<cuuint32_t>(rank), const_cast<void*>(base), d, s, b, e,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 int device_sm_count() {
   int dev = 0, n = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 148;
@@ -274,7 +292,7 @@ pf_status enqueue_layer(pf_session* s, int l, float* x, int M, cudaStream_t st) 
                                   start_dev, 0, M, q, s->k, s->v, st);
   }));
   PF_TRY(launch_k(s, PF_K_ATTENTION, st, "attention", [&] {
-    return launch_attention(c, q, s->k, s->v, l, start_dev, 0, M, attn, st);
+    return launch_attention(c, q, s->k, s->v, l, start_dev, 0, M, attn, wsp<int>(s, s->L.status), st);
   }));
   // 4. O projection + residual
   PF_TRY(enqueue_gemm(s, PF_K_GEMM_O, c.wfmt, EPI_RESID_ADD, attn, w.o_proj, M, H,
@@ -366,6 +384,7 @@ void prepare_all() {
   std::call_once(once, [] {
     prepare_gemm_kernels();
     prepare_attention_kernels();
+    prepare_attention_tc_kernels();
   });
 }
 
@@ -833,7 +852,7 @@ pf_status pf_op_attention(const pf_config* cfg, const void* q, const void* kc, c
       static_cast<int64_t>(start) + M > cfg->max_seq)
     return fail(PF_ERR_SHAPE, "M %d layer %d start %d", M, layer, start);
   prepare_all();
-  PF_CUDA(launch_attention(*cfg, q, kc, vc, layer, nullptr, start, M, out,
+  PF_CUDA(launch_attention(*cfg, q, kc, vc, layer, nullptr, start, M, out, nullptr,
                            static_cast<cudaStream_t>(stream)),
           "attention");
   return PF_OK;

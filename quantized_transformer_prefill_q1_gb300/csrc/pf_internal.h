@@ -2,6 +2,7 @@
 #pragma once
 #include <cstddef>
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "../../include/pf.h"
@@ -73,7 +74,7 @@ cudaError_t launch_qk_norm_rope_kv(const pf_config& c, const float* qkv, const f
                                    void* k_cache, void* v_cache, cudaStream_t stream);
 cudaError_t launch_attention(const pf_config& c, const void* q, const void* k_cache,
                              const void* v_cache, int layer, const int* start_dev, int start_host,
-                             int M, void* out_f16, cudaStream_t stream);
+                             int M, void* out_f16, int* status, cudaStream_t stream);
 cudaError_t launch_embed(const float* E, const int* tokens, int M, int H, int vocab, float* x,
                          int* status, cudaStream_t stream);
 cudaError_t launch_lm_head(int wfmt, const float* x_row, const float* norm_w, float eps,
@@ -84,6 +85,15 @@ cudaError_t launch_set_int(int* dst, int value, cudaStream_t stream);
 cudaError_t launch_wait_selftest(int* status, long long limit_ns, int arrive, cudaStream_t stream);
 
 int device_sm_count();
+// Tiled tensor map over a 16-bit (bf16 if `bf16`, else f16) array of `rank` dims
+// (innermost first), 128-B swizzle, zero fill out of bounds.
+bool encode_tmap_16(CUtensorMap* map, int bf16, int rank, const void* base, const uint64_t* dims,
+                    const uint64_t* strides_bytes, const uint32_t* box);
+bool attention_tc_supported(const pf_config& c);
+cudaError_t prepare_attention_tc_kernels();
+cudaError_t launch_attention_tc(const pf_config& c, const void* q, const void* k_cache,
+                                const void* v_cache, int layer, const int* start_dev, int start_host,
+                                int M, void* out, int* status, cudaStream_t stream);
 cudaError_t prepare_gemm_kernels();
 cudaError_t prepare_attention_kernels();
 
