@@ -216,9 +216,11 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int pos = start + t0 + t_loc;
     float m = -INFINITY, l = 0.f;
     bool ok = true;
+    // tcgen05.ld / tcgen05.st are warp-collective: every branch around them below is
+    // made warp-uniform (vote on wait outcomes and on the rescale decision).
     for (int j = 0; j < n_tiles; ++j) {
       const int s = j & 1;
-      if (!mbar_wait(s_full(s), (j >> 1) & 1, abort_flag)) {
+      if (!__all_sync(0xffffffffu, mbar_wait(s_full(s), (j >> 1) & 1, abort_flag))) {
         ok = false;
         break;
       }
@@ -237,13 +239,16 @@ __global__ void __launch_bounds__(THREADS, 1)
           mx = fmaxf(mx, x);
         }
       }
+      const bool need = j > 0 && mx > m + RESCALE_LOG2;
       if (j == 0) {
         m = mx;  // key 0 is visible to every row, so this is finite
-      } else if (mx > m + RESCALE_LOG2) {
-        const float alpha = exp2f(m - mx);
+      } else if (__any_sync(0xffffffffu, need)) {
+        // some row of this warp raises its max: the whole warp rescales its O rows, the
+        // rows that keep their max with alpha = 1
+        const float alpha = need ? exp2f(m - mx) : 1.0f;
         l *= alpha;
         // O holds P_0..P_{j-1} V: wait for PV_{j-1}, then scale it in place
-        if (!mbar_wait(o_done, (j - 1) & 1, abort_flag)) {
+        if (!__all_sync(0xffffffffu, mbar_wait(o_done, (j - 1) & 1, abort_flag))) {
           ok = false;
           break;
         }
@@ -258,9 +263,9 @@ __global__ void __launch_bounds__(THREADS, 1)
           tmem_st_32x32b_x32(tmem_o + lane_off + 32 * c, v);
         }
         tmem_st_wait();
-        m = mx;
+        if (need) m = mx;
       }
-      if (!mbar_wait(p_empty(s), ((j >> 1) & 1) ^ 1, abort_flag)) {
+      if (!__all_sync(0xffffffffu, mbar_wait(p_empty(s), ((j >> 1) & 1) ^ 1, abort_flag))) {
         ok = false;
         break;
       }
@@ -302,7 +307,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_arrive(p_full(s));
     }
     // ------------------------------------------------------------------ epilogue
-    if (ok && mbar_wait(o_final, 0, abort_flag)) {
+    if (__all_sync(0xffffffffu, ok && mbar_wait(o_final, 0, abort_flag))) {
       tc_fence_after();
       const float inv = 1.f / l;
       const int t = t0 + t_loc;
@@ -334,6 +339,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
+    __syncwarp();  // lane 0 ran the MMA loop: reconverge before the collective dealloc
     tmem_dealloc(tmem, 512);
   }
   if (threadIdx.x == 0 && *abort_flag && status != nullptr) atomicCAS(status, 0, PF_ERR_DEVICE_TIMEOUT);

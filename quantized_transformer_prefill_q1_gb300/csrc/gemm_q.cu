@@ -271,7 +271,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       units.decode(u, mt, nt, kb0, nkb);
       const int b = local & 1;
       const uint32_t use = static_cast<uint32_t>(local >> 1);
-      if (!mbar_wait(acc_full(b), use & 1, abort_flag)) break;
+      // warp-uniform: the tcgen05.ld below is warp-collective
+      if (!__all_sync(0xffffffffu, mbar_wait(acc_full(b), use & 1, abort_flag))) break;
       tc_fence_after();
       const int row = mt * BM + 32 * q + lane;
       const uint32_t tb = tmem_base + b * BN + (static_cast<uint32_t>(32 * q) << 16);
@@ -343,6 +344,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
+    __syncwarp();  // lane 0 ran the MMA loop: reconverge before the collective dealloc
     tmem_dealloc(tmem_base, TMEM_COLS);
   }
   if (threadIdx.x == 0 && *abort_flag && status != nullptr) atomicCAS(status, 0, PF_ERR_DEVICE_TIMEOUT);

@@ -199,13 +199,17 @@ def test_qk_norm_rope_kv(shape, m, start, layer, nl):
 
 
 # ----------------------------------------------------------------------------- attention
-@pytest.mark.parametrize("shape,m,start", [
-    (synth.TINY, 16, 0), (synth.TINY, 9, 40),
-    (synth.QWEN3_8B_LAYER, 512, 0), (synth.QWEN3_8B_LAYER, 37, 100),
-    (synth.QWEN3_8B_LAYER_LONG, 512, 3584),
-    (synth.LLAMA3_8B_INT4_LAYER, 1, 8192), (synth.LLAMA3_8B_INT4_LAYER, 64, 8192),
+@pytest.mark.parametrize("shape,m,start,qscale", [
+    (synth.TINY, 16, 0, 1), (synth.TINY, 9, 40, 1),
+    (synth.QWEN3_8B_LAYER, 512, 0, 1), (synth.QWEN3_8B_LAYER, 37, 100, 1),
+    (synth.QWEN3_8B_LAYER_LONG, 512, 3584, 1),
+    (synth.LLAMA3_8B_INT4_LAYER, 1, 8192, 1), (synth.LLAMA3_8B_INT4_LAYER, 64, 8192, 1),
+    # large scores: row maxima jump by more than 2^8 between key tiles, so the running
+    # max is raised and the partial output rescaled (for some rows of a warp only)
+    (synth.QWEN3_8B_LAYER, 200, 300, 8), (synth.LLAMA3_8B_INT4_LAYER, 1, 8192, 8),
+    (synth.TINY, 16, 40, 8),
 ])
-def test_attention_vs_oracle(shape, m, start):
+def test_attention_vs_oracle(shape, m, start, qscale):
     s = shape
     nq, nkv, hd = s.n_q_heads, s.n_kv_heads, s.head_dim
     cfg = pf.make_config(s, max_chunk=max(m, 16))
@@ -213,7 +217,7 @@ def test_attention_vs_oracle(shape, m, start):
     L = start + m
     qdt = torch.bfloat16 if s.kv_dtype == "bf16" else torch.float16
     tdt = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}[s.kv_dtype]
-    q = torch.from_numpy(rng.standard_normal((m, nq, hd)).astype(np.float32)).to(qdt).cuda()
+    q = torch.from_numpy(qscale * rng.standard_normal((m, nq, hd)).astype(np.float32)).to(qdt).cuda()
     kc = torch.full((1, nkv, s.max_seq, hd), float("nan"), dtype=tdt, device="cuda")
     vc = torch.full_like(kc, float("nan"))
     kc[0, :, :L] = torch.from_numpy(rng.standard_normal((nkv, L, hd)).astype(np.float32)).to(tdt).cuda()
