@@ -116,8 +116,8 @@ int32_t pf_abi_version(void);         /* bumps on any ABI change */
  *        w = scale * (q - zero); scales, zeros = f16 bits [N, K/128].
  * The device layout (tiles of 256 rows x 128 weights, scales beside their bits, sign
  * bits / nibbles permuted for the dequantiser) is private to libpf; only its size
- * is public. With interleave_gate_up = 1 (N = 2I, I % 128 == 0), each 256-row tile
- * holds 128 gate rows followed by the 128 matching up rows, so one GEMM tile sees
+ * is public. With interleave_gate_up = 1 (N = 2I, I % 128 == 0), each 128-row tile
+ * holds 64 gate rows followed by the 64 matching up rows, so one GEMM tile sees
  * both inputs of SwiGLU. Rows are padded to a multiple of 256 with zero scale.
  * Pure host code; safe without a GPU.
  */

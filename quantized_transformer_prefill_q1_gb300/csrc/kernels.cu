@@ -253,63 +253,48 @@ __global__ void __launch_bounds__(256) lm_head_kernel(const float* __restrict__ 
 
 // ------------------------------------------------------------------ split-K SwiGLU
 // Used when the gate_up GEMM is split along K (small chunks): gu holds the f32 GEMM
-// output in packed-row order, where each 256-column tile is 128 gate columns then the
-// 128 matching up columns. out[m, f] = silu(gate) * up, f16.
+// output in packed-row order, where each 128-column tile is 64 gate columns then the 64
+// matching up columns. out[m, f] = silu(gate) * up, f16.
 __global__ void swiglu_f32_kernel(const float* __restrict__ gu, int M, int I,
                                   __half* __restrict__ out) {
   const size_t idx = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (idx >= static_cast<size_t>(M) * I) return;
   const int m = static_cast<int>(idx / I);
   const int f = static_cast<int>(idx - static_cast<size_t>(m) * I);
-  const int t = f >> 7, r = f & 127;
+  const int t = f >> 6, r = f & 63;
   const size_t ld = 2 * static_cast<size_t>(I);
-  const float g = gu[m * ld + t * 256 + r];
-  const float u = gu[m * ld + t * 256 + 128 + r];
+  const float g = gu[m * ld + t * 128 + r];
+  const float u = gu[m * ld + t * 128 + 64 + r];
   out[idx] = __float2half_rn(g / (1.0f + __expf(-g)) * u);
 }
 
 // ------------------------------------------------------------------ dequant (test)
-// Runs the GEMM's own dequantiser into shared memory (swizzled UMMA layout), then
-// un-swizzles the 256 x 64 tile to w [N, K] f16 row-major. One CTA per (tile, stage).
+// Runs the GEMM's own dequantisers (dq_q1_32 / dq_i4_32) on every 32-weight run of the
+// packed tensor and writes w [N, K] f16 row-major. One thread per (row, 32-k run).
 template <int WFMT>
-__global__ void __launch_bounds__(128) dequant_kernel(const uint8_t* __restrict__ W, int64_t N,
+__global__ void __launch_bounds__(256) dequant_kernel(const uint8_t* __restrict__ W, int64_t N,
                                                       int64_t K, __half* __restrict__ w) {
-  __shared__ __align__(1024) uint8_t tile[256 * 128];
-  __shared__ __align__(16) uint8_t pk[TILE_N * 32 + TILE_N * 4];
-  const int t = blockIdx.x;
-  const int kb = blockIdx.y;  // 64-wide stage index
   const int G = static_cast<int>(K / GROUP);
-  const int d = threadIdx.x;
-  const size_t cb = chunk_bytes(WFMT);
-  const uint8_t* ch = W + (static_cast<size_t>(t) * G + (kb >> 1)) * cb;
-  // stage the packed block exactly as the GEMM's bulk copies lay it out
-  const int half_bytes = WFMT == PF_W_Q1_G128 ? Q1_HALF_BYTES : I4_HALF_BYTES;
-  const int meta_off = WFMT == PF_W_Q1_G128 ? Q1_SCALE_OFF : I4_SCALE_OFF;
-  const int meta = WFMT == PF_W_Q1_G128 ? TILE_N * 2 : TILE_N * 4;
-  for (int i = d; i < half_bytes / 16; i += blockDim.x)
-    reinterpret_cast<uint4*>(pk)[i] = reinterpret_cast<const uint4*>(ch + (kb & 1) * half_bytes)[i];
-  for (int i = d; i < meta / 16; i += blockDim.x)
-    reinterpret_cast<uint4*>(pk + half_bytes)[i] = reinterpret_cast<const uint4*>(ch + meta_off)[i];
-  __syncthreads();
-  const uint32_t bt = smem_u32(tile);
+  const int64_t n = static_cast<int64_t>(blockIdx.x) * 256 + threadIdx.x;  // packed row
+  const int run = blockIdx.y;                                             // 32-k run
+  if (n >= N) return;
+  const int t = static_cast<int>(n / TILE_N), r = static_cast<int>(n % TILE_N);
+  const int g = run >> 2, h = (run >> 1) & 1, half32 = run & 1;
+  const uint8_t* ch = W + (static_cast<size_t>(t) * G + g) * chunk_bytes(WFMT);
+  uint32_t v[16];
   if (WFMT == PF_W_Q1_G128) {
-    dequant_row_q1(pk, d, bt);
-    dequant_row_q1(pk, d + 128, bt);
+    const uint32_t Z = reinterpret_cast<const uint32_t*>(ch + h * Q1_HALF_BYTES + r * 8)[half32];
+    const uint32_t s16 = reinterpret_cast<const uint16_t*>(ch + Q1_SCALE_OFF)[r];
+    dq_q1_32(Z, s16 | (s16 << 16), v);
   } else {
-    dequant_row_int4(pk, d, bt);
-    dequant_row_int4(pk, d + 128, bt);
+    const uint4 q = reinterpret_cast<const uint4*>(ch + h * I4_HALF_BYTES + r * 32)[half32];
+    const uint16_t s16 = reinterpret_cast<const uint16_t*>(ch + I4_SCALE_OFF)[r];
+    const uint16_t z16 = reinterpret_cast<const uint16_t*>(ch + I4_ZERO_OFF)[r];
+    dq_i4_32(q, __half2half2(__ushort_as_half(s16)), __half2half2(__ushort_as_half(z16)), v);
   }
-  __syncthreads();
-  for (int rr = 0; rr < 2; ++rr) {
-    const int r = d + 128 * rr;
-    const int64_t n = static_cast<int64_t>(t) * TILE_N + r;
-    if (n >= N) continue;
-    for (int c = 0; c < 8; ++c) {
-      const uint4 v = *reinterpret_cast<const uint4*>(tile + (r >> 3) * 1024 + (r & 7) * 128 +
-                                                      ((c ^ (r & 7)) << 4));
-      *reinterpret_cast<uint4*>(w + n * K + kb * 64 + c * 8) = v;
-    }
-  }
+  uint4* dst = reinterpret_cast<uint4*>(w + n * K + static_cast<int64_t>(run) * 32);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) dst[j] = make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
 }
 
 __global__ void set_int_kernel(int* dst, int v) { *dst = v; }
@@ -422,12 +407,12 @@ cudaError_t launch_swiglu_f32(const float* gu, int M, int I, void* out, cudaStre
 
 cudaError_t launch_dequant(int wfmt, const uint8_t* packed, int64_t N, int64_t K, void* w,
                            cudaStream_t stream) {
-  dim3 grid(static_cast<unsigned>(padded_rows(N) / TILE_N), static_cast<unsigned>(K / 64));
+  dim3 grid(static_cast<unsigned>((N + 255) / 256), static_cast<unsigned>(K / 32));
   if (wfmt == PF_W_Q1_G128)
-    dequant_kernel<PF_W_Q1_G128><<<grid, 128, 0, stream>>>(packed, N, K,
+    dequant_kernel<PF_W_Q1_G128><<<grid, 256, 0, stream>>>(packed, N, K,
                                                            reinterpret_cast<__half*>(w));
   else
-    dequant_kernel<PF_W_INT4_AFFINE_G128><<<grid, 128, 0, stream>>>(packed, N, K,
+    dequant_kernel<PF_W_INT4_AFFINE_G128><<<grid, 256, 0, stream>>>(packed, N, K,
                                                                     reinterpret_cast<__half*>(w));
   return cudaGetLastError();
 }

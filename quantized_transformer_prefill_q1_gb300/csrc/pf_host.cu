@@ -458,8 +458,9 @@ pf_status pf_pack_weights_host(int32_t wfmt, const uint8_t* codes, const uint16_
   for (int64_t p = 0; p < Np; ++p) {
     int64_t src;
     if (interleave_gate_up) {
-      const int64_t t = p / 256, r = p % 256;
-      src = r < 128 ? t * 128 + r : I + t * 128 + (r - 128);
+      // every 128 packed rows: 64 gate rows, then the 64 matching up rows
+      const int64_t t = p / 128, r = p % 128;
+      src = r < 64 ? t * 64 + r : I + t * 64 + (r - 64);
     } else {
       src = p < N ? p : -1;
     }

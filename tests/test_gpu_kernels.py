@@ -65,9 +65,9 @@ def test_pack_interleave_gate_up():
     torch.cuda.synchronize()
     got = out.cpu().numpy()
     ref = O.dequant_q1(w["bits"], w["scales"]).astype(np.float16)
-    for t in range(2):
-        np.testing.assert_array_equal(got[256 * t: 256 * t + 128], ref[128 * t: 128 * t + 128])
-        np.testing.assert_array_equal(got[256 * t + 128: 256 * t + 256], ref[I + 128 * t: I + 128 * t + 128])
+    for t in range(4):  # each 128 packed rows: 64 gate rows, then the 64 matching up rows
+        np.testing.assert_array_equal(got[128 * t: 128 * t + 64], ref[64 * t: 64 * t + 64])
+        np.testing.assert_array_equal(got[128 * t + 64: 128 * t + 128], ref[I + 64 * t: I + 64 * t + 64])
 
 
 # ----------------------------------------------------------------------------- GEMM
