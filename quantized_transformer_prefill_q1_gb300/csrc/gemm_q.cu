@@ -12,15 +12,17 @@
 // W_tile x A_tokens^T), so shared memory only carries the activation tile (TMA in, MMA
 // out) and the small packed-weight stream. Persistent CTAs (one per SM) walk work units
 // = (128-row weight tile, 128-token tile, K split). Warp roles:
-//   warp 0       TMA producer of the activation ring (128 tokens x 64 k, 128-B swizzle);
-//   warp 14      bulk-copy producer of the packed-weight ring (128 rows x 64 k per stage);
-//   warps 6..13  dequantisers: warp w owns TMEM lane quarter w % 4 (32 weight rows) and
-//                one 32-wide half of the stage's 64 k; each thread turns its row's sign
+//   warp 0       TMA producer of the activation ring (128 tokens x 128 k per stage, as
+//                two 64-k atoms in the 128-B swizzle layout);
+//   warp 22      bulk-copy producer of the packed-weight ring (128 rows x one 128-weight
+//                scale group per stage);
+//   warps 6..21  dequantisers: warp w owns TMEM lane quarter w % 4 (32 weight rows) and
+//                one 32-wide quarter of the stage's 128 k; each thread turns its row's sign
 //                bits (or nibbles) into 16 f16x2 words and stores them with one tcgen05.st
-//                into the stage's A slot (32 TMEM columns per 64 k);
-//   warp 1       allocates all 512 TMEM columns (two 128 x 128 f32 accumulators + eight A
+//                into the stage's A slot (64 TMEM columns per 128 k);
+//   warp 1       allocates all 512 TMEM columns (two 128 x 128 f32 accumulators + four A
 //                slots) and one lane issues tcgen05.mma (A from TMEM, B = activations
-//                from shared memory; M=128, N=128, K=16) x 4 per stage;
+//                from shared memory; M=128, N=128, K=16) x 8 per stage;
 //   warps 2..5   epilogue: tcgen05.ld of a finished accumulator (thread = weight row,
 //                registers = 32 tokens), f32 store / residual add / SwiGLU, overlapping
 //                the next unit's main loop in the other accumulator.
@@ -35,22 +37,24 @@ namespace {
 
 constexpr int BW = 128;  // weight rows per unit (MMA M, TMEM lanes)
 constexpr int BT = 128;  // tokens per unit (MMA N)
-constexpr int BK = 64;   // k per stage
+constexpr int BK = 128;  // k per stage (one scale group)
 constexpr int NUM_EPI_WARPS = 4;
-constexpr int NUM_DQ_WARPS = 8;
+constexpr int NUM_DQ_WARPS = 16;  // 4 per TMEM lane quarter, one 32-k quarter each
 constexpr int FIRST_DQ_WARP = 2 + NUM_EPI_WARPS;
 constexpr int PK_WARP = FIRST_DQ_WARP + NUM_DQ_WARPS;
-constexpr int NUM_THREADS = 32 * (PK_WARP + 1);  // 480
+constexpr int NUM_THREADS = 32 * (PK_WARP + 1);  // 736
 constexpr int DQ_THREADS = NUM_DQ_WARPS * 32;
 constexpr int EPI_THREADS = NUM_EPI_WARPS * 32;
-constexpr int B_STAGE = BT * BK * 2;  // 16 KB activation tile
-constexpr int SB = 8;                 // activation ring depth
-constexpr int SA = 8;                 // A slots in TMEM (32 columns each)
+constexpr int B_STAGE = BT * BK * 2;  // 32 KB activation tile (two 64-k swizzle atoms)
+constexpr int B_ATOM = BT * 128;      // one 64-k atom: 128 tokens x 128 B
+constexpr int SB = 4;                 // activation ring depth
+constexpr int SA = 4;                 // A slots in TMEM (64 columns each)
+constexpr int A_SLOT_COLS = BK / 2;   // f16 pairs per row
 constexpr int ACC_COLS = BT;          // one accumulator: 128 f32 columns
 constexpr int A_COL0 = 2 * ACC_COLS;  // A slots after the two accumulators
 constexpr int TMEM_COLS = 512;
 constexpr int STAGE_BYTES = 64 * 32 * 4;  // SwiGLU epilogue staging: 64 rows x 32 tokens f32
-static_assert(A_COL0 + SA * 32 == TMEM_COLS, "TMEM budget");
+static_assert(A_COL0 + SA * A_SLOT_COLS == TMEM_COLS, "TMEM budget");
 
 template <int WFMT>
 struct Fmt;
@@ -58,11 +62,11 @@ template <>
 struct Fmt<PF_W_Q1_G128> {
   static constexpr int CHUNK = Q1_CHUNK_BYTES;
   static constexpr int HALF = Q1_HALF_BYTES;  // 256 rows x 8 B for one 64-k half of a chunk
-  static constexpr int ROWB = 8;              // bytes per row per stage
+  static constexpr int ROWB = 8;              // bytes per row per 64-k half
   static constexpr int META_OFF = Q1_SCALE_OFF;
   static constexpr int NMETA = 1;             // scales
-  static constexpr int P_STAGE = BW * ROWB + BW * 2 * NMETA;  // 1280
-  static constexpr int SP = 16;
+  static constexpr int P_STAGE = 2 * BW * ROWB + BW * 2 * NMETA;  // 2304
+  static constexpr int SP = 12;
 };
 template <>
 struct Fmt<PF_W_INT4_AFFINE_G128> {
@@ -71,8 +75,8 @@ struct Fmt<PF_W_INT4_AFFINE_G128> {
   static constexpr int ROWB = 32;
   static constexpr int META_OFF = I4_SCALE_OFF;
   static constexpr int NMETA = 2;             // scales, zeros
-  static constexpr int P_STAGE = BW * ROWB + BW * 2 * NMETA;  // 4608
-  static constexpr int SP = 10;
+  static constexpr int P_STAGE = 2 * BW * ROWB + BW * 2 * NMETA;  // 8704
+  static constexpr int SP = 6;
 };
 
 template <int WFMT>
@@ -218,17 +222,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           if (act) {
             mbar_arrive_expect_tx(full_b(s), B_STAGE);
             tma_load_2d(b_st + s * B_STAGE, &tmap_a, kb * BK, tt * BT, full_b(s));
+            tma_load_2d(b_st + s * B_STAGE + B_ATOM, &tmap_a, kb * BK + 64, tt * BT, full_b(s));
           } else {
-            // 128-row half (wt & 1) of the 256-row chunk (wt >> 1, kb >> 1), 64-k half kb & 1
-            const uint8_t* chunk = wpk + (static_cast<size_t>(wt >> 1) * G + (kb >> 1)) *
-                                             static_cast<size_t>(F::CHUNK);
+            // 128-row half (wt & 1) of the 256-row chunk (wt >> 1, group kb): both 64-k
+            // halves of the rows' codes, then their scales (and zeros)
+            const uint8_t* chunk =
+                wpk + (static_cast<size_t>(wt >> 1) * G + kb) * static_cast<size_t>(F::CHUNK);
             const int r0 = (wt & 1) * BW;
             const uint32_t dst = p_st + s * F::P_STAGE;
             mbar_arrive_expect_tx(full_p(s), F::P_STAGE);
-            bulk_load(dst, chunk + (kb & 1) * F::HALF + r0 * F::ROWB, BW * F::ROWB, full_p(s));
-            bulk_load(dst + BW * F::ROWB, chunk + F::META_OFF + r0 * 2, BW * 2, full_p(s));
+            bulk_load(dst, chunk + r0 * F::ROWB, BW * F::ROWB, full_p(s));
+            bulk_load(dst + BW * F::ROWB, chunk + F::HALF + r0 * F::ROWB, BW * F::ROWB, full_p(s));
+            bulk_load(dst + 2 * BW * F::ROWB, chunk + F::META_OFF + r0 * 2, BW * 2, full_p(s));
             if (F::NMETA == 2)
-              bulk_load(dst + BW * F::ROWB + BW * 2, chunk + F::META_OFF + TILE_N * 2 + r0 * 2,
+              bulk_load(dst + 2 * BW * F::ROWB + BW * 2, chunk + F::META_OFF + TILE_N * 2 + r0 * 2,
                         BW * 2, full_p(s));
           }
         }
@@ -263,11 +270,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             break;
           }
           tc_fence_after();
-          const uint32_t a_tmem = tmem_base + A_COL0 + sa * 32;
-          const uint64_t bd = sdesc_kmajor_sw128(b_st + sb * B_STAGE);
+          const uint32_t a_tmem = tmem_base + A_COL0 + sa * A_SLOT_COLS;
 #pragma unroll
-          for (int kk = 0; kk < BK / 16; ++kk)
-            umma_f16_ts(d_tmem, a_tmem + 8 * kk, bd + 2 * kk, idesc, (i | kk) != 0);
+          for (int kk = 0; kk < BK / 16; ++kk) {
+            const uint64_t bd = sdesc_kmajor_sw128(b_st + sb * B_STAGE + (kk >> 2) * B_ATOM) + 2 * (kk & 3);
+            umma_f16_ts(d_tmem, a_tmem + 8 * kk, bd, idesc, (i | kk) != 0);
+          }
           umma_commit(empty_a(sa));
           umma_commit(empty_b(sb));
         }
@@ -281,7 +289,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   } else if (warp >= FIRST_DQ_WARP) {
     // ---------------------------------------------------------------- dequantisers
     const int quarter = warp & 3;
-    const int khalf = (warp - FIRST_DQ_WARP) >> 2;  // which 32 of the stage's 64 k
+    const int kq = (warp - FIRST_DQ_WARP) >> 2;     // which 32 of the stage's 128 k
+    const int khalf = kq >> 1, kword = kq & 1;
     const int r = 32 * quarter + lane;              // weight row of the tile
     const uint32_t lane_off = static_cast<uint32_t>(32 * quarter) << 16;
     int it = 0;
@@ -300,16 +309,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const uint8_t* p = p_gen + sp * F::P_STAGE;
         uint32_t w[16];
         if (WFMT == PF_W_Q1_G128) {
-          const uint32_t Z = reinterpret_cast<const uint32_t*>(p + r * 8)[khalf];
-          const uint32_t s16 = reinterpret_cast<const uint16_t*>(p + BW * 8)[r];
+          const uint32_t Z = reinterpret_cast<const uint32_t*>(p + khalf * (BW * 8) + r * 8)[kword];
+          const uint32_t s16 = reinterpret_cast<const uint16_t*>(p + 2 * BW * 8)[r];
           dq_q1_32(Z, s16 | (s16 << 16), w);
         } else {
-          const uint4 q = reinterpret_cast<const uint4*>(p + r * 32)[khalf];
-          const uint16_t s16 = reinterpret_cast<const uint16_t*>(p + BW * 32)[r];
-          const uint16_t z16 = reinterpret_cast<const uint16_t*>(p + BW * 32 + BW * 2)[r];
+          const uint4 q = reinterpret_cast<const uint4*>(p + khalf * (BW * 32) + r * 32)[kword];
+          const uint16_t s16 = reinterpret_cast<const uint16_t*>(p + 2 * BW * 32)[r];
+          const uint16_t z16 = reinterpret_cast<const uint16_t*>(p + 2 * BW * 32 + BW * 2)[r];
           dq_i4_32(q, __half2half2(__ushort_as_half(s16)), __half2half2(__ushort_as_half(z16)), w);
         }
-        tmem_st_x16(tmem_base + lane_off + A_COL0 + sa * 32 + 16 * khalf, w);
+        tmem_st_x16(tmem_base + lane_off + A_COL0 + sa * A_SLOT_COLS + 16 * kq, w);
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(full_a(sa));
