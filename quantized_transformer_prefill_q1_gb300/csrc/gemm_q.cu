@@ -475,7 +475,8 @@ cudaError_t prepare_gemm_kernels() {
 
 cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t stream) {
   CUtensorMap tm;
-  if (!encode_tmap_f16_2d(&tm, g.a, static_cast<uint64_t>(g.K), static_cast<uint64_t>(g.M), BK, BT))
+  // 64-wide boxes (128 B, the swizzle span); each stage loads two of them
+  if (!encode_tmap_f16_2d(&tm, g.a, static_cast<uint64_t>(g.K), static_cast<uint64_t>(g.M), 64, BT))
     return cudaErrorInvalidValue;
   static int sms = device_sm_count();
   if (g.wfmt == PF_W_Q1_G128) {
