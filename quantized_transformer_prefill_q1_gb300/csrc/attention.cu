@@ -12,7 +12,7 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
-#include "pf_internal.h"
+#include "ptx.cuh"
 
 namespace pf {
 namespace {
@@ -128,6 +128,8 @@ __global__ void __launch_bounds__(THREADS) attention_kernel(
   constexpr int TILE = BC * HD * 2;
   constexpr int CH = HD / 8;
 
+  griddep_launch_dependents();
+  griddep_wait();
   const int G = nq / nkv;
   const int BT = BR / G;  // tokens per CTA
   const int n_ttiles = (M + BT - 1) / BT;
@@ -291,11 +293,10 @@ cudaError_t launch_t(const pf_config& c, const void* q, const void* kc, const vo
   auto kern = attention_kernel<HD, T, KT>;
   dim3 grid((M + BT - 1) / BT, c.n_kv_heads);
   const float scale_log2 = 1.4426950408889634f / sqrtf(static_cast<float>(HD));
-  kern<<<grid, THREADS, smem, st>>>(reinterpret_cast<const T*>(q), reinterpret_cast<const KT*>(kc),
-                                    reinterpret_cast<const KT*>(vc), M, c.n_q_heads, c.n_kv_heads,
-                                    c.max_seq, layer, start_dev, start_host, scale_log2,
-                                    reinterpret_cast<__half*>(out));
-  return cudaGetLastError();
+  return launch_pdl(kern, grid, dim3(THREADS), static_cast<size_t>(smem), st,
+                    reinterpret_cast<const T*>(q), reinterpret_cast<const KT*>(kc),
+                    reinterpret_cast<const KT*>(vc), M, c.n_q_heads, c.n_kv_heads, c.max_seq, layer,
+                    start_dev, start_host, scale_log2, reinterpret_cast<__half*>(out));
 }
 
 template <int HD>

@@ -97,6 +97,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   auto k_tile = [&](int s) { return kv_s + (2 * s) * L::KV; };
   auto v_tile = [&](int s) { return kv_s + (2 * s + 1) * L::KV; };
 
+  griddep_launch_dependents();
+  griddep_wait();  // the start position and q / cache come from earlier kernels
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = nq / nkv;
   const int BT = TQ / G;  // tokens per CTA
@@ -365,10 +367,9 @@ cudaError_t launch_tc(const pf_config& c, const void* q, const void* kc, const v
     return cudaErrorInvalidValue;
   dim3 grid((M + BT - 1) / BT, c.n_kv_heads);
   const float scale_log2 = 1.4426950408889634f / sqrtf(static_cast<float>(HD));
-  attn_tc_kernel<HD, BF16><<<grid, THREADS, ASmem<HD>::BYTES, st>>>(
-      tq, tk, tv, M, c.n_q_heads, c.n_kv_heads, c.max_seq, layer, start_dev, start_host, scale_log2,
-      reinterpret_cast<__half*>(out), status);
-  return cudaGetLastError();
+  return launch_pdl(attn_tc_kernel<HD, BF16>, grid, dim3(THREADS), ASmem<HD>::BYTES, st, tq, tk, tv,
+                    M, c.n_q_heads, c.n_kv_heads, c.max_seq, layer, start_dev, start_host, scale_log2,
+                    reinterpret_cast<__half*>(out), status);
 }
 
 template <int HD, int BF16>

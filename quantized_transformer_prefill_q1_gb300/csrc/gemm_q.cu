@@ -154,6 +154,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  griddep_launch_dependents();
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -179,6 +180,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  griddep_wait();  // inputs come from the previous kernel in the stream
   const int G = K / GROUP;
 
   if (warp == 0) {
@@ -373,9 +375,8 @@ cudaError_t launch_t(const GemmArgs& g, const CUtensorMap& tm, int num_sms, cuda
   u.nkb_total = nkb;
   const int n_units = u.n_mt * u.n_nt * splits;
   const int grid = min(n_units, num_sms);
-  gemm_q_kernel<WFMT, EPI><<<grid, NUM_THREADS, smem, stream>>>(tm, g.w, g.M, g.N, g.K, g.out, u,
-                                                              n_units, splits > 1 ? 1 : 0, g.status);
-  return cudaGetLastError();
+  return launch_pdl(gemm_q_kernel<WFMT, EPI>, dim3(grid), dim3(NUM_THREADS), smem, stream, tm, g.w,
+                    g.M, g.N, g.K, g.out, u, n_units, splits > 1 ? 1 : 0, g.status);
 }
 
 }  // namespace

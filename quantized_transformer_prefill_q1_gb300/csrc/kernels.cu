@@ -36,6 +36,8 @@ __global__ void __launch_bounds__(256) rmsnorm_kernel(const float* __restrict__ 
                                                       const float* __restrict__ w, float eps,
                                                       int H, __half* __restrict__ y) {
   __shared__ float red[32];
+  griddep_launch_dependents();
+  griddep_wait();
   const int row = blockIdx.x;
   const float4* xr = reinterpret_cast<const float4*>(x + static_cast<size_t>(row) * H);
   const float4* w4 = reinterpret_cast<const float4*>(w);
@@ -56,6 +58,41 @@ __global__ void __launch_bounds__(256) rmsnorm_kernel(const float* __restrict__ 
   }
 }
 
+// Same, for H = 512 * NV: 128 threads per row, each holding NV float4 of the row in
+// registers, so the row is read from global memory once; one barrier for the reduction.
+template <int NV>
+__global__ void __launch_bounds__(128) rmsnorm_reg_kernel(const float* __restrict__ x,
+                                                          const float* __restrict__ w, float eps,
+                                                          int H, __half* __restrict__ y) {
+  __shared__ float red[4];
+  griddep_launch_dependents();
+  griddep_wait();
+  const int row = blockIdx.x;
+  const float4* xr = reinterpret_cast<const float4*>(x + static_cast<size_t>(row) * H);
+  float4 v[NV];
+  float ss = 0.f;
+#pragma unroll
+  for (int i = 0; i < NV; ++i) {
+    v[i] = xr[threadIdx.x + 128 * i];
+    ss += v[i].x * v[i].x + v[i].y * v[i].y + v[i].z * v[i].z + v[i].w * v[i].w;
+  }
+  ss = warp_sum(ss);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
+  __syncthreads();
+  ss = red[0] + red[1] + red[2] + red[3];
+  const float r = rsqrtf(ss / static_cast<float>(H) + eps);
+  const float4* w4 = reinterpret_cast<const float4*>(w);
+  uint2* yr = reinterpret_cast<uint2*>(y + static_cast<size_t>(row) * H);
+#pragma unroll
+  for (int i = 0; i < NV; ++i) {
+    const int idx = threadIdx.x + 128 * i;
+    const float4 g = w4[idx];
+    const __half2 a = __floats2half2_rn(v[i].x * r * g.x, v[i].y * r * g.y);
+    const __half2 b = __floats2half2_rn(v[i].z * r * g.z, v[i].w * r * g.w);
+    yr[idx] = make_uint2(*reinterpret_cast<const uint32_t*>(&a), *reinterpret_cast<const uint32_t*>(&b));
+  }
+}
+
 // ------------------------------------------------------------------ QK-norm + RoPE + KV
 template <typename T>
 __device__ __forceinline__ T to_elem(float v);
@@ -68,7 +105,28 @@ __device__ __forceinline__ __nv_bfloat16 to_elem<__nv_bfloat16>(float v) {
   return __float2bfloat16_rn(v);
 }
 
-// One warp per (token, head) of the fused QKV output, heads ordered Q | K | V.
+template <typename T>
+__device__ __forceinline__ void store4(T* dst, float a, float b, float c, float d);
+template <>
+__device__ __forceinline__ void store4<float>(float* dst, float a, float b, float c, float d) {
+  *reinterpret_cast<float4*>(dst) = make_float4(a, b, c, d);
+}
+template <>
+__device__ __forceinline__ void store4<__half>(__half* dst, float a, float b, float c, float d) {
+  const __half2 x = __floats2half2_rn(a, b), y = __floats2half2_rn(c, d);
+  *reinterpret_cast<uint2*>(dst) =
+      make_uint2(*reinterpret_cast<const uint32_t*>(&x), *reinterpret_cast<const uint32_t*>(&y));
+}
+template <>
+__device__ __forceinline__ void store4<__nv_bfloat16>(__nv_bfloat16* dst, float a, float b, float c,
+                                                      float d) {
+  const __nv_bfloat162 x = __floats2bfloat162_rn(a, b), y = __floats2bfloat162_rn(c, d);
+  *reinterpret_cast<uint2*>(dst) =
+      make_uint2(*reinterpret_cast<const uint32_t*>(&x), *reinterpret_cast<const uint32_t*>(&y));
+}
+
+// One group of HD/8 lanes per (token, head) of the fused QKV output, heads ordered
+// Q | K | V; lane l holds elements 4l..4l+3 of each half of the head (128-bit loads).
 // metal_prefill.rs `encode_layer_prefill` section 3 (fused_qk_norm, fused_qk_rope,
 // fused_kv_store) and metal_full_layer.rs `dispatch_fused_qk_norm_rope`, batched over the
 // chunk: Q and K heads get an RMSNorm over head_dim (weights w_q / w_k, the layer eps)
@@ -83,69 +141,60 @@ __global__ void __launch_bounds__(256) qk_norm_rope_kv_kernel(
     const int* __restrict__ start_dev, int start_host, float eps, int qk_norm,
     QT* __restrict__ q_out, KT* __restrict__ kc, KT* __restrict__ vc) {
   constexpr int HALF = HD / 2;
-  constexpr int E = HALF / 32;  // elements per lane in each half
+  constexpr int LPH = HALF / 4;   // lanes per head
+  constexpr int HPW = 32 / LPH;   // heads per warp
+  griddep_launch_dependents();
+  griddep_wait();
   const int heads = nq + 2 * nkv;
   const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
-  const int t = gw / heads;
-  const int j = gw - t * heads;
-  if (t >= M) return;
+  const int l = lane % LPH;
+  const int gh = gw * HPW + lane / LPH;  // (token, head) index
+  const int t = gh / heads;
+  const int j = gh - t * heads;
+  const bool valid = t < M;
   const int start = start_dev ? *start_dev : start_host;
   const int pos = start + t;
-  const float* src = qkv + (static_cast<size_t>(t) * heads + j) * HD;
-  float a[E], b[E];
-#pragma unroll
-  for (int e = 0; e < E; ++e) {
-    a[e] = src[lane * E + e];
-    b[e] = src[HALF + lane * E + e];
+  float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a;
+  if (valid) {
+    const float4* src = reinterpret_cast<const float4*>(qkv + (static_cast<size_t>(t) * heads + j) * HD);
+    a = src[l];
+    b = src[LPH + l];
   }
-  if (j >= nq + nkv) {  // V head: straight to the cache
-    const int kvh = j - nq - nkv;
-    KT* dst = vc + ((static_cast<size_t>(layer) * nkv + kvh) * max_seq + pos) * HD;
+  // per-head sum of squares over the LPH lanes of the group (every lane takes part)
+  float ss = a.x * a.x + a.y * a.y + a.z * a.z + a.w * a.w + b.x * b.x + b.y * b.y + b.z * b.z + b.w * b.w;
 #pragma unroll
-    for (int e = 0; e < E; ++e) {
-      dst[lane * E + e] = to_elem<KT>(a[e]);
-      dst[HALF + lane * E + e] = to_elem<KT>(b[e]);
-    }
+  for (int o = LPH / 2; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+  if (!valid) return;
+  if (j >= nq + nkv) {  // V head: straight to the cache
+    KT* dst = vc + ((static_cast<size_t>(layer) * nkv + (j - nq - nkv)) * max_seq + pos) * HD;
+    store4<KT>(dst + 4 * l, a.x, a.y, a.z, a.w);
+    store4<KT>(dst + HALF + 4 * l, b.x, b.y, b.z, b.w);
     return;
   }
   const bool is_q = j < nq;
   if (qk_norm) {
-    float ss = 0.f;
-#pragma unroll
-    for (int e = 0; e < E; ++e) ss += a[e] * a[e] + b[e] * b[e];
-    ss = warp_sum(ss);
     const float r = rsqrtf(ss / static_cast<float>(HD) + eps);
-    const float* w = is_q ? qn : kn;
-#pragma unroll
-    for (int e = 0; e < E; ++e) {
-      a[e] = a[e] * r * w[lane * E + e];
-      b[e] = b[e] * r * w[HALF + lane * E + e];
-    }
+    const float4 wa = reinterpret_cast<const float4*>(is_q ? qn : kn)[l];
+    const float4 wb = reinterpret_cast<const float4*>(is_q ? qn : kn)[LPH + l];
+    a = make_float4(a.x * r * wa.x, a.y * r * wa.y, a.z * r * wa.z, a.w * r * wa.w);
+    b = make_float4(b.x * r * wb.x, b.y * r * wb.y, b.z * r * wb.z, b.w * r * wb.w);
   }
-  const float2* cs = reinterpret_cast<const float2*>(rope) + static_cast<size_t>(pos) * HALF;
-  float ra[E], rb[E];
-#pragma unroll
-  for (int e = 0; e < E; ++e) {
-    const float2 c = cs[lane * E + e];  // (cos, sin)
-    ra[e] = a[e] * c.x - b[e] * c.y;
-    rb[e] = b[e] * c.x + a[e] * c.y;
-  }
+  // (cos, sin) of pairs 4l .. 4l+3 at this position
+  const float4* cs = reinterpret_cast<const float4*>(rope + (static_cast<size_t>(pos) * HALF + 4 * l) * 2);
+  const float4 c01 = cs[0], c23 = cs[1];
+  const float ra0 = a.x * c01.x - b.x * c01.y, rb0 = b.x * c01.x + a.x * c01.y;
+  const float ra1 = a.y * c01.z - b.y * c01.w, rb1 = b.y * c01.z + a.y * c01.w;
+  const float ra2 = a.z * c23.x - b.z * c23.y, rb2 = b.z * c23.x + a.z * c23.y;
+  const float ra3 = a.w * c23.z - b.w * c23.w, rb3 = b.w * c23.z + a.w * c23.w;
   if (is_q) {
     QT* dst = q_out + (static_cast<size_t>(t) * nq + j) * HD;
-#pragma unroll
-    for (int e = 0; e < E; ++e) {
-      dst[lane * E + e] = to_elem<QT>(ra[e]);
-      dst[HALF + lane * E + e] = to_elem<QT>(rb[e]);
-    }
+    store4<QT>(dst + 4 * l, ra0, ra1, ra2, ra3);
+    store4<QT>(dst + HALF + 4 * l, rb0, rb1, rb2, rb3);
   } else {
-    const int kvh = j - nq;
-    KT* dst = kc + ((static_cast<size_t>(layer) * nkv + kvh) * max_seq + pos) * HD;
-#pragma unroll
-    for (int e = 0; e < E; ++e) {
-      dst[lane * E + e] = to_elem<KT>(ra[e]);
-      dst[HALF + lane * E + e] = to_elem<KT>(rb[e]);
-    }
+    KT* dst = kc + ((static_cast<size_t>(layer) * nkv + (j - nq)) * max_seq + pos) * HD;
+    store4<KT>(dst + 4 * l, ra0, ra1, ra2, ra3);
+    store4<KT>(dst + HALF + 4 * l, rb0, rb1, rb2, rb3);
   }
 }
 
@@ -156,6 +205,8 @@ __global__ void __launch_bounds__(256) embed_kernel(const float* __restrict__ E,
                                                     const int* __restrict__ tokens, int H,
                                                     int vocab, float* __restrict__ x,
                                                     int* __restrict__ status) {
+  griddep_launch_dependents();
+  griddep_wait();
   const int t = blockIdx.x;
   const int id = tokens[t];
   float4* dst = reinterpret_cast<float4*>(x + static_cast<size_t>(t) * H);
@@ -180,6 +231,8 @@ __global__ void __launch_bounds__(256) lm_head_kernel(const float* __restrict__ 
                                                       int H, float* __restrict__ logits) {
   extern __shared__ float ys[];  // [H] normalised row, then [H/128] group sums
   __shared__ float red[32];
+  griddep_launch_dependents();
+  griddep_wait();
   float ss = 0.f;
   for (int i = threadIdx.x; i < H; i += blockDim.x) {
     const float v = x_row[i];
@@ -257,6 +310,8 @@ __global__ void __launch_bounds__(256) lm_head_kernel(const float* __restrict__ 
 // matching up columns. out[m, f] = silu(gate) * up, f16.
 __global__ void swiglu_f32_kernel(const float* __restrict__ gu, int M, int I,
                                   __half* __restrict__ out) {
+  griddep_launch_dependents();
+  griddep_wait();
   const size_t idx = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (idx >= static_cast<size_t>(M) * I) return;
   const int m = static_cast<int>(idx / I);
@@ -297,12 +352,16 @@ __global__ void __launch_bounds__(256) dequant_kernel(const uint8_t* __restrict_
   for (int j = 0; j < 4; ++j) dst[j] = make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
 }
 
-__global__ void set_int_kernel(int* dst, int v) { *dst = v; }
+__global__ void set_int_kernel(int* dst, int v) {
+  griddep_launch_dependents();
+  griddep_wait(); *dst = v; }
 
 // Exercises the bounded wait every pipelined kernel uses: one mbarrier expecting one
 // arrival; with `arrive` set a thread provides it, otherwise nothing ever does and the
 // wait must give up after limit_ns and record PF_ERR_DEVICE_TIMEOUT.
 __global__ void wait_selftest_kernel(int* status, long long limit_ns, int arrive) {
+  griddep_launch_dependents();
+  griddep_wait();
   __shared__ __align__(8) uint64_t bar;
   __shared__ int abort_flag;
   const uint32_t b = smem_u32(&bar);
@@ -323,9 +382,19 @@ __global__ void wait_selftest_kernel(int* status, long long limit_ns, int arrive
 
 cudaError_t launch_rmsnorm(const float* x, const float* w, float eps, int M, int H, void* y,
                            cudaStream_t stream) {
+  __half* yh = reinterpret_cast<__half*>(y);
+  if (H % 512 == 0) {
+    switch (H / 512) {
+      case 1: return launch_pdl(rmsnorm_reg_kernel<1>, dim3(M), dim3(128), 0, stream, x, w, eps, H, yh);
+      case 2: return launch_pdl(rmsnorm_reg_kernel<2>, dim3(M), dim3(128), 0, stream, x, w, eps, H, yh);
+      case 4: return launch_pdl(rmsnorm_reg_kernel<4>, dim3(M), dim3(128), 0, stream, x, w, eps, H, yh);
+      case 8: return launch_pdl(rmsnorm_reg_kernel<8>, dim3(M), dim3(128), 0, stream, x, w, eps, H, yh);
+      case 16: return launch_pdl(rmsnorm_reg_kernel<16>, dim3(M), dim3(128), 0, stream, x, w, eps, H, yh);
+      default: break;
+    }
+  }
   const int threads = H / 4 >= 256 ? 256 : ((H / 4 + 31) / 32) * 32;
-  rmsnorm_kernel<<<M, threads, 0, stream>>>(x, w, eps, H, reinterpret_cast<__half*>(y));
-  return cudaGetLastError();
+  return launch_pdl(rmsnorm_kernel, dim3(M), dim3(threads), 0, stream, x, w, eps, H, yh);
 }
 
 template <int HD, typename QT, typename KT>
@@ -333,12 +402,13 @@ static void qk_launch(const pf_config& c, const float* qkv, const float* qn, con
                       const float* rope, int layer, const int* start_dev, int start_host, int M,
                       void* q, void* kc, void* vc, cudaStream_t stream) {
   const int heads = c.n_q_heads + 2 * c.n_kv_heads;
-  const long long warps = static_cast<long long>(M) * heads;
+  constexpr int HPW = 32 / (HD / 8);
+  const long long warps = (static_cast<long long>(M) * heads + HPW - 1) / HPW;
   const int blocks = static_cast<int>((warps * 32 + 255) / 256);
-  qk_norm_rope_kv_kernel<HD, QT, KT><<<blocks, 256, 0, stream>>>(
-      qkv, qn, kn, rope, M, c.n_q_heads, c.n_kv_heads, c.max_seq, layer, start_dev, start_host,
-      c.eps, c.qk_norm, reinterpret_cast<QT*>(q), reinterpret_cast<KT*>(kc),
-      reinterpret_cast<KT*>(vc));
+  launch_pdl(qk_norm_rope_kv_kernel<HD, QT, KT>, dim3(blocks), dim3(256), 0, stream, qkv, qn, kn,
+             rope, M, c.n_q_heads, c.n_kv_heads, c.max_seq, layer, start_dev, start_host, c.eps,
+             c.qk_norm, reinterpret_cast<QT*>(q), reinterpret_cast<KT*>(kc),
+             reinterpret_cast<KT*>(vc));
 }
 
 template <int HD>
@@ -373,8 +443,7 @@ cudaError_t launch_qk_norm_rope_kv(const pf_config& c, const float* qkv, const f
 
 cudaError_t launch_embed(const float* E, const int* tokens, int M, int H, int vocab, float* x,
                          int* status, cudaStream_t stream) {
-  embed_kernel<<<M, 256, 0, stream>>>(E, tokens, H, vocab, x, status);
-  return cudaGetLastError();
+  return launch_pdl(embed_kernel, dim3(M), dim3(256), 0, stream, E, tokens, H, vocab, x, status);
 }
 
 cudaError_t launch_lm_head(int wfmt, const float* x_row, const float* norm_w, float eps,
@@ -386,22 +455,22 @@ cudaError_t launch_lm_head(int wfmt, const float* x_row, const float* norm_w, fl
     if (smem > 48 * 1024)
       cudaFuncSetAttribute(lm_head_kernel<PF_W_Q1_G128>,
                            cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-    lm_head_kernel<PF_W_Q1_G128><<<tiles, 256, smem, stream>>>(x_row, norm_w, eps, packed, vocab,
-                                                              H, logits);
+    launch_pdl(lm_head_kernel<PF_W_Q1_G128>, dim3(tiles), dim3(256), smem, stream, x_row, norm_w,
+               eps, packed, vocab, H, logits);
   } else {
     if (smem > 48 * 1024)
       cudaFuncSetAttribute(lm_head_kernel<PF_W_INT4_AFFINE_G128>,
                            cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-    lm_head_kernel<PF_W_INT4_AFFINE_G128><<<tiles, 256, smem, stream>>>(x_row, norm_w, eps,
-                                                                       packed, vocab, H, logits);
+    launch_pdl(lm_head_kernel<PF_W_INT4_AFFINE_G128>, dim3(tiles), dim3(256), smem, stream, x_row,
+               norm_w, eps, packed, vocab, H, logits);
   }
   return cudaGetLastError();
 }
 
 cudaError_t launch_swiglu_f32(const float* gu, int M, int I, void* out, cudaStream_t stream) {
   const size_t n = static_cast<size_t>(M) * I;
-  swiglu_f32_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, stream>>>(
-      gu, M, I, reinterpret_cast<__half*>(out));
+  launch_pdl(swiglu_f32_kernel, dim3(static_cast<unsigned>((n + 255) / 256)), dim3(256), 0, stream,
+             gu, M, I, reinterpret_cast<__half*>(out));
   return cudaGetLastError();
 }
 
@@ -418,8 +487,7 @@ cudaError_t launch_dequant(int wfmt, const uint8_t* packed, int64_t N, int64_t K
 }
 
 cudaError_t launch_set_int(int* dst, int value, cudaStream_t stream) {
-  set_int_kernel<<<1, 1, 0, stream>>>(dst, value);
-  return cudaGetLastError();
+  return launch_pdl(set_int_kernel, dim3(1), dim3(1), 0, stream, dst, value);
 }
 
 cudaError_t launch_wait_selftest(int* status, long long limit_ns, int arrive, cudaStream_t stream) {

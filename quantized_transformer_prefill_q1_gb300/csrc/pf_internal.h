@@ -2,6 +2,7 @@
 #pragma once
 #include <cstddef>
 #include <cstdint>
+#include <utility>
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -83,6 +84,23 @@ cudaError_t launch_lm_head(int wfmt, const float* x_row, const float* norm_w, fl
 cudaError_t launch_swiglu_f32(const float* gu, int M, int I, void* out_f16, cudaStream_t stream);
 cudaError_t launch_set_int(int* dst, int value, cudaStream_t stream);
 cudaError_t launch_wait_selftest(int* status, long long limit_ns, int arrive, cudaStream_t stream);
+
+// Launches `kern` with programmatic stream serialisation (see griddep_wait in ptx.cuh).
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t stream, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
 
 int device_sm_count();
 // Tiled tensor map over a 16-bit (bf16 if `bf16`, else f16) array of `rank` dims

@@ -19,6 +19,18 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
   return t;
 }
 
+// ------------------------------------------------------------------ programmatic launch
+// Kernels are launched with programmatic stream serialisation: the next kernel in the
+// stream may start once every CTA of this one has called griddep_launch_dependents(), and
+// it must call griddep_wait() before its first global-memory access (read or write); the
+// wait returns once the previous kernel has completed and its writes are visible.
+__device__ __forceinline__ void griddep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ------------------------------------------------------------------ mbarrier
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
