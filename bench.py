@@ -51,10 +51,11 @@ def parse():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--seed", type=int, default=0)
     p.add_argument("--case", default=None,
-                   choices=["gemm_gate_up", "gemm_qkv", "gemm_down", "attention", "rmsnorm",
+                   choices=["gemm_gate_up", "gemm_qkv", "gemm_down", "gemm_o", "attention", "rmsnorm",
                             "qk_rope_kv", "lm_head"],
                    help="small single-kernel case at the workload's shapes (for ncu captures)")
     p.add_argument("--reps", type=int, default=3)
+    p.add_argument("--split", type=int, default=0, help="GEMM cases: K splits (0 = the library's choice)")
     return p.parse_args()
 
 
@@ -73,12 +74,13 @@ def run_case(args):
     cfg = pf.make_config(s, CHUNK, n_layers=1)
     if args.case.startswith("gemm"):
         n, k, epi = {"gemm_gate_up": (2 * I, H, pf.EPI_SWIGLU), "gemm_qkv": (s.qkv_rows, H, pf.EPI_STORE_F32),
-                     "gemm_down": (H, I, pf.EPI_RESID_ADD)}[args.case]
+                     "gemm_down": (H, I, pf.EPI_RESID_ADD),
+                     "gemm_o": (H, s.n_q_heads * s.head_dim, pf.EPI_RESID_ADD)}[args.case]
         a = dev(rng.standard_normal((M, k)).astype(np.float16))
         w = dev(pf.pf_pack_weights_host(synth.q1_weight(rng, n, k), epi == pf.EPI_SWIGLU))
         out = torch.zeros((M, n // 2 if epi == pf.EPI_SWIGLU else n),
                           dtype=torch.float16 if epi == pf.EPI_SWIGLU else torch.float32, device="cuda")
-        split = 1 if epi != pf.EPI_STORE_F32 else 0
+        split = args.split
         fn = lambda: pf.pf_op_gemm(pf.W_Q1, epi, a, w, M, n, k, out, split)  # noqa: E731
         flops = 2 * M * n * k
     elif args.case == "attention":
@@ -120,7 +122,7 @@ def run_case(args):
     e1.record()
     e1.synchronize()
     us = e0.elapsed_time(e1) / args.reps * 1e3
-    line = {"case": args.case, "us_per_launch": us}
+    line = {"case": args.case, "us_per_launch": us, "split": args.split}
     if flops:
         line["tflops"] = flops / us / 1e6
     print(json.dumps(line), flush=True)
