@@ -55,6 +55,14 @@ __device__ __forceinline__ void st_shared_v4a(uint32_t addr, uint32_t a, uint32_
                : "memory");
 }
 
+// 2^x with the hardware approximation (relative error ~2^-22; subnormal results flush to
+// zero, which for probabilities below 2^-126 is immaterial).
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 template <int BF16>
 __device__ __forceinline__ uint32_t pack_pair(float a, float b) {
   if (BF16) {
@@ -229,18 +237,24 @@ __global__ void __launch_bounds__(THREADS, 1)
       tc_fence_after();
       const uint32_t sbuf = tmem + lane_off + s * TK;
       const int kbase = j * TK;
-      float mx = -INFINITY;
-#pragma unroll 1
-      for (int c = 0; c < TK / 32; ++c) {
-        uint32_t v[32];
-        tmem_ld_32x32b_x32(sbuf + 32 * c, v);
-        tmem_ld_wait();
+      // the whole S row of this tile, read from TMEM once
+      uint32_t v[TK];
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const float x = (kbase + 32 * c + e <= pos) ? __uint_as_float(v[e]) * scale_log2 : -INFINITY;
-          mx = fmaxf(mx, x);
-        }
+      for (int c = 0; c < TK / 32; ++c)
+        tmem_ld_32x32b_x32(sbuf + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(v + 32 * c));
+      tmem_ld_wait();
+      // a tile wholly at or below the CTA's first position needs no causal mask
+      const bool diag = kbase + TK - 1 > start + t0;
+      float mraw = -INFINITY;
+      if (diag) {
+#pragma unroll
+        for (int e = 0; e < TK; ++e)
+          if (kbase + e <= pos) mraw = fmaxf(mraw, __uint_as_float(v[e]));
+      } else {
+#pragma unroll
+        for (int e = 0; e < TK; ++e) mraw = fmaxf(mraw, __uint_as_float(v[e]));
       }
+      const float mx = mraw * scale_log2;  // scale > 0 keeps the order
       const bool need = j > 0 && mx > m + RESCALE_LOG2;
       if (j == 0) {
         m = mx;  // key 0 is visible to every row, so this is finite
@@ -257,12 +271,12 @@ __global__ void __launch_bounds__(THREADS, 1)
         tc_fence_after();
 #pragma unroll 1
         for (int c = 0; c < HD / 32; ++c) {
-          uint32_t v[32];
-          tmem_ld_32x32b_x32(tmem_o + lane_off + 32 * c, v);
+          uint32_t o[32];
+          tmem_ld_32x32b_x32(tmem_o + lane_off + 32 * c, o);
           tmem_ld_wait();
 #pragma unroll
-          for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
-          tmem_st_32x32b_x32(tmem_o + lane_off + 32 * c, v);
+          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+          tmem_st_32x32b_x32(tmem_o + lane_off + 32 * c, o);
         }
         tmem_st_wait();
         if (need) m = mx;
@@ -272,29 +286,26 @@ __global__ void __launch_bounds__(THREADS, 1)
         break;
       }
       const uint32_t pbuf = p_s + s * L::P;
+      const float neg_m = -m;
       float rs = 0.f;
-#pragma unroll 1
-      for (int c = 0; c < TK / 32; ++c) {
-        uint32_t v[32];
-        tmem_ld_32x32b_x32(sbuf + 32 * c, v);
-        tmem_ld_wait();
-        uint32_t pk[16];
 #pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          const int kj = kbase + 32 * c + e;
-          const float p0 = (kj <= pos) ? exp2f(__uint_as_float(v[e]) * scale_log2 - m) : 0.f;
-          const float p1 = (kj + 1 <= pos) ? exp2f(__uint_as_float(v[e + 1]) * scale_log2 - m) : 0.f;
+      for (int ch = 0; ch < TK / 8; ++ch) {  // 16-B chunks of 8 keys
+        uint32_t pk[4];
+#pragma unroll
+        for (int e = 0; e < 8; e += 2) {
+          const int x = 8 * ch + e;
+          float p0 = ex2_approx(fmaf(__uint_as_float(v[x]), scale_log2, neg_m));
+          float p1 = ex2_approx(fmaf(__uint_as_float(v[x + 1]), scale_log2, neg_m));
+          if (diag) {
+            p0 = (kbase + x <= pos) ? p0 : 0.f;
+            p1 = (kbase + x + 1 <= pos) ? p1 : 0.f;
+          }
           rs += p0 + p1;
           pk[e >> 1] = pack_pair<BF16>(p0, p1);
         }
-        // keys 32c .. 32c+31 of this row: K-atom (c >> 1), chunks (c & 1) * 4 + 0..3
-        const uint32_t row_base = pbuf + (c >> 1) * (TQ * 128) + r * 128;
-#pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-          const int ch = (c & 1) * 4 + q4;
-          st_shared_v4a(row_base + ((ch ^ (r & 7)) << 4), pk[4 * q4], pk[4 * q4 + 1],
-                        pk[4 * q4 + 2], pk[4 * q4 + 3]);
-        }
+        // keys 8ch .. 8ch+7 of this row: K-atom (ch >> 3), chunk ch & 7 within it
+        const uint32_t row_base = pbuf + (ch >> 3) * (TQ * 128) + r * 128;
+        st_shared_v4a(row_base + (((ch & 7) ^ (r & 7)) << 4), pk[0], pk[1], pk[2], pk[3]);
       }
       l += rs;
       tc_fence_before();
