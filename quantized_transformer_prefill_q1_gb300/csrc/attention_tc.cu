@@ -245,15 +245,20 @@ __global__ void __launch_bounds__(THREADS, 1)
       tmem_ld_wait();
       // a tile wholly at or below the CTA's first position needs no causal mask
       const bool diag = kbase + TK - 1 > start + t0;
-      float mraw = -INFINITY;
+      // eight independent partial maxima (short dependency chains), then a tree
+      float mp[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) mp[i] = -INFINITY;
       if (diag) {
 #pragma unroll
         for (int e = 0; e < TK; ++e)
-          if (kbase + e <= pos) mraw = fmaxf(mraw, __uint_as_float(v[e]));
+          if (kbase + e <= pos) mp[e & 7] = fmaxf(mp[e & 7], __uint_as_float(v[e]));
       } else {
 #pragma unroll
-        for (int e = 0; e < TK; ++e) mraw = fmaxf(mraw, __uint_as_float(v[e]));
+        for (int e = 0; e < TK; ++e) mp[e & 7] = fmaxf(mp[e & 7], __uint_as_float(v[e]));
       }
+      const float mraw = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
+                               fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7])));
       const float mx = mraw * scale_log2;  // scale > 0 keeps the order
       const bool need = j > 0 && mx > m + RESCALE_LOG2;
       if (j == 0) {
@@ -287,7 +292,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
       const uint32_t pbuf = p_s + s * L::P;
       const float neg_m = -m;
-      float rs = 0.f;
+      float rsp[4] = {0.f, 0.f, 0.f, 0.f};  // independent partial row sums
 #pragma unroll
       for (int ch = 0; ch < TK / 8; ++ch) {  // 16-B chunks of 8 keys
         uint32_t pk[4];
@@ -300,14 +305,14 @@ __global__ void __launch_bounds__(THREADS, 1)
             p0 = (kbase + x <= pos) ? p0 : 0.f;
             p1 = (kbase + x + 1 <= pos) ? p1 : 0.f;
           }
-          rs += p0 + p1;
+          rsp[e >> 1] += p0 + p1;
           pk[e >> 1] = pack_pair<BF16>(p0, p1);
         }
         // keys 8ch .. 8ch+7 of this row: K-atom (ch >> 3), chunk ch & 7 within it
         const uint32_t row_base = pbuf + (ch >> 3) * (TQ * 128) + r * 128;
         st_shared_v4a(row_base + (((ch & 7) ^ (r & 7)) << 4), pk[0], pk[1], pk[2], pk[3]);
       }
-      l += rs;
+      l += (rsp[0] + rsp[1]) + (rsp[2] + rsp[3]);
       tc_fence_before();
       mbar_arrive(s_empty(s));
       if (j == n_tiles - 1 && kbase + r >= kv_len) {
