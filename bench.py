@@ -55,7 +55,7 @@ def parse():
                             "qk_rope_kv", "lm_head"],
                    help="small single-kernel case at the workload's shapes (for ncu captures)")
     p.add_argument("--reps", type=int, default=3)
-    p.add_argument("--split", type=int, default=0, help="GEMM cases: K splits (0 = the library's choice)")
+    p.add_argument("--ctas", type=int, default=0, help="GEMM cases: most persistent CTAs (0 = the library's choice)")
     return p.parse_args()
 
 
@@ -80,8 +80,8 @@ def run_case(args):
         w = dev(pf.pf_pack_weights_host(synth.q1_weight(rng, n, k), epi == pf.EPI_SWIGLU))
         out = torch.zeros((M, n // 2 if epi == pf.EPI_SWIGLU else n),
                           dtype=torch.float16 if epi == pf.EPI_SWIGLU else torch.float32, device="cuda")
-        split = args.split
-        fn = lambda: pf.pf_op_gemm(pf.W_Q1, epi, a, w, M, n, k, out, split)  # noqa: E731
+        scratch = pf.gemm_scratch(M, n, args.ctas)
+        fn = lambda: pf.pf_op_gemm(pf.W_Q1, epi, a, w, M, n, k, out, scratch, args.ctas)  # noqa: E731
         flops = 2 * M * n * k
     elif args.case == "attention":
         start = PROMPT - CHUNK
@@ -122,7 +122,7 @@ def run_case(args):
     e1.record()
     e1.synchronize()
     us = e0.elapsed_time(e1) / args.reps * 1e3
-    line = {"case": args.case, "us_per_launch": us, "split": args.split}
+    line = {"case": args.case, "us_per_launch": us, "ctas": args.ctas}
     if flops:
         line["tflops"] = flops / us / 1e6
     print(json.dumps(line), flush=True)

@@ -238,13 +238,22 @@ pf_status pf_op_rmsnorm(const float* x_dev, const float* w_dev, float eps, int32
 pf_status pf_op_dequant(int32_t wfmt, const void* packed_dev, int64_t N, int64_t K,
                         uint16_t* w_f16_dev, void* stream);
 /* Quantised GEMM out[m, n] (+)= sum_k a[m, k] w[n, k] on the tensor cores.
- * a: f16 [M, K] row-major; epilogue: 0 = store f32 out[M, N] (ld = N),
+ * a: f16 [M, K] row-major; out 16-B aligned; epilogue: 0 = store f32 out[M, N] (ld = N),
  * 1 = residual add into f32 out[M, N] (out += a W^T), 2 = SwiGLU of an interleaved
- * gate_up weight: out f16 [M, N/2] = silu(gate) * up. split_k >= 1 (0 = automatic;
- * epilogue 0 with split_k > 1 requires out zeroed beforehand; epilogue 2 forces 1). */
+ * gate_up weight: out f16 [M, N/2] = silu(gate) * up (N = 2I, I % 128 == 0).
+ * The 128 x 256 output tiles' k-blocks are shared out evenly over at most max_ctas
+ * persistent CTAs (0 = 160; never more than the SM count; 1..160 accepted). With
+ * epilogue 1 every CTA adds its share of a tile into out; with epilogues 0 and 2 a tile
+ * split between CTAs is summed through scratch_dev (device, 16-B aligned, at least
+ * pf_gemm_scratch_bytes(M, N, max_ctas) bytes, owned by the caller, required for every
+ * epilogue): its trailing per-tile counters must be zero before the first call, and each
+ * call that completes leaves them zero; after PF_ERR_DEVICE_TIMEOUT zero them again.
+ * Calls sharing one scratch must not overlap in time (same stream, or ordered). */
+size_t pf_gemm_scratch_bytes(int32_t M, int32_t N, int32_t max_ctas);
 pf_status pf_op_gemm(int32_t wfmt, int32_t epilogue, const uint16_t* a_f16_dev,
                      const void* packed_dev, int32_t M, int32_t N, int32_t K, void* out_dev,
-                     int32_t split_k, int32_t* status_dev, void* stream);
+                     int32_t max_ctas, void* scratch_dev, size_t scratch_bytes,
+                     int32_t* status_dev, void* stream);
 /* Fused per-head QK RMSNorm + RoPE + KV store ([P1] section 3 fused_qk_norm /
  * fused_qk_rope / fused_kv_store; [P2] dispatch_fused_qk_norm_rope): from qkv f32
  * [M, (nq+2nkv) hd], writes q_dev [M, nq, hd] (bf16 when kv_dtype is bf16, else f16)

@@ -3,23 +3,37 @@
 // out[m, n] (+)= sum_k a[m, k] * w[n, k] with a = f16 activations [M, K] (the RMSNorm /
 // SwiGLU / attention outputs) and w a packed Q1 or INT4-affine weight [N, K]. This is
 // the batched projection of oxibonsai-kernels metal_prefill.rs `encode_layer_prefill`:
-// section 2 (QKV GEMM, plain store), sections 4 and 7 (O / down GEMM with the residual
-// add fused, `dispatch_gemm_q1_v7_residual`) and section 6 (gate+up GEMM with SwiGLU
-// fused, `dispatch_fused_gate_up_swiglu_gemm`).
+// section 2 (QKV GEMM), sections 4 and 7 (O / down GEMM with the residual add fused,
+// `dispatch_gemm_q1_v7_residual`) and section 6 (gate+up GEMM with SwiGLU fused,
+// `dispatch_fused_gate_up_swiglu_gemm`).
 //
-// Persistent CTAs (one per SM) walk a list of work units = (128-token tile, 256-row
-// weight tile, K split). Warp roles:
-//   warp 0       TMA producer: activation tile (128 x 64 f16, 128-B swizzle) and the
-//                stage's packed weight block (bulk copy) into a ring of stages;
-//   warps 6..13  dequantise the packed block (one weight row per thread) into a 256 x 64
-//                f16 K-major tile in the same swizzled layout: the UMMA B operand;
-//   warp 1       allocates 512 TMEM columns (two 128 x 256 f32 accumulators) and one lane
-//                issues tcgen05.mma (M=128, N=256, K=16) x 4 per stage, committing each
-//                stage back to the ring and each finished unit to the epilogue;
-//   warps 2..5   epilogue: tcgen05.ld of the finished accumulator (f32 store / residual
-//                add / SwiGLU), overlapping the next unit's main loop in the other buffer.
+// Tiles are 128 tokens x 256 weight rows. The k-blocks (64 wide) of all tiles form one
+// list cut into equal contiguous ranges, one per persistent CTA ("stream-K"), so that no
+// SM idles while others finish a last round of tiles. The part of a tile inside one
+// CTA's range is a segment; a CTA runs its (at most two) partial segments first and its
+// whole tiles after them, so that split tiles complete early.
+//   * residual epilogue: every segment adds its accumulator into out with a TMA
+//     reduce-add (out += partial), whole or not; the order of the f32 additions varies.
+//   * store / SwiGLU epilogues: a whole tile is stored directly. A split tile is finished
+//     by the contributor that arrives last: the others store their partial accumulators
+//     in scratch and bump the tile's arrival counter; the last one adds them to its own,
+//     applies the epilogue and resets the counter. No CTA ever waits for another.
+//
+// Warp roles:
+//   warp 0      TMA producer: activation tile (128 x 64 f16, 128-B swizzle) and the
+//               stage's packed weight block (bulk copy) into a ring of stages;
+//   warps 6..13 dequantise the packed block (one weight row per thread) into a 256 x 64
+//               f16 K-major tile in the same swizzled layout: the UMMA B operand;
+//   warp 1      allocates 512 TMEM columns (two 128 x 256 f32 accumulators) and one lane
+//               issues tcgen05.mma (M=128, N=256, K=16) x 4 per stage, committing each
+//               stage back to the ring and each finished segment to the epilogue;
+//   warps 2..5  epilogue: tcgen05.ld of 32 rows x 32 columns at a time into registers,
+//               then through a per-warp shared staging tile to global memory by TMA
+//               (coalesced whole lines), overlapping the next segment's main loop.
 // Q1 weights are +-scale, exact in f16, so the f16 tensor-core operand loses nothing.
 #include <cuda_fp16.h>
+
+#include <algorithm>
 
 #include "dequant.cuh"
 #include "ptx.cuh"
@@ -38,7 +52,9 @@ constexpr int NUM_THREADS = 32 * (2 + NUM_EPI_WARPS + NUM_DQ_WARPS);  // 448
 constexpr int FIRST_DQ_WARP = 2 + NUM_EPI_WARPS;
 constexpr int A_STAGE = BM * BK * 2;  // 16 KB
 constexpr int B_STAGE = BN * BK * 2;  // 32 KB
-constexpr int TMEM_COLS = 512;        // two accumulators of 256 f32 columns
+constexpr int STG_BYTES = 32 * 32 * 4;  // per epilogue warp: 32 rows x 32 f32
+constexpr int TMEM_COLS = 512;          // two accumulators of 256 f32 columns
+constexpr size_t SLOT_FLOATS = static_cast<size_t>(BM) * BN;  // one partial tile
 static_assert(DQ_THREADS == BN, "one dequantising thread per weight row");
 
 template <int WFMT>
@@ -63,10 +79,16 @@ struct Fmt<PF_W_INT4_AFFINE_G128> {
 };
 
 template <int WFMT>
-constexpr int smem_bytes() {
-  return 1024 /*alignment slack*/ + Fmt<WFMT>::STAGES * (A_STAGE + B_STAGE + Fmt<WFMT>::P_STAGE) +
-         256 /*barriers and flags*/;
+constexpr int ring_bytes() {
+  return Fmt<WFMT>::STAGES * (A_STAGE + B_STAGE + Fmt<WFMT>::P_STAGE);
 }
+template <int WFMT>
+constexpr int smem_bytes() {
+  return 1024 /*alignment*/ + (ring_bytes<WFMT>() + 1023) / 1024 * 1024 +
+         NUM_EPI_WARPS * STG_BYTES + 256 /*barriers and flags*/;
+}
+static_assert(smem_bytes<PF_W_Q1_G128>() <= 232448, "Q1 GEMM shared memory");
+static_assert(smem_bytes<PF_W_INT4_AFFINE_G128>() <= 232448, "INT4 GEMM shared memory");
 
 // Bounded wait that ignores the abort flag (used while draining after an abort).
 __device__ __forceinline__ void mbar_wait_drain(uint32_t bar, uint32_t parity) {
@@ -83,6 +105,22 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
                "r"(d)
                : "memory");
+}
+
+__device__ __forceinline__ void named_bar_sync(int id, int threads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+// Barrier over `threads` threads that returns whether `pred` held in all of them.
+__device__ __forceinline__ bool named_bar_and(int id, int threads, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.and.pred q, %2, %3, p;\n"
+      " selp.u32 %0, 1, 0, q;\n}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(threads)
+      : "memory");
+  return r != 0;
 }
 
 // One weight row's 64 weights of a stage (packed block p) -> 8 16-B chunks of f16 in the
@@ -113,24 +151,75 @@ __device__ __forceinline__ void dequant_row_smem(const uint8_t* p, int r, uint32
   }
 }
 
-struct Units {
-  int n_mt, n_nt, per_split, nkb_total;
-  __device__ __forceinline__ void decode(int u, int& mt, int& nt, int& kb0, int& nkb) const {
-    const int tiles = n_mt * n_nt;
-    const int split = u / tiles;
-    const int r = u - split * tiles;
-    nt = r / n_mt;
-    mt = r - nt * n_mt;  // token tiles fastest: neighbouring CTAs share a weight tile
-    kb0 = split * per_split;
-    nkb = min(nkb_total, kb0 + per_split) - kb0;
+// ------------------------------------------------------------------ stream-K partition
+// n_mt x n_nt tiles of kbt k-blocks each, `total` k-blocks in all; CTA c owns
+// [total c / ctas, total (c + 1) / ctas).
+struct Plan {
+  int n_mt, n_nt, kbt;
+  long long total;
+  int ctas;
+  __device__ __forceinline__ long long begin(int c) const { return total * c / ctas; }
+  // CTA whose range holds k-block w
+  __device__ __forceinline__ int owner(long long w) const {
+    return static_cast<int>(((w + 1) * ctas - 1) / total);
+  }
+  // scratch slot (0 or 1) of contributor c's partial for `tile`: 0 if c's range begins
+  // inside the tile, 1 if it begins at or before the tile's start
+  __device__ __forceinline__ int slot(int c, int tile) const {
+    return begin(c) > static_cast<long long>(tile) * kbt ? 0 : 1;
   }
 };
 
+struct Segment {
+  int tile, mt, nt, kb0, nkb;
+  bool whole;
+};
+
+// The segments of one CTA's range in processing order: the partial first and last
+// segments (if any) come first, then the whole tiles in k order.
+struct Range {
+  long long b, e;
+  int t0, n, first_part, last_part;
+  __device__ __forceinline__ Range(const Plan& p, int c) {
+    b = p.begin(c);
+    e = p.begin(c + 1);
+    t0 = static_cast<int>(b / p.kbt);
+    const int t1 = static_cast<int>((e - 1) / p.kbt);
+    n = t1 - t0 + 1;
+    const long long s0_end = std::min<long long>(e, static_cast<long long>(t0 + 1) * p.kbt);
+    first_part = (b == static_cast<long long>(t0) * p.kbt && s0_end - b == p.kbt) ? 0 : 1;
+    last_part = (n > 1 && e != static_cast<long long>(t1 + 1) * p.kbt) ? 1 : 0;
+  }
+  __device__ __forceinline__ Segment at(const Plan& p, int k) const {
+    const int i = k < first_part ? 0 : (k < first_part + last_part ? n - 1 : k - last_part);
+    Segment s;
+    s.tile = t0 + i;
+    const long long ts = static_cast<long long>(s.tile) * p.kbt;
+    const long long lo = std::max(b, ts), hi = std::min(e, ts + p.kbt);
+    s.kb0 = static_cast<int>(lo - ts);
+    s.nkb = static_cast<int>(hi - lo);
+    s.whole = s.nkb == p.kbt;
+    s.nt = s.tile / p.n_mt;
+    s.mt = s.tile - s.nt * p.n_mt;  // token tiles fastest: neighbouring tiles share weights
+    return s;
+  }
+};
+
+// Staging tile of one epilogue warp, f32 32 x 32 in the TMA 128-B swizzle: row r at
+// r * 128, 16-B unit j at (j ^ (r % 8)) * 16 (a warp's store of unit j hits all banks).
+__device__ __forceinline__ void stage_f32(uint32_t stg, int r, const uint32_t (&v)[32]) {
+#pragma unroll
+  for (int j = 0; j < 8; ++j)
+    st_shared_v4(stg + r * 128 + ((j ^ (r & 7)) << 4), v[4 * j], v[4 * j + 1], v[4 * j + 2],
+                 v[4 * j + 3]);
+}
+
 template <int WFMT, int EPI>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
-    gemm_q_kernel(const __grid_constant__ CUtensorMap tmap_a, const uint8_t* __restrict__ wpk,
-                  int M, int N, int K, void* __restrict__ out, Units units, int n_units,
-                  int atomic_out, int* __restrict__ status) {
+    gemm_q_kernel(const __grid_constant__ CUtensorMap tmap_a,
+                  const __grid_constant__ CUtensorMap tmap_out, const uint8_t* __restrict__ wpk,
+                  int M, int N, int K, Plan plan, float* __restrict__ scratch,
+                  int* __restrict__ counters, int* __restrict__ status) {
   using F = Fmt<WFMT>;
   constexpr int S = F::STAGES;
   extern __shared__ uint8_t smem_raw[];
@@ -141,7 +230,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const uint32_t b_st = a_st + S * A_STAGE;
   const uint32_t p_st = b_st + S * B_STAGE;
   const uint8_t* p_gen = gbase + (p_st - base);
-  const uint32_t bar0 = p_st + S * F::P_STAGE;
+  const uint32_t stg0 = base + (ring_bytes<WFMT>() + 1023) / 1024 * 1024;
+  const uint32_t bar0 = stg0 + NUM_EPI_WARPS * STG_BYTES;
   // barriers: full[S], bfull[S], empty[S], acc_full[2], acc_empty[2], drain; then flags
   auto full = [&](int s) { return bar0 + 8u * s; };
   auto bfull = [&](int s) { return bar0 + 8u * (S + s); };
@@ -151,6 +241,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const uint32_t drain_bar = bar0 + 8u * (3 * S + 4);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + (drain_bar + 8u - base));
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + (drain_bar + 16u - base));
+  volatile int* flags = reinterpret_cast<volatile int*>(gbase + (drain_bar + 24u - base));  // [4]
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -182,27 +273,27 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const uint32_t tmem_base = *tmem_slot;
   griddep_wait();  // inputs come from the previous kernel in the stream
   const int G = K / GROUP;
+  const Range rg(plan, blockIdx.x);
 
   if (warp == 0) {
     // ---------------------------------------------------------------- TMA producer
     if (lane == 0) {
       int it = 0;
       bool ok = true;
-      for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
-        int mt, nt, kb0, nkb;
-        units.decode(u, mt, nt, kb0, nkb);
-        for (int i = 0; i < nkb; ++i, ++it) {
+      for (int k = 0; k < rg.n && ok; ++k) {
+        const Segment sg = rg.at(plan, k);
+        for (int i = 0; i < sg.nkb; ++i, ++it) {
           const int s = it % S;
           const uint32_t ph = (it / S) & 1;
           if (!mbar_wait(empty(s), ph ^ 1, abort_flag)) {
             ok = false;
             break;
           }
-          const int kb = kb0 + i;
+          const int kb = sg.kb0 + i;
           const uint8_t* chunk =
-              wpk + (static_cast<size_t>(nt) * G + (kb >> 1)) * static_cast<size_t>(F::CHUNK);
+              wpk + (static_cast<size_t>(sg.nt) * G + (kb >> 1)) * static_cast<size_t>(F::CHUNK);
           mbar_arrive_expect_tx(full(s), A_STAGE + F::P_STAGE);
-          tma_load_2d(a_st + s * A_STAGE, &tmap_a, kb * BK, mt * BM, full(s));
+          tma_load_2d(a_st + s * A_STAGE, &tmap_a, kb * BK, sg.mt * BM, full(s));
           bulk_load(p_st + s * F::P_STAGE, chunk + (kb & 1) * F::HALF, F::HALF, full(s));
           bulk_load(p_st + s * F::P_STAGE + F::HALF, chunk + F::META_OFF, F::META, full(s));
         }
@@ -215,26 +306,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // ---------------------------------------------------------------- MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_f16(BM, BN, 0);
-      int it = 0, local = 0;
+      int it = 0;
       bool ok = true;
-      for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++local) {
-        int mt, nt, kb0, nkb;
-        units.decode(u, mt, nt, kb0, nkb);
-        const int b = local & 1;
-        const uint32_t use = static_cast<uint32_t>(local >> 1);
+      for (int k = 0; k < rg.n && ok; ++k) {
+        const Segment sg = rg.at(plan, k);
+        const int b = k & 1;
+        const uint32_t use = static_cast<uint32_t>(k >> 1);
         if (!mbar_wait(acc_empty(b), (use & 1) ^ 1, abort_flag)) {
           ok = false;
           break;
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + b * BN;
-        for (int i = 0; i < nkb; ++i, ++it) {
+        for (int i = 0; i < sg.nkb; ++i, ++it) {
           const int s = it % S;
           const uint32_t ph = (it / S) & 1;
-          if (!(mbar_wait(bfull(s), ph, abort_flag) && mbar_wait(full(s), ph, abort_flag))) {
-            ok = false;
-            break;
-          }
+          ok = mbar_wait(bfull(s), ph, abort_flag) && mbar_wait(full(s), ph, abort_flag);
+          if (!ok) break;
           tc_fence_after();
           const uint64_t ad = sdesc_kmajor_sw128(a_st + s * A_STAGE);
           const uint64_t bd = sdesc_kmajor_sw128(b_st + s * B_STAGE);
@@ -255,51 +343,146 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int d = threadIdx.x - FIRST_DQ_WARP * 32;  // weight row of the tile
     int it = 0;
     bool ok = true;
-    for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
-      int mt, nt, kb0, nkb;
-      units.decode(u, mt, nt, kb0, nkb);
-      for (int i = 0; i < nkb; ++i, ++it) {
+    for (int k = 0; k < rg.n && ok; ++k) {
+      const Segment sg = rg.at(plan, k);
+      for (int i = 0; i < sg.nkb; ++i, ++it) {
         const int s = it % S;
         const uint32_t ph = (it / S) & 1;
         if (!mbar_wait(full(s), ph, abort_flag)) {
           ok = false;
           break;
         }
-        const uint8_t* p = p_gen + s * F::P_STAGE;
-        const uint32_t bt = b_st + s * B_STAGE;
-        dequant_row_smem<WFMT>(p, d, bt);
+        dequant_row_smem<WFMT>(p_gen + s * F::P_STAGE, d, b_st + s * B_STAGE);
         fence_proxy_async_smem();
         mbar_arrive(bfull(s));
       }
     }
   } else {
     // ---------------------------------------------------------------- epilogue (warps 2..5)
-    const int q = warp & 3;  // TMEM lane quarter this warp may read
-    int local = 0;
-    for (int u = blockIdx.x; u < n_units; u += gridDim.x, ++local) {
-      int mt, nt, kb0, nkb;
-      units.decode(u, mt, nt, kb0, nkb);
-      const int b = local & 1;
-      const uint32_t use = static_cast<uint32_t>(local >> 1);
-      // warp-uniform: the tcgen05.ld below is warp-collective
-      if (!__all_sync(0xffffffffu, mbar_wait(acc_full(b), use & 1, abort_flag))) break;
+    const int q = warp & 3;           // TMEM lane quarter this warp may read
+    const int et = threadIdx.x - 64;  // 0..127
+    const uint32_t stg = stg0 + q * STG_BYTES;
+    // hands the staging tile (after its 32 x 32 values were written) to TMA
+    auto stage_out = [&](int x, int y) {
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        if (EPI == EPI_RESID_ADD)
+          tma_reduce_add_2d(&tmap_out, stg, x, y);
+        else
+          tma_store_2d(&tmap_out, stg, x, y);
+        bulk_commit();
+      }
+    };
+    // the previous TMA store has finished reading the staging tile
+    auto stage_free = [&]() {
+      if (lane == 0) bulk_wait_read0();
+      __syncwarp();
+    };
+    for (int k = 0; k < rg.n; ++k) {
+      const Segment sg = rg.at(plan, k);
+      const int b = k & 1;
+      const uint32_t use = static_cast<uint32_t>(k >> 1);
+      // uniform over the four epilogue warps: tcgen05.ld is warp-collective and the partial
+      // hand-off synchronises the four warps
+      const bool got = mbar_wait(acc_full(b), use & 1, abort_flag);
+      if (!named_bar_and(1, EPI_THREADS, got)) break;
       tc_fence_after();
-      const int row = mt * BM + 32 * q + lane;
+      const int row0 = sg.mt * BM + 32 * q;  // first row of this warp's quarter
+      const int lrow = 32 * q + lane;        // row within the tile
+      const bool valid = row0 + lane < M;
       const uint32_t tb = tmem_base + b * BN + (static_cast<uint32_t>(32 * q) << 16);
-      if (EPI == EPI_SWIGLU) {
-        // each 128 columns of the tile: 64 gate columns, then the 64 matching up columns
-        const int NO = N >> 1;
-        __half* o = reinterpret_cast<__half*>(out);
+
+      if (EPI == EPI_RESID_ADD) {
+        // out += this segment's partial sum, whole tile or not
 #pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
-          const int h = c >> 1, q2 = c & 1;  // 128-column half, 32-column quarter of its gates
-          uint32_t g[32], v[32];
-          tmem_ld_32x32b_x32(tb + 128 * h + 32 * q2, g);
-          tmem_ld_32x32b_x32(tb + 128 * h + 64 + 32 * q2, v);
+        for (int c = 0; c < BN / 32; ++c) {
+          uint32_t v[32];
+          tmem_ld_32x32b_x32(tb + 32 * c, v);
           tmem_ld_wait();
-          const int col = nt * 128 + 64 * h + 32 * q2;
-          if (row < M && col < NO) {
-            uint4* dst = reinterpret_cast<uint4*>(o + static_cast<size_t>(row) * NO + col);
+          stage_free();
+          stage_f32(stg, lane, v);
+          stage_out(sg.nt * BN + 32 * c, row0);
+        }
+      } else {
+        // ---- a tile split across CTAs: hand the partial off, or finish the tile if last.
+        // Partials are float4 [chunk 0..7][j 0..7][tile row 0..127]: a warp's store or load
+        // of one (chunk, j) covers 512 contiguous bytes.
+        bool finish = sg.whole;
+        int c_lo = 0, c_hi = -1;
+        if (!sg.whole) {
+          c_lo = plan.owner(static_cast<long long>(sg.tile) * plan.kbt);
+          c_hi = plan.owner(static_cast<long long>(sg.tile + 1) * plan.kbt - 1);
+          const int others = c_hi - c_lo;  // contributors besides this CTA
+          const int slot = plan.slot(blockIdx.x, sg.tile);
+          volatile int* flag = flags + 2 * slot;  // each slot serves one segment only
+          // if every other contributor has arrived already, finish without storing
+          if (et == 0) flag[0] = ld_acquire_gpu(counters + sg.tile) == others ? 1 : 0;
+          named_bar_sync(1, EPI_THREADS);
+          finish = flag[0] != 0;
+          if (!finish) {
+            float4* mine = reinterpret_cast<float4*>(scratch) +
+                           (static_cast<size_t>(blockIdx.x) * 2 + slot) * (SLOT_FLOATS / 4) + lrow;
+#pragma unroll 1
+            for (int c = 0; c < BN / 32; ++c) {
+              uint32_t v[32];
+              tmem_ld_32x32b_x32(tb + 32 * c, v);
+              tmem_ld_wait();
+              if (valid) {
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                  __stcg(mine + (c * 8 + j) * BM,
+                         make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
+                                     __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3])));
+              }
+            }
+            __threadfence();
+            named_bar_sync(1, EPI_THREADS);
+            if (et == 0) flag[1] = atomicAdd(counters + sg.tile, 1) == others ? 1 : 0;
+            named_bar_sync(1, EPI_THREADS);
+            finish = flag[1] != 0;
+          }
+          if (finish) {
+            if (et == 0) counters[sg.tile] = 0;  // every contributor is in: ready for reuse
+            __threadfence();
+          }
+        }
+        // adds the other contributors' partials of 32-column chunk `chunk` of this row to v
+        auto add_partials = [&](uint32_t (&v)[32], int chunk) {
+          for (int c = c_lo; c <= c_hi; ++c) {
+            if (c == static_cast<int>(blockIdx.x)) continue;
+            const float4* src = reinterpret_cast<const float4*>(scratch) +
+                                (static_cast<size_t>(c) * 2 + plan.slot(c, sg.tile)) * (SLOT_FLOATS / 4) +
+                                lrow;
+            float4 x[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) x[j] = __ldcg(src + (chunk * 8 + j) * BM);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              v[4 * j] = __float_as_uint(__uint_as_float(v[4 * j]) + x[j].x);
+              v[4 * j + 1] = __float_as_uint(__uint_as_float(v[4 * j + 1]) + x[j].y);
+              v[4 * j + 2] = __float_as_uint(__uint_as_float(v[4 * j + 2]) + x[j].z);
+              v[4 * j + 3] = __float_as_uint(__uint_as_float(v[4 * j + 3]) + x[j].w);
+            }
+          }
+        };
+
+        if (finish && EPI == EPI_SWIGLU) {
+          // each 128 columns of the tile: 64 gate columns, then the 64 matching up columns;
+          // out f16 32 x 32 staged in the 64-B swizzle (row r at r * 64, unit j at
+          // (j ^ ((r / 2) % 4)) * 16)
+#pragma unroll 1
+          for (int c = 0; c < 4; ++c) {
+            const int h = c >> 1, q2 = c & 1;
+            uint32_t g[32], u[32];
+            tmem_ld_32x32b_x32(tb + 128 * h + 32 * q2, g);
+            tmem_ld_32x32b_x32(tb + 128 * h + 64 + 32 * q2, u);
+            tmem_ld_wait();
+            if (!sg.whole && valid) {
+              add_partials(g, 4 * h + q2);
+              add_partials(u, 4 * h + 2 + q2);
+            }
+            stage_free();
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
               uint32_t pk[4];
@@ -307,49 +490,32 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               for (int e = 0; e < 4; ++e) {
                 const int x = 8 * j + 2 * e;
                 const __half2 hv = __floats2half2_rn(
-                    silu_mul(__uint_as_float(g[x]), __uint_as_float(v[x])),
-                    silu_mul(__uint_as_float(g[x + 1]), __uint_as_float(v[x + 1])));
+                    silu_mul(__uint_as_float(g[x]), __uint_as_float(u[x])),
+                    silu_mul(__uint_as_float(g[x + 1]), __uint_as_float(u[x + 1])));
                 pk[e] = *reinterpret_cast<const uint32_t*>(&hv);
               }
-              dst[j] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+              st_shared_v4(stg + lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4), pk[0], pk[1], pk[2], pk[3]);
             }
+            stage_out(sg.nt * 128 + 64 * h + 32 * q2, row0);
           }
-        }
-      } else {
-        float* o = reinterpret_cast<float*>(out);
+        } else if (finish) {
 #pragma unroll 1
-        for (int c = 0; c < 8; ++c) {
-          uint32_t v[32];
-          tmem_ld_32x32b_x32(tb + 32 * c, v);
-          tmem_ld_wait();
-          const int col = nt * BN + 32 * c;
-          if (row < M) {
-            float4* dst = reinterpret_cast<float4*>(o + static_cast<size_t>(row) * N + col);
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              if (col + 4 * j >= N) break;
-              const float4 val = make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
-                                             __uint_as_float(v[4 * j + 2]),
-                                             __uint_as_float(v[4 * j + 3]));
-              if (atomic_out) {
-                atomicAdd(dst + j, val);
-              } else if (EPI == EPI_RESID_ADD) {
-                float4 x = dst[j];
-                x.x += val.x;
-                x.y += val.y;
-                x.z += val.z;
-                x.w += val.w;
-                dst[j] = x;
-              } else {
-                dst[j] = val;
-              }
-            }
+          for (int c = 0; c < BN / 32; ++c) {
+            uint32_t v[32];
+            tmem_ld_32x32b_x32(tb + 32 * c, v);
+            tmem_ld_wait();
+            if (!sg.whole && valid) add_partials(v, c);
+            stage_free();
+            stage_f32(stg, lane, v);
+            stage_out(sg.nt * BN + 32 * c, row0);
           }
         }
       }
       tc_fence_before();
       mbar_arrive(acc_empty(b));
     }
+    if (lane == 0) bulk_wait0();  // TMA writes complete before the CTA retires
+    __syncwarp();
   }
 
   tc_fence_before();
@@ -363,20 +529,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 }
 
 template <int WFMT, int EPI>
-cudaError_t launch_t(const GemmArgs& g, const CUtensorMap& tm, int num_sms, cudaStream_t stream) {
+cudaError_t launch_t(const GemmArgs& g, const CUtensorMap& ta, const CUtensorMap& to, int num_sms,
+                     cudaStream_t stream) {
   constexpr int smem = smem_bytes<WFMT>();
-  const int nkb = g.K / BK;
-  const int split = EPI == EPI_SWIGLU ? 1 : max(1, min(g.split_k, nkb));
-  Units u;
-  u.per_split = (nkb + split - 1) / split;
-  const int splits = (nkb + u.per_split - 1) / u.per_split;
-  u.n_mt = (g.M + BM - 1) / BM;
-  u.n_nt = static_cast<int>(padded_rows(g.N) / TILE_N);
-  u.nkb_total = nkb;
-  const int n_units = u.n_mt * u.n_nt * splits;
-  const int grid = min(n_units, num_sms);
-  return launch_pdl(gemm_q_kernel<WFMT, EPI>, dim3(grid), dim3(NUM_THREADS), smem, stream, tm, g.w,
-                    g.M, g.N, g.K, g.out, u, n_units, splits > 1 ? 1 : 0, g.status);
+  Plan p;
+  p.n_mt = (g.M + BM - 1) / BM;
+  p.n_nt = static_cast<int>(padded_rows(g.N) / TILE_N);
+  p.kbt = g.K / BK;
+  p.total = static_cast<long long>(p.n_mt) * p.n_nt * p.kbt;
+  p.ctas = static_cast<int>(std::min<long long>(std::min(g.max_ctas, num_sms), p.total));
+  float* scratch = reinterpret_cast<float*>(g.scratch);
+  int* counters = reinterpret_cast<int*>(scratch + static_cast<size_t>(2) * g.max_ctas * SLOT_FLOATS);
+  return launch_pdl(gemm_q_kernel<WFMT, EPI>, dim3(p.ctas), dim3(NUM_THREADS), smem, stream, ta, to,
+                    g.w, g.M, g.N, g.K, p, scratch, counters, g.status);
 }
 
 }  // namespace
@@ -384,28 +549,12 @@ cudaError_t launch_t(const GemmArgs& g, const CUtensorMap& tm, int num_sms, cuda
 bool encode_tmap_f16_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
                         uint32_t box_inner, uint32_t box_outer);
 
-// Split along K when that shortens the critical path: cost = rounds of units per SM x
-// k-blocks per unit (+ a fixed per-unit overhead), with persistent CTAs.
-int choose_split_k(int M, int N, int K, int epilogue, int num_sms) {
-  if (epilogue == EPI_SWIGLU) return 1;
-  const int tiles = static_cast<int>(padded_rows(N) / TILE_N) * ((M + BM - 1) / BM);
-  const int nkb = K / BK;
-  int best = 1;
-  double best_cost = 1e30;
-  for (int s = 1; s <= 16 && s <= nkb / 4; ++s) {
-    const int per = (nkb + s - 1) / s;
-    const int splits = (nkb + per - 1) / per;
-    const int rounds = (tiles * splits + num_sms - 1) / num_sms;
-    // each extra split adds an f32 atomic reduction of the M x N output; measured on
-    // GB300 at ~1.6e-6 k-block-times per output byte and split
-    const double atomics = splits > 1 ? splits * static_cast<double>(M) * N * 1.6e-6 : 0.0;
-    const double cost = rounds * (per + 3.0) + atomics;
-    if (cost < best_cost - 1e-9) {
-      best_cost = cost;
-      best = s;
-    }
-  }
-  return best;
+// Scratch of a launch with at most max_ctas CTAs: two partial tiles per CTA (a CTA's range
+// begins and ends inside at most two tiles), then one arrival counter per output tile, which
+// must be zero before the first launch (every launch that completes leaves them zero).
+size_t gemm_scratch_bytes(int M, int N, int max_ctas) {
+  const size_t tiles = static_cast<size_t>((M + BM - 1) / BM) * (padded_rows(N) / TILE_N);
+  return static_cast<size_t>(2) * max_ctas * SLOT_FLOATS * sizeof(float) + tiles * sizeof(int);
 }
 
 template <int WFMT, int EPI>
@@ -427,21 +576,26 @@ cudaError_t prepare_gemm_kernels() {
 }
 
 cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t stream) {
-  CUtensorMap tm;
-  if (!encode_tmap_f16_2d(&tm, g.a, static_cast<uint64_t>(g.K), static_cast<uint64_t>(g.M), BK, BM))
+  CUtensorMap ta, to;
+  if (!encode_tmap_f16_2d(&ta, g.a, static_cast<uint64_t>(g.K), static_cast<uint64_t>(g.M), BK, BM))
+    return cudaErrorInvalidValue;
+  const bool swiglu = g.epilogue == EPI_SWIGLU;
+  // 32 x 32 output boxes: f32 rows of 128 B (128-B swizzle) or f16 rows of 64 B (64-B swizzle)
+  if (!encode_tmap_out_2d(&to, !swiglu, g.out, static_cast<uint64_t>(swiglu ? g.N / 2 : g.N),
+                          static_cast<uint64_t>(g.M), 32, 32, swiglu ? 64 : 128))
     return cudaErrorInvalidValue;
   static int sms = device_sm_count();
   if (g.wfmt == PF_W_Q1_G128) {
     switch (g.epilogue) {
-      case EPI_STORE_F32: return launch_t<PF_W_Q1_G128, EPI_STORE_F32>(g, tm, sms, stream);
-      case EPI_RESID_ADD: return launch_t<PF_W_Q1_G128, EPI_RESID_ADD>(g, tm, sms, stream);
-      case EPI_SWIGLU: return launch_t<PF_W_Q1_G128, EPI_SWIGLU>(g, tm, sms, stream);
+      case EPI_STORE_F32: return launch_t<PF_W_Q1_G128, EPI_STORE_F32>(g, ta, to, sms, stream);
+      case EPI_RESID_ADD: return launch_t<PF_W_Q1_G128, EPI_RESID_ADD>(g, ta, to, sms, stream);
+      case EPI_SWIGLU: return launch_t<PF_W_Q1_G128, EPI_SWIGLU>(g, ta, to, sms, stream);
     }
   } else {
     switch (g.epilogue) {
-      case EPI_STORE_F32: return launch_t<PF_W_INT4_AFFINE_G128, EPI_STORE_F32>(g, tm, sms, stream);
-      case EPI_RESID_ADD: return launch_t<PF_W_INT4_AFFINE_G128, EPI_RESID_ADD>(g, tm, sms, stream);
-      case EPI_SWIGLU: return launch_t<PF_W_INT4_AFFINE_G128, EPI_SWIGLU>(g, tm, sms, stream);
+      case EPI_STORE_F32: return launch_t<PF_W_INT4_AFFINE_G128, EPI_STORE_F32>(g, ta, to, sms, stream);
+      case EPI_RESID_ADD: return launch_t<PF_W_INT4_AFFINE_G128, EPI_RESID_ADD>(g, ta, to, sms, stream);
+      case EPI_SWIGLU: return launch_t<PF_W_INT4_AFFINE_G128, EPI_SWIGLU>(g, ta, to, sms, stream);
     }
   }
   return cudaErrorInvalidValue;

@@ -136,9 +136,9 @@ __device__ __forceinline__ void store4<__nv_bfloat16>(__nv_bfloat16* dst, float 
 // [n_layers][nkv][max_seq][hd].
 template <int HD, typename QT, typename KT>
 __global__ void __launch_bounds__(256) qk_norm_rope_kv_kernel(
-    const float* __restrict__ qkv, const float* __restrict__ qn, const float* __restrict__ kn,
+    float* qkv, const float* __restrict__ qn, const float* __restrict__ kn,
     const float* __restrict__ rope, int M, int nq, int nkv, int max_seq, int layer,
-    const int* __restrict__ start_dev, int start_host, float eps, int qk_norm,
+    const int* __restrict__ start_dev, int start_host, float eps, int qk_norm, int zero_qkv,
     QT* __restrict__ q_out, KT* __restrict__ kc, KT* __restrict__ vc) {
   constexpr int HALF = HD / 2;
   constexpr int LPH = HALF / 4;   // lanes per head
@@ -157,9 +157,13 @@ __global__ void __launch_bounds__(256) qk_norm_rope_kv_kernel(
   const int pos = start + t;
   float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a;
   if (valid) {
-    const float4* src = reinterpret_cast<const float4*>(qkv + (static_cast<size_t>(t) * heads + j) * HD);
+    float4* src = reinterpret_cast<float4*>(qkv + (static_cast<size_t>(t) * heads + j) * HD);
     a = src[l];
     b = src[LPH + l];
+    if (zero_qkv) {  // leave the rows zero for the next projection, which accumulates into them
+      src[l] = make_float4(0.f, 0.f, 0.f, 0.f);
+      src[LPH + l] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
   }
   // per-head sum of squares over the LPH lanes of the group (every lane takes part)
   float ss = a.x * a.x + a.y * a.y + a.z * a.z + a.w * a.w + b.x * b.x + b.y * b.y + b.z * b.z + b.w * b.w;
@@ -304,25 +308,6 @@ __global__ void __launch_bounds__(256) lm_head_kernel(const float* __restrict__ 
   if (row < vocab) logits[row] = acc;
 }
 
-// ------------------------------------------------------------------ split-K SwiGLU
-// Used when the gate_up GEMM is split along K (small chunks): gu holds the f32 GEMM
-// output in packed-row order, where each 128-column tile is 64 gate columns then the 64
-// matching up columns. out[m, f] = silu(gate) * up, f16.
-__global__ void swiglu_f32_kernel(const float* __restrict__ gu, int M, int I,
-                                  __half* __restrict__ out) {
-  griddep_launch_dependents();
-  griddep_wait();
-  const size_t idx = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (idx >= static_cast<size_t>(M) * I) return;
-  const int m = static_cast<int>(idx / I);
-  const int f = static_cast<int>(idx - static_cast<size_t>(m) * I);
-  const int t = f >> 6, r = f & 63;
-  const size_t ld = 2 * static_cast<size_t>(I);
-  const float g = gu[m * ld + t * 128 + r];
-  const float u = gu[m * ld + t * 128 + 64 + r];
-  out[idx] = __float2half_rn(g / (1.0f + __expf(-g)) * u);
-}
-
 // ------------------------------------------------------------------ dequant (test)
 // Runs the GEMM's own dequantisers (dq_q1_32 / dq_i4_32) on every 32-weight run of the
 // packed tensor and writes w [N, K] f16 row-major. One thread per (row, 32-k run).
@@ -400,30 +385,31 @@ cudaError_t launch_rmsnorm(const float* x, const float* w, float eps, int M, int
 template <int HD, typename QT, typename KT>
 static void qk_launch(const pf_config& c, const float* qkv, const float* qn, const float* kn,
                       const float* rope, int layer, const int* start_dev, int start_host, int M,
-                      void* q, void* kc, void* vc, cudaStream_t stream) {
+                      void* q, void* kc, void* vc, int zero_qkv, cudaStream_t stream) {
   const int heads = c.n_q_heads + 2 * c.n_kv_heads;
   constexpr int HPW = 32 / (HD / 8);
   const long long warps = (static_cast<long long>(M) * heads + HPW - 1) / HPW;
   const int blocks = static_cast<int>((warps * 32 + 255) / 256);
-  launch_pdl(qk_norm_rope_kv_kernel<HD, QT, KT>, dim3(blocks), dim3(256), 0, stream, qkv, qn, kn,
-             rope, M, c.n_q_heads, c.n_kv_heads, c.max_seq, layer, start_dev, start_host, c.eps,
-             c.qk_norm, reinterpret_cast<QT*>(q), reinterpret_cast<KT*>(kc),
+  // qkv is written only when zero_qkv is set, i.e. when the caller owns it as scratch
+  launch_pdl(qk_norm_rope_kv_kernel<HD, QT, KT>, dim3(blocks), dim3(256), 0, stream,
+             const_cast<float*>(qkv), qn, kn, rope, M, c.n_q_heads, c.n_kv_heads, c.max_seq, layer,
+             start_dev, start_host, c.eps, c.qk_norm, zero_qkv, reinterpret_cast<QT*>(q), reinterpret_cast<KT*>(kc),
              reinterpret_cast<KT*>(vc));
 }
 
 template <int HD>
 static void qk_dispatch_kv(const pf_config& c, const float* qkv, const float* qn, const float* kn,
                            const float* rope, int layer, const int* sd, int sh, int M, void* q,
-                           void* kc, void* vc, cudaStream_t st) {
+                           void* kc, void* vc, int z, cudaStream_t st) {
   switch (c.kv_dtype) {
     case PF_KV_BF16:
-      qk_launch<HD, __nv_bfloat16, __nv_bfloat16>(c, qkv, qn, kn, rope, layer, sd, sh, M, q, kc, vc, st);
+      qk_launch<HD, __nv_bfloat16, __nv_bfloat16>(c, qkv, qn, kn, rope, layer, sd, sh, M, q, kc, vc, z, st);
       break;
     case PF_KV_F16:
-      qk_launch<HD, __half, __half>(c, qkv, qn, kn, rope, layer, sd, sh, M, q, kc, vc, st);
+      qk_launch<HD, __half, __half>(c, qkv, qn, kn, rope, layer, sd, sh, M, q, kc, vc, z, st);
       break;
     default:
-      qk_launch<HD, __half, float>(c, qkv, qn, kn, rope, layer, sd, sh, M, q, kc, vc, st);
+      qk_launch<HD, __half, float>(c, qkv, qn, kn, rope, layer, sd, sh, M, q, kc, vc, z, st);
       break;
   }
 }
@@ -431,13 +417,13 @@ static void qk_dispatch_kv(const pf_config& c, const float* qkv, const float* qn
 cudaError_t launch_qk_norm_rope_kv(const pf_config& c, const float* qkv, const float* q_norm,
                                    const float* k_norm, const float* rope, int layer,
                                    const int* start_dev, int start_host, int M, void* q_out,
-                                   void* k_cache, void* v_cache, cudaStream_t stream) {
+                                   void* k_cache, void* v_cache, int zero_qkv, cudaStream_t stream) {
   if (c.head_dim == 128)
     qk_dispatch_kv<128>(c, qkv, q_norm, k_norm, rope, layer, start_dev, start_host, M, q_out,
-                        k_cache, v_cache, stream);
+                        k_cache, v_cache, zero_qkv, stream);
   else
     qk_dispatch_kv<64>(c, qkv, q_norm, k_norm, rope, layer, start_dev, start_host, M, q_out,
-                       k_cache, v_cache, stream);
+                       k_cache, v_cache, zero_qkv, stream);
   return cudaGetLastError();
 }
 
@@ -464,13 +450,6 @@ cudaError_t launch_lm_head(int wfmt, const float* x_row, const float* norm_w, fl
     launch_pdl(lm_head_kernel<PF_W_INT4_AFFINE_G128>, dim3(tiles), dim3(256), smem, stream, x_row,
                norm_w, eps, packed, vocab, H, logits);
   }
-  return cudaGetLastError();
-}
-
-cudaError_t launch_swiglu_f32(const float* gu, int M, int I, void* out, cudaStream_t stream) {
-  const size_t n = static_cast<size_t>(M) * I;
-  launch_pdl(swiglu_f32_kernel, dim3(static_cast<unsigned>((n + 255) / 256)), dim3(256), 0, stream,
-             gu, M, I, reinterpret_cast<__half*>(out));
   return cudaGetLastError();
 }
 

@@ -49,7 +49,7 @@ size_t kv_elem_bytes(int kv_dtype) { return kv_dtype == PF_KV_F32 ? 4 : 2; }
 
 // ------------------------------------------------------------------ workspace layout
 struct WsLayout {
-  size_t status, params, tokens, x, y, qkv, q, attn, act, gu, rope, total;
+  size_t status, params, tokens, x, y, qkv, q, attn, act, logits, gemm, gemm_bytes, rope, total;
 };
 
 WsLayout ws_layout(const pf_config& c) {
@@ -72,7 +72,11 @@ WsLayout ws_layout(const pf_config& c) {
   L.q = take(C * c.n_q_heads * hd * 2);
   L.attn = take(C * c.n_q_heads * hd * 2);
   L.act = take(C * I * 2);
-  L.gu = take(C * 2 * I * 4);
+  L.logits = take(static_cast<size_t>(c.vocab > 0 ? c.vocab : 1) * 4);
+  // GEMM scratch sized for the widest projection of a full chunk
+  const int widest = static_cast<int>(std::max<size_t>({qkv_rows, H, 2 * I}));
+  L.gemm_bytes = gemm_scratch_bytes(c.max_chunk, widest, GEMM_MAX_CTAS);
+  L.gemm = take(L.gemm_bytes);
   L.rope = take(static_cast<size_t>(c.max_seq) * (hd / 2) * 2 * 4);
   L.total = o;
   return L;
@@ -129,6 +133,23 @@ bool encode_tmap_16(CUtensorMap* map, int bf16, int rank, const void* base, cons
             static_cast<cuuint32_t>(rank), const_cast<void*>(base), d, s, b, e,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool encode_tmap_out_2d(CUtensorMap* map, bool f32, const void* base, uint64_t inner, uint64_t outer,
+                        uint32_t box_inner, uint32_t box_outer, int swizzle_bytes) {
+  EncodeTiledFn fn = get_encode_fn();
+  if (!fn) return false;
+  const uint64_t esz = f32 ? 4 : 2;
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {inner * esz};
+  const cuuint32_t box[2] = {box_inner, box_outer};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUtensorMapSwizzle sw = swizzle_bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
+                                : swizzle_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                                      : CU_TENSOR_MAP_SWIZZLE_NONE;
+  return fn(map, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
+            const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 int device_sm_count() {
@@ -262,10 +283,9 @@ pf_status enqueue_gemm(pf_session* s, int cls, int wfmt, int epi, const void* a,
   g.N = N;
   g.K = K;
   g.out = out;
-  g.split_k = choose_split_k(M, N, K, epi, s->sms);
+  g.max_ctas = GEMM_MAX_CTAS;
+  g.scratch = wsp<void>(s, s->L.gemm);
   g.status = wsp<int>(s, s->L.status);
-  if (epi == EPI_STORE_F32 && g.split_k > 1)
-    PF_CUDA(cudaMemsetAsync(out, 0, static_cast<size_t>(M) * N * 4, st), "memset gemm output");
   return launch_k(s, cls, st, "gemm launch", [&] { return launch_gemm(g, st); });
 }
 
@@ -284,12 +304,13 @@ pf_status enqueue_layer(pf_session* s, int l, float* x, int M, cudaStream_t st) 
   // 1. pre-attention RMSNorm
   PF_TRY(launch_k(s, PF_K_RMSNORM, st, "rmsnorm",
                   [&] { return launch_rmsnorm(x, w.attn_norm, c.eps, M, H, y, st); }));
-  // 2. fused QKV projection
-  PF_TRY(enqueue_gemm(s, PF_K_GEMM_QKV, c.wfmt, EPI_STORE_F32, y, w.qkv, M, qkv_rows, H, qkv, st));
+  // 2. fused QKV projection, accumulated into the qkv rows that the QK-norm step below
+  // leaves zero after reading them (zeroed once at session creation)
+  PF_TRY(enqueue_gemm(s, PF_K_GEMM_QKV, c.wfmt, EPI_RESID_ADD, y, w.qkv, M, qkv_rows, H, qkv, st));
   // 3. QK-norm + RoPE + KV store, then causal GQA attention over cache + chunk
   PF_TRY(launch_k(s, PF_K_QK_ROPE_KV, st, "qk_norm_rope_kv", [&] {
     return launch_qk_norm_rope_kv(c, qkv, w.q_norm, w.k_norm, wsp<float>(s, s->L.rope), l,
-                                  start_dev, 0, M, q, s->k, s->v, st);
+                                  start_dev, 0, M, q, s->k, s->v, 1, st);
   }));
   PF_TRY(launch_k(s, PF_K_ATTENTION, st, "attention", [&] {
     return launch_attention(c, q, s->k, s->v, l, start_dev, 0, M, attn, wsp<int>(s, s->L.status), st);
@@ -300,15 +321,8 @@ pf_status enqueue_layer(pf_session* s, int l, float* x, int M, cudaStream_t st) 
   // 5. FFN RMSNorm
   PF_TRY(launch_k(s, PF_K_RMSNORM, st, "rmsnorm",
                   [&] { return launch_rmsnorm(x, w.ffn_norm, c.eps, M, H, y, st); }));
-  // 6. gate_up + SwiGLU (split along K through an f32 scratch when that fills the GPU better)
-  const int split_gu = choose_split_k(M, 2 * I, H, EPI_STORE_F32, s->sms);
-  if (split_gu > 1) {
-    float* gu = wsp<float>(s, s->L.gu);
-    PF_TRY(enqueue_gemm(s, PF_K_GEMM_GATE_UP, c.wfmt, EPI_STORE_F32, y, w.gate_up, M, 2 * I, H, gu, st));
-    PF_TRY(launch_k(s, PF_K_OTHER, st, "swiglu", [&] { return launch_swiglu_f32(gu, M, I, act, st); }));
-  } else {
-    PF_TRY(enqueue_gemm(s, PF_K_GEMM_GATE_UP, c.wfmt, EPI_SWIGLU, y, w.gate_up, M, 2 * I, H, act, st));
-  }
+  // 6. gate_up + SwiGLU
+  PF_TRY(enqueue_gemm(s, PF_K_GEMM_GATE_UP, c.wfmt, EPI_SWIGLU, y, w.gate_up, M, 2 * I, H, act, st));
   // 7. down projection + residual
   PF_TRY(enqueue_gemm(s, PF_K_GEMM_DOWN, c.wfmt, EPI_RESID_ADD, act, w.down, M, H, I, x, st));
   return PF_OK;
@@ -589,6 +603,8 @@ pf_status pf_session_create(const pf_model* model, void* k, void* v, void* ws, s
   pf_rope_table_host(c.rope_theta, c.head_dim, c.max_seq, rope.data());
   cudaError_t e = cudaMemcpyAsync(s->ws + L.rope, rope.data(), rope.size() * 4, cudaMemcpyHostToDevice, st);
   if (e == cudaSuccess) e = cudaMemsetAsync(s->ws + L.status, 0, STATUS_WORDS * 4, st);
+  if (e == cudaSuccess) e = cudaMemsetAsync(s->ws + L.gemm, 0, L.gemm_bytes, st);  // tile counters
+  if (e == cudaSuccess) e = cudaMemsetAsync(s->ws + L.qkv, 0, L.q - L.qkv, st);  // QKV accumulator
   if (e == cudaSuccess) e = cudaStreamSynchronize(st);
   if (e != cudaSuccess) {
     delete s;
@@ -768,10 +784,7 @@ pf_status pf_prefill_tokens_host(pf_session* s, const int32_t* tokens_host, int3
   float* lg_dev = nullptr;
   if (logits_host) {
     if (!s->model.lm_head || c.vocab <= 0) return fail(PF_ERR_LOGITS, "no LM head");
-    // logits land in the f32 gate_up scratch (>= vocab floats is checked) before the copy out
-    const size_t room = static_cast<size_t>(c.max_chunk) * 2 * c.intermediate;
-    if (room < static_cast<size_t>(c.vocab)) return fail(PF_ERR_WORKSPACE, "workspace too small for logits");
-    lg_dev = wsp<float>(s, s->L.gu);
+    lg_dev = wsp<float>(s, s->L.logits);  // device copy of the logits before the download
   }
   pf_status r = pf_prefill_chunk(s, tokens_host, M, start_pos, lg_dev, stream);
   if (r != PF_OK) return r;
@@ -803,15 +816,28 @@ pf_status pf_op_dequant(int32_t wfmt, const void* packed, int64_t N, int64_t K, 
   return PF_OK;
 }
 
+size_t pf_gemm_scratch_bytes(int32_t M, int32_t N, int32_t max_ctas) {
+  if (M <= 0 || N <= 0 || max_ctas < 0 || max_ctas > GEMM_MAX_CTAS) return 0;
+  return gemm_scratch_bytes(M, N, max_ctas == 0 ? GEMM_MAX_CTAS : max_ctas);
+}
+
 pf_status pf_op_gemm(int32_t wfmt, int32_t epi, const uint16_t* a, const void* packed, int32_t M,
-                     int32_t N, int32_t K, void* out, int32_t split_k, int32_t* status,
-                     void* stream) {
+                     int32_t N, int32_t K, void* out, int32_t max_ctas, void* scratch,
+                     size_t scratch_bytes, int32_t* status, void* stream) {
   if (!a || !packed || !out) return fail(PF_ERR_INVALID_ARG, "NULL pointer");
   if (wfmt != PF_W_Q1_G128 && wfmt != PF_W_INT4_AFFINE_G128) return fail(PF_ERR_INVALID_ARG, "format");
   if (epi < EPI_STORE_F32 || epi > EPI_SWIGLU) return fail(PF_ERR_INVALID_ARG, "epilogue %d", epi);
   if (M <= 0 || N <= 0 || K <= 0 || K % 128 || N % 8) return fail(PF_ERR_SHAPE, "M %d N %d K %d", M, N, K);
   if (epi == EPI_SWIGLU && N % 256) return fail(PF_ERR_SHAPE, "SwiGLU needs N = 2I with I %% 128 == 0");
-  if (reinterpret_cast<uintptr_t>(a) & 15) return fail(PF_ERR_INVALID_ARG, "a must be 16-B aligned");
+  if ((reinterpret_cast<uintptr_t>(a) & 15) || (reinterpret_cast<uintptr_t>(out) & 15))
+    return fail(PF_ERR_INVALID_ARG, "a and out must be 16-B aligned");
+  if (max_ctas < 0 || max_ctas > GEMM_MAX_CTAS)
+    return fail(PF_ERR_INVALID_ARG, "max_ctas %d outside [0, %d]", max_ctas, GEMM_MAX_CTAS);
+  if (max_ctas == 0) max_ctas = GEMM_MAX_CTAS;
+  const size_t need = gemm_scratch_bytes(M, N, max_ctas);
+  if (!scratch || scratch_bytes < need)
+    return fail(PF_ERR_WORKSPACE, "GEMM scratch %zu bytes, need %zu", scratch_bytes, need);
+  if (reinterpret_cast<uintptr_t>(scratch) & 15) return fail(PF_ERR_INVALID_ARG, "scratch must be 16-B aligned");
   prepare_all();
   GemmArgs g{};
   g.wfmt = wfmt;
@@ -822,7 +848,8 @@ pf_status pf_op_gemm(int32_t wfmt, int32_t epi, const uint16_t* a, const void* p
   g.N = N;
   g.K = K;
   g.out = out;
-  g.split_k = split_k > 0 ? split_k : choose_split_k(M, N, K, epi, device_sm_count());
+  g.max_ctas = max_ctas;
+  g.scratch = scratch;
   g.status = status;
   PF_CUDA(launch_gemm(g, static_cast<cudaStream_t>(stream)), "gemm");
   return PF_OK;
@@ -838,7 +865,7 @@ pf_status pf_op_qk_norm_rope_kv(const pf_config* cfg, const float* qkv, const fl
   if (M <= 0 || layer < 0 || layer >= cfg->n_layers || start < 0 ||
       static_cast<int64_t>(start) + M > cfg->max_seq)
     return fail(PF_ERR_SHAPE, "M %d layer %d start %d", M, layer, start);
-  PF_CUDA(launch_qk_norm_rope_kv(*cfg, qkv, qn, kn, rope, layer, nullptr, start, M, q, kc, vc,
+  PF_CUDA(launch_qk_norm_rope_kv(*cfg, qkv, qn, kn, rope, layer, nullptr, start, M, q, kc, vc, 0,
                                  static_cast<cudaStream_t>(stream)),
           "qk_norm_rope_kv");
   return PF_OK;

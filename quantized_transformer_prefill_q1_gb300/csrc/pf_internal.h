@@ -58,12 +58,16 @@ struct GemmArgs {
   const void* a;        // f16 [M, K] row-major
   const uint8_t* w;     // packed
   int M, N, K;
-  void* out;            // f32 [M, N] or f16 [M, N/2]
-  int split_k;          // >= 1
+  void* out;            // f32 [M, N] or f16 [M, N/2], 16-B aligned
+  int max_ctas;         // 1..GEMM_MAX_CTAS; the scratch layout depends on it
+  void* scratch;        // gemm_scratch_bytes(M, N, max_ctas); its counters zero before the launch
   int* status;          // may be NULL
 };
 cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t stream);
-int choose_split_k(int M, int N, int K, int epilogue, int num_sms);
+// The GEMM runs at most min(max_ctas, SMs) persistent CTAs; its scratch holds two f32
+// 128 x 256 partial tiles per CTA and one arrival counter per output tile.
+constexpr int GEMM_MAX_CTAS = 160;
+size_t gemm_scratch_bytes(int M, int N, int max_ctas);
 
 cudaError_t launch_rmsnorm(const float* x, const float* w, float eps, int M, int H, void* y_f16,
                            cudaStream_t stream);
@@ -72,7 +76,7 @@ cudaError_t launch_dequant(int wfmt, const uint8_t* packed, int64_t N, int64_t K
 cudaError_t launch_qk_norm_rope_kv(const pf_config& c, const float* qkv, const float* q_norm,
                                    const float* k_norm, const float* rope, int layer,
                                    const int* start_dev, int start_host, int M, void* q_out,
-                                   void* k_cache, void* v_cache, cudaStream_t stream);
+                                   void* k_cache, void* v_cache, int zero_qkv, cudaStream_t stream);
 cudaError_t launch_attention(const pf_config& c, const void* q, const void* k_cache,
                              const void* v_cache, int layer, const int* start_dev, int start_host,
                              int M, void* out_f16, int* status, cudaStream_t stream);
@@ -81,7 +85,6 @@ cudaError_t launch_embed(const float* E, const int* tokens, int M, int H, int vo
 cudaError_t launch_lm_head(int wfmt, const float* x_row, const float* norm_w, float eps,
                            const uint8_t* packed, int vocab, int H, float* logits,
                            cudaStream_t stream);
-cudaError_t launch_swiglu_f32(const float* gu, int M, int I, void* out_f16, cudaStream_t stream);
 cudaError_t launch_set_int(int* dst, int value, cudaStream_t stream);
 cudaError_t launch_wait_selftest(int* status, long long limit_ns, int arrive, cudaStream_t stream);
 
@@ -107,6 +110,10 @@ int device_sm_count();
 // (innermost first), 128-B swizzle, zero fill out of bounds.
 bool encode_tmap_16(CUtensorMap* map, int bf16, int rank, const void* base, const uint64_t* dims,
                     const uint64_t* strides_bytes, const uint32_t* box);
+// Tiled 2-D tensor map over a row-major f32 (or f16) [outer, inner] array for TMA stores,
+// swizzle 128 or 64 bytes (or 0 = none).
+bool encode_tmap_out_2d(CUtensorMap* map, bool f32, const void* base, uint64_t inner, uint64_t outer,
+                        uint32_t box_inner, uint32_t box_outer, int swizzle_bytes);
 bool attention_tc_supported(const pf_config& c);
 cudaError_t prepare_attention_tc_kernels();
 cudaError_t launch_attention_tc(const pf_config& c, const void* q, const void* k_cache,

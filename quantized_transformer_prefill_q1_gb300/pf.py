@@ -87,7 +87,8 @@ _SIGS = {
     "pf_prefill_tokens_host": ([_VP, _VP, _I32, _I32, _VP, _VP], _I32),
     "pf_op_rmsnorm": ([_VP, _VP, _F, _I32, _I32, _VP, _VP], _I32),
     "pf_op_dequant": ([_I32, _VP, _I64, _I64, _VP, _VP], _I32),
-    "pf_op_gemm": ([_I32, _I32, _VP, _VP, _I32, _I32, _I32, _VP, _I32, _VP, _VP], _I32),
+    "pf_op_gemm": ([_I32, _I32, _VP, _VP, _I32, _I32, _I32, _VP, _I32, _VP, _SZ, _VP, _VP], _I32),
+    "pf_gemm_scratch_bytes": ([_I32, _I32, _I32], _SZ),
     "pf_op_qk_norm_rope_kv": ([ctypes.POINTER(pf_config), _VP, _VP, _VP, _VP, _I32, _I32, _I32,
                                _VP, _VP, _VP, _VP], _I32),
     "pf_op_attention": ([ctypes.POINTER(pf_config), _VP, _VP, _VP, _I32, _I32, _I32, _VP, _VP], _I32),
@@ -197,9 +198,21 @@ def pf_op_dequant(wfmt, packed, n, k, out, stream=None):
     check(lib().pf_op_dequant(wfmt, _ptr(packed), n, k, _ptr(out), _stream(stream)))
 
 
-def pf_op_gemm(wfmt, epilogue, a, packed, m, n, k, out, split_k=0, status=None, stream=None):
-    check(lib().pf_op_gemm(wfmt, epilogue, _ptr(a), _ptr(packed), m, n, k, _ptr(out), split_k,
-                           _ptr(status), _stream(stream)))
+def pf_gemm_scratch_bytes(m, n, max_ctas=0):
+    return lib().pf_gemm_scratch_bytes(m, n, max_ctas)
+
+
+def gemm_scratch(m, n, max_ctas=0, device="cuda"):
+    """Zeroed scratch (uint8 tensor) for pf_op_gemm on an M x N output."""
+    import torch
+    return torch.zeros(pf_gemm_scratch_bytes(m, n, max_ctas), dtype=torch.uint8, device=device)
+
+
+def pf_op_gemm(wfmt, epilogue, a, packed, m, n, k, out, scratch, max_ctas=0, status=None,
+               stream=None):
+    check(lib().pf_op_gemm(wfmt, epilogue, _ptr(a), _ptr(packed), m, n, k, _ptr(out), max_ctas,
+                           _ptr(scratch), scratch.numel() * scratch.element_size(), _ptr(status),
+                           _stream(stream)))
 
 
 def pf_op_qk_norm_rope_kv(cfg, qkv, qn, kn, rope, layer, start, m, q, kc, vc, stream=None):

@@ -29,7 +29,8 @@ def test_bounded_wait_times_out_and_context_survives():
     w = synth.q1_weight(rng, 256, 256)
     out = torch.zeros((64, 256), dtype=torch.float32, device="cuda")
     pf.pf_op_gemm(pf.W_Q1, pf.EPI_STORE_F32, torch.from_numpy(a).cuda(),
-                  torch.from_numpy(pf.pf_pack_weights_host(w)).cuda(), 64, 256, 256, out, 1, status)
+                  torch.from_numpy(pf.pf_pack_weights_host(w)).cuda(), 64, 256, 256, out,
+                  pf.gemm_scratch(64, 256), 0, status)
     pf.pf_status_read(status)
     ref = a.astype(np.float64) @ O.dequant(w).T
     assert O.rel_l2(out.cpu().numpy(), ref) <= 1e-5

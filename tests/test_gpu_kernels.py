@@ -71,16 +71,26 @@ def test_pack_interleave_gate_up():
 
 
 # ----------------------------------------------------------------------------- GEMM
+# (M, N, K, most CTAs): 0 = one per SM. Few CTAs over many k-blocks split tiles between
+# CTAs in every way the k-range partition allows (head / tail / middle / three-way).
 GEMM_CASES = [
     (1, 256, 128, 1), (16, 512, 256, 0), (127, 768, 384, 2), (129, 256, 1024, 3),
-    (300, 6144, 4096, 0), (512, 4096, 4096, 1), (512, 4096, 12288, 0), (64, 1280, 512, 5),
+    (300, 6144, 4096, 0), (512, 4096, 4096, 7), (512, 4096, 12288, 0), (64, 1280, 512, 5),
+    (200, 512, 1024, 9), (40, 24576, 256, 0),
 ]
 
 
+def assert_counters_zero(scratch, m, n):
+    """Every launch that completes leaves the per-tile arrival counters zero."""
+    tiles = -(-m // 128) * -(-n // 256)
+    counters = scratch[scratch.numel() - 4 * tiles:].view(torch.int32)
+    assert int(counters.abs().sum()) == 0
+
+
 @pytest.mark.parametrize("fmt", ["q1", "int4"])
-@pytest.mark.parametrize("m,n,k,split", GEMM_CASES)
+@pytest.mark.parametrize("m,n,k,ctas", GEMM_CASES)
 @pytest.mark.parametrize("epi", [pf.EPI_STORE_F32, pf.EPI_RESID_ADD, pf.EPI_SWIGLU])
-def test_gemm_vs_oracle(fmt, m, n, k, split, epi):
+def test_gemm_vs_oracle(fmt, m, n, k, ctas, epi):
     if epi == pf.EPI_SWIGLU and n % 256:
         pytest.skip("SwiGLU needs N = 2I with I % 128 == 0")
     rng = synth.rng_for(13, m, n, k)
@@ -91,14 +101,17 @@ def test_gemm_vs_oracle(fmt, m, n, k, split, epi):
     packed = dev(pf.pf_pack_weights_host(w, interleave_gate_up=(epi == pf.EPI_SWIGLU)))
     a_d = dev(a)
     status = torch.zeros(4, dtype=torch.int32, device="cuda")
+    scratch = pf.gemm_scratch(m, n, ctas)
     # Q1: exact f16 products, f32 accumulation of up to 12288 of them in the tensor core
-    # (and, split along K, in f32 atomics): ~sqrt(K) * 2^-24 plus the tensor core's internal
+    # (and, for a tile split between CTAs, in the f32 partial sums): ~sqrt(K) * 2^-24 plus the
+    # tensor core's internal
     # alignment -> 5e-5. INT4: the f16 rounding of each weight (2^-11) dominates -> 1e-3.
     tol = 5e-5 if fmt == "q1" else 1e-3
     if epi == pf.EPI_SWIGLU:
         out = torch.full((m, n // 2), float("nan"), dtype=torch.float16, device="cuda")
-        pf.pf_op_gemm(pf._WFMT[fmt], epi, a_d, packed, m, n, k, out, split, status)
+        pf.pf_op_gemm(pf._WFMT[fmt], epi, a_d, packed, m, n, k, out, scratch, ctas, status)
         pf.pf_status_read(status)
+        assert_counters_zero(scratch, m, n)
         g, u = ref[:, : n // 2], ref[:, n // 2:]
         exp = O.silu(g) * u
         assert rel_l2(out.cpu().numpy(), exp) <= 2e-3
@@ -108,10 +121,11 @@ def test_gemm_vs_oracle(fmt, m, n, k, split, epi):
         out = dev(x0)
         exp = x0.astype(np.float64) + ref
     else:
-        out = torch.zeros((m, n), dtype=torch.float32, device="cuda")
+        out = torch.full((m, n), float("nan"), dtype=torch.float32, device="cuda")
         exp = ref
-    pf.pf_op_gemm(pf._WFMT[fmt], epi, a_d, packed, m, n, k, out, split, status)
+    pf.pf_op_gemm(pf._WFMT[fmt], epi, a_d, packed, m, n, k, out, scratch, ctas, status)
     pf.pf_status_read(status)
+    assert_counters_zero(scratch, m, n)
     got = out.cpu().numpy()
     if epi == pf.EPI_RESID_ADD:
         assert rel_l2(got - x0, ref) <= tol
