@@ -254,6 +254,20 @@ pf_status pf_op_gemm(int32_t wfmt, int32_t epilogue, const uint16_t* a_f16_dev,
                      const void* packed_dev, int32_t M, int32_t N, int32_t K, void* out_dev,
                      int32_t max_ctas, void* scratch_dev, size_t scratch_bytes,
                      int32_t* status_dev, void* stream);
+/* The same GEMM for callers that may not allocate device memory (a plug-in whose host
+ * owns all device memory, or a service that cannot risk the device synchronisation an
+ * allocation may cause): no scratch argument; the split-tile partials and counters live in
+ * one fixed 4 MiB + 64 KiB array inside the library, which every GPU that loads the library
+ * keeps until the process exits. The pages have no counterpart of this call. It runs at
+ * most 16 CTAs (slower than pf_op_gemm on large shapes) and rejects with PF_ERR_SHAPE an
+ * output of more than 16384 tiles of 128 x 256. The first call on a device looks the
+ * array's device address up (cudaGetSymbolAddress) and should come before any stream
+ * capture; each call clears the tile counters it uses on `stream`. Every call on a device
+ * shares the array: calls that overlap on the GPU (other streams, other threads) race and
+ * corrupt each other's results. Allocates nothing; arguments otherwise as pf_op_gemm. */
+pf_status pf_op_gemm_static_scratch(int32_t wfmt, int32_t epilogue, const uint16_t* a_f16_dev,
+                                    const void* packed_dev, int32_t M, int32_t N, int32_t K,
+                                    void* out_dev, int32_t* status_dev, void* stream);
 /* Fused per-head QK RMSNorm + RoPE + KV store ([P1] section 3 fused_qk_norm /
  * fused_qk_rope / fused_kv_store; [P2] dispatch_fused_qk_norm_rope): from qkv f32
  * [M, (nq+2nkv) hd], writes q_dev [M, nq, hd] (bf16 when kv_dtype is bf16, else f16)

@@ -855,6 +855,81 @@ pf_status pf_op_gemm(int32_t wfmt, int32_t epi, const uint16_t* a, const void* p
   return PF_OK;
 }
 
+// ---------------------------------------------------------------------- GEMM without allocation
+// For callers that may not allocate device memory: a plug-in whose host owns every device
+// allocation through its own pool, or a latency-bound service that cannot afford the device
+// synchronisation cudaMalloc / cudaFree may cause once it runs. The GEMM's scratch then lives
+// in this fixed array, which every GPU that loads the library keeps until the process exits.
+namespace {
+constexpr int STATIC_GEMM_CTAS = 16;          // partial tiles for at most 16 CTAs: 4 MiB
+constexpr size_t STATIC_GEMM_TILES = 16384;   // arrival counters: 64 KiB
+constexpr size_t STATIC_GEMM_BYTES =
+    static_cast<size_t>(2) * STATIC_GEMM_CTAS * 128 * 256 * sizeof(float) + STATIC_GEMM_TILES * sizeof(int);
+static __device__ __align__(256) unsigned char g_static_gemm_scratch[STATIC_GEMM_BYTES];
+
+constexpr int MAX_DEVICES = 64;
+std::mutex g_static_gemm_mu;
+void* g_static_gemm_ptr[MAX_DEVICES] = {};
+
+// Device address of the array on the current device (host code cannot use the symbol
+// itself: on the host it names a stand-in, not device memory). Looked up once per device.
+pf_status static_gemm_scratch(void** out) {
+  int dev = 0;
+  PF_CUDA(cudaGetDevice(&dev), "cudaGetDevice");
+  if (dev < 0 || dev >= MAX_DEVICES) return fail(PF_ERR_INVALID_ARG, "device %d out of range", dev);
+  std::lock_guard<std::mutex> lock(g_static_gemm_mu);
+  if (!g_static_gemm_ptr[dev]) {
+    void* p = nullptr;
+    PF_CUDA(cudaGetSymbolAddress(&p, g_static_gemm_scratch), "cudaGetSymbolAddress");
+    g_static_gemm_ptr[dev] = p;
+  }
+  *out = g_static_gemm_ptr[dev];
+  return PF_OK;
+}
+}  // namespace
+
+pf_status pf_op_gemm_static_scratch(int32_t wfmt, int32_t epi, const uint16_t* a, const void* packed,
+                                    int32_t M, int32_t N, int32_t K, void* out, int32_t* status,
+                                    void* stream) {
+  if (!a || !packed || !out) return fail(PF_ERR_INVALID_ARG, "NULL pointer");
+  if (wfmt != PF_W_Q1_G128 && wfmt != PF_W_INT4_AFFINE_G128) return fail(PF_ERR_INVALID_ARG, "format");
+  if (epi < EPI_STORE_F32 || epi > EPI_SWIGLU) return fail(PF_ERR_INVALID_ARG, "epilogue %d", epi);
+  if (M <= 0 || N <= 0 || K <= 0 || K % 128 || N % 8) return fail(PF_ERR_SHAPE, "M %d N %d K %d", M, N, K);
+  if (epi == EPI_SWIGLU && N % 256) return fail(PF_ERR_SHAPE, "SwiGLU needs N = 2I with I %% 128 == 0");
+  if ((reinterpret_cast<uintptr_t>(a) & 15) || (reinterpret_cast<uintptr_t>(out) & 15))
+    return fail(PF_ERR_INVALID_ARG, "a and out must be 16-B aligned");
+  const size_t tiles = static_cast<size_t>((M + 127) / 128) * static_cast<size_t>((N + 255) / 256);
+  if (tiles > STATIC_GEMM_TILES)
+    return fail(PF_ERR_SHAPE,
+                "M %d x N %d is %zu output tiles of 128 x 256; the static GEMM scratch holds at most %zu",
+                M, N, tiles, STATIC_GEMM_TILES);
+  if (gemm_scratch_bytes(M, N, STATIC_GEMM_CTAS) > STATIC_GEMM_BYTES)
+    return fail(PF_ERR_SHAPE, "M %d x N %d needs more than the static GEMM scratch", M, N);
+  void* scratch = nullptr;
+  pf_status r = static_gemm_scratch(&scratch);
+  if (r != PF_OK) return r;
+  prepare_all();
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // the arrival counters must start at zero; a call that completes leaves them zero, one that
+  // timed out may not, so clear the ones this call uses
+  void* counters = static_cast<unsigned char*>(scratch) + (STATIC_GEMM_BYTES - STATIC_GEMM_TILES * sizeof(int));
+  PF_CUDA(cudaMemsetAsync(counters, 0, tiles * sizeof(int), st), "clear GEMM counters");
+  GemmArgs g{};
+  g.wfmt = wfmt;
+  g.epilogue = epi;
+  g.a = a;
+  g.w = static_cast<const uint8_t*>(packed);
+  g.M = M;
+  g.N = N;
+  g.K = K;
+  g.out = out;
+  g.max_ctas = STATIC_GEMM_CTAS;
+  g.scratch = scratch;
+  g.status = status;
+  PF_CUDA(launch_gemm(g, st), "gemm");
+  return PF_OK;
+}
+
 pf_status pf_op_qk_norm_rope_kv(const pf_config* cfg, const float* qkv, const float* qn,
                                 const float* kn, const float* rope, int32_t layer, int32_t start,
                                 int32_t M, void* q, void* kc, void* vc, void* stream) {

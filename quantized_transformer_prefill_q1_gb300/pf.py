@@ -89,6 +89,7 @@ _SIGS = {
     "pf_op_dequant": ([_I32, _VP, _I64, _I64, _VP, _VP], _I32),
     "pf_op_gemm": ([_I32, _I32, _VP, _VP, _I32, _I32, _I32, _VP, _I32, _VP, _SZ, _VP, _VP], _I32),
     "pf_gemm_scratch_bytes": ([_I32, _I32, _I32], _SZ),
+    "pf_op_gemm_static_scratch": ([_I32, _I32, _VP, _VP, _I32, _I32, _I32, _VP, _VP, _VP], _I32),
     "pf_op_qk_norm_rope_kv": ([ctypes.POINTER(pf_config), _VP, _VP, _VP, _VP, _I32, _I32, _I32,
                                _VP, _VP, _VP, _VP], _I32),
     "pf_op_attention": ([ctypes.POINTER(pf_config), _VP, _VP, _VP, _I32, _I32, _I32, _VP, _VP], _I32),
@@ -213,6 +214,12 @@ def pf_op_gemm(wfmt, epilogue, a, packed, m, n, k, out, scratch, max_ctas=0, sta
     check(lib().pf_op_gemm(wfmt, epilogue, _ptr(a), _ptr(packed), m, n, k, _ptr(out), max_ctas,
                            _ptr(scratch), scratch.numel() * scratch.element_size(), _ptr(status),
                            _stream(stream)))
+
+
+def pf_op_gemm_static_scratch(wfmt, epilogue, a, packed, m, n, k, out, status=None, stream=None):
+    """pf_op_gemm with the library's fixed scratch: for callers that may not allocate."""
+    check(lib().pf_op_gemm_static_scratch(wfmt, epilogue, _ptr(a), _ptr(packed), m, n, k, _ptr(out),
+                                          _ptr(status), _stream(stream)))
 
 
 def pf_op_qk_norm_rope_kv(cfg, qkv, qn, kn, rope, layer, start, m, q, kc, vc, stream=None):
