@@ -538,6 +538,10 @@ cudaError_t launch_t(const GemmArgs& g, const CUtensorMap& ta, const CUtensorMap
   p.kbt = g.K / BK;
   p.total = static_cast<long long>(p.n_mt) * p.n_nt * p.kbt;
   p.ctas = static_cast<int>(std::min<long long>(std::min(g.max_ctas, num_sms), p.total));
+  // store / SwiGLU epilogues: a tile split between CTAs costs a partial hand-off, so when
+  // the tiles alone fill at least half of the CTAs, run one whole tile per CTA instead
+  const int tiles = p.n_mt * p.n_nt;
+  if (EPI != EPI_RESID_ADD && tiles < p.ctas && 2 * tiles >= p.ctas) p.ctas = tiles;
   float* scratch = reinterpret_cast<float*>(g.scratch);
   int* counters = reinterpret_cast<int*>(scratch + static_cast<size_t>(2) * g.max_ctas * SLOT_FLOATS);
   return launch_pdl(gemm_q_kernel<WFMT, EPI>, dim3(p.ctas), dim3(NUM_THREADS), smem, stream, ta, to,

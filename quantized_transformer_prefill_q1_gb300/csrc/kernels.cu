@@ -136,9 +136,9 @@ __device__ __forceinline__ void store4<__nv_bfloat16>(__nv_bfloat16* dst, float 
 // [n_layers][nkv][max_seq][hd].
 template <int HD, typename QT, typename KT>
 __global__ void __launch_bounds__(256) qk_norm_rope_kv_kernel(
-    float* qkv, const float* __restrict__ qn, const float* __restrict__ kn,
+    const float* __restrict__ qkv, const float* __restrict__ qn, const float* __restrict__ kn,
     const float* __restrict__ rope, int M, int nq, int nkv, int max_seq, int layer,
-    const int* __restrict__ start_dev, int start_host, float eps, int qk_norm, int zero_qkv,
+    const int* __restrict__ start_dev, int start_host, float eps, int qk_norm,
     QT* __restrict__ q_out, KT* __restrict__ kc, KT* __restrict__ vc) {
   constexpr int HALF = HD / 2;
   constexpr int LPH = HALF / 4;   // lanes per head
@@ -157,13 +157,9 @@ __global__ void __launch_bounds__(256) qk_norm_rope_kv_kernel(
   const int pos = start + t;
   float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a;
   if (valid) {
-    float4* src = reinterpret_cast<float4*>(qkv + (static_cast<size_t>(t) * heads + j) * HD);
+    const float4* src = reinterpret_cast<const float4*>(qkv + (static_cast<size_t>(t) * heads + j) * HD);
     a = src[l];
     b = src[LPH + l];
-    if (zero_qkv) {  // leave the rows zero for the next projection, which accumulates into them
-      src[l] = make_float4(0.f, 0.f, 0.f, 0.f);
-      src[LPH + l] = make_float4(0.f, 0.f, 0.f, 0.f);
-    }
   }
   // per-head sum of squares over the LPH lanes of the group (every lane takes part)
   float ss = a.x * a.x + a.y * a.y + a.z * a.z + a.w * a.w + b.x * b.x + b.y * b.y + b.z * b.z + b.w * b.w;
@@ -385,31 +381,30 @@ cudaError_t launch_rmsnorm(const float* x, const float* w, float eps, int M, int
 template <int HD, typename QT, typename KT>
 static void qk_launch(const pf_config& c, const float* qkv, const float* qn, const float* kn,
                       const float* rope, int layer, const int* start_dev, int start_host, int M,
-                      void* q, void* kc, void* vc, int zero_qkv, cudaStream_t stream) {
+                      void* q, void* kc, void* vc, cudaStream_t stream) {
   const int heads = c.n_q_heads + 2 * c.n_kv_heads;
   constexpr int HPW = 32 / (HD / 8);
   const long long warps = (static_cast<long long>(M) * heads + HPW - 1) / HPW;
   const int blocks = static_cast<int>((warps * 32 + 255) / 256);
-  // qkv is written only when zero_qkv is set, i.e. when the caller owns it as scratch
-  launch_pdl(qk_norm_rope_kv_kernel<HD, QT, KT>, dim3(blocks), dim3(256), 0, stream,
-             const_cast<float*>(qkv), qn, kn, rope, M, c.n_q_heads, c.n_kv_heads, c.max_seq, layer,
-             start_dev, start_host, c.eps, c.qk_norm, zero_qkv, reinterpret_cast<QT*>(q), reinterpret_cast<KT*>(kc),
+  launch_pdl(qk_norm_rope_kv_kernel<HD, QT, KT>, dim3(blocks), dim3(256), 0, stream, qkv, qn, kn,
+             rope, M, c.n_q_heads, c.n_kv_heads, c.max_seq, layer, start_dev, start_host, c.eps,
+             c.qk_norm, reinterpret_cast<QT*>(q), reinterpret_cast<KT*>(kc),
              reinterpret_cast<KT*>(vc));
 }
 
 template <int HD>
 static void qk_dispatch_kv(const pf_config& c, const float* qkv, const float* qn, const float* kn,
                            const float* rope, int layer, const int* sd, int sh, int M, void* q,
-                           void* kc, void* vc, int z, cudaStream_t st) {
+                           void* kc, void* vc, cudaStream_t st) {
   switch (c.kv_dtype) {
     case PF_KV_BF16:
-      qk_launch<HD, __nv_bfloat16, __nv_bfloat16>(c, qkv, qn, kn, rope, layer, sd, sh, M, q, kc, vc, z, st);
+      qk_launch<HD, __nv_bfloat16, __nv_bfloat16>(c, qkv, qn, kn, rope, layer, sd, sh, M, q, kc, vc, st);
       break;
     case PF_KV_F16:
-      qk_launch<HD, __half, __half>(c, qkv, qn, kn, rope, layer, sd, sh, M, q, kc, vc, z, st);
+      qk_launch<HD, __half, __half>(c, qkv, qn, kn, rope, layer, sd, sh, M, q, kc, vc, st);
       break;
     default:
-      qk_launch<HD, __half, float>(c, qkv, qn, kn, rope, layer, sd, sh, M, q, kc, vc, z, st);
+      qk_launch<HD, __half, float>(c, qkv, qn, kn, rope, layer, sd, sh, M, q, kc, vc, st);
       break;
   }
 }
@@ -417,13 +412,13 @@ static void qk_dispatch_kv(const pf_config& c, const float* qkv, const float* qn
 cudaError_t launch_qk_norm_rope_kv(const pf_config& c, const float* qkv, const float* q_norm,
                                    const float* k_norm, const float* rope, int layer,
                                    const int* start_dev, int start_host, int M, void* q_out,
-                                   void* k_cache, void* v_cache, int zero_qkv, cudaStream_t stream) {
+                                   void* k_cache, void* v_cache, cudaStream_t stream) {
   if (c.head_dim == 128)
     qk_dispatch_kv<128>(c, qkv, q_norm, k_norm, rope, layer, start_dev, start_host, M, q_out,
-                        k_cache, v_cache, zero_qkv, stream);
+                        k_cache, v_cache, stream);
   else
     qk_dispatch_kv<64>(c, qkv, q_norm, k_norm, rope, layer, start_dev, start_host, M, q_out,
-                       k_cache, v_cache, zero_qkv, stream);
+                       k_cache, v_cache, stream);
   return cudaGetLastError();
 }
 

@@ -304,13 +304,12 @@ pf_status enqueue_layer(pf_session* s, int l, float* x, int M, cudaStream_t st) 
   // 1. pre-attention RMSNorm
   PF_TRY(launch_k(s, PF_K_RMSNORM, st, "rmsnorm",
                   [&] { return launch_rmsnorm(x, w.attn_norm, c.eps, M, H, y, st); }));
-  // 2. fused QKV projection, accumulated into the qkv rows that the QK-norm step below
-  // leaves zero after reading them (zeroed once at session creation)
-  PF_TRY(enqueue_gemm(s, PF_K_GEMM_QKV, c.wfmt, EPI_RESID_ADD, y, w.qkv, M, qkv_rows, H, qkv, st));
+  // 2. fused QKV projection
+  PF_TRY(enqueue_gemm(s, PF_K_GEMM_QKV, c.wfmt, EPI_STORE_F32, y, w.qkv, M, qkv_rows, H, qkv, st));
   // 3. QK-norm + RoPE + KV store, then causal GQA attention over cache + chunk
   PF_TRY(launch_k(s, PF_K_QK_ROPE_KV, st, "qk_norm_rope_kv", [&] {
     return launch_qk_norm_rope_kv(c, qkv, w.q_norm, w.k_norm, wsp<float>(s, s->L.rope), l,
-                                  start_dev, 0, M, q, s->k, s->v, 1, st);
+                                  start_dev, 0, M, q, s->k, s->v, st);
   }));
   PF_TRY(launch_k(s, PF_K_ATTENTION, st, "attention", [&] {
     return launch_attention(c, q, s->k, s->v, l, start_dev, 0, M, attn, wsp<int>(s, s->L.status), st);
@@ -604,7 +603,6 @@ pf_status pf_session_create(const pf_model* model, void* k, void* v, void* ws, s
   cudaError_t e = cudaMemcpyAsync(s->ws + L.rope, rope.data(), rope.size() * 4, cudaMemcpyHostToDevice, st);
   if (e == cudaSuccess) e = cudaMemsetAsync(s->ws + L.status, 0, STATUS_WORDS * 4, st);
   if (e == cudaSuccess) e = cudaMemsetAsync(s->ws + L.gemm, 0, L.gemm_bytes, st);  // tile counters
-  if (e == cudaSuccess) e = cudaMemsetAsync(s->ws + L.qkv, 0, L.q - L.qkv, st);  // QKV accumulator
   if (e == cudaSuccess) e = cudaStreamSynchronize(st);
   if (e != cudaSuccess) {
     delete s;
@@ -940,7 +938,7 @@ pf_status pf_op_qk_norm_rope_kv(const pf_config* cfg, const float* qkv, const fl
   if (M <= 0 || layer < 0 || layer >= cfg->n_layers || start < 0 ||
       static_cast<int64_t>(start) + M > cfg->max_seq)
     return fail(PF_ERR_SHAPE, "M %d layer %d start %d", M, layer, start);
-  PF_CUDA(launch_qk_norm_rope_kv(*cfg, qkv, qn, kn, rope, layer, nullptr, start, M, q, kc, vc, 0,
+  PF_CUDA(launch_qk_norm_rope_kv(*cfg, qkv, qn, kn, rope, layer, nullptr, start, M, q, kc, vc,
                                  static_cast<cudaStream_t>(stream)),
           "qk_norm_rope_kv");
   return PF_OK;

@@ -76,7 +76,7 @@ cudaError_t launch_dequant(int wfmt, const uint8_t* packed, int64_t N, int64_t K
 cudaError_t launch_qk_norm_rope_kv(const pf_config& c, const float* qkv, const float* q_norm,
                                    const float* k_norm, const float* rope, int layer,
                                    const int* start_dev, int start_host, int M, void* q_out,
-                                   void* k_cache, void* v_cache, int zero_qkv, cudaStream_t stream);
+                                   void* k_cache, void* v_cache, cudaStream_t stream);
 cudaError_t launch_attention(const pf_config& c, const void* q, const void* k_cache,
                              const void* v_cache, int layer, const int* start_dev, int start_host,
                              int M, void* out_f16, int* status, cudaStream_t stream);
