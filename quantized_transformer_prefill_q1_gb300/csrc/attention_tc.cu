@@ -9,16 +9,21 @@
 // One CTA = one kv head and 128 query rows (128/G tokens x the G query heads that share
 // the kv head; row = token * G + head-in-group), so every row reads the same K/V tiles:
 //   warp 0      TMA: the Q tile once (3-D map over q[M][nq][hd]), then 128-key K and V
-//               tiles straight from the cache [layer][kvh][pos][hd] into a 2-stage ring;
+//               tiles straight from the cache [layer][kvh][pos][hd] into two 2-stage rings;
+//               a K stage is free again once its QK^T is done, so K runs a tile ahead of V;
 //   warp 1      TMEM (512 columns: two S buffers of 128 + the O accumulator) and the MMAs:
 //               S_j = Q K_j^T (K-major operands), then O += P_{j-1} V_{j-1} (V used
 //               MN-major, as it lies in the cache), so QK^T of tile j overlaps the softmax
 //               of tile j-1;
-//   warps 2..5  one query row per thread: read S_j from TMEM, causal mask (key > pos:
-//               -inf), online softmax in the exp2 domain, P_j (bf16/f16) into shared
-//               memory; the running max is raised only when a tile's max exceeds it by
-//               more than 2^8 (then O is rescaled in TMEM), so probabilities stay <= 256
-//               and f32 accumulation is exact enough; final O / l to f16.
+//   warps 2..9  softmax, two threads per query row: warp w reads TMEM lane quarter w % 4
+//               and takes key columns [0, 64) (warps 2..5) or [64, 128) (warps 6..9) of
+//               each tile, so two warps per scheduler hide each other's latency. Read
+//               S_j from TMEM, causal mask (key > pos: -inf), row max combined with the
+//               partner thread through shared memory, online softmax in the exp2 domain,
+//               P_j (bf16/f16) into shared memory; the running max is raised only when a
+//               tile's max exceeds it by more than 2^8 (then O is rescaled in TMEM), so
+//               probabilities stay <= 256 and f32 accumulation is exact enough; final
+//               O / l to f16.
 // Every wait is bounded; a timeout aborts the CTA and records PF_ERR_DEVICE_TIMEOUT.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -30,7 +35,9 @@ namespace {
 
 constexpr int TQ = 128;       // query rows per CTA (MMA M)
 constexpr int TK = 128;       // keys per tile
-constexpr int THREADS = 192;  // warp 0 TMA, warp 1 MMA, warps 2..5 softmax
+constexpr int THREADS = 320;  // warp 0 TMA, warp 1 MMA, warps 2..9 softmax
+constexpr int SM_THREADS = 256;  // softmax threads: two per query row
+constexpr int HK = TK / 2;       // keys per softmax thread and tile
 constexpr float RESCALE_LOG2 = 8.0f;
 
 template <int HD>
@@ -38,7 +45,9 @@ struct ASmem {
   static constexpr int Q = TQ * HD * 2;
   static constexpr int KV = TK * HD * 2;  // one of K or V
   static constexpr int P = TQ * TK * 2;
-  static constexpr int BYTES = 1024 + Q + 2 * 2 * KV + 2 * P + 256;
+  static constexpr int RED = 2 * TQ * 4;  // partner exchange: [half][row] f32
+  static constexpr int BYTES = 1024 + Q + 2 * 2 * KV + 2 * P + RED + 256;
+  static_assert(BYTES <= 232448, "attention shared memory");
 };
 
 __device__ __forceinline__ void mbar_wait_drain_a(uint32_t bar, uint32_t parity) {
@@ -46,6 +55,22 @@ __device__ __forceinline__ void mbar_wait_drain_a(uint32_t bar, uint32_t parity)
   while (!mbar_try_wait(bar, parity)) {
     if (global_timer_ns() - t0 > PF_WAIT_LIMIT_NS) return;
   }
+}
+
+__device__ __forceinline__ void named_bar_sync_a(int id, int threads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+// Barrier over `threads` threads that returns whether `pred` held in all of them.
+__device__ __forceinline__ bool named_bar_and_a(int id, int threads, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.and.pred q, %2, %3, p;\n"
+      " selp.u32 %0, 1, 0, q;\n}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(threads)
+      : "memory");
+  return r != 0;
 }
 
 __device__ __forceinline__ void st_shared_v4a(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
@@ -89,19 +114,22 @@ __global__ void __launch_bounds__(THREADS, 1)
   const uint32_t q_s = base;
   const uint32_t kv_s = q_s + L::Q;  // stage s: K at kv_s + 2s*KV, V at kv_s + (2s+1)*KV
   const uint32_t p_s = kv_s + 4 * L::KV;
-  const uint32_t bar0 = p_s + 2 * L::P;
+  const uint32_t red_s = p_s + 2 * L::P;
+  const uint32_t bar0 = red_s + L::RED;
   const uint32_t q_full = bar0;
-  auto kv_full = [&](int s) { return bar0 + 8u * (1 + s); };
-  auto kv_empty = [&](int s) { return bar0 + 8u * (3 + s); };
-  auto s_full = [&](int s) { return bar0 + 8u * (5 + s); };
-  auto s_empty = [&](int s) { return bar0 + 8u * (7 + s); };
-  auto p_full = [&](int s) { return bar0 + 8u * (9 + s); };
-  auto p_empty = [&](int s) { return bar0 + 8u * (11 + s); };
-  const uint32_t o_done = bar0 + 8u * 13;
-  const uint32_t o_final = bar0 + 8u * 14;
-  const uint32_t drain_bar = bar0 + 8u * 15;
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + (bar0 + 128u - base));
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + (bar0 + 136u - base));
+  auto k_full = [&](int s) { return bar0 + 8u * (1 + s); };
+  auto k_empty = [&](int s) { return bar0 + 8u * (3 + s); };
+  auto v_full = [&](int s) { return bar0 + 8u * (5 + s); };
+  auto v_empty = [&](int s) { return bar0 + 8u * (7 + s); };
+  auto s_full = [&](int s) { return bar0 + 8u * (9 + s); };
+  auto s_empty = [&](int s) { return bar0 + 8u * (11 + s); };
+  auto p_full = [&](int s) { return bar0 + 8u * (13 + s); };
+  auto p_empty = [&](int s) { return bar0 + 8u * (15 + s); };
+  const uint32_t o_done = bar0 + 8u * 17;
+  const uint32_t o_final = bar0 + 8u * 18;
+  const uint32_t drain_bar = bar0 + 8u * 19;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + (bar0 + 160u - base));
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + (bar0 + 168u - base));
   auto k_tile = [&](int s) { return kv_s + (2 * s) * L::KV; };
   auto v_tile = [&](int s) { return kv_s + (2 * s + 1) * L::KV; };
 
@@ -122,11 +150,13 @@ __global__ void __launch_bounds__(THREADS, 1)
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
     for (int s = 0; s < 2; ++s) {
-      mbar_init(kv_full(s), 1);
-      mbar_init(kv_empty(s), 1);
+      mbar_init(k_full(s), 1);
+      mbar_init(k_empty(s), 1);
+      mbar_init(v_full(s), 1);
+      mbar_init(v_empty(s), 1);
       mbar_init(s_full(s), 1);
-      mbar_init(s_empty(s), 128);
-      mbar_init(p_full(s), 128);
+      mbar_init(s_empty(s), SM_THREADS);
+      mbar_init(p_full(s), SM_THREADS);
       mbar_init(p_empty(s), 1);
     }
     mbar_init(o_done, 1);
@@ -152,19 +182,37 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_arrive_expect_tx(q_full, L::Q);
       for (int h = 0; h < NH; ++h)
         tma_load_3d(q_s + h * (TQ * 128), &tm_q, h * 64, kvh * G, t0, q_full);
-      int issued = 0;
-      for (int j = 0; j < n_tiles; ++j, ++issued) {
-        const int s = j & 1;
-        if (!mbar_wait(kv_empty(s), ((j >> 1) & 1) ^ 1, abort_flag)) break;
-        mbar_arrive_expect_tx(kv_full(s), 2 * L::KV);
-        for (int h = 0; h < NH; ++h) {
-          tma_load_2d(k_tile(s) + h * (TK * 128), &tm_k, h * 64, row0 + j * TK, kv_full(s));
-          tma_load_2d(v_tile(s) + h * (TK * 128), &tm_v, h * 64, row0 + j * TK, kv_full(s));
+      // K_i, then V_{i-1}: K runs one tile ahead of V
+      int k_issued = 0, v_issued = 0;
+      bool ok = true;
+      for (int i = 0; i <= n_tiles && ok; ++i) {
+        if (i < n_tiles) {
+          const int s = i & 1;
+          if (!mbar_wait(k_empty(s), ((i >> 1) & 1) ^ 1, abort_flag)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(k_full(s), L::KV);
+          for (int h = 0; h < NH; ++h)
+            tma_load_2d(k_tile(s) + h * (TK * 128), &tm_k, h * 64, row0 + i * TK, k_full(s));
+          ++k_issued;
+        }
+        if (i >= 1) {
+          const int jv = i - 1, s = jv & 1;
+          if (!mbar_wait(v_empty(s), ((jv >> 1) & 1) ^ 1, abort_flag)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(v_full(s), L::KV);
+          for (int h = 0; h < NH; ++h)
+            tma_load_2d(v_tile(s) + h * (TK * 128), &tm_v, h * 64, row0 + jv * TK, v_full(s));
+          ++v_issued;
         }
       }
       if (*abort_flag) {
         mbar_wait_drain_a(q_full, 0);
-        for (int j = max(0, issued - 2); j < issued; ++j) mbar_wait_drain_a(kv_full(j & 1), (j >> 1) & 1);
+        for (int j = max(0, k_issued - 2); j < k_issued; ++j) mbar_wait_drain_a(k_full(j & 1), (j >> 1) & 1);
+        for (int j = max(0, v_issued - 2); j < v_issued; ++j) mbar_wait_drain_a(v_full(j & 1), (j >> 1) & 1);
       }
     }
   } else if (warp == 1) {
@@ -176,7 +224,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       for (int j = 0; j <= n_tiles && ok; ++j) {
         if (j < n_tiles) {  // S_j = Q K_j^T
           const int s = j & 1;
-          if (!(mbar_wait(kv_full(s), (j >> 1) & 1, abort_flag) &&
+          if (!(mbar_wait(k_full(s), (j >> 1) & 1, abort_flag) &&
                 mbar_wait(s_empty(s), ((j >> 1) & 1) ^ 1, abort_flag))) {
             ok = false;
             break;
@@ -190,10 +238,12 @@ __global__ void __launch_bounds__(THREADS, 1)
                         sdesc_kmajor_sw128(k_tile(s) + offk), idesc_s, kc > 0);
           }
           umma_commit(s_full(s));
+          umma_commit(k_empty(s));  // K_j is free once QK^T is done
         }
         if (j >= 1) {  // O += P_{j-1} V_{j-1}
           const int i = j - 1, s = i & 1;
-          if (!mbar_wait(p_full(s), (i >> 1) & 1, abort_flag)) {
+          if (!(mbar_wait(p_full(s), (i >> 1) & 1, abort_flag) &&
+                mbar_wait(v_full(s), (i >> 1) & 1, abort_flag))) {
             ok = false;
             break;
           }
@@ -206,7 +256,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                         (i > 0 || kc > 0));
           }
           umma_commit(p_empty(s));
-          umma_commit(kv_empty(s));
+          umma_commit(v_empty(s));
           umma_commit(o_done);
         }
       }
@@ -220,118 +270,128 @@ __global__ void __launch_bounds__(THREADS, 1)
   } else {
     // ------------------------------------------------------------------ softmax rows
     const int quarter = warp & 3;
+    const int half = (warp - 2) >> 2;  // key columns [64 half, 64 half + 64) of each tile
     const int r = 32 * quarter + lane;
     const uint32_t lane_off = static_cast<uint32_t>(32 * quarter) << 16;
     const int t_loc = r / G, h_loc = r - (r / G) * G;
     const int pos = start + t0 + t_loc;
+    volatile float* red = reinterpret_cast<volatile float*>(gbase + (red_s - base));  // [2][TQ]
     float m = -INFINITY, l = 0.f;
-    bool ok = true;
-    // tcgen05.ld / tcgen05.st are warp-collective: every branch around them below is
-    // made warp-uniform (vote on wait outcomes and on the rescale decision).
+    bool ok = true, failed = false;
+    // tcgen05.ld / tcgen05.st are warp-collective: every branch around them is warp-uniform.
+    // The 256 softmax threads meet at named barrier 1 twice per tile; a failed wait is
+    // carried to the next barrier-and, where all of them stop together.
     for (int j = 0; j < n_tiles; ++j) {
       const int s = j & 1;
-      if (!__all_sync(0xffffffffu, mbar_wait(s_full(s), (j >> 1) & 1, abort_flag))) {
+      const bool got = mbar_wait(s_full(s), (j >> 1) & 1, abort_flag);
+      if (!named_bar_and_a(1, SM_THREADS, got && !failed)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      const uint32_t sbuf = tmem + lane_off + s * TK;
-      const int kbase = j * TK;
-      // the whole S row of this tile, read from TMEM once
-      uint32_t v[TK];
+      const uint32_t sbuf = tmem + lane_off + s * TK + half * HK;
+      const int kbase = j * TK + half * HK;  // first key of this thread's columns
+      uint32_t v[HK];
 #pragma unroll
-      for (int c = 0; c < TK / 32; ++c)
+      for (int c = 0; c < HK / 32; ++c)
         tmem_ld_32x32b_x32(sbuf + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(v + 32 * c));
       tmem_ld_wait();
+      tc_fence_before();
+      mbar_arrive(s_empty(s));  // S_j is in registers: the MMA may reuse its columns
       // a tile wholly at or below the CTA's first position needs no causal mask
-      const bool diag = kbase + TK - 1 > start + t0;
-      // eight independent partial maxima (short dependency chains), then a tree
+      const bool diag = j * TK + TK - 1 > start + t0;
       float mp[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) mp[i] = -INFINITY;
       if (diag) {
 #pragma unroll
-        for (int e = 0; e < TK; ++e)
+        for (int e = 0; e < HK; ++e)
           if (kbase + e <= pos) mp[e & 7] = fmaxf(mp[e & 7], __uint_as_float(v[e]));
       } else {
 #pragma unroll
-        for (int e = 0; e < TK; ++e) mp[e & 7] = fmaxf(mp[e & 7], __uint_as_float(v[e]));
+        for (int e = 0; e < HK; ++e) mp[e & 7] = fmaxf(mp[e & 7], __uint_as_float(v[e]));
       }
-      const float mraw = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
-                               fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7])));
+      float mraw = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
+                         fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7])));
+      red[half * TQ + r] = mraw;
+      named_bar_sync_a(1, SM_THREADS);
+      mraw = fmaxf(mraw, red[(1 - half) * TQ + r]);  // the row's max over all 128 keys
       const float mx = mraw * scale_log2;  // scale > 0 keeps the order
       const bool need = j > 0 && mx > m + RESCALE_LOG2;
       if (j == 0) {
         m = mx;  // key 0 is visible to every row, so this is finite
       } else if (__any_sync(0xffffffffu, need)) {
-        // some row of this warp raises its max: the whole warp rescales its O rows, the
-        // rows that keep their max with alpha = 1
+        // some row of this warp raises its max: the warp rescales its half of those O rows,
+        // the rows that keep their max with alpha = 1 (the partner warp decides the same)
         const float alpha = need ? exp2f(m - mx) : 1.0f;
         l *= alpha;
         // O holds P_0..P_{j-1} V: wait for PV_{j-1}, then scale it in place
-        if (!__all_sync(0xffffffffu, mbar_wait(o_done, (j - 1) & 1, abort_flag))) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
+        if (__all_sync(0xffffffffu, mbar_wait(o_done, (j - 1) & 1, abort_flag))) {
+          tc_fence_after();
 #pragma unroll 1
-        for (int c = 0; c < HD / 32; ++c) {
-          uint32_t o[32];
-          tmem_ld_32x32b_x32(tmem_o + lane_off + 32 * c, o);
-          tmem_ld_wait();
+          for (int c = half * (HD / 64); c < (half + 1) * (HD / 64); ++c) {
+            uint32_t o[32];
+            tmem_ld_32x32b_x32(tmem_o + lane_off + 32 * c, o);
+            tmem_ld_wait();
 #pragma unroll
-          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-          tmem_st_32x32b_x32(tmem_o + lane_off + 32 * c, o);
+            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+            tmem_st_32x32b_x32(tmem_o + lane_off + 32 * c, o);
+          }
+          tmem_st_wait();
+        } else {
+          failed = true;
         }
-        tmem_st_wait();
         if (need) m = mx;
       }
-      if (!__all_sync(0xffffffffu, mbar_wait(p_empty(s), ((j >> 1) & 1) ^ 1, abort_flag))) {
-        ok = false;
-        break;
-      }
+      if (!failed && !mbar_wait(p_empty(s), ((j >> 1) & 1) ^ 1, abort_flag)) failed = true;
       const uint32_t pbuf = p_s + s * L::P;
       const float neg_m = -m;
       float rsp[4] = {0.f, 0.f, 0.f, 0.f};  // independent partial row sums
+      if (!failed) {
+        // keys 8ch .. 8ch+7 of this thread: K-atom `half`, chunk ch within it
+        const uint32_t row_base = pbuf + half * (TQ * 128) + r * 128;
 #pragma unroll
-      for (int ch = 0; ch < TK / 8; ++ch) {  // 16-B chunks of 8 keys
-        uint32_t pk[4];
+        for (int ch = 0; ch < HK / 8; ++ch) {
+          uint32_t pk[4];
 #pragma unroll
-        for (int e = 0; e < 8; e += 2) {
-          const int x = 8 * ch + e;
-          float p0 = ex2_approx(fmaf(__uint_as_float(v[x]), scale_log2, neg_m));
-          float p1 = ex2_approx(fmaf(__uint_as_float(v[x + 1]), scale_log2, neg_m));
-          if (diag) {
-            p0 = (kbase + x <= pos) ? p0 : 0.f;
-            p1 = (kbase + x + 1 <= pos) ? p1 : 0.f;
+          for (int e = 0; e < 8; e += 2) {
+            const int x = 8 * ch + e;
+            float p0 = ex2_approx(fmaf(__uint_as_float(v[x]), scale_log2, neg_m));
+            float p1 = ex2_approx(fmaf(__uint_as_float(v[x + 1]), scale_log2, neg_m));
+            if (diag) {
+              p0 = (kbase + x <= pos) ? p0 : 0.f;
+              p1 = (kbase + x + 1 <= pos) ? p1 : 0.f;
+            }
+            rsp[e >> 1] += p0 + p1;
+            pk[e >> 1] = pack_pair<BF16>(p0, p1);
           }
-          rsp[e >> 1] += p0 + p1;
-          pk[e >> 1] = pack_pair<BF16>(p0, p1);
+          st_shared_v4a(row_base + ((ch ^ (r & 7)) << 4), pk[0], pk[1], pk[2], pk[3]);
         }
-        // keys 8ch .. 8ch+7 of this row: K-atom (ch >> 3), chunk ch & 7 within it
-        const uint32_t row_base = pbuf + (ch >> 3) * (TQ * 128) + r * 128;
-        st_shared_v4a(row_base + (((ch & 7) ^ (r & 7)) << 4), pk[0], pk[1], pk[2], pk[3]);
-      }
-      l += (rsp[0] + rsp[1]) + (rsp[2] + rsp[3]);
-      tc_fence_before();
-      mbar_arrive(s_empty(s));
-      if (j == n_tiles - 1 && kbase + r >= kv_len) {
-        // key row r of this tile lies past the cache's filled range: zero its V row so a
-        // zero probability never meets a stale NaN / Inf in the PV product
-        for (int h = 0; h < NH; ++h)
-          for (int ch = 0; ch < 8; ++ch) st_shared_v4a(v_tile(s) + h * (TK * 128) + r * 128 + ch * 16, 0, 0, 0, 0);
+        l += (rsp[0] + rsp[1]) + (rsp[2] + rsp[3]);
+        if (j == n_tiles - 1 && j * TK + r >= kv_len) {
+          // key row r of this tile lies past the cache's filled range: zero its V row (once
+          // the tile has landed) so a zero probability never meets a stale NaN / Inf in the
+          // PV product
+          if (!mbar_wait(v_full(s), (j >> 1) & 1, abort_flag)) failed = true;
+          for (int h = half; h < NH; h += 2)
+            for (int ch = 0; ch < 8; ++ch) st_shared_v4a(v_tile(s) + h * (TK * 128) + r * 128 + ch * 16, 0, 0, 0, 0);
+        }
       }
       fence_proxy_async_smem();
       mbar_arrive(p_full(s));
     }
     // ------------------------------------------------------------------ epilogue
-    if (__all_sync(0xffffffffu, ok && mbar_wait(o_final, 0, abort_flag))) {
+    const bool fin = ok && !failed && mbar_wait(o_final, 0, abort_flag);
+    const bool all_ok = named_bar_and_a(1, SM_THREADS, fin);  // partners are done with red
+    red[half * TQ + r] = l;
+    named_bar_sync_a(1, SM_THREADS);
+    if (all_ok) {
       tc_fence_after();
-      const float inv = 1.f / l;
+      const float inv = 1.f / (l + red[(1 - half) * TQ + r]);
       const int t = t0 + t_loc;
       const int h = kvh * G + h_loc;
 #pragma unroll 1
-      for (int c = 0; c < HD / 32; ++c) {
+      for (int c = half * (HD / 64); c < (half + 1) * (HD / 64); ++c) {
         uint32_t v[32];
         tmem_ld_32x32b_x32(tmem_o + lane_off + 32 * c, v);
         tmem_ld_wait();
