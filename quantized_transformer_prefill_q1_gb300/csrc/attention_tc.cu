@@ -7,23 +7,24 @@
 // as in turbospark-runtime prefill.rs `encode_attention_decode_batch`.
 //
 // One CTA = one kv head and 128 query rows (128/G tokens x the G query heads that share
-// the kv head; row = token * G + head-in-group), so every row reads the same K/V tiles:
-//   warp 0      TMA: the Q tile once (3-D map over q[M][nq][hd]), then 128-key K and V
-//               tiles straight from the cache [layer][kvh][pos][hd] into two 2-stage rings;
-//               a K stage is free again once its QK^T is done, so K runs a tile ahead of V;
-//   warp 1      TMEM (512 columns: two S buffers of 128 + the O accumulator) and the MMAs:
-//               S_j = Q K_j^T (K-major operands), then O += P_{j-1} V_{j-1} (V used
-//               MN-major, as it lies in the cache), so QK^T of tile j overlaps the softmax
-//               of tile j-1;
+// the kv head; row = token * G + head-in-group), so every row reads the same K/V tiles.
+// Q and the probabilities P live in tensor memory and are the MMAs' A operand, so the
+// shared-memory traffic per 128-key tile is K and V only (written by TMA, read by the MMA):
+//   warp 0      TMA: 128-key K and V tiles straight from the cache [layer][kvh][pos][hd]
+//               into two 3-stage rings; a K stage is free again once its QK^T is done, so
+//               K runs a tile ahead of V;
+//   warp 1      TMEM (512 columns: two S buffers of 128, O, Q) and the MMAs:
+//               S_j = Q K_j^T (Q from TMEM, K K-major), then O += P_{j-1} V_{j-1} (P from
+//               TMEM over S_{j-1}'s columns, V used MN-major as it lies in the cache), so
+//               QK^T of tile j overlaps the softmax of tile j-1;
 //   warps 2..9  softmax, two threads per query row: warp w reads TMEM lane quarter w % 4
 //               and takes key columns [0, 64) (warps 2..5) or [64, 128) (warps 6..9) of
-//               each tile, so two warps per scheduler hide each other's latency. Read
-//               S_j from TMEM, causal mask (key > pos: -inf), row max combined with the
-//               partner thread through shared memory, online softmax in the exp2 domain,
-//               P_j (bf16/f16) into shared memory; the running max is raised only when a
-//               tile's max exceeds it by more than 2^8 (then O is rescaled in TMEM), so
-//               probabilities stay <= 256 and f32 accumulation is exact enough; final
-//               O / l to f16.
+//               each tile. First they write the Q rows into TMEM. Per tile: read S_j,
+//               causal mask (key > pos: -inf), row max combined with the partner thread
+//               through shared memory, online softmax in the exp2 domain, P_j (bf16/f16)
+//               back into TMEM; the running max is raised only when a tile's max exceeds it
+//               by more than 2^8 (then O is rescaled in TMEM), so probabilities stay <= 256
+//               and f32 accumulation is exact enough; final O / l to f16.
 // Every wait is bounded; a timeout aborts the CTA and records PF_ERR_DEVICE_TIMEOUT.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -33,20 +34,23 @@
 namespace pf {
 namespace {
 
-constexpr int TQ = 128;       // query rows per CTA (MMA M)
-constexpr int TK = 128;       // keys per tile
-constexpr int THREADS = 320;  // warp 0 TMA, warp 1 MMA, warps 2..9 softmax
+constexpr int TQ = 128;          // query rows per CTA (MMA M)
+constexpr int TK = 128;          // keys per tile
+constexpr int KS = 3;            // K and V ring stages
+constexpr int THREADS = 320;     // warp 0 TMA, warp 1 MMA, warps 2..9 softmax
 constexpr int SM_THREADS = 256;  // softmax threads: two per query row
 constexpr int HK = TK / 2;       // keys per softmax thread and tile
 constexpr float RESCALE_LOG2 = 8.0f;
+// TMEM columns: S buffers at 0 and TK (P_j over the first TK/2 columns of its buffer),
+// O at 2 TK, Q at 3 TK
+constexpr uint32_t COL_O = 2 * TK;
+constexpr uint32_t COL_Q = 3 * TK;
 
 template <int HD>
 struct ASmem {
-  static constexpr int Q = TQ * HD * 2;
-  static constexpr int KV = TK * HD * 2;  // one of K or V
-  static constexpr int P = TQ * TK * 2;
+  static constexpr int KV = TK * HD * 2;  // one K or V tile
   static constexpr int RED = 2 * TQ * 4;  // partner exchange: [half][row] f32
-  static constexpr int BYTES = 1024 + Q + 2 * 2 * KV + 2 * P + RED + 256;
+  static constexpr int BYTES = 1024 + 2 * KS * KV + RED + 256;
   static_assert(BYTES <= 232448, "attention shared memory");
 };
 
@@ -101,9 +105,9 @@ __device__ __forceinline__ uint32_t pack_pair(float a, float b) {
 
 template <int HD, int BF16>
 __global__ void __launch_bounds__(THREADS, 1)
-    attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                   const __grid_constant__ CUtensorMap tm_v, int M, int nq, int nkv, int max_seq,
-                   int layer, const int* __restrict__ start_dev, int start_host, float scale_log2,
+    attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                   const uint16_t* __restrict__ q, int M, int nq, int nkv, int max_seq, int layer,
+                   const int* __restrict__ start_dev, int start_host, float scale_log2,
                    __half* __restrict__ out, int* __restrict__ status) {
   using L = ASmem<HD>;
   constexpr int NH = HD / 64;  // 64-wide (128-B) swizzle regions along head_dim
@@ -111,27 +115,25 @@ __global__ void __launch_bounds__(THREADS, 1)
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* gbase = smem_raw + (base - raw);
-  const uint32_t q_s = base;
-  const uint32_t kv_s = q_s + L::Q;  // stage s: K at kv_s + 2s*KV, V at kv_s + (2s+1)*KV
-  const uint32_t p_s = kv_s + 4 * L::KV;
-  const uint32_t red_s = p_s + 2 * L::P;
+  const uint32_t k_s = base;                // K stage s at k_s + s * KV
+  const uint32_t v_s = k_s + KS * L::KV;    // V stage s at v_s + s * KV
+  const uint32_t red_s = v_s + KS * L::KV;
   const uint32_t bar0 = red_s + L::RED;
-  const uint32_t q_full = bar0;
-  auto k_full = [&](int s) { return bar0 + 8u * (1 + s); };
-  auto k_empty = [&](int s) { return bar0 + 8u * (3 + s); };
-  auto v_full = [&](int s) { return bar0 + 8u * (5 + s); };
-  auto v_empty = [&](int s) { return bar0 + 8u * (7 + s); };
-  auto s_full = [&](int s) { return bar0 + 8u * (9 + s); };
-  auto s_empty = [&](int s) { return bar0 + 8u * (11 + s); };
-  auto p_full = [&](int s) { return bar0 + 8u * (13 + s); };
-  auto p_empty = [&](int s) { return bar0 + 8u * (15 + s); };
-  const uint32_t o_done = bar0 + 8u * 17;
-  const uint32_t o_final = bar0 + 8u * 18;
-  const uint32_t drain_bar = bar0 + 8u * 19;
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + (bar0 + 160u - base));
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + (bar0 + 168u - base));
-  auto k_tile = [&](int s) { return kv_s + (2 * s) * L::KV; };
-  auto v_tile = [&](int s) { return kv_s + (2 * s + 1) * L::KV; };
+  auto k_full = [&](int s) { return bar0 + 8u * s; };
+  auto k_empty = [&](int s) { return bar0 + 8u * (KS + s); };
+  auto v_full = [&](int s) { return bar0 + 8u * (2 * KS + s); };
+  auto v_empty = [&](int s) { return bar0 + 8u * (3 * KS + s); };
+  auto s_full = [&](int s) { return bar0 + 8u * (4 * KS + s); };
+  auto s_empty = [&](int s) { return bar0 + 8u * (4 * KS + 2 + s); };
+  auto p_full = [&](int s) { return bar0 + 8u * (4 * KS + 4 + s); };
+  const uint32_t q_ready = bar0 + 8u * (4 * KS + 6);
+  const uint32_t o_done = bar0 + 8u * (4 * KS + 7);
+  const uint32_t o_final = bar0 + 8u * (4 * KS + 8);
+  const uint32_t drain_bar = bar0 + 8u * (4 * KS + 9);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + (bar0 + 8u * (4 * KS + 10) - base));
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + (bar0 + 8u * (4 * KS + 11) - base));
+  auto k_tile = [&](int s) { return k_s + s * L::KV; };
+  auto v_tile = [&](int s) { return v_s + s * L::KV; };
 
   griddep_launch_dependents();
   griddep_wait();  // the start position and q / cache come from earlier kernels
@@ -148,17 +150,18 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int row0 = (layer * nkv + kvh) * max_seq;
 
   if (threadIdx.x == 0) {
-    mbar_init(q_full, 1);
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < KS; ++s) {
       mbar_init(k_full(s), 1);
       mbar_init(k_empty(s), 1);
       mbar_init(v_full(s), 1);
       mbar_init(v_empty(s), 1);
-      mbar_init(s_full(s), 1);
-      mbar_init(s_empty(s), SM_THREADS);
-      mbar_init(p_full(s), SM_THREADS);
-      mbar_init(p_empty(s), 1);
     }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(s_full(s), 1);
+      mbar_init(s_empty(s), 1);
+      mbar_init(p_full(s), SM_THREADS);
+    }
+    mbar_init(q_ready, SM_THREADS);
     mbar_init(o_done, 1);
     mbar_init(o_final, 1);
     mbar_init(drain_bar, 1);
@@ -174,21 +177,19 @@ __global__ void __launch_bounds__(THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t tmem_o = tmem + 256;
+  const uint32_t tmem_o = tmem + COL_O;
+  const uint32_t tmem_q = tmem + COL_Q;
 
   if (warp == 0) {
     // ------------------------------------------------------------------ TMA producer
     if (lane == 0) {
-      mbar_arrive_expect_tx(q_full, L::Q);
-      for (int h = 0; h < NH; ++h)
-        tma_load_3d(q_s + h * (TQ * 128), &tm_q, h * 64, kvh * G, t0, q_full);
       // K_i, then V_{i-1}: K runs one tile ahead of V
       int k_issued = 0, v_issued = 0;
       bool ok = true;
       for (int i = 0; i <= n_tiles && ok; ++i) {
         if (i < n_tiles) {
-          const int s = i & 1;
-          if (!mbar_wait(k_empty(s), ((i >> 1) & 1) ^ 1, abort_flag)) {
+          const int s = i % KS;
+          if (!mbar_wait(k_empty(s), ((i / KS) & 1) ^ 1, abort_flag)) {
             ok = false;
             break;
           }
@@ -198,8 +199,8 @@ __global__ void __launch_bounds__(THREADS, 1)
           ++k_issued;
         }
         if (i >= 1) {
-          const int jv = i - 1, s = jv & 1;
-          if (!mbar_wait(v_empty(s), ((jv >> 1) & 1) ^ 1, abort_flag)) {
+          const int jv = i - 1, s = jv % KS;
+          if (!mbar_wait(v_empty(s), ((jv / KS) & 1) ^ 1, abort_flag)) {
             ok = false;
             break;
           }
@@ -209,63 +210,59 @@ __global__ void __launch_bounds__(THREADS, 1)
           ++v_issued;
         }
       }
-      if (*abort_flag) {
-        mbar_wait_drain_a(q_full, 0);
-        for (int j = max(0, k_issued - 2); j < k_issued; ++j) mbar_wait_drain_a(k_full(j & 1), (j >> 1) & 1);
-        for (int j = max(0, v_issued - 2); j < v_issued; ++j) mbar_wait_drain_a(v_full(j & 1), (j >> 1) & 1);
+      if (*abort_flag) {  // let copies already in flight land before shared memory is released
+        for (int j = max(0, k_issued - KS); j < k_issued; ++j) mbar_wait_drain_a(k_full(j % KS), (j / KS) & 1);
+        for (int j = max(0, v_issued - KS); j < v_issued; ++j) mbar_wait_drain_a(v_full(j % KS), (j / KS) & 1);
       }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t idesc_s = idesc_f16(TQ, TK, BF16, 0);
-      constexpr uint32_t idesc_o = idesc_f16(TQ, HD, BF16, 1);
-      bool ok = mbar_wait(q_full, 0, abort_flag);
-      for (int j = 0; j <= n_tiles && ok; ++j) {
-        if (j < n_tiles) {  // S_j = Q K_j^T
-          const int s = j & 1;
-          if (!(mbar_wait(k_full(s), (j >> 1) & 1, abort_flag) &&
-                mbar_wait(s_empty(s), ((j >> 1) & 1) ^ 1, abort_flag))) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-#pragma unroll
-          for (int kc = 0; kc < HD / 16; ++kc) {
-            const uint32_t off = (kc >> 2) * (TQ * 128) + (kc & 3) * 32;
-            const uint32_t offk = (kc >> 2) * (TK * 128) + (kc & 3) * 32;
-            umma_f16_ss(tmem + s * TK, sdesc_kmajor_sw128(q_s + off),
-                        sdesc_kmajor_sw128(k_tile(s) + offk), idesc_s, kc > 0);
-          }
-          umma_commit(s_full(s));
-          umma_commit(k_empty(s));  // K_j is free once QK^T is done
+    // The whole warp runs the loop (uniform control flow and operands); one elected lane
+    // issues each MMA / commit. Wait outcomes are made warp-uniform by vote.
+    constexpr uint32_t idesc_s = idesc_f16(TQ, TK, BF16, 0);
+    constexpr uint32_t idesc_o = idesc_f16(TQ, HD, BF16, 1);
+    bool ok = __all_sync(0xffffffffu, mbar_wait(q_ready, 0, abort_flag));
+    for (int j = 0; j <= n_tiles && ok; ++j) {
+      if (j < n_tiles) {  // S_j = Q K_j^T into S buffer j % 2
+        const int s = j & 1, ks = j % KS;
+        if (!__all_sync(0xffffffffu, mbar_wait(k_full(ks), (j / KS) & 1, abort_flag) &&
+                                         mbar_wait(s_empty(s), ((j >> 1) & 1) ^ 1, abort_flag))) {
+          ok = false;
+          break;
         }
-        if (j >= 1) {  // O += P_{j-1} V_{j-1}
-          const int i = j - 1, s = i & 1;
-          if (!(mbar_wait(p_full(s), (i >> 1) & 1, abort_flag) &&
-                mbar_wait(v_full(s), (i >> 1) & 1, abort_flag))) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
+        tc_fence_after();
 #pragma unroll
-          for (int kc = 0; kc < TK / 16; ++kc) {
-            const uint32_t offp = s * L::P + (kc >> 2) * (TQ * 128) + (kc & 3) * 32;
-            umma_f16_ss(tmem_o, sdesc_kmajor_sw128(p_s + offp),
-                        sdesc_mnmajor_sw128(v_tile(s) + kc * 2048, TK * 128), idesc_o,
-                        (i > 0 || kc > 0));
-          }
-          umma_commit(p_empty(s));
-          umma_commit(v_empty(s));
-          umma_commit(o_done);
+        for (int kc = 0; kc < HD / 16; ++kc) {
+          const uint32_t offk = (kc >> 2) * (TK * 128) + (kc & 3) * 32;
+          umma_f16_ts_warp(tmem + s * TK, tmem_q + 8 * kc, sdesc_kmajor_sw128(k_tile(ks) + offk),
+                           idesc_s, kc > 0);
         }
+        umma_commit_warp(s_full(s));
+        umma_commit_warp(k_empty(ks));  // K_j is free once QK^T is done
       }
-      if (ok) {
-        umma_commit(o_final);
-      } else {
-        umma_commit(drain_bar);
-        mbar_wait_drain_a(drain_bar, 0);
+      if (j >= 1) {  // O += P_{j-1} V_{j-1}, P from TMEM over S_{j-1}'s columns
+        const int i = j - 1, s = i & 1, vs = i % KS;
+        if (!__all_sync(0xffffffffu, mbar_wait(p_full(s), (i >> 1) & 1, abort_flag) &&
+                                         mbar_wait(v_full(vs), (i / KS) & 1, abort_flag))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+#pragma unroll
+        for (int kc = 0; kc < TK / 16; ++kc)
+          umma_f16_ts_warp(tmem_o, tmem + s * TK + 8 * kc,
+                           sdesc_mnmajor_sw128(v_tile(vs) + kc * 2048, TK * 128), idesc_o,
+                           (i > 0 || kc > 0));
+        umma_commit_warp(s_empty(s));  // P_{j-1} consumed: S buffer reusable
+        umma_commit_warp(v_empty(vs));
+        umma_commit_warp(o_done);
       }
+    }
+    if (ok) {
+      umma_commit_warp(o_final);
+    } else {
+      umma_commit_warp(drain_bar);
+      mbar_wait_drain_a(drain_bar, 0);
     }
   } else {
     // ------------------------------------------------------------------ softmax rows
@@ -276,6 +273,31 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int t_loc = r / G, h_loc = r - (r / G) * G;
     const int pos = start + t0 + t_loc;
     volatile float* red = reinterpret_cast<volatile float*>(gbase + (red_s - base));  // [2][TQ]
+    // Q row r into TMEM (lane r, head-dim pairs packed per column): this thread writes
+    // dims [64 half, 64 half + 64) when they exist; rows past the chunk are zero
+    if (64 * half < HD) {
+      uint32_t qv[32];
+      const int t = t0 + t_loc;
+      if (t < M) {
+        const uint4* src = reinterpret_cast<const uint4*>(
+            q + (static_cast<size_t>(t) * nq + kvh * G + h_loc) * HD + 64 * half);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const uint4 x = src[i];
+          qv[4 * i] = x.x;
+          qv[4 * i + 1] = x.y;
+          qv[4 * i + 2] = x.z;
+          qv[4 * i + 3] = x.w;
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) qv[i] = 0u;
+      }
+      tmem_st_32x32b_x32(tmem_q + lane_off + 32 * half, qv);
+      tmem_st_wait();
+    }
+    tc_fence_before();
+    mbar_arrive(q_ready);
     float m = -INFINITY, l = 0.f;
     bool ok = true, failed = false;
     // tcgen05.ld / tcgen05.st are warp-collective: every branch around them is warp-uniform.
@@ -289,15 +311,13 @@ __global__ void __launch_bounds__(THREADS, 1)
         break;
       }
       tc_fence_after();
-      const uint32_t sbuf = tmem + lane_off + s * TK + half * HK;
+      const uint32_t sbuf = tmem + lane_off + s * TK;
       const int kbase = j * TK + half * HK;  // first key of this thread's columns
       uint32_t v[HK];
 #pragma unroll
       for (int c = 0; c < HK / 32; ++c)
-        tmem_ld_32x32b_x32(sbuf + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(v + 32 * c));
+        tmem_ld_32x32b_x32(sbuf + half * HK + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(v + 32 * c));
       tmem_ld_wait();
-      tc_fence_before();
-      mbar_arrive(s_empty(s));  // S_j is in registers: the MMA may reuse its columns
       // a tile wholly at or below the CTA's first position needs no causal mask
       const bool diag = j * TK + TK - 1 > start + t0;
       float mp[8];
@@ -314,7 +334,10 @@ __global__ void __launch_bounds__(THREADS, 1)
       float mraw = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
                          fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7])));
       red[half * TQ + r] = mraw;
+      // both partners have read their S columns before either writes P over them
+      tc_fence_before();
       named_bar_sync_a(1, SM_THREADS);
+      tc_fence_after();
       mraw = fmaxf(mraw, red[(1 - half) * TQ + r]);  // the row's max over all 128 keys
       const float mx = mraw * scale_log2;  // scale > 0 keeps the order
       const bool need = j > 0 && mx > m + RESCALE_LOG2;
@@ -343,41 +366,35 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         if (need) m = mx;
       }
-      if (!failed && !mbar_wait(p_empty(s), ((j >> 1) & 1) ^ 1, abort_flag)) failed = true;
-      const uint32_t pbuf = p_s + s * L::P;
       const float neg_m = -m;
       float rsp[4] = {0.f, 0.f, 0.f, 0.f};  // independent partial row sums
-      if (!failed) {
-        // keys 8ch .. 8ch+7 of this thread: K-atom `half`, chunk ch within it
-        const uint32_t row_base = pbuf + half * (TQ * 128) + r * 128;
+      uint32_t pk[HK / 2];                  // this thread's 64 probabilities, packed in pairs
 #pragma unroll
-        for (int ch = 0; ch < HK / 8; ++ch) {
-          uint32_t pk[4];
-#pragma unroll
-          for (int e = 0; e < 8; e += 2) {
-            const int x = 8 * ch + e;
-            float p0 = ex2_approx(fmaf(__uint_as_float(v[x]), scale_log2, neg_m));
-            float p1 = ex2_approx(fmaf(__uint_as_float(v[x + 1]), scale_log2, neg_m));
-            if (diag) {
-              p0 = (kbase + x <= pos) ? p0 : 0.f;
-              p1 = (kbase + x + 1 <= pos) ? p1 : 0.f;
-            }
-            rsp[e >> 1] += p0 + p1;
-            pk[e >> 1] = pack_pair<BF16>(p0, p1);
-          }
-          st_shared_v4a(row_base + ((ch ^ (r & 7)) << 4), pk[0], pk[1], pk[2], pk[3]);
+      for (int x = 0; x < HK; x += 2) {
+        float p0 = ex2_approx(fmaf(__uint_as_float(v[x]), scale_log2, neg_m));
+        float p1 = ex2_approx(fmaf(__uint_as_float(v[x + 1]), scale_log2, neg_m));
+        if (diag) {
+          p0 = (kbase + x <= pos) ? p0 : 0.f;
+          p1 = (kbase + x + 1 <= pos) ? p1 : 0.f;
         }
-        l += (rsp[0] + rsp[1]) + (rsp[2] + rsp[3]);
-        if (j == n_tiles - 1 && j * TK + r >= kv_len) {
-          // key row r of this tile lies past the cache's filled range: zero its V row (once
-          // the tile has landed) so a zero probability never meets a stale NaN / Inf in the
-          // PV product
-          if (!mbar_wait(v_full(s), (j >> 1) & 1, abort_flag)) failed = true;
-          for (int h = half; h < NH; h += 2)
-            for (int ch = 0; ch < 8; ++ch) st_shared_v4a(v_tile(s) + h * (TK * 128) + r * 128 + ch * 16, 0, 0, 0, 0);
-        }
+        rsp[(x >> 1) & 3] += p0 + p1;
+        pk[x >> 1] = pack_pair<BF16>(p0, p1);
       }
-      fence_proxy_async_smem();
+      l += (rsp[0] + rsp[1]) + (rsp[2] + rsp[3]);
+      // P_j over the first TK/2 columns of S buffer s: keys 2c, 2c+1 in column c
+      tmem_st_32x32b_x32(sbuf + half * (HK / 2), pk);
+      if (j == n_tiles - 1 && j * TK + r >= kv_len) {
+        // key row r of this tile lies past the cache's filled range: zero its V row (once
+        // the tile has landed) so a zero probability never meets a stale NaN / Inf in the
+        // PV product
+        const int vs = j % KS;
+        if (!mbar_wait(v_full(vs), (j / KS) & 1, abort_flag)) failed = true;
+        for (int h = half; h < NH; h += 2)
+          for (int ch = 0; ch < 8; ++ch) st_shared_v4a(v_tile(vs) + h * (TK * 128) + r * 128 + ch * 16, 0, 0, 0, 0);
+        fence_proxy_async_smem();
+      }
+      tmem_st_wait();
+      tc_fence_before();
       mbar_arrive(p_full(s));
     }
     // ------------------------------------------------------------------ epilogue
@@ -430,22 +447,17 @@ cudaError_t launch_tc(const pf_config& c, const void* q, const void* kc, const v
   const int G = c.n_q_heads / c.n_kv_heads;
   const int BT = TQ / G;
   const uint64_t rows = static_cast<uint64_t>(c.n_layers) * c.n_kv_heads * c.max_seq;
-  CUtensorMap tq, tk, tv;
-  const uint64_t qd[3] = {static_cast<uint64_t>(HD), static_cast<uint64_t>(c.n_q_heads),
-                          static_cast<uint64_t>(M)};
-  const uint64_t qs[2] = {static_cast<uint64_t>(HD) * 2, static_cast<uint64_t>(c.n_q_heads) * HD * 2};
-  const uint32_t qb[3] = {64, static_cast<uint32_t>(G), static_cast<uint32_t>(BT)};
+  CUtensorMap tk, tv;
   const uint64_t kd[2] = {static_cast<uint64_t>(HD), rows};
   const uint64_t ks[1] = {static_cast<uint64_t>(HD) * 2};
   const uint32_t kb[2] = {64, static_cast<uint32_t>(TK)};
-  if (!encode_tmap_16(&tq, BF16, 3, q, qd, qs, qb) || !encode_tmap_16(&tk, BF16, 2, kc, kd, ks, kb) ||
-      !encode_tmap_16(&tv, BF16, 2, vc, kd, ks, kb))
+  if (!encode_tmap_16(&tk, BF16, 2, kc, kd, ks, kb) || !encode_tmap_16(&tv, BF16, 2, vc, kd, ks, kb))
     return cudaErrorInvalidValue;
   dim3 grid((M + BT - 1) / BT, c.n_kv_heads);
   const float scale_log2 = 1.4426950408889634f / sqrtf(static_cast<float>(HD));
-  return launch_pdl(attn_tc_kernel<HD, BF16>, grid, dim3(THREADS), ASmem<HD>::BYTES, st, tq, tk, tv,
-                    M, c.n_q_heads, c.n_kv_heads, c.max_seq, layer, start_dev, start_host, scale_log2,
-                    reinterpret_cast<__half*>(out), status);
+  return launch_pdl(attn_tc_kernel<HD, BF16>, grid, dim3(THREADS), ASmem<HD>::BYTES, st, tk, tv,
+                    reinterpret_cast<const uint16_t*>(q), M, c.n_q_heads, c.n_kv_heads, c.max_seq,
+                    layer, start_dev, start_host, scale_log2, reinterpret_cast<__half*>(out), status);
 }
 
 template <int HD, int BF16>
