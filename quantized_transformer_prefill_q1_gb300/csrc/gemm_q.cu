@@ -304,39 +304,40 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t idesc = idesc_f16(BM, BN, 0);
-      int it = 0;
-      bool ok = true;
-      for (int k = 0; k < rg.n && ok; ++k) {
-        const Segment sg = rg.at(plan, k);
-        const int b = k & 1;
-        const uint32_t use = static_cast<uint32_t>(k >> 1);
-        if (!mbar_wait(acc_empty(b), (use & 1) ^ 1, abort_flag)) {
-          ok = false;
-          break;
-        }
+    // The whole warp runs the loop (uniform control flow and operands); one elected lane
+    // issues each MMA / commit. Wait outcomes are made warp-uniform by vote.
+    constexpr uint32_t idesc = idesc_f16(BM, BN, 0);
+    int it = 0;
+    bool ok = true;
+    for (int k = 0; k < rg.n && ok; ++k) {
+      const Segment sg = rg.at(plan, k);
+      const int b = k & 1;
+      const uint32_t use = static_cast<uint32_t>(k >> 1);
+      if (!__all_sync(0xffffffffu, mbar_wait(acc_empty(b), (use & 1) ^ 1, abort_flag))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t d_tmem = tmem_base + b * BN;
+      for (int i = 0; i < sg.nkb; ++i, ++it) {
+        const int s = it % S;
+        const uint32_t ph = (it / S) & 1;
+        ok = __all_sync(0xffffffffu,
+                        mbar_wait(bfull(s), ph, abort_flag) && mbar_wait(full(s), ph, abort_flag));
+        if (!ok) break;
         tc_fence_after();
-        const uint32_t d_tmem = tmem_base + b * BN;
-        for (int i = 0; i < sg.nkb; ++i, ++it) {
-          const int s = it % S;
-          const uint32_t ph = (it / S) & 1;
-          ok = mbar_wait(bfull(s), ph, abort_flag) && mbar_wait(full(s), ph, abort_flag);
-          if (!ok) break;
-          tc_fence_after();
-          const uint64_t ad = sdesc_kmajor_sw128(a_st + s * A_STAGE);
-          const uint64_t bd = sdesc_kmajor_sw128(b_st + s * B_STAGE);
+        const uint64_t ad = sdesc_kmajor_sw128(a_st + s * A_STAGE);
+        const uint64_t bd = sdesc_kmajor_sw128(b_st + s * B_STAGE);
 #pragma unroll
-          for (int kk = 0; kk < BK / 16; ++kk)
-            umma_f16_ss(d_tmem, ad + 2 * kk, bd + 2 * kk, idesc, (i | kk) != 0);
-          umma_commit(empty(s));
-        }
-        if (ok) umma_commit(acc_full(b));
+        for (int kk = 0; kk < BK / 16; ++kk)
+          umma_f16_ss_warp(d_tmem, ad + 2 * kk, bd + 2 * kk, idesc, (i | kk) != 0);
+        umma_commit_warp(empty(s));
       }
-      if (!ok) {
-        umma_commit(drain_bar);  // wait for any MMA still reading shared memory / TMEM
-        mbar_wait_drain(drain_bar, 0);
-      }
+      if (ok) umma_commit_warp(acc_full(b));
+    }
+    if (!ok) {
+      umma_commit_warp(drain_bar);  // wait for any MMA still reading shared memory / TMEM
+      mbar_wait_drain(drain_bar, 0);
     }
   } else if (warp >= FIRST_DQ_WARP) {
     // ---------------------------------------------------------------- dequantisers
@@ -522,7 +523,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    __syncwarp();  // lane 0 ran the MMA loop: reconverge before the collective dealloc
+    __syncwarp();  // reconverge before the collective dealloc
     tmem_dealloc(tmem_base, TMEM_COLS);
   }
   if (threadIdx.x == 0 && *abort_flag && status != nullptr) atomicCAS(status, 0, PF_ERR_DEVICE_TIMEOUT);
