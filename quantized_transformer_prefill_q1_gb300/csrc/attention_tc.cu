@@ -8,18 +8,18 @@
 //
 // One CTA = one kv head and 128 query rows (128/G tokens x the G query heads that share
 // the kv head; row = token * G + head-in-group), so every row reads the same K/V tiles.
-// Q and the probabilities P live in tensor memory and are the MMAs' A operand, so the
-// shared-memory traffic per 128-key tile is K and V only (written by TMA, read by the MMA):
-//   warp 0      TMA: 128-key K and V tiles straight from the cache [layer][kvh][pos][hd]
-//               into two 3-stage rings; a K stage is free again once its QK^T is done, so
-//               K runs a tile ahead of V;
-//   warp 1      TMEM (512 columns: two S buffers of 128, O, Q) and the MMAs:
-//               S_j = Q K_j^T (Q from TMEM, K K-major), then O += P_{j-1} V_{j-1} (P from
-//               TMEM over S_{j-1}'s columns, V used MN-major as it lies in the cache), so
-//               QK^T of tile j overlaps the softmax of tile j-1;
+// The probabilities P stay in tensor memory as the A operand of the PV product:
+//   warp 0      TMA: the Q tile once (3-D map over q[M][nq][hd]), then 128-key K and V tiles
+//               straight from the cache [layer][kvh][pos][hd] into two 3-stage rings; a K
+//               stage is free again once its QK^T is done, so K runs a tile ahead of V;
+//   warp 1      TMEM (512 columns: three S buffers of 128 and O) and the MMAs, issued by
+//               the whole warp with one elected lane: S_0, S_1, then per tile
+//               O += P_j V_j (P from TMEM over S_j's columns, V used MN-major as it lies in
+//               the cache) followed by S_{j+2} = Q K_{j+2}^T, so the scores of the next
+//               tile are ready before the softmax reaches it;
 //   warps 2..9  softmax, two threads per query row: warp w reads TMEM lane quarter w % 4
 //               and takes key columns [0, 64) (warps 2..5) or [64, 128) (warps 6..9) of
-//               each tile. First they write the Q rows into TMEM. Per tile: read S_j,
+//               each tile. Per tile: read S_j,
 //               causal mask (key > pos: -inf), row max combined with the partner thread
 //               through shared memory, online softmax in the exp2 domain, P_j (bf16/f16)
 //               back into TMEM; the running max is raised only when a tile's max exceeds it
@@ -40,17 +40,17 @@ constexpr int KS = 3;            // K and V ring stages
 constexpr int THREADS = 320;     // warp 0 TMA, warp 1 MMA, warps 2..9 softmax
 constexpr int SM_THREADS = 256;  // softmax threads: two per query row
 constexpr int HK = TK / 2;       // keys per softmax thread and tile
+constexpr int NSB = 3;           // S / P buffers in TMEM
 constexpr float RESCALE_LOG2 = 8.0f;
-// TMEM columns: S buffers at 0 and TK (P_j over the first TK/2 columns of its buffer),
-// O at 2 TK, Q at 3 TK
-constexpr uint32_t COL_O = 2 * TK;
-constexpr uint32_t COL_Q = 3 * TK;
+// TMEM columns: S buffers b at b TK (P_j over the first TK/2 columns of its buffer), O at 3 TK
+constexpr uint32_t COL_O = NSB * TK;
 
 template <int HD>
 struct ASmem {
+  static constexpr int Q = TQ * HD * 2;
   static constexpr int KV = TK * HD * 2;  // one K or V tile
   static constexpr int RED = 2 * TQ * 4;  // partner exchange: [half][row] f32
-  static constexpr int BYTES = 1024 + 2 * KS * KV + RED + 256;
+  static constexpr int BYTES = 1024 + Q + 2 * KS * KV + RED + 256;
   static_assert(BYTES <= 232448, "attention shared memory");
 };
 
@@ -105,8 +105,8 @@ __device__ __forceinline__ uint32_t pack_pair(float a, float b) {
 
 template <int HD, int BF16>
 __global__ void __launch_bounds__(THREADS, 1)
-    attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-                   const uint16_t* __restrict__ q, int M, int nq, int nkv, int max_seq, int layer,
+    attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                   const __grid_constant__ CUtensorMap tm_v, int M, int nq, int nkv, int max_seq, int layer,
                    const int* __restrict__ start_dev, int start_host, float scale_log2,
                    __half* __restrict__ out, int* __restrict__ status) {
   using L = ASmem<HD>;
@@ -115,7 +115,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* gbase = smem_raw + (base - raw);
-  const uint32_t k_s = base;                // K stage s at k_s + s * KV
+  const uint32_t q_s = base;
+  const uint32_t k_s = q_s + L::Q;          // K stage s at k_s + s * KV
   const uint32_t v_s = k_s + KS * L::KV;    // V stage s at v_s + s * KV
   const uint32_t red_s = v_s + KS * L::KV;
   const uint32_t bar0 = red_s + L::RED;
@@ -123,15 +124,17 @@ __global__ void __launch_bounds__(THREADS, 1)
   auto k_empty = [&](int s) { return bar0 + 8u * (KS + s); };
   auto v_full = [&](int s) { return bar0 + 8u * (2 * KS + s); };
   auto v_empty = [&](int s) { return bar0 + 8u * (3 * KS + s); };
-  auto s_full = [&](int s) { return bar0 + 8u * (4 * KS + s); };
-  auto s_empty = [&](int s) { return bar0 + 8u * (4 * KS + 2 + s); };
-  auto p_full = [&](int s) { return bar0 + 8u * (4 * KS + 4 + s); };
-  const uint32_t q_ready = bar0 + 8u * (4 * KS + 6);
-  const uint32_t o_done = bar0 + 8u * (4 * KS + 7);
-  const uint32_t o_final = bar0 + 8u * (4 * KS + 8);
-  const uint32_t drain_bar = bar0 + 8u * (4 * KS + 9);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + (bar0 + 8u * (4 * KS + 10) - base));
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + (bar0 + 8u * (4 * KS + 11) - base));
+  auto s_full = [&](int b) { return bar0 + 8u * (4 * KS + b); };
+  auto s_empty = [&](int b) { return bar0 + 8u * (4 * KS + NSB + b); };
+  auto p_full = [&](int b) { return bar0 + 8u * (4 * KS + 2 * NSB + b); };
+  constexpr int NB = 4 * KS + 3 * NSB;  // barriers so far
+  const uint32_t q_full = bar0 + 8u * NB;
+  const uint32_t o_done = bar0 + 8u * (NB + 1);
+  const uint32_t o_final = bar0 + 8u * (NB + 2);
+  const uint32_t drain_bar = bar0 + 8u * (NB + 3);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + (bar0 + 8u * (NB + 4) - base));
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + (bar0 + 8u * (NB + 5) - base));
+  static_assert(8 * (NB + 6) <= 256, "barrier area");
   auto k_tile = [&](int s) { return k_s + s * L::KV; };
   auto v_tile = [&](int s) { return v_s + s * L::KV; };
 
@@ -156,12 +159,12 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_init(v_full(s), 1);
       mbar_init(v_empty(s), 1);
     }
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(s_full(s), 1);
-      mbar_init(s_empty(s), 1);
-      mbar_init(p_full(s), SM_THREADS);
+    for (int b = 0; b < NSB; ++b) {
+      mbar_init(s_full(b), 1);
+      mbar_init(s_empty(b), 1);
+      mbar_init(p_full(b), SM_THREADS);
     }
-    mbar_init(q_ready, SM_THREADS);
+    mbar_init(q_full, 1);
     mbar_init(o_done, 1);
     mbar_init(o_final, 1);
     mbar_init(drain_bar, 1);
@@ -178,11 +181,13 @@ __global__ void __launch_bounds__(THREADS, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const uint32_t tmem_o = tmem + COL_O;
-  const uint32_t tmem_q = tmem + COL_Q;
 
   if (warp == 0) {
     // ------------------------------------------------------------------ TMA producer
     if (lane == 0) {
+      mbar_arrive_expect_tx(q_full, L::Q);
+      for (int h = 0; h < NH; ++h)
+        tma_load_3d(q_s + h * (TQ * 128), &tm_q, h * 64, kvh * G, t0, q_full);
       // K_i, then V_{i-1}: K runs one tile ahead of V
       int k_issued = 0, v_issued = 0;
       bool ok = true;
@@ -211,6 +216,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
       }
       if (*abort_flag) {  // let copies already in flight land before shared memory is released
+        mbar_wait_drain_a(q_full, 0);
         for (int j = max(0, k_issued - KS); j < k_issued; ++j) mbar_wait_drain_a(k_full(j % KS), (j / KS) & 1);
         for (int j = max(0, v_issued - KS); j < v_issued; ++j) mbar_wait_drain_a(v_full(j % KS), (j / KS) & 1);
       }
@@ -221,42 +227,45 @@ __global__ void __launch_bounds__(THREADS, 1)
     // issues each MMA / commit. Wait outcomes are made warp-uniform by vote.
     constexpr uint32_t idesc_s = idesc_f16(TQ, TK, BF16, 0);
     constexpr uint32_t idesc_o = idesc_f16(TQ, HD, BF16, 1);
-    bool ok = __all_sync(0xffffffffu, mbar_wait(q_ready, 0, abort_flag));
-    for (int j = 0; j <= n_tiles && ok; ++j) {
-      if (j < n_tiles) {  // S_j = Q K_j^T into S buffer j % 2
-        const int s = j & 1, ks = j % KS;
-        if (!__all_sync(0xffffffffu, mbar_wait(k_full(ks), (j / KS) & 1, abort_flag) &&
-                                         mbar_wait(s_empty(s), ((j >> 1) & 1) ^ 1, abort_flag))) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
+    // S_j = Q K_j^T into S buffer j % 3
+    auto issue_s = [&](int j) -> bool {
+      const int sb = j % NSB, ks = j % KS;
+      if (!__all_sync(0xffffffffu, mbar_wait(k_full(ks), (j / KS) & 1, abort_flag) &&
+                                       mbar_wait(s_empty(sb), ((j / NSB) & 1) ^ 1, abort_flag)))
+        return false;
+      tc_fence_after();
 #pragma unroll
-        for (int kc = 0; kc < HD / 16; ++kc) {
-          const uint32_t offk = (kc >> 2) * (TK * 128) + (kc & 3) * 32;
-          umma_f16_ts_warp(tmem + s * TK, tmem_q + 8 * kc, sdesc_kmajor_sw128(k_tile(ks) + offk),
-                           idesc_s, kc > 0);
-        }
-        umma_commit_warp(s_full(s));
-        umma_commit_warp(k_empty(ks));  // K_j is free once QK^T is done
+      for (int kc = 0; kc < HD / 16; ++kc) {
+        const uint32_t off = (kc >> 2) * (TQ * 128) + (kc & 3) * 32;
+        const uint32_t offk = (kc >> 2) * (TK * 128) + (kc & 3) * 32;
+        umma_f16_ss_warp(tmem + sb * TK, sdesc_kmajor_sw128(q_s + off),
+                         sdesc_kmajor_sw128(k_tile(ks) + offk), idesc_s, kc > 0);
       }
-      if (j >= 1) {  // O += P_{j-1} V_{j-1}, P from TMEM over S_{j-1}'s columns
-        const int i = j - 1, s = i & 1, vs = i % KS;
-        if (!__all_sync(0xffffffffu, mbar_wait(p_full(s), (i >> 1) & 1, abort_flag) &&
-                                         mbar_wait(v_full(vs), (i / KS) & 1, abort_flag))) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
+      umma_commit_warp(s_full(sb));
+      umma_commit_warp(k_empty(ks));  // K_j is free once QK^T is done
+      return true;
+    };
+    bool ok = __all_sync(0xffffffffu, mbar_wait(q_full, 0, abort_flag));
+    if (ok) ok = issue_s(0);
+    if (ok && n_tiles > 1) ok = issue_s(1);
+    for (int j = 0; j < n_tiles && ok; ++j) {
+      // O += P_j V_j, P from TMEM over S_j's columns
+      const int sb = j % NSB, vs = j % KS;
+      if (!__all_sync(0xffffffffu, mbar_wait(p_full(sb), (j / NSB) & 1, abort_flag) &&
+                                       mbar_wait(v_full(vs), (j / KS) & 1, abort_flag))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
 #pragma unroll
-        for (int kc = 0; kc < TK / 16; ++kc)
-          umma_f16_ts_warp(tmem_o, tmem + s * TK + 8 * kc,
-                           sdesc_mnmajor_sw128(v_tile(vs) + kc * 2048, TK * 128), idesc_o,
-                           (i > 0 || kc > 0));
-        umma_commit_warp(s_empty(s));  // P_{j-1} consumed: S buffer reusable
-        umma_commit_warp(v_empty(vs));
-        umma_commit_warp(o_done);
-      }
+      for (int kc = 0; kc < TK / 16; ++kc)
+        umma_f16_ts_warp(tmem_o, tmem + sb * TK + 8 * kc,
+                         sdesc_mnmajor_sw128(v_tile(vs) + kc * 2048, TK * 128), idesc_o,
+                         (j > 0 || kc > 0));
+      umma_commit_warp(s_empty(sb));  // P_j consumed: S buffer reusable
+      umma_commit_warp(v_empty(vs));
+      umma_commit_warp(o_done);
+      if (j + 2 < n_tiles) ok = issue_s(j + 2);
     }
     if (ok) {
       umma_commit_warp(o_final);
@@ -273,39 +282,14 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int t_loc = r / G, h_loc = r - (r / G) * G;
     const int pos = start + t0 + t_loc;
     volatile float* red = reinterpret_cast<volatile float*>(gbase + (red_s - base));  // [2][TQ]
-    // Q row r into TMEM (lane r, head-dim pairs packed per column): this thread writes
-    // dims [64 half, 64 half + 64) when they exist; rows past the chunk are zero
-    if (64 * half < HD) {
-      uint32_t qv[32];
-      const int t = t0 + t_loc;
-      if (t < M) {
-        const uint4* src = reinterpret_cast<const uint4*>(
-            q + (static_cast<size_t>(t) * nq + kvh * G + h_loc) * HD + 64 * half);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const uint4 x = src[i];
-          qv[4 * i] = x.x;
-          qv[4 * i + 1] = x.y;
-          qv[4 * i + 2] = x.z;
-          qv[4 * i + 3] = x.w;
-        }
-      } else {
-#pragma unroll
-        for (int i = 0; i < 32; ++i) qv[i] = 0u;
-      }
-      tmem_st_32x32b_x32(tmem_q + lane_off + 32 * half, qv);
-      tmem_st_wait();
-    }
-    tc_fence_before();
-    mbar_arrive(q_ready);
     float m = -INFINITY, l = 0.f;
     bool ok = true, failed = false;
     // tcgen05.ld / tcgen05.st are warp-collective: every branch around them is warp-uniform.
     // The 256 softmax threads meet at named barrier 1 twice per tile; a failed wait is
     // carried to the next barrier-and, where all of them stop together.
     for (int j = 0; j < n_tiles; ++j) {
-      const int s = j & 1;
-      const bool got = mbar_wait(s_full(s), (j >> 1) & 1, abort_flag);
+      const int s = j % NSB;
+      const bool got = mbar_wait(s_full(s), (j / NSB) & 1, abort_flag);
       if (!named_bar_and_a(1, SM_THREADS, got && !failed)) {
         ok = false;
         break;
@@ -447,17 +431,22 @@ cudaError_t launch_tc(const pf_config& c, const void* q, const void* kc, const v
   const int G = c.n_q_heads / c.n_kv_heads;
   const int BT = TQ / G;
   const uint64_t rows = static_cast<uint64_t>(c.n_layers) * c.n_kv_heads * c.max_seq;
-  CUtensorMap tk, tv;
+  CUtensorMap tq, tk, tv;
+  const uint64_t qd[3] = {static_cast<uint64_t>(HD), static_cast<uint64_t>(c.n_q_heads),
+                          static_cast<uint64_t>(M)};
+  const uint64_t qs[2] = {static_cast<uint64_t>(HD) * 2, static_cast<uint64_t>(c.n_q_heads) * HD * 2};
+  const uint32_t qb[3] = {64, static_cast<uint32_t>(G), static_cast<uint32_t>(BT)};
   const uint64_t kd[2] = {static_cast<uint64_t>(HD), rows};
   const uint64_t ks[1] = {static_cast<uint64_t>(HD) * 2};
   const uint32_t kb[2] = {64, static_cast<uint32_t>(TK)};
-  if (!encode_tmap_16(&tk, BF16, 2, kc, kd, ks, kb) || !encode_tmap_16(&tv, BF16, 2, vc, kd, ks, kb))
+  if (!encode_tmap_16(&tq, BF16, 3, q, qd, qs, qb) || !encode_tmap_16(&tk, BF16, 2, kc, kd, ks, kb) ||
+      !encode_tmap_16(&tv, BF16, 2, vc, kd, ks, kb))
     return cudaErrorInvalidValue;
   dim3 grid((M + BT - 1) / BT, c.n_kv_heads);
   const float scale_log2 = 1.4426950408889634f / sqrtf(static_cast<float>(HD));
-  return launch_pdl(attn_tc_kernel<HD, BF16>, grid, dim3(THREADS), ASmem<HD>::BYTES, st, tk, tv,
-                    reinterpret_cast<const uint16_t*>(q), M, c.n_q_heads, c.n_kv_heads, c.max_seq,
-                    layer, start_dev, start_host, scale_log2, reinterpret_cast<__half*>(out), status);
+  return launch_pdl(attn_tc_kernel<HD, BF16>, grid, dim3(THREADS), ASmem<HD>::BYTES, st, tq, tk, tv,
+                    M, c.n_q_heads, c.n_kv_heads, c.max_seq, layer, start_dev, start_host,
+                    scale_log2, reinterpret_cast<__half*>(out), status);
 }
 
 template <int HD, int BF16>
