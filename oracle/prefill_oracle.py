@@ -19,8 +19,8 @@ Step order follows oxibonsai-kernels metal_prefill.rs ``encode_layer_prefill``
 turbospark-runtime families/llama/prefill.rs ``prefill_chunk_real_llama_dense``.
 The per-token decode restatement follows metal_full_layer.rs ``encode_layer_into``.
 
-Readings where the pages are silent are listed in the design doc (A1-A16); each
-function names the reading it takes.
+Where the pages are silent, each function states the reading it takes (numbered
+A1-A16 throughout this package's notes).
 
 Parity status: every function below is pinned by ``tests/test_oracle_pins.py``
 except the composition of a full stack's logits, which has no worked example on

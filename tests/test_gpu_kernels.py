@@ -1,6 +1,6 @@
 """Step-level parity: each libpf kernel (through the C ABI) against the CPU oracle on the
 same seeded inputs. Integer / byte / index work is compared bit-exactly; floating point
-within the tolerance stated at each test (derived in the design doc)."""
+within the tolerance stated (and derived) at each test."""
 import numpy as np
 import pytest
 
