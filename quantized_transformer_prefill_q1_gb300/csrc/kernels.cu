@@ -7,6 +7,8 @@
 #include "dequant.cuh"
 #include "ptx.cuh"
 
+#include <algorithm>
+
 namespace pf {
 namespace {
 
@@ -427,12 +429,121 @@ cudaError_t launch_embed(const float* E, const int* tokens, int M, int H, int vo
   return launch_pdl(embed_kernel, dim3(M), dim3(256), 0, stream, E, tokens, H, vocab, x, status);
 }
 
+// Q1 LM head (P1 section "LM-head GEMV"): logits[n] = sum_g s[n,g] sum_{k in g} (+-y_k) with
+// y = RMSNorm(x_row). Each 32-bit sign word holds 8 nibbles; nibble n of word u covers four
+// elements of one parity (even for n < 4, odd for n >= 4, see the packed layout), so the 16
+// signed sums of those four y values are tabulated once per CTA (64 KB for H = 4096) and
+// every nibble of every row costs one table lookup and one add. A warp's 32 rows read the
+// same nibble table: at most 16 distinct words in distinct banks, no conflicts.
+__device__ __forceinline__ int q1_nibble_elem(int n, int b) {  // element of bit b of nibble n
+  return n < 4 ? 30 - 8 * n - 2 * b : 31 - 8 * (n - 4) - 2 * b;
+}
+
+// Table value for nibble N of sign word Z, the word's table at shared address `base`
+// (512-B aligned): one shift, one LOP3 merging (nibble * 4) into the address, one load with
+// the nibble's 64-B slot as immediate offset.
+template <int N>
+__device__ __forceinline__ float q1_lut_ld(uint32_t Z, uint32_t base) {
+  const uint32_t sh = N == 0 ? (Z << 2) : (Z >> (4 * N - 2));
+  uint32_t a;
+  asm("lop3.b32 %0, %1, 0x3C, %2, 0xEA;" : "=r"(a) : "r"(sh), "r"(base));
+  float t;
+  // volatile: the table is written before a barrier; the load must stay after it
+  asm volatile("ld.shared.f32 %0, [%1+%2];" : "=f"(t) : "r"(a), "n"(64 * N));
+  return t;
+}
+
+__global__ void __launch_bounds__(512) lm_head_q1_kernel(const float* __restrict__ x_row,
+                                                         const float* __restrict__ nw, float eps,
+                                                         const uint8_t* __restrict__ W, int vocab,
+                                                         int H, float* __restrict__ logits) {
+  // [H/32 words][8 nibbles][16 values] (each word's table 512-B aligned), then y [H], then [256]
+  extern __shared__ __align__(1024) float lut[];
+  __shared__ float red[32];
+  float* ys = lut + (H / 32) * 8 * 16;
+  float* half_sum = ys + H;
+  const uint32_t lut_s = smem_u32(lut);
+  griddep_launch_dependents();
+  griddep_wait();
+  float ss = 0.f;
+  for (int i = threadIdx.x; i < H; i += blockDim.x) {
+    const float v = x_row[i];
+    ss += v * v;
+  }
+  ss = block_sum(ss, red);
+  const float r = rsqrtf(ss / static_cast<float>(H) + eps);
+  for (int i = threadIdx.x; i < H; i += blockDim.x) ys[i] = x_row[i] * r * nw[i];
+  __syncthreads();
+  // table entry (u, n, v): sum over the nibble's four elements, negated where v's bit is set
+  for (int e = threadIdx.x; e < (H / 32) * 8 * 16; e += blockDim.x) {
+    const int v = e & 15, n = (e >> 4) & 7, u = e >> 7;
+    const float* yu = ys + 32 * u;
+    float t = 0.f;
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      const float y = yu[q1_nibble_elem(n, b)];
+      t += (v >> b) & 1 ? -y : y;
+    }
+    lut[e] = t;
+  }
+  __syncthreads();
+  // two threads per weight row, each over half of the groups (more loads in flight per SM)
+  const int G = H / GROUP;
+  const int tiles = (vocab + TILE_N - 1) / TILE_N;
+  const int rr = threadIdx.x & (TILE_N - 1);
+  const int part = threadIdx.x >> 8;
+  const int g0 = part * (G / 2), g1 = part ? G : G / 2;
+  for (int tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
+    const uint8_t* tw = W + static_cast<size_t>(tile) * G * Q1_CHUNK_BYTES;
+    float acc = 0.f;
+#pragma unroll 4
+    for (int g = g0; g < g1; ++g) {
+      const uint8_t* ch = tw + static_cast<size_t>(g) * Q1_CHUNK_BYTES;
+      const uint2 h0 = __ldg(reinterpret_cast<const uint2*>(ch + rr * 8));
+      const uint2 h1 = __ldg(reinterpret_cast<const uint2*>(ch + Q1_HALF_BYTES + rr * 8));
+      const float s = __half2float(__ushort_as_half(__ldg(reinterpret_cast<const unsigned short*>(ch + Q1_SCALE_OFF) + rr)));
+      const uint32_t words[4] = {h0.x, h0.y, h1.x, h1.y};
+      float p[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int w = 0; w < 4; ++w) {
+        // word w's table starts 512-B aligned, so (nibble * 4) merges into the address with
+        // one LOP3 and the nibble's 64-B slot is the load's immediate offset
+        const uint32_t base = lut_s + (4 * g + w) * 512;
+        const uint32_t Z = words[w];
+        p[0] += q1_lut_ld<0>(Z, base);
+        p[1] += q1_lut_ld<1>(Z, base);
+        p[2] += q1_lut_ld<2>(Z, base);
+        p[3] += q1_lut_ld<3>(Z, base);
+        p[0] += q1_lut_ld<4>(Z, base);
+        p[1] += q1_lut_ld<5>(Z, base);
+        p[2] += q1_lut_ld<6>(Z, base);
+        p[3] += q1_lut_ld<7>(Z, base);
+      }
+      acc = fmaf(s, (p[0] + p[1]) + (p[2] + p[3]), acc);
+    }
+    if (part) half_sum[rr] = acc;
+    __syncthreads();
+    const int row = tile * TILE_N + rr;
+    if (!part && row < vocab) logits[row] = acc + half_sum[rr];
+    __syncthreads();
+  }
+}
+
 cudaError_t launch_lm_head(int wfmt, const float* x_row, const float* norm_w, float eps,
                            const uint8_t* packed, int vocab, int H, float* logits,
                            cudaStream_t stream) {
   const int tiles = static_cast<int>(padded_rows(vocab) / TILE_N);
   const size_t smem = (static_cast<size_t>(H) + H / GROUP) * sizeof(float);
-  if (wfmt == PF_W_Q1_G128) {
+  // H % 32 == 0 (H % 128 is checked); table + y row: 68 KB at H = 4096, two CTAs per SM
+  const size_t smem_q1 = (static_cast<size_t>(H / 32) * 8 * 16 + H + TILE_N) * sizeof(float);
+  if (wfmt == PF_W_Q1_G128 && smem_q1 <= 227 * 1024) {
+    if (smem_q1 > 48 * 1024)
+      cudaFuncSetAttribute(lm_head_q1_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(smem_q1));
+    const int ctas = std::min(tiles, 2 * device_sm_count());
+    launch_pdl(lm_head_q1_kernel, dim3(ctas), dim3(512), smem_q1, stream, x_row, norm_w, eps, packed,
+               vocab, H, logits);
+  } else if (wfmt == PF_W_Q1_G128) {  // rows too wide for the table: one row per thread
     if (smem > 48 * 1024)
       cudaFuncSetAttribute(lm_head_kernel<PF_W_Q1_G128>,
                            cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));

@@ -269,7 +269,8 @@ def test_embed_bit_exact():
     assert np.all(got[5] == 0) and np.array_equal(np.delete(got, 5, 0), np.delete(E[toks], 5, 0))
 
 
-@pytest.mark.parametrize("fmt,vocab,h", [("q1", 1000, 256), ("int4", 1000, 256), ("q1", 151936, 4096)])
+@pytest.mark.parametrize("fmt,vocab,h", [("q1", 1000, 256), ("int4", 1000, 256), ("q1", 151936, 4096),
+                                         ("q1", 77777, 1024), ("q1", 300, 16384)])
 def test_lm_head_vs_oracle(fmt, vocab, h):
     rng = synth.rng_for(18, vocab, h)
     w = synth.quant_weight(fmt, rng, vocab, h)
