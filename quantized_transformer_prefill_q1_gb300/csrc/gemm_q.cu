@@ -37,9 +37,13 @@
 
 #include "dequant.cuh"
 #include "ptx.cuh"
+#include "streamk.cuh"
 
 namespace pf {
 namespace {
+using sk::Plan;
+using sk::Range;
+using sk::Segment;
 
 constexpr int BM = 128;
 constexpr int BN = 256;
@@ -150,60 +154,6 @@ __device__ __forceinline__ void dequant_row_smem(const uint8_t* p, int r, uint32
     }
   }
 }
-
-// ------------------------------------------------------------------ stream-K partition
-// n_mt x n_nt tiles of kbt k-blocks each, `total` k-blocks in all; CTA c owns
-// [total c / ctas, total (c + 1) / ctas).
-struct Plan {
-  int n_mt, n_nt, kbt;
-  long long total;
-  int ctas;
-  __device__ __forceinline__ long long begin(int c) const { return total * c / ctas; }
-  // CTA whose range holds k-block w
-  __device__ __forceinline__ int owner(long long w) const {
-    return static_cast<int>(((w + 1) * ctas - 1) / total);
-  }
-  // scratch slot (0 or 1) of contributor c's partial for `tile`: 0 if c's range begins
-  // inside the tile, 1 if it begins at or before the tile's start
-  __device__ __forceinline__ int slot(int c, int tile) const {
-    return begin(c) > static_cast<long long>(tile) * kbt ? 0 : 1;
-  }
-};
-
-struct Segment {
-  int tile, mt, nt, kb0, nkb;
-  bool whole;
-};
-
-// The segments of one CTA's range in processing order: the partial first and last
-// segments (if any) come first, then the whole tiles in k order.
-struct Range {
-  long long b, e;
-  int t0, n, first_part, last_part;
-  __device__ __forceinline__ Range(const Plan& p, int c) {
-    b = p.begin(c);
-    e = p.begin(c + 1);
-    t0 = static_cast<int>(b / p.kbt);
-    const int t1 = static_cast<int>((e - 1) / p.kbt);
-    n = t1 - t0 + 1;
-    const long long s0_end = std::min<long long>(e, static_cast<long long>(t0 + 1) * p.kbt);
-    first_part = (b == static_cast<long long>(t0) * p.kbt && s0_end - b == p.kbt) ? 0 : 1;
-    last_part = (n > 1 && e != static_cast<long long>(t1 + 1) * p.kbt) ? 1 : 0;
-  }
-  __device__ __forceinline__ Segment at(const Plan& p, int k) const {
-    const int i = k < first_part ? 0 : (k < first_part + last_part ? n - 1 : k - last_part);
-    Segment s;
-    s.tile = t0 + i;
-    const long long ts = static_cast<long long>(s.tile) * p.kbt;
-    const long long lo = std::max(b, ts), hi = std::min(e, ts + p.kbt);
-    s.kb0 = static_cast<int>(lo - ts);
-    s.nkb = static_cast<int>(hi - lo);
-    s.whole = s.nkb == p.kbt;
-    s.nt = s.tile / p.n_mt;
-    s.mt = s.tile - s.nt * p.n_mt;  // token tiles fastest: neighbouring tiles share weights
-    return s;
-  }
-};
 
 // Staging tile of one epilogue warp, f32 32 x 32 in the TMA 128-B swizzle: row r at
 // r * 128, 16-B unit j at (j ^ (r % 8)) * 16 (a warp's store of unit j hits all banks).
@@ -551,13 +501,12 @@ cudaError_t launch_t(const GemmArgs& g, const CUtensorMap& ta, const CUtensorMap
 
 }  // namespace
 
-bool encode_tmap_f16_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
-                        uint32_t box_inner, uint32_t box_outer);
 
 // Scratch of a launch with at most max_ctas CTAs: two partial tiles per CTA (a CTA's range
 // begins and ends inside at most two tiles), then one arrival counter per output tile, which
 // must be zero before the first launch (every launch that completes leaves them zero).
 size_t gemm_scratch_bytes(int M, int N, int max_ctas) {
+  // one counter per 128 x 256 tile (the small-M kernel's 256-row tiles are fewer)
   const size_t tiles = static_cast<size_t>((M + BM - 1) / BM) * (padded_rows(N) / TILE_N);
   return static_cast<size_t>(2) * max_ctas * SLOT_FLOATS * sizeof(float) + tiles * sizeof(int);
 }
@@ -581,6 +530,7 @@ cudaError_t prepare_gemm_kernels() {
 }
 
 cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t stream) {
+  if (g.M <= SMALL_M_MAX) return launch_gemm_small(g, stream);
   CUtensorMap ta, to;
   if (!encode_tmap_f16_2d(&ta, g.a, static_cast<uint64_t>(g.K), static_cast<uint64_t>(g.M), BK, BM))
     return cudaErrorInvalidValue;

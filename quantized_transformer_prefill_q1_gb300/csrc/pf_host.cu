@@ -396,6 +396,7 @@ void prepare_all() {
   static std::once_flag once;
   std::call_once(once, [] {
     prepare_gemm_kernels();
+    prepare_gemm_small_kernels();
     prepare_attention_kernels();
     prepare_attention_tc_kernels();
   });

@@ -64,6 +64,12 @@ struct GemmArgs {
   int* status;          // may be NULL
 };
 cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t stream);
+// M <= SMALL_M_MAX: the weight rows are the MMA's M side (gemm_small.cu); launch_gemm routes
+cudaError_t launch_gemm_small(const GemmArgs& g, cudaStream_t stream);
+cudaError_t prepare_gemm_small_kernels();
+constexpr int SMALL_M_MAX = 64;
+bool encode_tmap_f16_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
+                        uint32_t box_inner, uint32_t box_outer);
 // The GEMM runs at most min(max_ctas, SMs) persistent CTAs; its scratch holds two f32
 // 128 x 256 partial tiles per CTA and one arrival counter per output tile.
 constexpr int GEMM_MAX_CTAS = 160;
