@@ -52,10 +52,11 @@ def parse():
     p.add_argument("--seed", type=int, default=0)
     p.add_argument("--case", default=None,
                    choices=["gemm_gate_up", "gemm_qkv", "gemm_down", "gemm_o", "attention", "rmsnorm",
-                            "qk_rope_kv", "lm_head"],
+                            "qk_rope_kv", "lm_head", "int4_gate_up", "int4_qkv", "int4_o", "int4_down"],
                    help="small single-kernel case at the workload's shapes (for ncu captures)")
     p.add_argument("--reps", type=int, default=3)
     p.add_argument("--ctas", type=int, default=0, help="GEMM cases: most persistent CTAs (0 = the library's choice)")
+    p.add_argument("--m", type=int, default=1, help="int4_* cases: chunk tokens (Llama-3-8B-shaped INT4 layer)")
     return p.parse_args()
 
 
@@ -72,7 +73,23 @@ def run_case(args):
     M, H, I = CHUNK, s.hidden, s.intermediate
     dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()  # noqa: E731
     cfg = pf.make_config(s, CHUNK, n_layers=1)
-    if args.case.startswith("gemm"):
+    if args.case.startswith("int4"):
+        # the INT4-affine Llama-3-8B-shaped layer's projections at a few tokens (GEMV end)
+        li = synth.LLAMA3_8B_INT4_LAYER
+        n, k, epi = {"int4_gate_up": (2 * li.intermediate, li.hidden, pf.EPI_SWIGLU),
+                     "int4_qkv": (li.qkv_rows, li.hidden, pf.EPI_STORE_F32),
+                     "int4_o": (li.hidden, li.n_q_heads * li.head_dim, pf.EPI_RESID_ADD),
+                     "int4_down": (li.hidden, li.intermediate, pf.EPI_RESID_ADD)}[args.case]
+        M = args.m
+        a = dev(rng.standard_normal((M, k)).astype(np.float16))
+        w = dev(pf.pf_pack_weights_host(synth.int4_weight(rng, n, k), epi == pf.EPI_SWIGLU))
+        out = torch.zeros((M, n // 2 if epi == pf.EPI_SWIGLU else n),
+                          dtype=torch.float16 if epi == pf.EPI_SWIGLU else torch.float32, device="cuda")
+        scratch = pf.gemm_scratch(M, n, args.ctas)
+        fn = lambda: pf.pf_op_gemm(pf.W_INT4, epi, a, w, M, n, k, out, scratch, args.ctas)  # noqa: E731
+        flops = 2 * M * n * k
+        wbytes = w.numel()
+    elif args.case.startswith("gemm"):
         n, k, epi = {"gemm_gate_up": (2 * I, H, pf.EPI_SWIGLU), "gemm_qkv": (s.qkv_rows, H, pf.EPI_STORE_F32),
                      "gemm_down": (H, I, pf.EPI_RESID_ADD),
                      "gemm_o": (H, s.n_q_heads * s.head_dim, pf.EPI_RESID_ADD)}[args.case]
@@ -123,6 +140,8 @@ def run_case(args):
     e1.synchronize()
     us = e0.elapsed_time(e1) / args.reps * 1e3
     line = {"case": args.case, "us_per_launch": us, "ctas": args.ctas}
+    if args.case.startswith("int4"):
+        line.update({"m": args.m, "weight_bytes": wbytes, "weight_GBps": wbytes / us / 1e3})
     if flops:
         line["tflops"] = flops / us / 1e6
     print(json.dumps(line), flush=True)

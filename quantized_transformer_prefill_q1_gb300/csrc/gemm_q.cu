@@ -531,6 +531,15 @@ cudaError_t prepare_gemm_kernels() {
 
 cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t stream) {
   if (g.M <= SMALL_M_MAX) return launch_gemm_small(g, stream);
+  if (g.epilogue == EPI_STORE_F32 && g.max_ctas >= 0) {
+    // zero the output and accumulate every CTA's share by TMA reduce-add (no partial
+    // hand-off, all SMs busy), as the residual form does
+    cudaError_t e = cudaMemsetAsync(g.out, 0, static_cast<size_t>(g.M) * g.N * sizeof(float), stream);
+    if (e != cudaSuccess) return e;
+    GemmArgs r = g;
+    r.epilogue = EPI_RESID_ADD;
+    return launch_gemm(r, stream);
+  }
   CUtensorMap ta, to;
   if (!encode_tmap_f16_2d(&ta, g.a, static_cast<uint64_t>(g.K), static_cast<uint64_t>(g.M), BK, BM))
     return cudaErrorInvalidValue;
