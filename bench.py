@@ -37,7 +37,9 @@ PROMPT, CHUNK = 2048, 512
 
 # DRAM traffic per launch from an ncu capture of the current kernels (bytes), keyed by
 # kernel class; None when no capture matches the kernel as it now stands.
-NCU_TRAFFIC = {"gemm_gate_up": 18409216 + 420864}  # profiles/gemm_gate_up_q1_512x24576x4096.md
+# gate_up: dram__bytes_read.sum + dram__bytes_write.sum of one --set full capture of
+# `bench.py --case gemm_gate_up` (M 512, N 24576, K 4096)
+NCU_TRAFFIC = {"gemm_gate_up": 18409216 + 420864}
 
 
 def parse():
