@@ -221,18 +221,39 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  griddep_wait();  // inputs come from the previous kernel in the stream
+  // Only the activation tiles and the epilogue's global accesses depend on the previous
+  // kernel in the stream (griddep_wait below); the packed weights do not, so the producer
+  // issues the first stages' weight copies before waiting for it.
   const int G = K / GROUP;
   const Range rg(plan, blockIdx.x);
 
   if (warp == 0) {
     // ---------------------------------------------------------------- TMA producer
     if (lane == 0) {
+      int pre = 0;            // stages whose weight copies are issued before the wait
+      for (int k = 0; k < rg.n && pre < S; ++k) {
+        const Segment sg = rg.at(plan, k);
+        for (int i = 0; i < sg.nkb && pre < S; ++i, ++pre) {
+          const int kb = sg.kb0 + i;
+          const uint8_t* chunk =
+              wpk + (static_cast<size_t>(sg.nt) * G + (kb >> 1)) * static_cast<size_t>(F::CHUNK);
+          mbar_arrive_expect_tx(full(pre), A_STAGE + F::P_STAGE);
+          bulk_load(p_st + pre * F::P_STAGE, chunk + (kb & 1) * F::HALF, F::HALF, full(pre));
+          bulk_load(p_st + pre * F::P_STAGE + F::HALF, chunk + F::META_OFF, F::META, full(pre));
+        }
+      }
+      griddep_wait();  // the activations come from the previous kernel
+      for (int k = 0, j = 0; k < rg.n && j < pre; ++k) {
+        const Segment sg = rg.at(plan, k);
+        for (int i = 0; i < sg.nkb && j < pre; ++i, ++j)
+          tma_load_2d(a_st + j * A_STAGE, &tmap_a, (sg.kb0 + i) * BK, sg.mt * BM, full(j));
+      }
       int it = 0;
       bool ok = true;
       for (int k = 0; k < rg.n && ok; ++k) {
         const Segment sg = rg.at(plan, k);
         for (int i = 0; i < sg.nkb; ++i, ++it) {
+          if (it < pre) continue;  // issued above
           const int s = it % S;
           const uint32_t ph = (it / S) & 1;
           if (!mbar_wait(empty(s), ph ^ 1, abort_flag)) {
@@ -310,6 +331,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
   } else {
     // ---------------------------------------------------------------- epilogue (warps 2..5)
+    griddep_wait();  // out / scratch / counters are shared with the previous kernels
     const int q = warp & 3;           // TMEM lane quarter this warp may read
     const int et = threadIdx.x - 64;  // 0..127
     const uint32_t stg = stg0 + q * STG_BYTES;

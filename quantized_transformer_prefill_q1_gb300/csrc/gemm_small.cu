@@ -140,18 +140,35 @@ __global__ void __launch_bounds__(THREADS_S, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  griddep_wait();  // inputs come from the previous kernel in the stream
+  // Only the activation tiles and the epilogue's global accesses depend on the previous
+  // kernel (griddep_wait below); the producer issues the first stages' weight chunks first.
   const int G = K / GROUP;
   const Range rg(plan, blockIdx.x);
 
   if (warp == 0) {
     // ---------------------------------------------------------------- TMA producer
     if (lane == 0) {
+      int pre = 0;  // stages whose weight chunk is issued before the wait
+      for (int k = 0; k < rg.n && pre < S; ++k) {
+        const Segment sg = rg.at(plan, k);
+        for (int i = 0; i < sg.nkb && pre < S; ++i, ++pre) {
+          mbar_arrive_expect_tx(full(pre), L::B + F::P);
+          bulk_load(p_st + pre * F::P, wpk + (static_cast<size_t>(sg.nt) * G + sg.kb0 + i) * F::P, F::P,
+                    full(pre));
+        }
+      }
+      griddep_wait();  // the activations come from the previous kernel
+      for (int k = 0, j = 0; k < rg.n && j < pre; ++k) {
+        const Segment sg = rg.at(plan, k);
+        for (int i = 0; i < sg.nkb && j < pre; ++i, ++j)
+          tma_load_3d(b_st + j * L::B, &tmap_x, 0, 0, 2 * (sg.kb0 + i), full(j));
+      }
       int it = 0;
       bool ok = true;
       for (int k = 0; k < rg.n && ok; ++k) {
         const Segment sg = rg.at(plan, k);
         for (int i = 0; i < sg.nkb; ++i, ++it) {
+          if (it < pre) continue;  // issued above
           const int s = it % S;
           if (!mbar_wait(empty(s), ((it / S) & 1) ^ 1, abort_flag)) {
             ok = false;
@@ -206,6 +223,7 @@ __global__ void __launch_bounds__(THREADS_S, 1)
     }
   } else {
     // ---------------------------------------------------------------- dequant + epilogue
+    griddep_wait();  // out / scratch / counters are shared with the previous kernels
     const int dw = warp - 2;
     const int q = warp & 3;
     const int hh = (dw >> 2) & 1;       // 128-row half of the tile
