@@ -68,6 +68,11 @@ __global__ void __launch_bounds__(128) rmsnorm_reg_kernel(const float* __restric
                                                           int H, __half* __restrict__ y) {
   __shared__ float red[4];
   griddep_launch_dependents();
+  // the norm weights never depend on the previous kernel: load them while it finishes
+  const float4* w4 = reinterpret_cast<const float4*>(w);
+  float4 g[NV];
+#pragma unroll
+  for (int i = 0; i < NV; ++i) g[i] = w4[threadIdx.x + 128 * i];
   griddep_wait();
   const int row = blockIdx.x;
   const float4* xr = reinterpret_cast<const float4*>(x + static_cast<size_t>(row) * H);
@@ -83,14 +88,12 @@ __global__ void __launch_bounds__(128) rmsnorm_reg_kernel(const float* __restric
   __syncthreads();
   ss = red[0] + red[1] + red[2] + red[3];
   const float r = rsqrtf(ss / static_cast<float>(H) + eps);
-  const float4* w4 = reinterpret_cast<const float4*>(w);
   uint2* yr = reinterpret_cast<uint2*>(y + static_cast<size_t>(row) * H);
 #pragma unroll
   for (int i = 0; i < NV; ++i) {
     const int idx = threadIdx.x + 128 * i;
-    const float4 g = w4[idx];
-    const __half2 a = __floats2half2_rn(v[i].x * r * g.x, v[i].y * r * g.y);
-    const __half2 b = __floats2half2_rn(v[i].z * r * g.z, v[i].w * r * g.w);
+    const __half2 a = __floats2half2_rn(v[i].x * r * g[i].x, v[i].y * r * g[i].y);
+    const __half2 b = __floats2half2_rn(v[i].z * r * g[i].z, v[i].w * r * g[i].w);
     yr[idx] = make_uint2(*reinterpret_cast<const uint32_t*>(&a), *reinterpret_cast<const uint32_t*>(&b));
   }
 }
@@ -146,7 +149,6 @@ __global__ void __launch_bounds__(256) qk_norm_rope_kv_kernel(
   constexpr int LPH = HALF / 4;   // lanes per head
   constexpr int HPW = 32 / LPH;   // heads per warp
   griddep_launch_dependents();
-  griddep_wait();
   const int heads = nq + 2 * nkv;
   const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
@@ -155,36 +157,44 @@ __global__ void __launch_bounds__(256) qk_norm_rope_kv_kernel(
   const int t = gh / heads;
   const int j = gh - t * heads;
   const bool valid = t < M;
+  const bool is_q = j < nq, is_v = j >= nq + nkv;
+  // the norm weights never depend on the previous kernel: load them while it finishes
+  float4 wa = make_float4(1.f, 1.f, 1.f, 1.f), wb = wa;
+  if (qk_norm && valid && !is_v) {
+    wa = reinterpret_cast<const float4*>(is_q ? qn : kn)[l];
+    wb = reinterpret_cast<const float4*>(is_q ? qn : kn)[LPH + l];
+  }
+  griddep_wait();
   const int start = start_dev ? *start_dev : start_host;
   const int pos = start + t;
-  float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a;
+  // the head's values and its (cos, sin) of pairs 4l .. 4l+3 in one round trip
+  float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a, c01 = a, c23 = a;
   if (valid) {
     const float4* src = reinterpret_cast<const float4*>(qkv + (static_cast<size_t>(t) * heads + j) * HD);
     a = src[l];
     b = src[LPH + l];
+    if (!is_v) {
+      const float4* cs = reinterpret_cast<const float4*>(rope + (static_cast<size_t>(pos) * HALF + 4 * l) * 2);
+      c01 = cs[0];
+      c23 = cs[1];
+    }
   }
   // per-head sum of squares over the LPH lanes of the group (every lane takes part)
   float ss = a.x * a.x + a.y * a.y + a.z * a.z + a.w * a.w + b.x * b.x + b.y * b.y + b.z * b.z + b.w * b.w;
 #pragma unroll
   for (int o = LPH / 2; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
   if (!valid) return;
-  if (j >= nq + nkv) {  // V head: straight to the cache
+  if (is_v) {  // V head: straight to the cache
     KT* dst = vc + ((static_cast<size_t>(layer) * nkv + (j - nq - nkv)) * max_seq + pos) * HD;
     store4<KT>(dst + 4 * l, a.x, a.y, a.z, a.w);
     store4<KT>(dst + HALF + 4 * l, b.x, b.y, b.z, b.w);
     return;
   }
-  const bool is_q = j < nq;
   if (qk_norm) {
     const float r = rsqrtf(ss / static_cast<float>(HD) + eps);
-    const float4 wa = reinterpret_cast<const float4*>(is_q ? qn : kn)[l];
-    const float4 wb = reinterpret_cast<const float4*>(is_q ? qn : kn)[LPH + l];
     a = make_float4(a.x * r * wa.x, a.y * r * wa.y, a.z * r * wa.z, a.w * r * wa.w);
     b = make_float4(b.x * r * wb.x, b.y * r * wb.y, b.z * r * wb.z, b.w * r * wb.w);
   }
-  // (cos, sin) of pairs 4l .. 4l+3 at this position
-  const float4* cs = reinterpret_cast<const float4*>(rope + (static_cast<size_t>(pos) * HALF + 4 * l) * 2);
-  const float4 c01 = cs[0], c23 = cs[1];
   const float ra0 = a.x * c01.x - b.x * c01.y, rb0 = b.x * c01.x + a.x * c01.y;
   const float ra1 = a.y * c01.z - b.y * c01.w, rb1 = b.y * c01.z + a.y * c01.w;
   const float ra2 = a.z * c23.x - b.z * c23.y, rb2 = b.z * c23.x + a.z * c23.y;
