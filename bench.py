@@ -54,7 +54,7 @@ def parse():
     p.add_argument("--seed", type=int, default=0)
     p.add_argument("--case", default=None,
                    choices=["gemm_gate_up", "gemm_qkv", "gemm_down", "gemm_o", "attention", "rmsnorm",
-                            "qk_rope_kv", "lm_head", "int4_gate_up", "int4_qkv", "int4_o", "int4_down"],
+                            "qk_rope_kv", "lm_head", "int4_gate_up", "int4_qkv", "int4_o", "int4_down", "decode"],
                    help="small single-kernel case at the workload's shapes (for ncu captures)")
     p.add_argument("--reps", type=int, default=3)
     p.add_argument("--ctas", type=int, default=0, help="GEMM cases: most persistent CTAs (0 = the library's choice)")
@@ -75,6 +75,33 @@ def run_case(args):
     M, H, I = CHUNK, s.hidden, s.intermediate
     dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()  # noqa: E731
     cfg = pf.make_config(s, CHUNK, n_layers=1)
+    if args.case == "decode":
+        # token-by-token decode on the 36-layer stack after a 512-token prefill: each step one
+        # pf_decode_step (token from device memory, logits of the new position)
+        shape = synth.QWEN3_8B_STACK
+        layers, extra = synth.model_inputs(shape, seed=args.seed)
+        dm = pf.DeviceModel(shape, layers, extra, max_chunk=CHUNK)
+        sess = pf.Session(dm)
+        toks = dev(synth.tokens(CHUNK + 64, shape.vocab, seed=args.seed).astype(np.int32))
+        logits = torch.empty(shape.vocab, device="cuda")
+        steps = max(args.reps, 8)
+        sess.prefill_chunk_dev(toks[:CHUNK], 0)
+        for i in range(4):  # warm-up (records the one-token graph)
+            sess.decode_step(toks[CHUNK + i:CHUNK + i + 1], logits)
+        sess.sync()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for i in range(4, 4 + steps):
+            sess.decode_step(toks[CHUNK + i % 64:CHUNK + i % 64 + 1], logits)
+        e1.record()
+        e1.synchronize()
+        us = e0.elapsed_time(e1) / steps * 1e3
+        wbytes = 36 * 27.13e6 + 87.5e6  # packed layer weights + LM head read per step
+        print(json.dumps({"case": "decode", "us_per_token": us, "tokens_per_s": 1e6 / us,
+                          "weight_GBps": wbytes / us / 1e3, "kv_position_end": sess.position}),
+              flush=True)
+        return
     if args.case.startswith("int4"):
         # the INT4-affine Llama-3-8B-shaped layer's projections at a few tokens (GEMV end)
         li = synth.LLAMA3_8B_INT4_LAYER
@@ -142,6 +169,33 @@ def run_case(args):
     e1.synchronize()
     us = e0.elapsed_time(e1) / args.reps * 1e3
     line = {"case": args.case, "us_per_launch": us, "ctas": args.ctas}
+    if args.case == "decode":
+        # token-by-token decode on the 36-layer stack after a 512-token prefill: each step one
+        # pf_decode_step (token from device memory, logits of the new position)
+        shape = synth.QWEN3_8B_STACK
+        layers, extra = synth.model_inputs(shape, seed=args.seed)
+        dm = pf.DeviceModel(shape, layers, extra, max_chunk=CHUNK)
+        sess = pf.Session(dm)
+        toks = dev(synth.tokens(CHUNK + 64, shape.vocab, seed=args.seed).astype(np.int32))
+        logits = torch.empty(shape.vocab, device="cuda")
+        steps = max(args.reps, 8)
+        sess.prefill_chunk_dev(toks[:CHUNK], 0)
+        for i in range(4):  # warm-up (records the one-token graph)
+            sess.decode_step(toks[CHUNK + i:CHUNK + i + 1], logits)
+        sess.sync()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for i in range(4, 4 + steps):
+            sess.decode_step(toks[CHUNK + i % 64:CHUNK + i % 64 + 1], logits)
+        e1.record()
+        e1.synchronize()
+        us = e0.elapsed_time(e1) / steps * 1e3
+        wbytes = 36 * 27.13e6 + 87.5e6  # packed layer weights + LM head read per step
+        print(json.dumps({"case": "decode", "us_per_token": us, "tokens_per_s": 1e6 / us,
+                          "weight_GBps": wbytes / us / 1e3, "kv_position_end": sess.position}),
+              flush=True)
+        return
     if args.case.startswith("int4"):
         line.update({"m": args.m, "weight_bytes": wbytes, "weight_GBps": wbytes / us / 1e3})
     if flops:

@@ -217,6 +217,14 @@ pf_status pf_layer_forward(pf_session* s, int32_t layer, float* x_dev, int32_t M
 pf_status pf_prefill_chunk_dev(pf_session* s, const int32_t* tokens_dev, int32_t M,
                                int32_t start_pos, float* logits_dev, void* stream);
 
+/* One decode step ([P2] encode_layer_into for every layer, then the decode tail: final
+ * norm + LM head): the token at *token_dev (device int32, e.g. the previous step's argmax)
+ * at the session's KV position, which advances by one; logits_dev [vocab] f32 receives its
+ * logits. Same kernels as a one-token chunk (the small-M GEMM path); the recorded graph of
+ * M = 1 is reused from step to step. Errors as pf_prefill_chunk_dev (PF_ERR_LOGITS when the
+ * model has no LM head or logits_dev is NULL). */
+pf_status pf_decode_step(pf_session* s, const int32_t* token_dev, float* logits_dev, void* stream);
+
 /* End to end from host memory: copies tokens_host to the device, runs
  * pf_prefill_chunk, copies the last position's logits into logits_host [vocab]
  * (may be NULL) and synchronises the stream. */

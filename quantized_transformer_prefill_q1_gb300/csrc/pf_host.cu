@@ -752,6 +752,13 @@ pf_status pf_prefill_chunk_dev(pf_session* s, const int32_t* tokens_dev, int32_t
   return prefill_common(s, tokens_dev, true, nullptr, M, start_pos, logits_dev, stream);
 }
 
+pf_status pf_decode_step(pf_session* s, const int32_t* token_dev, float* logits_dev, void* stream) {
+  if (!s) return fail(PF_ERR_INVALID_ARG, "session is NULL");
+  if (!token_dev) return fail(PF_ERR_INVALID_ARG, "token is NULL");
+  if (!logits_dev) return fail(PF_ERR_LOGITS, "decode needs logits");
+  return prefill_common(s, token_dev, true, nullptr, 1, s->position, logits_dev, stream);
+}
+
 pf_status pf_prefill_hidden(pf_session* s, float* x_dev, int32_t M, int32_t start_pos,
                             float* logits_dev, void* stream) {
   if (s && M > 0 && !x_dev) return fail(PF_ERR_INVALID_ARG, "x is NULL");

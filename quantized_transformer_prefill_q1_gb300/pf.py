@@ -78,6 +78,7 @@ _SIGS = {
     "pf_session_sync": ([_VP, _VP], _I32),
     "pf_prefill_chunk": ([_VP, _VP, _I32, _I32, _VP, _VP], _I32),
     "pf_prefill_chunk_dev": ([_VP, _VP, _I32, _I32, _VP, _VP], _I32),
+    "pf_decode_step": ([_VP, _VP, _VP, _VP], _I32),
     "pf_session_set_profile": ([_VP, _I32], _I32),
     "pf_session_profile_read": ([_VP, _VP, ctypes.POINTER(ctypes.c_double),
                                  ctypes.POINTER(ctypes.c_int64)], _I32),
@@ -338,6 +339,10 @@ class Session:
     def prefill_chunk_dev(self, tokens_dev, start: int, logits=None, stream=None) -> None:
         check(lib().pf_prefill_chunk_dev(self.h, _ptr(tokens_dev), tokens_dev.shape[0], start,
                                          _ptr(logits), _stream(stream)))
+
+    def decode_step(self, token_dev, logits, stream=None) -> None:
+        """One decode step: the token at token_dev (device int32) at the current position."""
+        check(lib().pf_decode_step(self.h, _ptr(token_dev), _ptr(logits), _stream(stream)))
 
     def set_profile(self, on: bool) -> None:
         check(lib().pf_session_set_profile(self.h, int(on)))

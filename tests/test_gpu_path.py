@@ -170,6 +170,33 @@ def test_stack_tokens_logits_and_chunking():
     assert O.rel_l2(host, ref_logits) <= TOL
 
 
+def test_decode_steps_match_oracle_prefixes():
+    """pf_decode_step: after a 32-token prefill, each step feeds the next token from device
+    memory at the session's position; its logits equal the oracle's last-position logits of
+    the prefix (prefill = decode, the pages' token-by-token path)."""
+    s = _small_stack()
+    layers, extra = synth.model_inputs(s)
+    toks = synth.tokens(38, s.vocab)
+    om = O.OracleModel(s, layers, extra)
+    dm = pf.DeviceModel(s, layers, extra, max_chunk=32)
+    sess = pf.Session(dm, kv_fill_bits=SENT[s.kv_dtype])
+    logits = torch.full((s.vocab,), float("nan"), dtype=torch.float32, device="cuda")
+    sess.prefill_chunk(toks[:32], 0)
+    tok_d = torch.from_numpy(toks.astype(np.int32)).cuda()
+    for n in range(32, 38):
+        sess.decode_step(tok_d[n:n + 1], logits)
+        sess.sync()
+        assert sess.position == n + 1
+        _, ref = O.OracleModel(s, layers, extra).prefill(toks[:n + 1], [n + 1], True, True)
+        assert O.rel_l2(logits.cpu().numpy(), ref) <= TOL
+    om.prefill(toks, [38], True, True)
+    check_kv(sess, om, s, 0, 38)
+    with pytest.raises(pf.PfError) as e:  # a decode step needs a logits buffer
+        pf.check(pf.lib().pf_decode_step(sess.h, tok_d.data_ptr(), None, None))
+    assert e.value.status == 7  # PF_ERR_LOGITS
+    assert sess.position == 38
+
+
 def test_session_validation_leaves_state_unchanged():
     s = _small_stack(n_layers=1, vocab=100)
     layers, extra = synth.model_inputs(s)
