@@ -42,6 +42,10 @@ PROMPT, CHUNK = 2048, 512
 NCU_TRAFFIC = {"gemm_gate_up": 18409216 + 420864}
 
 
+CASES = ["gemm_gate_up", "gemm_qkv", "gemm_down", "gemm_o", "attention", "rmsnorm", "qk_rope_kv", "lm_head",
+         "int4_gate_up", "int4_qkv", "int4_o", "int4_down", "decode"]
+
+
 def parse():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
@@ -53,154 +57,161 @@ def parse():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--seed", type=int, default=0)
     p.add_argument("--case", default=None,
-                   choices=["gemm_gate_up", "gemm_qkv", "gemm_down", "gemm_o", "attention", "rmsnorm",
-                            "qk_rope_kv", "lm_head", "int4_gate_up", "int4_qkv", "int4_o", "int4_down", "decode"],
-                   help="small single-kernel case at the workload's shapes (for ncu captures)")
+                   help="comma list of single-kernel cases at the workload's shapes (for ncu captures): "
+                        + ", ".join(CASES))
     p.add_argument("--reps", type=int, default=3)
     p.add_argument("--ctas", type=int, default=0, help="GEMM cases: most persistent CTAs (0 = the library's choice)")
-    p.add_argument("--m", type=int, default=1, help="int4_* cases: chunk tokens (Llama-3-8B-shaped INT4 layer)")
+    p.add_argument("--m", default=None,
+                   help="comma list of chunk tokens for the int4_* (Llama-3-8B-shaped INT4 layer, default 1) "
+                        "and gemm_* (Qwen3-8B-shaped Q1 layer, default 512) cases")
     return p.parse_args()
 
 
 def run_case(args):
-    """Runs one kernel of the workload `--reps` times at its production shape (chunk of
-    512 rows, last chunk's positions for attention) with a few hundred MB on the device;
-    prints the average CUDA-event time per launch."""
+    """Runs kernels of the workload at their production shapes (chunk of 512 rows, last
+    chunk's positions for attention; `--m` tokens for the projections at small M) with a few
+    hundred MB on the device. Each launch is timed alone with CUDA events after a 256 MB write
+    that evicts L2, so weights come from HBM as in the layer step; prints one JSON line per
+    (case, M) with the average time per launch. `--case` and `--m` take comma lists."""
     import numpy as np
     import torch
 
     from quantized_transformer_prefill_q1_gb300 import pf, synth
     s = synth.QWEN3_8B_STACK
-    rng = synth.rng_for(99)
-    M, H, I = CHUNK, s.hidden, s.intermediate
+    H, I = s.hidden, s.intermediate
     dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()  # noqa: E731
     cfg = pf.make_config(s, CHUNK, n_layers=1)
-    if args.case == "decode":
-        # token-by-token decode on the 36-layer stack after a 512-token prefill: each step one
-        # pf_decode_step (token from device memory, logits of the new position)
-        shape = synth.QWEN3_8B_STACK
-        layers, extra = synth.model_inputs(shape, seed=args.seed)
-        dm = pf.DeviceModel(shape, layers, extra, max_chunk=CHUNK)
-        sess = pf.Session(dm)
-        toks = dev(synth.tokens(CHUNK + 64, shape.vocab, seed=args.seed).astype(np.int32))
-        logits = torch.empty(shape.vocab, device="cuda")
-        steps = max(args.reps, 8)
-        sess.prefill_chunk_dev(toks[:CHUNK], 0)
-        for i in range(4):  # warm-up (records the one-token graph)
-            sess.decode_step(toks[CHUNK + i:CHUNK + i + 1], logits)
-        sess.sync()
+    # 256 MB > L2, read before each launch: L2 then holds clean lines of it (a write would
+    # leave dirty lines whose write-back the timed kernel would pay for)
+    flush_buf = torch.ones(64 << 20, dtype=torch.float32, device="cuda")
+    packed = {}
+
+    def timed(fn, reps):
+        fn()
         torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record()
-        for i in range(4, 4 + steps):
-            sess.decode_step(toks[CHUNK + i % 64:CHUNK + i % 64 + 1], logits)
-        e1.record()
-        e1.synchronize()
-        us = e0.elapsed_time(e1) / steps * 1e3
-        wbytes = 36 * 27.13e6 + 87.5e6  # packed layer weights + LM head read per step
-        print(json.dumps({"case": "decode", "us_per_token": us, "tokens_per_s": 1e6 / us,
-                          "weight_GBps": wbytes / us / 1e3, "kv_position_end": sess.position}),
-              flush=True)
-        return
-    if args.case.startswith("int4"):
-        # the INT4-affine Llama-3-8B-shaped layer's projections at a few tokens (GEMV end)
-        li = synth.LLAMA3_8B_INT4_LAYER
-        n, k, epi = {"int4_gate_up": (2 * li.intermediate, li.hidden, pf.EPI_SWIGLU),
-                     "int4_qkv": (li.qkv_rows, li.hidden, pf.EPI_STORE_F32),
-                     "int4_o": (li.hidden, li.n_q_heads * li.head_dim, pf.EPI_RESID_ADD),
-                     "int4_down": (li.hidden, li.intermediate, pf.EPI_RESID_ADD)}[args.case]
-        M = args.m
-        a = dev(rng.standard_normal((M, k)).astype(np.float16))
-        w = dev(pf.pf_pack_weights_host(synth.int4_weight(rng, n, k), epi == pf.EPI_SWIGLU))
-        out = torch.zeros((M, n // 2 if epi == pf.EPI_SWIGLU else n),
-                          dtype=torch.float16 if epi == pf.EPI_SWIGLU else torch.float32, device="cuda")
-        scratch = pf.gemm_scratch(M, n, args.ctas)
-        fn = lambda: pf.pf_op_gemm(pf.W_INT4, epi, a, w, M, n, k, out, scratch, args.ctas)  # noqa: E731
-        flops = 2 * M * n * k
-        wbytes = w.numel()
-    elif args.case.startswith("gemm"):
-        n, k, epi = {"gemm_gate_up": (2 * I, H, pf.EPI_SWIGLU), "gemm_qkv": (s.qkv_rows, H, pf.EPI_STORE_F32),
-                     "gemm_down": (H, I, pf.EPI_RESID_ADD),
-                     "gemm_o": (H, s.n_q_heads * s.head_dim, pf.EPI_RESID_ADD)}[args.case]
-        a = dev(rng.standard_normal((M, k)).astype(np.float16))
-        w = dev(pf.pf_pack_weights_host(synth.q1_weight(rng, n, k), epi == pf.EPI_SWIGLU))
-        out = torch.zeros((M, n // 2 if epi == pf.EPI_SWIGLU else n),
-                          dtype=torch.float16 if epi == pf.EPI_SWIGLU else torch.float32, device="cuda")
-        scratch = pf.gemm_scratch(M, n, args.ctas)
-        fn = lambda: pf.pf_op_gemm(pf.W_Q1, epi, a, w, M, n, k, out, scratch, args.ctas)  # noqa: E731
-        flops = 2 * M * n * k
-    elif args.case == "attention":
-        start = PROMPT - CHUNK
-        q = torch.randn((M, s.n_q_heads, s.head_dim), device="cuda").to(torch.bfloat16)
-        kc = torch.randn((1, s.n_kv_heads, s.max_seq, s.head_dim), device="cuda").to(torch.bfloat16)
-        vc = torch.randn_like(kc)
-        out = torch.empty((M, s.n_q_heads * s.head_dim), dtype=torch.float16, device="cuda")
-        fn = lambda: pf.pf_op_attention(cfg, q, kc, vc, 0, start, M, out)  # noqa: E731
-        flops = sum(4 * s.n_q_heads * s.head_dim * (p + 1) for p in range(start, start + M))
-    elif args.case == "rmsnorm":
-        x = torch.randn((M, H), device="cuda")
-        wv = torch.ones(H, device="cuda")
-        y = torch.empty((M, H), dtype=torch.float16, device="cuda")
-        fn = lambda: pf.pf_op_rmsnorm(x, wv, 1e-6, y)  # noqa: E731
-        flops = None
-    elif args.case == "qk_rope_kv":
-        qkv = torch.randn((M, s.qkv_rows), device="cuda")
-        qn = torch.ones(s.head_dim, device="cuda")
-        rope = dev(pf.pf_rope_table_host(s.rope_theta, s.head_dim, s.max_seq))
-        q = torch.empty((M, s.n_q_heads, s.head_dim), dtype=torch.bfloat16, device="cuda")
-        kc = torch.empty((1, s.n_kv_heads, s.max_seq, s.head_dim), dtype=torch.bfloat16, device="cuda")
-        vc = torch.empty_like(kc)
-        fn = lambda: pf.pf_op_qk_norm_rope_kv(cfg, qkv, qn, qn, rope, 0, 0, M, q, kc, vc)  # noqa: E731
-        flops = None
-    else:  # lm_head
-        w = dev(pf.pf_pack_weights_host(synth.q1_weight(rng, s.vocab, H)))
-        x = torch.randn(H, device="cuda")
-        nw = torch.ones(H, device="cuda")
-        logits = torch.empty(s.vocab, device="cuda")
-        fn = lambda: pf.pf_op_lm_head(pf.W_Q1, x, nw, 1e-6, w, s.vocab, H, logits)  # noqa: E731
-        flops = None
-    fn()
+        total = 0.0
+        for _ in range(reps):
+            flush_buf.sum()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            e1.synchronize()
+            total += e0.elapsed_time(e1)
+        return total / reps * 1e3
+
+    ms = [int(v) for v in str(args.m).split(",")] if args.m else None
+    for case in args.case.split(","):
+        if case == "decode":
+            run_decode(args, pf, synth, dev)
+            continue
+        for M in (ms or [1 if case.startswith("int4") else CHUNK]):
+            rng = synth.rng_for(99)
+            flops = wbytes = None
+            if case.startswith("int4") or case.startswith("gemm"):
+                if case.startswith("int4"):
+                    # the INT4-affine Llama-3-8B-shaped layer's projections
+                    li = synth.LLAMA3_8B_INT4_LAYER
+                    n, k, epi = {"int4_gate_up": (2 * li.intermediate, li.hidden, pf.EPI_SWIGLU),
+                                 "int4_qkv": (li.qkv_rows, li.hidden, pf.EPI_STORE_F32),
+                                 "int4_o": (li.hidden, li.n_q_heads * li.head_dim, pf.EPI_RESID_ADD),
+                                 "int4_down": (li.hidden, li.intermediate, pf.EPI_RESID_ADD)}[case]
+                    fmt = pf.W_INT4
+                else:
+                    n, k, epi = {"gemm_gate_up": (2 * I, H, pf.EPI_SWIGLU), "gemm_qkv": (s.qkv_rows, H, pf.EPI_STORE_F32),
+                                 "gemm_down": (H, I, pf.EPI_RESID_ADD),
+                                 "gemm_o": (H, s.n_q_heads * s.head_dim, pf.EPI_RESID_ADD)}[case]
+                    fmt = pf.W_Q1
+                if case not in packed:
+                    wq = synth.int4_weight(rng, n, k) if fmt == pf.W_INT4 else synth.q1_weight(rng, n, k)
+                    packed[case] = dev(pf.pf_pack_weights_host(wq, epi == pf.EPI_SWIGLU))
+                w = packed[case]
+                a = dev(rng.standard_normal((M, k)).astype(np.float16))
+                out = torch.zeros((M, n // 2 if epi == pf.EPI_SWIGLU else n),
+                                  dtype=torch.float16 if epi == pf.EPI_SWIGLU else torch.float32, device="cuda")
+                scratch = pf.gemm_scratch(M, n, args.ctas)
+                fn = lambda: pf.pf_op_gemm(fmt, epi, a, w, M, n, k, out, scratch, args.ctas)  # noqa: E731
+                flops = 2 * M * n * k
+                wbytes = w.numel()
+            elif case == "attention":
+                start = PROMPT - CHUNK
+                q = torch.randn((M, s.n_q_heads, s.head_dim), device="cuda").to(torch.bfloat16)
+                kc = torch.randn((1, s.n_kv_heads, s.max_seq, s.head_dim), device="cuda").to(torch.bfloat16)
+                vc = torch.randn_like(kc)
+                out = torch.empty((M, s.n_q_heads * s.head_dim), dtype=torch.float16, device="cuda")
+                fn = lambda: pf.pf_op_attention(cfg, q, kc, vc, 0, start, M, out)  # noqa: E731
+                flops = sum(4 * s.n_q_heads * s.head_dim * (p + 1) for p in range(start, start + M))
+            elif case == "rmsnorm":
+                x = torch.randn((M, H), device="cuda")
+                wv = torch.ones(H, device="cuda")
+                y = torch.empty((M, H), dtype=torch.float16, device="cuda")
+                fn = lambda: pf.pf_op_rmsnorm(x, wv, 1e-6, y)  # noqa: E731
+            elif case == "qk_rope_kv":
+                qkv = torch.randn((M, s.qkv_rows), device="cuda")
+                qn = torch.ones(s.head_dim, device="cuda")
+                rope = dev(pf.pf_rope_table_host(s.rope_theta, s.head_dim, s.max_seq))
+                q = torch.empty((M, s.n_q_heads, s.head_dim), dtype=torch.bfloat16, device="cuda")
+                kc = torch.empty((1, s.n_kv_heads, s.max_seq, s.head_dim), dtype=torch.bfloat16, device="cuda")
+                vc = torch.empty_like(kc)
+                fn = lambda: pf.pf_op_qk_norm_rope_kv(cfg, qkv, qn, qn, rope, 0, 0, M, q, kc, vc)  # noqa: E731
+            else:  # lm_head
+                if "lm_head" not in packed:
+                    packed["lm_head"] = dev(pf.pf_pack_weights_host(synth.q1_weight(rng, s.vocab, H)))
+                w = packed["lm_head"]
+                x = torch.randn(H, device="cuda")
+                nw = torch.ones(H, device="cuda")
+                logits = torch.empty(s.vocab, device="cuda")
+                fn = lambda: pf.pf_op_lm_head(pf.W_Q1, x, nw, 1e-6, w, s.vocab, H, logits)  # noqa: E731
+                wbytes = w.numel()
+            us = timed(fn, args.reps)
+            line = {"case": case, "m": M, "us_per_launch": us, "ctas": args.ctas,
+                    "l2": "256 MB read before each launch"}
+            if wbytes:
+                line.update({"weight_bytes": wbytes, "weight_GBps": wbytes / us / 1e3})
+            if flops:
+                line["tflops"] = flops / us / 1e6
+            print(json.dumps(line), flush=True)
+            del fn
+        packed.pop(case, None)
+
+
+def run_decode(args, pf, synth, dev):
+    """Token-by-token decode on the 36-layer stack after a 512-token prefill: each step one
+    pf_decode_step (token from device memory, logits of the new position)."""
+    import numpy as np
+    import torch
+    shape = synth.QWEN3_8B_STACK
+    layers, extra = synth.model_inputs(shape, seed=args.seed)
+    dm = pf.DeviceModel(shape, layers, extra, max_chunk=CHUNK)
+    sess = pf.Session(dm)
+    toks = dev(synth.tokens(CHUNK + 64, shape.vocab, seed=args.seed).astype(np.int32))
+    logits = torch.empty(shape.vocab, device="cuda")
+    steps = max(args.reps, 8)
+    sess.prefill_chunk_dev(toks[:CHUNK], 0)
+    for i in range(4):  # warm-up (records the one-token graph)
+        sess.decode_step(toks[CHUNK + i:CHUNK + i + 1], logits)
+    sess.sync()
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record()
-    for _ in range(args.reps):
-        fn()
+    for i in range(4, 4 + steps):
+        sess.decode_step(toks[CHUNK + i % 64:CHUNK + i % 64 + 1], logits)
     e1.record()
     e1.synchronize()
-    us = e0.elapsed_time(e1) / args.reps * 1e3
-    line = {"case": args.case, "us_per_launch": us, "ctas": args.ctas}
-    if args.case == "decode":
-        # token-by-token decode on the 36-layer stack after a 512-token prefill: each step one
-        # pf_decode_step (token from device memory, logits of the new position)
-        shape = synth.QWEN3_8B_STACK
-        layers, extra = synth.model_inputs(shape, seed=args.seed)
-        dm = pf.DeviceModel(shape, layers, extra, max_chunk=CHUNK)
-        sess = pf.Session(dm)
-        toks = dev(synth.tokens(CHUNK + 64, shape.vocab, seed=args.seed).astype(np.int32))
-        logits = torch.empty(shape.vocab, device="cuda")
-        steps = max(args.reps, 8)
-        sess.prefill_chunk_dev(toks[:CHUNK], 0)
-        for i in range(4):  # warm-up (records the one-token graph)
-            sess.decode_step(toks[CHUNK + i:CHUNK + i + 1], logits)
-        sess.sync()
-        torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record()
-        for i in range(4, 4 + steps):
-            sess.decode_step(toks[CHUNK + i % 64:CHUNK + i % 64 + 1], logits)
-        e1.record()
-        e1.synchronize()
-        us = e0.elapsed_time(e1) / steps * 1e3
-        wbytes = 36 * 27.13e6 + 87.5e6  # packed layer weights + LM head read per step
-        print(json.dumps({"case": "decode", "us_per_token": us, "tokens_per_s": 1e6 / us,
-                          "weight_GBps": wbytes / us / 1e3, "kv_position_end": sess.position}),
-              flush=True)
-        return
-    if args.case.startswith("int4"):
-        line.update({"m": args.m, "weight_bytes": wbytes, "weight_GBps": wbytes / us / 1e3})
-    if flops:
-        line["tflops"] = flops / us / 1e6
-    print(json.dumps(line), flush=True)
+    us = e0.elapsed_time(e1) / steps * 1e3
+    # profiled pass: per-launch CUDA events (no graph replay), per kernel class
+    sess.set_profile(True)
+    sess.profile_read()
+    for i in range(4 + steps, 4 + steps + 4):
+        sess.decode_step(toks[CHUNK + i % 64:CHUNK + i % 64 + 1], logits)
+    prof = sess.profile_read()
+    sess.set_profile(False)
+    breakdown = {k: round(v[0] / 4 * 1e3, 2) for k, v in prof.items() if v[1]}
+    wbytes = shape.n_layers * 27.13e6 + 87.5e6  # packed layer weights + LM head read per step
+    print(json.dumps({"case": "decode", "us_per_token": us, "tokens_per_s": 1e6 / us,
+                      "weight_GBps": wbytes / us / 1e3, "kv_position_end": sess.position,
+                      "profiled_us_per_token": breakdown}),
+          flush=True)
 
 
 def load_peaks():
@@ -494,6 +505,9 @@ def run_ours(args):
 def main():
     args = parse()
     if args.case:
+        bad = [c for c in args.case.split(",") if c not in CASES]
+        if bad:
+            raise SystemExit(f"unknown case(s) {bad}; choose from {CASES}")
         run_case(args)
     elif args.impl == "reference":
         run_reference(args)

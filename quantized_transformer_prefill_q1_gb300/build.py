@@ -16,7 +16,7 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(PKG, "csrc")
 LIB = os.path.join(PKG, "libpf.so")
 BUILD_DIR = os.path.join(PKG, "_build")
-SOURCES = ["pf_host.cu", "gemm_q.cu", "gemm_small.cu", "attention.cu", "attention_tc.cu", "kernels.cu"]
+SOURCES = ["pf_host.cu", "gemm_q.cu", "gemm_small.cu", "gemv.cu", "attention.cu", "attention_tc.cu", "kernels.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
          "--expt-relaxed-constexpr", "-Xptxas", "-v"]

@@ -552,6 +552,7 @@ cudaError_t prepare_gemm_kernels() {
 }
 
 cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t stream) {
+  if (g.M <= gemv_max_m(g.wfmt)) return launch_gemv(g, stream);
   if (g.M <= SMALL_M_MAX) return launch_gemm_small(g, stream);
   if (g.epilogue == EPI_STORE_F32 && g.max_ctas >= 0) {
     // zero the output and accumulate every CTA's share by TMA reduce-add (no partial

@@ -77,8 +77,11 @@ GEMM_CASES = [
     (1, 256, 128, 1), (16, 512, 256, 0), (127, 768, 384, 2), (129, 256, 1024, 3),
     (300, 6144, 4096, 0), (512, 4096, 4096, 7), (512, 4096, 12288, 0), (64, 1280, 512, 5),
     (200, 512, 1024, 9), (40, 24576, 256, 0),
-    # M <= 64: weight rows as the MMA's M side (tokens padded to 16 / 32 / 64)
-    (4, 4096, 4096, 0), (2, 24576, 4096, 3), (33, 6144, 1024, 0), (64, 4096, 14336, 0),
+    # 8 < M <= 64: weight rows as the MMA's M side (tokens padded to 16 / 32 / 64)
+    (12, 1280, 512, 0), (33, 6144, 1024, 0), (64, 4096, 14336, 0),
+    # M <= 8: the warp-MMA GEMV (ragged M and N, long K, several CTAs per row block)
+    (4, 4096, 4096, 0), (2, 24576, 4096, 3), (3, 768, 384, 0), (8, 2048, 1024, 0), (5, 776, 640, 0),
+    (1, 4096, 14336, 0),
 ]
 
 
