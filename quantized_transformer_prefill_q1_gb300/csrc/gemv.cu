@@ -3,24 +3,27 @@
 // layer, whose projections are one pass over the weights per token). At M <= 8 streaming the
 // packed weights from HBM is the whole cost; the tcgen05 path reads its A operand (the
 // weights) from tensor memory at a fixed ~22 weights per clock per SM whatever the token
-// count, so here the weights go from registers straight into warp-level MMAs.
+// count, so here the weights go from shared memory through registers into warp-level MMAs.
 //
-// A warp owns 16 weight rows and computes out^T[16 rows, 8 tokens] with
-// mma.sync m16n8k16 (f16 operands, f32 accumulation): the dequantised codes are the A
-// fragment, the activations (tokens >= M zero) the B fragment. The reduction order inside a
-// 16-wide k-step is free, so each thread's four A columns are taken from the packed word it
-// loaded itself (k permuted identically in A and B): lane (g, c) = (lane / 4, lane % 4) reads,
-// per 64-wide half of a group, 8 bytes (INT4: codes 16c .. 16c+15 of the half) or one sign
-// word (Q1: elements 32 (c / 2) .. +31) of rows g and g + 8, and the 16 activations
-// 16c .. 16c+15 of the half for token g. Per group the accumulator is scaled by the row's
-// scale (INT4: the codes enter as the f16 value q - z, rounded like the tcgen05 path's
-// dequantiser rounds it) and added to the row's total in f32.
+// Every warp is independent. It owns 16 weight rows (for SwiGLU 8 gate rows and their 8 up
+// rows) and computes out^T[16 rows, 8 tokens] with mma.sync m16n8k16 (f16 operands, f32
+// accumulation): the dequantised codes are the A fragment, the activations (tokens >= M zero)
+// the B fragment. The (16-row tile, group) units are shared out in equal contiguous ranges,
+// one per warp (SwiGLU: one whole tile per warp, so that silu(gate) * up is formed in the
+// warp). A warp streams its rows' slice of each packed chunk (16 rows x 128 weights: 1024 B of
+// INT4 codes + scales and zeros, or 256 B of Q1 signs + scales) into a ring of stages in
+// shared memory with cp.async, many groups ahead, so that enough bytes are in flight per SM
+// to keep HBM busy without holding them in registers.
 //
-// A CTA is 8 warps = one 128-row block (half a packed 256-row tile: for SwiGLU its 64 gate
-// rows and their 64 up rows). The (row block, group) units are shared out in equal contiguous
-// ranges, one per CTA (SwiGLU: one whole row block per CTA, so gate and up meet in one CTA).
-// Residual form: each range's share is added into out (an f32 atomic add where other CTAs
-// share the row block); store form: out is zeroed first and added to the same way.
+// The reduction order inside a 16-wide k-step is free, so each thread's four A columns are
+// taken from the packed word it reads (k permuted identically in A and B): lane (g, c) =
+// (lane / 4, lane % 4) reads, per 64-wide half of a group, 8 bytes (INT4: codes
+// 16c .. 16c+15 of the half) or one sign word (Q1: elements 32 (c / 2) .. +31) of MMA rows g
+// and g + 8, and the 16 activations 16c .. 16c+15 of the half for token g. Per group the
+// accumulator is scaled by the row's scale (INT4: the codes enter as the f16 value q - z,
+// rounded like the tcgen05 path's dequantiser rounds it) and added to the row's total in f32.
+// Residual form: each range's share is added into out (an f32 atomic add where another warp
+// shares the tile); store form: out is zeroed first and added to the same way.
 #include <cuda_fp16.h>
 
 #include <algorithm>
@@ -31,24 +34,34 @@
 namespace pf {
 namespace {
 
-constexpr int RB = 128;              // weight rows per CTA (row block)
-constexpr int THREADS_V = 256;       // 8 warps x 16 rows
-constexpr int D_PREFETCH = 4;        // groups of packed weights in flight per thread
+constexpr int WARPS_V = 4;
+constexpr int THREADS_V = 32 * WARPS_V;
 
-__device__ __forceinline__ uint2 ld_stream8(const void* p) {
-  uint2 v;
-  asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
-  return v;
+// One warp's stage: its 16 rows of one packed chunk. MMA rows 0-7 come from source rows
+// roA .. roA+7 of the 256-row tile, MMA rows 8-15 from roB .. roB+7.
+template <int WFMT>
+struct ST;
+template <>
+struct ST<PF_W_Q1_G128> {
+  static constexpr int SC = 2 * 16 * 8;  // [half][row][2 sign words], then scales [16]
+  static constexpr int BYTES = SC + 32;  // 288
+  static constexpr int DS = 24;          // stages in flight per warp
+};
+template <>
+struct ST<PF_W_INT4_AFFINE_G128> {
+  static constexpr int SC = 2 * 16 * 32;  // [half][row][8 nibble words], then scales, zeros
+  static constexpr int ZP = SC + 32;
+  static constexpr int BYTES = ZP + 32;   // 1088
+  static constexpr int DS = 8;
+};
+
+__device__ __forceinline__ void cp16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
 }
-__device__ __forceinline__ uint32_t ld_stream4(const void* p) {
-  uint32_t v;
-  asm volatile("ld.global.nc.L1::no_allocate.u32 %0, [%1];" : "=r"(v) : "l"(p));
-  return v;
-}
-__device__ __forceinline__ uint32_t ld_stream2(const void* p) {
-  uint16_t v;
-  asm volatile("ld.global.nc.L1::no_allocate.u16 %0, [%1];" : "=h"(v) : "l"(p));
-  return v;
+__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 // Activations are written by the previous kernel: a coherent load, kept after
 // griddepcontrol.wait by being volatile (an invariant load could be hoisted above it).
@@ -58,6 +71,21 @@ __device__ __forceinline__ uint4 ld_act16(const void* p) {
                : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
                : "l"(p)
                : "memory");
+  return v;
+}
+__device__ __forceinline__ uint32_t lds32(uint32_t a) {
+  uint32_t v;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a) : "memory");
+  return v;
+}
+__device__ __forceinline__ uint2 lds64(uint32_t a) {
+  uint2 v;
+  asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(a) : "memory");
+  return v;
+}
+__device__ __forceinline__ uint32_t lds16(uint32_t a) {
+  uint16_t v;
+  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(a) : "memory");
   return v;
 }
 
@@ -74,190 +102,292 @@ __device__ __forceinline__ float h2f(uint32_t bits) {
   return __half2float(__ushort_as_half(static_cast<unsigned short>(bits)));
 }
 
-// One thread's packed weights of one group: rows g and g + 8 of the warp, both halves.
+// Copies one warp's stage (chunk `ch`, source rows roA.., roB..) into shared memory at `st`.
+__device__ __forceinline__ void issue_q1(uint32_t st, const uint8_t* ch, int roA, int roB, int lane) {
+  if (lane < 16) {  // signs: [half h][block b][4 x 16 B]
+    const int h = lane >> 3, b = (lane >> 2) & 1, p = lane & 3;
+    cp16(st + h * 128 + b * 64 + 16 * p, ch + h * Q1_HALF_BYTES + (b ? roB : roA) * 8 + 16 * p);
+  } else if (lane < 18) {
+    const int b = lane - 16;
+    cp16(st + ST<PF_W_Q1_G128>::SC + 16 * b, ch + Q1_SCALE_OFF + (b ? roB : roA) * 2);
+  }
+}
+__device__ __forceinline__ void issue_i4(uint32_t st, const uint8_t* ch, int roA, int roB, int lane) {
+  const int b = (lane >> 4) & 1, p = lane & 15;  // codes: [half][block b][16 x 16 B]
+#pragma unroll
+  for (int h = 0; h < 2; ++h)
+    cp16(st + h * 512 + b * 256 + 16 * p, ch + h * I4_HALF_BYTES + (b ? roB : roA) * 32 + 16 * p);
+  if (lane < 4) {
+    const int bb = lane & 1;
+    const bool zero = lane >= 2;
+    cp16(st + (zero ? ST<PF_W_INT4_AFFINE_G128>::ZP : ST<PF_W_INT4_AFFINE_G128>::SC) + 16 * bb,
+         ch + (zero ? I4_ZERO_OFF : I4_SCALE_OFF) + (bb ? roB : roA) * 2);
+  }
+}
+
+// A fragment of k-step ks of half h from the stage at `st` (lane g = gq, c):
+// Q1: +-1.0 for pairs i0, i0 + 1 of sign word c / 2 (pair i keeps its negative flags at bits
+//     15 - i / 31 - i);
+// INT4: pairs 2 (ks % 2), 2 (ks % 2) + 1 of nibble word 2c + ks / 2, as the f16 values q - z
+//     ((1024 + q) and (1024 + 16 q) are exact f16 bit patterns).
 template <int WFMT>
-struct WU;
+struct Frag;
 template <>
-struct WU<PF_W_Q1_G128> {
-  uint32_t z[2][2];  // [half][row]: sign word c / 2 of the half-row
-  uint32_t s[2];
-  __device__ __forceinline__ void load(const uint8_t* ch, int row2, int c) {
+struct Frag<PF_W_Q1_G128> {
+  uint32_t z[2][2];  // [half][row g, g + 8]
+  float s[2];
+  __device__ __forceinline__ void read(uint32_t st, int gq, int c) {
 #pragma unroll
     for (int h = 0; h < 2; ++h)
 #pragma unroll
-      for (int i = 0; i < 2; ++i) z[h][i] = ld_stream4(ch + h * Q1_HALF_BYTES + (row2 + 8 * i) * 8 + (c >> 1) * 4);
+      for (int i = 0; i < 2; ++i) z[h][i] = lds32(st + h * 128 + i * 64 + gq * 8 + (c >> 1) * 4);
 #pragma unroll
-    for (int i = 0; i < 2; ++i) s[i] = ld_stream2(ch + Q1_SCALE_OFF + (row2 + 8 * i) * 2);
+    for (int i = 0; i < 2; ++i) s[i] = h2f(lds16(st + ST<PF_W_Q1_G128>::SC + i * 16 + gq * 2));
   }
-  // A fragment of k-step ks of half h: +-1.0 for pairs i0, i0 + 1 of the word (the word's
-  // pair i keeps its negative flags at bits 15 - i / 31 - i)
-  __device__ __forceinline__ void frag(int h, int ks, int c, uint32_t (&a)[4]) const {
+  __device__ __forceinline__ void a(int h, int ks, int c, uint32_t (&f)[4]) const {
     const int i0 = 8 * (c & 1) + 2 * ks;
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
-      a[i] = ((z[h][i] << i0) & 0x80008000u) | 0x3C003C00u;
-      a[2 + i] = ((z[h][i] << (i0 + 1)) & 0x80008000u) | 0x3C003C00u;
+      f[i] = ((z[h][i] << i0) & 0x80008000u) | 0x3C003C00u;
+      f[2 + i] = ((z[h][i] << (i0 + 1)) & 0x80008000u) | 0x3C003C00u;
     }
   }
 };
 template <>
-struct WU<PF_W_INT4_AFFINE_G128> {
-  uint2 q[2][2];  // [half][row]: nibble words 2c, 2c + 1 of the half-row
-  uint32_t s[2], zp[2];
-  __device__ __forceinline__ void load(const uint8_t* ch, int row2, int c) {
+struct Frag<PF_W_INT4_AFFINE_G128> {
+  uint2 q[2][2];
+  uint32_t zp[2];
+  float s[2];
+  __device__ __forceinline__ void read(uint32_t st, int gq, int c) {
 #pragma unroll
     for (int h = 0; h < 2; ++h)
 #pragma unroll
-      for (int i = 0; i < 2; ++i) q[h][i] = ld_stream8(ch + h * I4_HALF_BYTES + (row2 + 8 * i) * 32 + c * 8);
+      for (int i = 0; i < 2; ++i) q[h][i] = lds64(st + h * 512 + i * 256 + gq * 32 + c * 8);
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
-      s[i] = ld_stream2(ch + I4_SCALE_OFF + (row2 + 8 * i) * 2);
-      zp[i] = ld_stream2(ch + I4_ZERO_OFF + (row2 + 8 * i) * 2);
+      s[i] = h2f(lds16(st + ST<PF_W_INT4_AFFINE_G128>::SC + i * 16 + gq * 2));
+      zp[i] = lds16(st + ST<PF_W_INT4_AFFINE_G128>::ZP + i * 16 + gq * 2);
     }
   }
-  // A fragment of k-step ks: pairs 2 (ks % 2), 2 (ks % 2) + 1 of word 2c + ks / 2, as the f16
-  // values q - z ((1024 + q) and (1024 + 16 q) are exact f16 bit patterns)
-  __device__ __forceinline__ void frag(int h, int ks, int c, uint32_t (&a)[4]) const {
+  __device__ __forceinline__ void a(int h, int ks, int c, uint32_t (&f)[4]) const {
     const __half2 k1024 = u2h(0x64006400u), k16th = u2h(0x2C002C00u), km64 = u2h(0xD400D400u);
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
       uint32_t W = (ks >> 1) ? q[h][i].y : q[h][i].x;
       if (ks & 1) W >>= 8;
       const __half2 z2 = u2h(zp[i] | (zp[i] << 16));
-      a[i] = h2u(__hsub2(__hsub2(u2h((W & 0x000F000Fu) | 0x64006400u), k1024), z2));
-      a[2 + i] = h2u(__hsub2(__hfma2(u2h((W & 0x00F000F0u) | 0x64006400u), k16th, km64), z2));
+      f[i] = h2u(__hsub2(__hsub2(u2h((W & 0x000F000Fu) | 0x64006400u), k1024), z2));
+      f[2 + i] = h2u(__hsub2(__hfma2(u2h((W & 0x00F000F0u) | 0x64006400u), k16th, km64), z2));
     }
   }
 };
 
 __device__ __forceinline__ float silu_mul_v(float g, float u) { return g / (1.0f + __expf(-g)) * u; }
 
+// Unit u = (16-row tile t, group g). Tile t covers, for SwiGLU, gate rows 8q .. 8q+7 and the
+// matching up rows of 128-row packed group b = t / 8 (q = t % 8: source rows 128 (b % 2) + 8q
+// and + 64 of the 256-row tile b / 2); otherwise rows 16t .. 16t+15.
+template <int EPI>
+__device__ __forceinline__ void tile_rows(int t, int& tile256, int& roA, int& roB) {
+  if (EPI == EPI_SWIGLU) {
+    const int b = t >> 3;
+    tile256 = b >> 1;
+    roA = (b & 1) * 128 + 8 * (t & 7);
+    roB = roA + 64;
+  } else {
+    tile256 = t >> 4;
+    roA = (t & 15) * 16;
+    roB = roA + 8;
+  }
+}
+
 template <int WFMT, int EPI>
-__global__ void __launch_bounds__(THREADS_V, 2)
+__global__ void __launch_bounds__(THREADS_V)
     gemv_kernel(const __half* a, const uint8_t* __restrict__ wpk, int M, int N, int K,
-                void* __restrict__ out, long long units, int ctas) {
+                void* __restrict__ out, long long units, int warps) {
+  using S = ST<WFMT>;
+  constexpr int DS = S::DS;
   constexpr size_t P = WFMT == PF_W_Q1_G128 ? Q1_CHUNK_BYTES : I4_CHUNK_BYTES;
-  __shared__ float xch[RB / 2][8];  // SwiGLU: up rows' totals handed to the gate rows
+  extern __shared__ __align__(16) uint8_t gv_smem[];
+  __shared__ float part[WARPS_V / 2][32][4];  // SwiGLU: the odd-group half of a tile's sums
   griddep_launch_dependents();
   const int G = K / GROUP;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gq = lane >> 2, c = lane & 3;
-  const int r0 = 16 * warp + gq;  // rows r0 and r0 + 8 of the row block
-  const bool tok = gq < M;        // this lane's B column (token gq) exists
-  const long long u0 = units * blockIdx.x / ctas, u1 = units * (blockIdx.x + 1) / ctas;
-  bool waited = false;
-  for (long long u = u0; u < u1;) {
-    // ---- one segment: groups [g0, g1) of row block rb
-    const int rb = static_cast<int>(u / G);
-    const int g0 = static_cast<int>(u - static_cast<long long>(rb) * G);
-    const int g1 = static_cast<int>(std::min<long long>(G, g0 + (u1 - u)));
-    const bool whole = g0 == 0 && g1 == G;
-    u += g1 - g0;
-    const int n = g1 - g0;
-    const int row2 = (rb & 1) * RB + r0;  // row within the 256-row packed tile
-    const uint8_t* tile = wpk + static_cast<size_t>(rb >> 1) * G * P + static_cast<size_t>(g0) * P;
-    const __half* xrow = a + static_cast<size_t>(tok ? gq : 0) * K + g0 * GROUP + 16 * c;
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};  // (r0, 2c), (r0, 2c+1), (r0+8, 2c), (r0+8, 2c+1)
-    WU<WFMT> un[D_PREFETCH];
-#pragma unroll
-    for (int d = 0; d < D_PREFETCH; ++d)
-      if (d < n) un[d].load(tile + d * P, row2, c);
-    if (!waited) {  // the weights never depend on the previous kernel; the activations do
-      griddep_wait();
-      waited = true;
+  const bool tok = gq < M;  // this lane's B column (token gq) exists
+  const int gw = blockIdx.x * WARPS_V + warp;
+  // This warp's units as a cursor (t, g) stepping by `gs`: SwiGLU tiles are split between two
+  // warps of the CTA by group parity (warp 2i + p takes groups p, p + 2, ... of tile
+  // 2 blockIdx + i); otherwise an equal contiguous range of (tile, group) units.
+  int t0, g0, gs, n;
+  if (EPI == EPI_SWIGLU) {
+    t0 = gw >> 1;
+    g0 = gw & 1;
+    gs = 2;
+    n = t0 < warps ? (G - g0 + 1) >> 1 : 0;
+  } else {
+    const long long u0 = gw < warps ? units * gw / warps : 0;
+    const long long u1 = gw < warps ? units * (gw + 1) / warps : 0;
+    t0 = static_cast<int>(u0 / G);
+    g0 = static_cast<int>(u0 - static_cast<long long>(t0) * G);
+    gs = 1;
+    n = static_cast<int>(u1 - u0);
+  }
+  const uint32_t ring = smem_u32(gv_smem) + static_cast<uint32_t>(warp * DS * S::BYTES);
+
+  int ti = t0, gi = g0, si = 0;  // issue cursor and its stage
+  auto issue_next = [&]() {
+    int tile256, roA, roB;
+    tile_rows<EPI>(ti, tile256, roA, roB);
+    const uint8_t* ch = wpk + (static_cast<size_t>(tile256) * G + gi) * P;
+    const uint32_t st = ring + static_cast<uint32_t>(si * S::BYTES);
+    if (WFMT == PF_W_Q1_G128) issue_q1(st, ch, roA, roB, lane);
+    else issue_i4(st, ch, roA, roB, lane);
+    gi += gs;
+    if (gi >= G) {
+      gi -= G;
+      ++ti;
     }
-    for (int j0 = 0; j0 < n; j0 += D_PREFETCH) {
+    si = si + 1 == DS ? 0 : si + 1;
+  };
+  // the weights never depend on the previous kernel: start streaming them before the wait
+#pragma unroll 1
+  for (int j = 0; j < DS - 1; ++j) {
+    if (j < n) issue_next();
+    cp_commit();
+  }
+  griddep_wait();  // the activations and the output do
+
+  int tc = t0, gc = g0, sc = 0;  // compute cursor
+  const __half* xbase = a + static_cast<size_t>(tok ? gq : 0) * K + 16 * c;
+  uint4 xn[4] = {};  // the next unit's 16 activations of each half (token gq)
+  auto load_x = [&](int g, uint4 (&x)[4]) {
 #pragma unroll
-      for (int d = 0; d < D_PREFETCH; ++d) {
-        const int j = j0 + d;
-        if (j < n) {
-          uint4 xb[2][2];  // [half][8 of the 16 activations]
+    for (int e = 0; e < 4; ++e)
+      x[e] = tok ? ld_act16(xbase + g * GROUP + 64 * (e >> 1) + 8 * (e & 1)) : make_uint4(0u, 0u, 0u, 0u);
+  };
+  if (n > 0) load_x(gc, xn);
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};  // (row g, token 2c), (g, 2c+1), (g+8, 2c), (g+8, 2c+1)
+  bool seg_first = true;
+  int seg_g0 = 0;
+#pragma unroll 1
+  for (int j = 0; j < n; ++j) {
+    if (j + DS - 1 < n) issue_next();
+    cp_commit();
+    uint4 xc[4];
 #pragma unroll
-          for (int h = 0; h < 2; ++h)
+    for (int e = 0; e < 4; ++e) xc[e] = xn[e];
+    int tn = tc, gn = gc + gs;
+    if (gn >= G) {
+      gn -= G;
+      ++tn;
+    }
+    if (j + 1 < n) load_x(gn, xn);
+    cp_wait<DS - 1>();  // this lane's copies of unit j have landed
+    __syncwarp();       // and every other lane's
+    if (seg_first) {
+      seg_g0 = gc;
+      seg_first = false;
+    }
+    Frag<WFMT> fr;
+    fr.read(ring + static_cast<uint32_t>(sc * S::BYTES), gq, c);
+    float d[4][4] = {};  // four independent chains: (half, k-step parity)
 #pragma unroll
-            for (int e = 0; e < 2; ++e)
-              xb[h][e] = tok ? ld_act16(xrow + j * GROUP + 64 * h + 8 * e) : make_uint4(0u, 0u, 0u, 0u);
-          float dd[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int h = 0; h < 2; ++h) {
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {
-#pragma unroll
-            for (int ks = 0; ks < 4; ++ks) {
-              uint32_t af[4];
-              un[d].frag(h, ks, c, af);
-              const uint4& xv = xb[h][ks >> 1];
-              mma16816(af, (ks & 1) ? xv.z : xv.x, (ks & 1) ? xv.w : xv.y, dd);
-            }
-          }
-          const float s0 = h2f(un[d].s[0]), s1 = h2f(un[d].s[1]);
-          acc[0] = fmaf(s0, dd[0], acc[0]);
-          acc[1] = fmaf(s0, dd[1], acc[1]);
-          acc[2] = fmaf(s1, dd[2], acc[2]);
-          acc[3] = fmaf(s1, dd[3], acc[3]);
-          if (j + D_PREFETCH < n) un[d].load(tile + static_cast<size_t>(j + D_PREFETCH) * P, row2, c);
-        }
+      for (int ks = 0; ks < 4; ++ks) {
+        uint32_t af[4];
+        fr.a(h, ks, c, af);
+        const uint4& xv = xc[2 * h + (ks >> 1)];
+        mma16816(af, (ks & 1) ? xv.z : xv.x, (ks & 1) ? xv.w : xv.y, d[2 * h + (ks & 1)]);
       }
     }
-    // ---- the segment's share: acc[2i + t] is row r0 + 8i, token 2c + t
-    if (EPI == EPI_SWIGLU) {
-      // every SwiGLU range is one whole row block: rows 0..63 gate, 64..127 the matching up
-      if (warp >= 4) {
+    __syncwarp();  // the stage is read: it may be refilled
 #pragma unroll
-        for (int i = 0; i < 2; ++i)
-#pragma unroll
-          for (int t = 0; t < 2; ++t) xch[r0 + 8 * i - RB / 2][2 * c + t] = acc[2 * i + t];
-      }
-      __syncthreads();
-      if (warp < 4) {
-        __half* o = reinterpret_cast<__half*>(out);
-#pragma unroll
-        for (int i = 0; i < 2; ++i) {
-          const int col = rb * (RB / 2) + r0 + 8 * i;
-#pragma unroll
-          for (int t = 0; t < 2; ++t) {
-            const int m = 2 * c + t;
-            if (m < M && col < (N >> 1))
-              o[static_cast<size_t>(m) * (N >> 1) + col] =
-                  __float2half_rn(silu_mul_v(acc[2 * i + t], xch[r0 + 8 * i][m]));
-          }
-        }
-      }
-      __syncthreads();  // xch is free for the next segment
-    } else {
+    for (int i = 0; i < 4; ++i) {
+      const float v = (d[0][i] + d[1][i]) + (d[2][i] + d[3][i]);
+      acc[i] = fmaf(fr.s[i >> 1], v, acc[i]);
+    }
+    const bool tile_end = EPI == EPI_SWIGLU ? j == n - 1 : (gc == G - 1 || j == n - 1);
+    const int t = tc;
+    const int g = gc;
+    tc = tn;
+    gc = gn;
+    sc = sc + 1 == DS ? 0 : sc + 1;
+    if (!tile_end) continue;
+    // ---- end of a segment of tile t: its share (acc[2i + e]: MMA row g + 8i, token 2c + e)
+    if (EPI != EPI_SWIGLU) {
+      const bool whole = seg_g0 == 0 && g == G - 1;
       float* o = reinterpret_cast<float*>(out);
 #pragma unroll
       for (int i = 0; i < 2; ++i) {
-        const int row = rb * RB + r0 + 8 * i;
+        const int row = 16 * t + gq + 8 * i;
         if (row >= N) continue;
 #pragma unroll
-        for (int t = 0; t < 2; ++t) {
-          const int m = 2 * c + t;
+        for (int e = 0; e < 2; ++e) {
+          const int m = 2 * c + e;
           if (m >= M) continue;
           float* p = o + static_cast<size_t>(m) * N + row;
-          if (whole) *p += acc[2 * i + t];  // no other CTA has this row block
-          else atomicAdd(p, acc[2 * i + t]);
+          if (whole) *p += acc[2 * i + e];  // no other warp has this tile
+          else atomicAdd(p, acc[2 * i + e]);
         }
+      }
+      acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
+      seg_first = true;
+    }
+  }
+  if (EPI == EPI_SWIGLU) {
+    // the odd-group warp hands its sums to the even-group warp of the same tile, which forms
+    // silu(gate) * up: MMA rows g are gate rows, g + 8 their up rows
+    const int pair = warp >> 1;
+    if (warp & 1) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) part[pair][lane][i] = acc[i];
+    }
+    __syncthreads();
+    if (!(warp & 1) && n > 0) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) acc[i] += part[pair][lane][i];
+      const int col = 8 * t0 + gq;
+      __half* o = reinterpret_cast<__half*>(out);
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int m = 2 * c + e;
+        if (m < M && col < (N >> 1))
+          o[static_cast<size_t>(m) * (N >> 1) + col] = __float2half_rn(silu_mul_v(acc[e], acc[2 + e]));
       }
     }
   }
-  if (!waited) griddep_wait();
+  cp_wait<0>();
 }
 
 template <int WFMT, int EPI>
 cudaError_t launch_v(const GemmArgs& g, cudaStream_t stream) {
-  static const int ctas_max = [] {
+  constexpr int smem = WARPS_V * ST<WFMT>::DS * ST<WFMT>::BYTES;
+  static_assert(smem <= 48 * 1024, "GEMV stages");
+  static const int warps_max = [] {
     int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gemv_kernel<WFMT, EPI>, THREADS_V, 0) != cudaSuccess ||
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gemv_kernel<WFMT, EPI>, THREADS_V, smem) !=
+            cudaSuccess ||
         per_sm < 1)
       per_sm = 1;
-    return per_sm * device_sm_count();
+    return per_sm * device_sm_count() * WARPS_V;
   }();
   const int G = g.K / GROUP;
-  const long long nrb = padded_rows(g.N) / RB;
-  const long long units = nrb * G;
-  // SwiGLU: one whole row block per CTA (gate and up rows meet in it); otherwise equal ranges
-  const int ctas = EPI == EPI_SWIGLU ? static_cast<int>(nrb) : static_cast<int>(std::min<long long>(units, ctas_max));
-  return launch_pdl(gemv_kernel<WFMT, EPI>, dim3(ctas), dim3(THREADS_V), 0, stream,
-                    reinterpret_cast<const __half*>(g.a), g.w, g.M, g.N, g.K, g.out, units, ctas);
+  const long long tiles = EPI == EPI_SWIGLU ? g.N / 16 : padded_rows(g.N) / 16;
+  const long long units = tiles * G;
+  // SwiGLU: two warps per tile (gate and up rows meet in the CTA); `warps` counts tiles there.
+  // Otherwise equal ranges of units, one per warp.
+  int warps, ctas;
+  if (EPI == EPI_SWIGLU) {
+    warps = static_cast<int>(tiles);
+    ctas = static_cast<int>((2 * tiles + WARPS_V - 1) / WARPS_V);
+  } else {
+    warps = static_cast<int>(std::min<long long>(units, warps_max));
+    ctas = (warps + WARPS_V - 1) / WARPS_V;
+  }
+  return launch_pdl(gemv_kernel<WFMT, EPI>, dim3(ctas), dim3(THREADS_V), smem, stream,
+                    reinterpret_cast<const __half*>(g.a), g.w, g.M, g.N, g.K, g.out, units, warps);
 }
 
 template <int WFMT>
@@ -272,6 +402,7 @@ int gemv_max_m(int wfmt) { return wfmt == PF_W_Q1_G128 ? GEMV_M_MAX_Q1 : GEMV_M_
 
 cudaError_t launch_gemv(const GemmArgs& g, cudaStream_t stream) {
   if (g.M < 1 || g.M > 8 || g.K % GROUP) return cudaErrorInvalidValue;
+  if (g.epilogue == EPI_SWIGLU && g.N % 256) return cudaErrorInvalidValue;
   if (g.epilogue == EPI_STORE_F32) {
     // zero the M x N output and add every range's share, as the residual form does
     cudaError_t e = cudaMemsetAsync(g.out, 0, static_cast<size_t>(g.M) * g.N * sizeof(float), stream);
