@@ -220,10 +220,27 @@ pf_status pf_prefill_chunk_dev(pf_session* s, const int32_t* tokens_dev, int32_t
 /* One decode step ([P2] encode_layer_into for every layer, then the decode tail: final
  * norm + LM head): the token at *token_dev (device int32, e.g. the previous step's argmax)
  * at the session's KV position, which advances by one; logits_dev [vocab] f32 receives its
- * logits. Same kernels as a one-token chunk (the small-M GEMM path); the recorded graph of
- * M = 1 is reused from step to step. Errors as pf_prefill_chunk_dev (PF_ERR_LOGITS when the
+ * logits. Same kernels as a one-token chunk (the projections on the GEMV path); the recorded
+ * graph of M = 1 is reused from step to step. Errors as pf_prefill_chunk_dev (PF_ERR_LOGITS when the
  * model has no LM head or logits_dev is NULL). */
 pf_status pf_decode_step(pf_session* s, const int32_t* token_dev, float* logits_dev, void* stream);
+
+/* Greedy decode step ([P1] encode_full_forward_prefill, greedy decoding: the argmax of the
+ * logits taken on the GPU so that one token id, not the logits, is the step's result):
+ * pf_decode_step on *token_in_dev, then the index of the largest logit (lowest index on
+ * ties) written to *token_out_dev (device int32; may be token_in_dev). Consecutive calls
+ * can chain tokens without a host round trip. Errors as pf_decode_step. */
+pf_status pf_decode_step_greedy(pf_session* s, const int32_t* token_in_dev, int32_t* token_out_dev,
+                                float* logits_dev, void* stream);
+
+/* Speculative-verify prefill ([P1] encode_full_forward_prefill_verify): the M device token
+ * ids at start_pos through every layer as one micro-batch (1 <= M <= max_chunk), then the
+ * final RMSNorm and the LM head on EVERY position and the argmax of each position's logits.
+ * logits_all_dev: f32 [M][vocab] (row t = logits after token t); ids_dev: int32 [M], the
+ * greedy next token after each position (lowest index on ties). The KV position advances
+ * by M. Needs an LM head and vocab % 8 == 0; PF_ERR_SHAPE for M > max_chunk. */
+pf_status pf_prefill_verify(pf_session* s, const int32_t* tokens_dev, int32_t M, int32_t start_pos,
+                            float* logits_all_dev, int32_t* ids_dev, void* stream);
 
 /* End to end from host memory: copies tokens_host to the device, runs
  * pf_prefill_chunk, copies the last position's logits into logits_host [vocab]
@@ -303,6 +320,11 @@ pf_status pf_op_embed(const float* embed_dev, const int32_t* tokens_dev, int32_t
 pf_status pf_op_lm_head(int32_t wfmt, const float* x_row_dev, const float* norm_w_dev,
                         float eps, const void* packed_dev, int32_t vocab, int32_t H,
                         float* logits_dev, void* stream);
+/* Greedy argmax of each row ([P1] dispatch_argmax, one 1024-thread group per row):
+ * out_dev[r] = index of the largest of x_dev[r * ld .. r * ld + n - 1] (f32), lowest index
+ * on ties, NaN never chosen (a row without a number gives 0). rows >= 1, n >= 1, ld >= n. */
+pf_status pf_op_argmax(const float* x_dev, int32_t rows, int32_t n, int64_t ld, int32_t* out_dev,
+                       void* stream);
 /* Host RoPE table [max_seq][hd/2][2] = (cos, sin)(p * theta^(-2i/hd)), computed in
  * double and rounded to f32. */
 pf_status pf_rope_table_host(float theta, int32_t head_dim, int32_t max_seq, float* dst_host);

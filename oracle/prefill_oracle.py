@@ -280,6 +280,19 @@ class OracleModel:
         y = rmsnorm(x_last, self.extra["final_norm"], self.shape.final_eps).astype(np.float32)
         return (self.lm_w @ y.astype(np.float64)).astype(np.float32)
 
+    def head_all(self, x_rows: np.ndarray) -> np.ndarray:
+        """The verify tail (oxibonsai-kernels metal_prefill.rs
+        ``encode_full_forward_prefill_verify``): final norm and LM head on every row, the
+        same per-row arithmetic as ``head``. Returns f32 logits [rows, vocab]."""
+        return np.stack([self.head(r) for r in np.asarray(x_rows, dtype=np.float32)])
+
+    def prefill_verify(self, tokens: np.ndarray):
+        """One chunk of token ids through every layer, then the logits of every position
+        and each position's greedy next token."""
+        x, _ = self.forward_chunk(self.embed(tokens), self.position, False)
+        logits = self.head_all(x)
+        return logits, argmax_first(logits)
+
     def embed(self, tokens: np.ndarray) -> np.ndarray:
         """x[t] = E[token_t] with no sqrt(hidden) scale (reading A13; turbospark-runtime
         prefill.rs embeds each token at scale 1.0)."""
@@ -418,6 +431,23 @@ def decode_prompt(model: OracleModel, x: np.ndarray, start: int = 0) -> np.ndarr
         outs.append(r)
     model.position = start + x.shape[0]
     return np.stack(outs)
+
+
+def argmax_first(logits: np.ndarray) -> np.ndarray:
+    """Greedy selection (oxibonsai-kernels metal_prefill.rs: the argmax of the logits on
+    the GPU, one token id per position). Per row of the last axis: the index of the largest
+    value; ties go to the lowest index (reading A15, the pages do not print the kernel);
+    NaN is never chosen and a row without a number gives 0. Written out row by row."""
+    x = np.asarray(logits, dtype=np.float64)
+    rows = x.reshape(-1, x.shape[-1])
+    out = np.zeros(rows.shape[0], dtype=np.int64)
+    for i, r in enumerate(rows):
+        best, idx = -math.inf, -1
+        for j, v in enumerate(r):
+            if v > best or (v == best and idx < 0):
+                best, idx = v, j
+        out[i] = max(idx, 0)
+    return out.reshape(x.shape[:-1])
 
 
 def rel_l2(a: np.ndarray, b: np.ndarray) -> float:

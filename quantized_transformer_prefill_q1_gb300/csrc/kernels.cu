@@ -8,6 +8,7 @@
 #include "ptx.cuh"
 
 #include <algorithm>
+#include <climits>
 
 namespace pf {
 namespace {
@@ -349,6 +350,53 @@ __global__ void set_int_kernel(int* dst, int v) {
   griddep_launch_dependents();
   griddep_wait(); *dst = v; }
 
+// ------------------------------------------------------------------ greedy argmax
+// oxibonsai-kernels metal_prefill.rs `dispatch_argmax` (greedy decoding on the GPU; the
+// verify tail dispatches it once per position with 1024 threads): one CTA of 1024 threads
+// per row. The largest value wins; ties go to the lowest index (the pages do not print the
+// kernel); NaN never wins, and a row with no number gives 0.
+__device__ __forceinline__ void argmax_take(float v, int i, float& best, int& bi) {
+  if (v > best || (v == best && i < bi)) {
+    best = v;
+    bi = i;
+  }
+}
+__global__ void __launch_bounds__(1024) argmax_rows_kernel(const float* __restrict__ x, int n,
+                                                           long long ld, int* __restrict__ out) {
+  __shared__ float wb[32];
+  __shared__ int wi[32];
+  griddep_launch_dependents();
+  griddep_wait();
+  const float* row = x + static_cast<long long>(blockIdx.x) * ld;
+  float best = -INFINITY;
+  int bi = INT_MAX;
+  for (int i = threadIdx.x; i < n; i += blockDim.x) argmax_take(row[i], i, best, bi);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float ob = __shfl_xor_sync(0xffffffffu, best, o);
+    const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+    argmax_take(ob, oi, best, bi);
+  }
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (lane == 0) {
+    wb[warp] = best;
+    wi[warp] = bi;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    const int nw = blockDim.x >> 5;
+    best = lane < nw ? wb[lane] : -INFINITY;
+    bi = lane < nw ? wi[lane] : INT_MAX;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ob = __shfl_xor_sync(0xffffffffu, best, o);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+      argmax_take(ob, oi, best, bi);
+    }
+    if (lane == 0) out[blockIdx.x] = bi == INT_MAX ? 0 : bi;
+  }
+}
+
 // Exercises the bounded wait every pipelined kernel uses: one mbarrier expecting one
 // arrival; with `arrive` set a thread provides it, otherwise nothing ever does and the
 // wait must give up after limit_ns and record PF_ERR_DEVICE_TIMEOUT.
@@ -579,6 +627,11 @@ cudaError_t launch_dequant(int wfmt, const uint8_t* packed, int64_t N, int64_t K
     dequant_kernel<PF_W_INT4_AFFINE_G128><<<grid, 256, 0, stream>>>(packed, N, K,
                                                                     reinterpret_cast<__half*>(w));
   return cudaGetLastError();
+}
+
+cudaError_t launch_argmax_rows(const float* x, int rows, int n, long long ld, int* out, cudaStream_t stream) {
+  if (rows <= 0 || n <= 0 || ld < n) return cudaErrorInvalidValue;
+  return launch_pdl(argmax_rows_kernel, dim3(rows), dim3(1024), 0, stream, x, n, ld, out);
 }
 
 cudaError_t launch_set_int(int* dst, int value, cudaStream_t stream) {

@@ -759,6 +759,47 @@ pf_status pf_decode_step(pf_session* s, const int32_t* token_dev, float* logits_
   return prefill_common(s, token_dev, true, nullptr, 1, s->position, logits_dev, stream);
 }
 
+pf_status pf_decode_step_greedy(pf_session* s, const int32_t* token_in_dev, int32_t* token_out_dev,
+                                float* logits_dev, void* stream) {
+  if (!s) return fail(PF_ERR_INVALID_ARG, "session is NULL");
+  if (!token_in_dev || !token_out_dev) return fail(PF_ERR_INVALID_ARG, "token is NULL");
+  if (!logits_dev) return fail(PF_ERR_LOGITS, "decode needs logits");
+  pf_status r = prefill_common(s, token_in_dev, true, nullptr, 1, s->position, logits_dev, stream);
+  if (r != PF_OK) return r;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int vocab = s->model.cfg.vocab;
+  return launch_k(s, PF_K_OTHER, st, "argmax",
+                  [&] { return launch_argmax_rows(logits_dev, 1, vocab, vocab, token_out_dev, st); });
+}
+
+// P1 encode_full_forward_prefill_verify: the layer loop of one micro-batch, then the
+// batched final RMSNorm on all positions, the LM-head GEMM on all positions and one argmax
+// per position.
+pf_status pf_prefill_verify(pf_session* s, const int32_t* tokens_dev, int32_t M, int32_t start_pos,
+                            float* logits_all_dev, int32_t* ids_dev, void* stream) {
+  if (!s) return fail(PF_ERR_INVALID_ARG, "session is NULL");
+  const pf_config& c = s->model.cfg;
+  if (!tokens_dev || !logits_all_dev || !ids_dev) return fail(PF_ERR_INVALID_ARG, "NULL pointer");
+  if (!s->model.lm_head || !s->model.final_norm || c.vocab <= 0)
+    return fail(PF_ERR_LOGITS, "verify needs the final norm and LM head");
+  if (M > c.max_chunk) return fail(PF_ERR_SHAPE, "verify chunk M %d exceeds max_chunk %d", M, c.max_chunk);
+  if (c.vocab % 8) return fail(PF_ERR_SHAPE, "verify needs vocab %% 8 == 0 (vocab %d)", c.vocab);
+  if (reinterpret_cast<uintptr_t>(logits_all_dev) & 15) return fail(PF_ERR_INVALID_ARG, "logits must be 16-B aligned");
+  pf_status r = prefill_common(s, tokens_dev, true, nullptr, M, start_pos, nullptr, stream);
+  if (r != PF_OK) return r;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const float* x = wsp<float>(s, s->L.x);  // the final hidden rows of the micro-batch
+  void* y = wsp<void>(s, s->L.y);
+  PF_TRY(launch_k(s, PF_K_RMSNORM, st, "final rmsnorm", [&] {
+    return launch_rmsnorm(x, s->model.final_norm, c.final_eps, M, c.hidden, y, st);
+  }));
+  PF_TRY(enqueue_gemm(s, PF_K_LM_HEAD, c.wfmt, EPI_STORE_F32, y, s->model.lm_head, M, c.vocab, c.hidden,
+                      logits_all_dev, st));
+  return launch_k(s, PF_K_OTHER, st, "argmax", [&] {
+    return launch_argmax_rows(logits_all_dev, M, c.vocab, c.vocab, ids_dev, st);
+  });
+}
+
 pf_status pf_prefill_hidden(pf_session* s, float* x_dev, int32_t M, int32_t start_pos,
                             float* logits_dev, void* stream) {
   if (s && M > 0 && !x_dev) return fail(PF_ERR_INVALID_ARG, "x is NULL");
@@ -982,6 +1023,13 @@ pf_status pf_op_lm_head(int32_t wfmt, const float* x_row, const float* nw, float
   PF_CUDA(launch_lm_head(wfmt, x_row, nw, eps, static_cast<const uint8_t*>(packed), vocab, H,
                          logits, static_cast<cudaStream_t>(stream)),
           "lm_head");
+  return PF_OK;
+}
+
+pf_status pf_op_argmax(const float* x, int32_t rows, int32_t n, int64_t ld, int32_t* out, void* stream) {
+  if (!x || !out) return fail(PF_ERR_INVALID_ARG, "NULL pointer");
+  if (rows <= 0 || n <= 0 || ld < n) return fail(PF_ERR_SHAPE, "rows %d n %d ld %lld", rows, n, (long long)ld);
+  PF_CUDA(launch_argmax_rows(x, rows, n, ld, out, static_cast<cudaStream_t>(stream)), "argmax");
   return PF_OK;
 }
 

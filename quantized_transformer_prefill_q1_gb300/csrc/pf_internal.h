@@ -98,6 +98,8 @@ cudaError_t launch_lm_head(int wfmt, const float* x_row, const float* norm_w, fl
                            const uint8_t* packed, int vocab, int H, float* logits,
                            cudaStream_t stream);
 cudaError_t launch_set_int(int* dst, int value, cudaStream_t stream);
+// out[r] = index of the largest of x[r * ld + 0 .. n-1] (lowest index on ties, NaN never wins)
+cudaError_t launch_argmax_rows(const float* x, int rows, int n, long long ld, int* out, cudaStream_t stream);
 cudaError_t launch_wait_selftest(int* status, long long limit_ns, int arrive, cudaStream_t stream);
 
 // Launches `kern` with programmatic stream serialisation (see griddep_wait in ptx.cuh).

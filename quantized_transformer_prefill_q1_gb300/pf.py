@@ -79,6 +79,8 @@ _SIGS = {
     "pf_prefill_chunk": ([_VP, _VP, _I32, _I32, _VP, _VP], _I32),
     "pf_prefill_chunk_dev": ([_VP, _VP, _I32, _I32, _VP, _VP], _I32),
     "pf_decode_step": ([_VP, _VP, _VP, _VP], _I32),
+    "pf_decode_step_greedy": ([_VP, _VP, _VP, _VP, _VP], _I32),
+    "pf_prefill_verify": ([_VP, _VP, _I32, _I32, _VP, _VP, _VP], _I32),
     "pf_session_set_profile": ([_VP, _I32], _I32),
     "pf_session_profile_read": ([_VP, _VP, ctypes.POINTER(ctypes.c_double),
                                  ctypes.POINTER(ctypes.c_int64)], _I32),
@@ -96,6 +98,7 @@ _SIGS = {
     "pf_op_attention": ([ctypes.POINTER(pf_config), _VP, _VP, _VP, _I32, _I32, _I32, _VP, _VP], _I32),
     "pf_op_embed": ([_VP, _VP, _I32, _I32, _I32, _VP, _VP, _VP], _I32),
     "pf_op_lm_head": ([_I32, _VP, _VP, _F, _VP, _I32, _I32, _VP, _VP], _I32),
+    "pf_op_argmax": ([_VP, _I32, _I32, _I64, _VP, _VP], _I32),
     "pf_rope_table_host": ([_F, _I32, _I32, _VP], _I32),
     "pf_status_read": ([_VP, _VP], _I32),
     "pf_selftest_bounded_wait": ([_VP, _I64, _I32, _VP], _I32),
@@ -233,6 +236,10 @@ def pf_op_attention(cfg, q, kc, vc, layer, start, m, out, stream=None):
                                 _ptr(out), _stream(stream)))
 
 
+def pf_op_argmax(x, rows, n, ld, out, stream=None):
+    check(lib().pf_op_argmax(_ptr(x), rows, n, ld, _ptr(out), _stream(stream)))
+
+
 def pf_op_embed(e, tokens, m, h, vocab, x, status=None, stream=None):
     check(lib().pf_op_embed(_ptr(e), _ptr(tokens), m, h, vocab, _ptr(x), _ptr(status),
                             _stream(stream)))
@@ -343,6 +350,16 @@ class Session:
     def decode_step(self, token_dev, logits, stream=None) -> None:
         """One decode step: the token at token_dev (device int32) at the current position."""
         check(lib().pf_decode_step(self.h, _ptr(token_dev), _ptr(logits), _stream(stream)))
+
+    def decode_step_greedy(self, token_in_dev, token_out_dev, logits, stream=None) -> None:
+        """A decode step whose logits' argmax (device int32) is written to token_out_dev."""
+        check(lib().pf_decode_step_greedy(self.h, _ptr(token_in_dev), _ptr(token_out_dev), _ptr(logits),
+                                          _stream(stream)))
+
+    def prefill_verify(self, tokens_dev, start: int, logits_all, ids, stream=None) -> None:
+        """Prefill of tokens_dev, then logits [M, vocab] and their argmax [M] at every position."""
+        check(lib().pf_prefill_verify(self.h, _ptr(tokens_dev), tokens_dev.shape[0], start, _ptr(logits_all),
+                                      _ptr(ids), _stream(stream)))
 
     def set_profile(self, on: bool) -> None:
         check(lib().pf_session_set_profile(self.h, int(on)))

@@ -288,3 +288,23 @@ def test_lm_head_vs_oracle(fmt, vocab, h):
     y = O.rmsnorm(x, nw, 1e-6).astype(np.float32)
     ref = O.dequant(w) @ y.astype(np.float64)
     assert rel_l2(logits.cpu().numpy(), ref) <= 1e-4
+
+
+# ----------------------------------------------------------------------------- greedy argmax
+@pytest.mark.parametrize("rows,n,ld", [(1, 151936, 151936), (3, 5000, 5000), (4, 1031, 1040), (2, 1, 1)])
+def test_argmax_rows_exact(rows, n, ld):
+    """pf_op_argmax (one 1024-thread CTA per row) against the oracle's argmax on the same f32
+    values: integer results, so bit-exact; planted ties, NaN and -inf included."""
+    rng = synth.rng_for(77, rows, n)
+    x = np.full((rows, ld), np.nan, np.float32)  # padding past n must never be read
+    x[:, :n] = rng.standard_normal((rows, n)).astype(np.float32)
+    if n > 8:
+        x[0, n - 1] = x[0, :n].max()      # a tie with an earlier maximum
+        x[-1, 3] = np.nan                  # NaN never wins
+        x[-1, 5] = np.float32(1e30)        # but a later number may
+    if rows > 2:
+        x[1, :n] = -np.inf                 # a row of -inf gives 0
+    out = torch.full((rows,), -7, dtype=torch.int32, device="cuda")
+    pf.pf_op_argmax(dev(x), rows, n, ld, out)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(out.cpu().numpy(), O.argmax_first(x[:, :n]))

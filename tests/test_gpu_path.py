@@ -221,3 +221,58 @@ def test_session_validation_leaves_state_unchanged():
     with pytest.raises(pf.PfError) as e:
         sess.prefill_chunk(np.array([1], np.int32), 0)
     assert e.value.status == 4 and sess.position == 3
+
+
+@pytest.mark.parametrize("m", [8, 24, 72])
+def test_verify_tail_matches_oracle(m):
+    """pf_prefill_verify after a 16-token prefill: logits of every position against the
+    oracle's verify tail (the LM head as a GEMV, small-M and large GEMM by M), and ids equal
+    to the argmax of the GPU's own logits (the decision taken in the kernel's precision);
+    the oracle's choice is the GPU's or within the tolerance of it."""
+    s = _small_stack()
+    layers, extra = synth.model_inputs(s)
+    toks = synth.tokens(16 + m, s.vocab)
+    om = O.OracleModel(s, layers, extra)
+    om.prefill(toks[:16], [16], True, False)
+    ref, _ = om.prefill_verify(toks[16:])
+    sess = pf.Session(pf.DeviceModel(s, layers, extra, max_chunk=72), kv_fill_bits=SENT[s.kv_dtype])
+    sess.prefill_chunk(toks[:16], 0)
+    lg = torch.full((m, s.vocab), float("nan"), dtype=torch.float32, device="cuda")
+    ids = torch.full((m,), -1, dtype=torch.int32, device="cuda")
+    sess.prefill_verify(dev(toks[16:].astype(np.int32)), 16, lg, ids)
+    sess.sync()
+    assert sess.position == 16 + m
+    got = lg.cpu().numpy()
+    assert np.isfinite(got).all()
+    for t in range(m):
+        assert O.rel_l2(got[t], ref[t]) <= TOL, t
+        top = int(O.argmax_first(ref[t]))
+        assert got[t, top] >= got[t].max() - TOL * np.abs(got[t]).max()
+    np.testing.assert_array_equal(ids.cpu().numpy(), O.argmax_first(got))
+    check_kv(sess, om, s, 0, 16 + m)
+
+
+def test_greedy_decode_chain_on_device():
+    """pf_decode_step_greedy: five steps enqueued back to back, each reading the token the
+    previous one chose on the device; every chosen token is the argmax of its step's logits,
+    and the logits match the oracle's last-position logits of the prefix actually fed."""
+    s = _small_stack()
+    layers, extra = synth.model_inputs(s)
+    toks = synth.tokens(16, s.vocab)
+    sess = pf.Session(pf.DeviceModel(s, layers, extra, max_chunk=16), kv_fill_bits=SENT[s.kv_dtype])
+    sess.prefill_chunk(toks[:15], 0)
+    K = 5
+    chain = torch.zeros(K + 1, dtype=torch.int32, device="cuda")
+    chain[0] = int(toks[15])
+    lg = torch.full((K, s.vocab), float("nan"), dtype=torch.float32, device="cuda")
+    for i in range(K):
+        sess.decode_step_greedy(chain[i:i + 1], chain[i + 1:i + 2], lg[i])
+    sess.sync()
+    assert sess.position == 15 + K
+    got = lg.cpu().numpy()
+    ch = chain.cpu().numpy()
+    np.testing.assert_array_equal(ch[1:], O.argmax_first(got))
+    fed = np.concatenate([toks[:15], ch[:K]]).astype(np.int64)
+    for i in range(K):
+        _, ref = O.OracleModel(s, layers, extra).prefill(fed[:16 + i], [16 + i], True, True)
+        assert O.rel_l2(got[i], ref) <= TOL, i

@@ -274,3 +274,37 @@ def test_validation_errors():
         m.embed(np.array([5, 100]))
     with pytest.raises(ValueError):
         m.forward_chunk(np.zeros((17, s.hidden), np.float32), 0, False)
+
+
+# ----------------------------------------------------------------------------- greedy tail
+def test_argmax_first_special_cases_and_library():
+    # Catches: the last (not first) of equal maxima, NaN winning or poisoning the row, an
+    # all -inf or all-NaN row giving -1, and an off-by-one on the row axis.
+    rows = np.array([[1.0, 5.0, 5.0, 2.0],
+                     [np.nan, 1.0, np.nan, 3.0],
+                     [np.nan, np.nan, np.nan, np.nan],
+                     [-np.inf, -np.inf, -np.inf, -np.inf],
+                     [0.0, -0.0, 0.0, -1.0]], np.float32)
+    np.testing.assert_array_equal(O.argmax_first(rows), [1, 3, 0, 0, 0])
+    assert int(O.argmax_first(np.array([7.0], np.float32))) == 0
+    # without NaNs, numpy's argmax (which also returns the first maximum) agrees, ties
+    # planted at random places included
+    rng = np.random.default_rng(5)
+    x = rng.standard_normal((40, 257)).astype(np.float32)
+    x[::3, 200] = x[::3].max(axis=1)  # a tie with an earlier maximum in every third row
+    np.testing.assert_array_equal(O.argmax_first(x), np.argmax(x, axis=1))
+
+
+def test_verify_tail_is_the_head_at_every_position():
+    # The verify tail scores every position: row t must be the single-token tail of the
+    # prefix that ends at t. Catches: the norm or head applied to the wrong row, a shifted
+    # row order, and the ids not being the rows' argmax.
+    s = _tiny(n_layers=2, vocab=257, max_seq=32)
+    layers, extra = synth.model_inputs(s)
+    toks = synth.tokens(6, s.vocab)
+    lg, ids = O.OracleModel(s, layers, extra).prefill_verify(toks)
+    assert lg.shape == (6, s.vocab) and ids.shape == (6,)
+    np.testing.assert_array_equal(ids, O.argmax_first(lg))
+    for t in range(6):
+        _, ref = O.OracleModel(s, layers, extra).prefill(toks[:t + 1], [t + 1], True, True)
+        assert O.rel_l2(lg[t], ref) <= 1e-12
