@@ -149,3 +149,19 @@ def test_rope_table_matches_definition(lib):
     ang = p * (1e6 ** (-2 * i / 128))
     assert t[p, i, 0] == np.float32(np.cos(ang)) and t[p, i, 1] == np.float32(np.sin(ang))
     assert np.all(t[0, :, 0] == 1) and np.all(t[0, :, 1] == 0)
+
+
+def test_greedy_and_verify_reject_bad_arguments_before_any_launch(lib):
+    """The argmax, greedy-decode and verify entry points refuse NULL / malformed arguments
+    on the host (no device memory is touched, so this runs without a GPU): status 1 is
+    PF_ERR_INVALID_ARG, 2 PF_ERR_SHAPE."""
+    out = ctypes.c_int32()
+    x = np.zeros(4, np.float32)
+    assert lib.pf_op_argmax(None, 1, 4, 4, ctypes.addressof(out), None) == 1
+    assert lib.pf_op_argmax(x.ctypes.data, 1, 4, 4, None, None) == 1
+    assert lib.pf_op_argmax(x.ctypes.data, 0, 4, 4, ctypes.addressof(out), None) == 2
+    assert lib.pf_op_argmax(x.ctypes.data, 1, 0, 4, ctypes.addressof(out), None) == 2
+    assert lib.pf_op_argmax(x.ctypes.data, 1, 4, 3, ctypes.addressof(out), None) == 2
+    assert lib.pf_decode_step_greedy(None, None, None, None, None) == 1
+    assert lib.pf_prefill_verify(None, None, 1, 0, None, None, None) == 1
+    assert b"session" in lib.pf_last_error()
