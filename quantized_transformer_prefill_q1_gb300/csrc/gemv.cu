@@ -5,12 +5,12 @@
 // weights) from tensor memory at a fixed ~22 weights per clock per SM whatever the token
 // count, so here the weights go from shared memory through registers into warp-level MMAs.
 //
-// Every warp is independent. It owns 16 weight rows (for SwiGLU 8 gate rows and their 8 up
-// rows) and computes out^T[16 rows, 8 tokens] with mma.sync m16n8k16 (f16 operands, f32
-// accumulation): the dequantised codes are the A fragment, the activations (tokens >= M zero)
-// the B fragment. The (16-row tile, group) units are shared out in equal contiguous ranges,
-// one per warp (SwiGLU: one whole tile per warp, so that silu(gate) * up is formed in the
-// warp). A warp streams its rows' slice of each packed chunk (16 rows x 128 weights: 1024 B of
+// A warp owns 16 weight rows (for SwiGLU 8 gate rows and their 8 up rows) and computes
+// out^T[16 rows, 8 tokens] with mma.sync m16n8k16 (f16 operands, f32 accumulation): the
+// dequantised codes are the A fragment, the activations (tokens >= M zero) the B fragment.
+// The (16-row tile, group) units are shared out in equal contiguous ranges, one per warp,
+// and warps never wait for one another; only SwiGLU pairs two warps of a CTA on one tile
+// (even and odd groups), which meet in shared memory to form silu(gate) * up. A warp streams its rows' slice of each packed chunk (16 rows x 128 weights: 1024 B of
 // INT4 codes + scales and zeros, or 256 B of Q1 signs + scales) into a ring of stages in
 // shared memory with cp.async, many groups ahead, so that enough bytes are in flight per SM
 // to keep HBM busy without holding them in registers.
