@@ -20,7 +20,7 @@ turbospark-runtime families/llama/prefill.rs ``prefill_chunk_real_llama_dense``.
 The per-token decode restatement follows metal_full_layer.rs ``encode_layer_into``.
 
 Where the pages are silent, each function states the reading it takes (numbered
-A1-A16 throughout this package's notes).
+A1-A19 throughout this package's notes).
 
 Parity status: every function below is pinned by ``tests/test_oracle_pins.py``
 except the composition of a full stack's logits, which has no worked example on
@@ -148,15 +148,19 @@ def round_to_cache(x: np.ndarray, kv_dtype: str) -> np.ndarray:
 
 
 def causal_gqa_attention(q: np.ndarray, k_cache: np.ndarray, v_cache: np.ndarray,
-                         start: int) -> np.ndarray:
+                         start: int, window: Optional[int] = None, sinks: int = 0) -> np.ndarray:
     """Causal GQA attention for query rows at positions start .. start+T-1.
 
     q: [T, nq, hd] (float64 or float32); k_cache, v_cache: [nkv, >=start+T, hd] holding
-    the cache for this layer. Query at position p sees keys 0..p inclusive
-    (reading A9: ``seq_len = pos + 1`` in metal_prefill.rs ``encode_layer_prefill``
-    section 3). Scores use 1/sqrt(hd) (``inv_sqrt_hd``); q head h reads kv head
-    h // (nq/nkv) (``heads_per_group``, reading A7). Softmax subtracts the row max
-    and is evaluated in float64. Returns float64 [T, nq, hd].
+    the cache for this layer by absolute position. Query at position p sees keys 0..p
+    inclusive (reading A9: ``seq_len = pos + 1`` in metal_prefill.rs
+    ``encode_layer_prefill`` section 3). Scores use 1/sqrt(hd) (``inv_sqrt_hd``); q head h
+    reads kv head h // (nq/nkv) (``heads_per_group``, reading A7). Softmax subtracts the
+    row max and is evaluated in float64. Returns float64 [T, nq, hd].
+
+    With a ring cache (turbospark-runtime prefill.rs ``BatchAttentionInputContract``:
+    ``ring_capacity``, ``sink_count``; reading A19) the query at p sees only the first
+    ``sinks`` positions and the ``window`` most recent positions up to p.
     """
     T, nq, hd = q.shape
     nkv = k_cache.shape[0]
@@ -166,6 +170,8 @@ def causal_gqa_attention(q: np.ndarray, k_cache: np.ndarray, v_cache: np.ndarray
     key_pos = np.arange(L)
     qry_pos = start + np.arange(T)
     mask = key_pos[None, :] > qry_pos[:, None]  # True where the key is in the future
+    if window is not None:  # older than the window and not a sink
+        mask |= (key_pos[None, :] <= qry_pos[:, None] - window) & (key_pos[None, :] >= sinks)
     scale = 1.0 / math.sqrt(hd)
     for h in range(nq):
         kvh = h // G
@@ -195,7 +201,12 @@ class OracleModel:
     """
 
     def __init__(self, shape, layers: Sequence[Dict], extra: Optional[Dict] = None,
-                 cache_dequant: bool = True):
+                 cache_dequant: bool = True, ring_capacity: Optional[int] = None,
+                 sink_count: int = 0):
+        if ring_capacity is not None and not 0 <= sink_count < ring_capacity:
+            raise ValueError("ring cache: need 0 <= sink_count < ring_capacity")
+        self.ring_capacity = ring_capacity
+        self.sink_count = sink_count
         self.shape = shape
         self.raw_layers = list(layers)
         self.cache_dequant = cache_dequant
@@ -205,6 +216,10 @@ class OracleModel:
         s = shape
         self.k_cache = np.full((s.n_layers, s.n_kv_heads, s.max_seq, s.head_dim), np.nan, np.float32)
         self.v_cache = np.full_like(self.k_cache, np.nan)
+        if ring_capacity is not None:  # the physical ring the per-token restatement uses
+            self.ring_k = np.full((s.n_layers, s.n_kv_heads, ring_capacity, s.head_dim), np.nan, np.float32)
+            self.ring_v = np.full_like(self.ring_k, np.nan)
+            self.ring_pos = np.full((s.n_layers, ring_capacity), -1, np.int64)
         self.position = 0
 
     @property
@@ -232,6 +247,10 @@ class OracleModel:
     def reset(self):
         self.k_cache[:] = np.nan
         self.v_cache[:] = np.nan
+        if self.ring_capacity is not None:
+            self.ring_k[:] = np.nan
+            self.ring_v[:] = np.nan
+            self.ring_pos[:] = -1
         self.position = 0
 
     # ---- one layer, a chunk of T rows (metal_prefill.rs encode_layer_prefill) --------
@@ -261,8 +280,11 @@ class OracleModel:
         # 3c. KV store at [l, kvh, pos, :] — K after RoPE, V as projected
         self.k_cache[l, :, start:start + T, :] = round_to_cache(k, s.kv_dtype).transpose(1, 0, 2)
         self.v_cache[l, :, start:start + T, :] = round_to_cache(v, s.kv_dtype).transpose(1, 0, 2)
-        # 3d. causal GQA attention over cache positions 0 .. pos
-        o = causal_gqa_attention(q, self.k_cache[l], self.v_cache[l], start).astype(np.float32)
+        # 3d. causal GQA attention over cache positions 0 .. pos (a ring cache: the sinks and
+        #     the last ring_capacity - sink_count positions)
+        window = None if self.ring_capacity is None else self.ring_capacity - self.sink_count
+        o = causal_gqa_attention(q, self.k_cache[l], self.v_cache[l], start, window,
+                                 self.sink_count).astype(np.float32)
         # 4. O projection + residual
         x = (x.astype(np.float64) + o.reshape(T, nq * hd).astype(np.float64) @ w["o_w"].T).astype(np.float32)
         # 5. FFN RMSNorm
@@ -274,6 +296,27 @@ class OracleModel:
         # 7. down projection + residual
         x = (x.astype(np.float64) + act.astype(np.float64) @ w["down_w"].T).astype(np.float32)
         return x
+
+    # ---- the ring cache's slots (reading A19) -----------------------------------------
+    def ring_slot(self, p: int) -> int:
+        """Slot of absolute position p in a ring cache of ring_capacity slots: the first
+        sink_count positions keep slots 0 .. sink_count-1; later positions cycle through
+        the remaining ring_capacity - sink_count slots."""
+        R, S = self.ring_capacity, self.sink_count
+        return p if p < S else S + (p - S) % (R - S)
+
+    def ring_cache(self, l: int):
+        """Layer l's K and V as a ring cache of ring_capacity slots would hold them after
+        positions 0 .. position-1 were stored in order (a slot keeps the last position
+        stored into it; slots never written keep NaN). Returns ([nkv, R, hd], [nkv, R, hd])."""
+        R = self.ring_capacity
+        s = self.shape
+        k = np.full((s.n_kv_heads, R, s.head_dim), np.nan, np.float32)
+        v = np.full_like(k, np.nan)
+        for p in range(self.position):
+            k[:, self.ring_slot(p)] = self.k_cache[l, :, p]
+            v[:, self.ring_slot(p)] = self.v_cache[l, :, p]
+        return k, v
 
     # ---- tail: final norm on the last row + LM head (encode_full_forward_prefill) -------
     def head(self, x_last: np.ndarray) -> np.ndarray:
@@ -400,17 +443,31 @@ def decode_token(model: OracleModel, l: int, x_row: np.ndarray, pos: int) -> np.
     for g in range(nkv):
         model.k_cache[l, g, pos] = round_to_cache(rotated[nq + g], s.kv_dtype)
         model.v_cache[l, g, pos] = round_to_cache(heads[nq + nkv + g], s.kv_dtype)
+    if model.ring_capacity is None:
+        keys = [(model.k_cache[l, g_], model.v_cache[l, g_]) for g_ in range(nkv)]
+        n_keys = pos + 1
+    else:
+        # a physical ring of ring_capacity slots: store at the position's slot, then attend
+        # over every slot in use (the sinks and the most recent positions)
+        slot = model.ring_slot(pos)
+        for g in range(nkv):
+            model.ring_k[l, g, slot] = model.k_cache[l, g, pos]
+            model.ring_v[l, g, slot] = model.v_cache[l, g, pos]
+        model.ring_pos[l, slot] = pos
+        used = np.flatnonzero(model.ring_pos[l] >= 0)
+        keys = [(model.ring_k[l, g_, used], model.ring_v[l, g_, used]) for g_ in range(nkv)]
+        n_keys = used.size
     o = np.empty(nq * hd, dtype=np.float32)
     for h in range(nq):
         g = h // G
+        kh, vh = keys[g]
         qh = rotated[h].astype(np.float64)
-        sc = np.array([float(qh @ model.k_cache[l, g, j].astype(np.float64)) / math.sqrt(hd)
-                       for j in range(pos + 1)])
+        sc = np.array([float(qh @ kh[j].astype(np.float64)) / math.sqrt(hd) for j in range(n_keys)])
         e = np.exp(sc - sc.max())
         p = e / e.sum()
         acc = np.zeros(hd)
-        for j in range(pos + 1):
-            acc += p[j] * model.v_cache[l, g, j].astype(np.float64)
+        for j in range(n_keys):
+            acc += p[j] * vh[j].astype(np.float64)
         o[h * hd:(h + 1) * hd] = acc.astype(np.float32)
     x_row = (x_row.astype(np.float64) + w["o_w"] @ o.astype(np.float64)).astype(np.float32)
     y = rmsnorm(x_row, w["ffn_norm"], s.eps).astype(np.float32)

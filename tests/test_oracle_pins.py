@@ -308,3 +308,83 @@ def test_verify_tail_is_the_head_at_every_position():
     for t in range(6):
         _, ref = O.OracleModel(s, layers, extra).prefill(toks[:t + 1], [t + 1], True, True)
         assert O.rel_l2(lg[t], ref) <= 1e-12
+
+
+# ----------------------------------------------------------------------------- ring / sink KV
+def test_ring_attention_brute_force():
+    # Windowed attention with sinks against an explicit gather of the keys each query may
+    # see, in pure Python loops. Catches: a window off by one, sinks that let a query see
+    # the future, a mask of the wrong sign, the kv-head mapping lost in the windowed path.
+    rng = np.random.default_rng(11)
+    nq, nkv, hd, L, start, T, window, sinks = 4, 2, 16, 20, 12, 8, 5, 2
+    q = rng.standard_normal((T, nq, hd))
+    k = rng.standard_normal((nkv, L, hd)).astype(np.float32)
+    v = rng.standard_normal((nkv, L, hd)).astype(np.float32)
+    out = O.causal_gqa_attention(q, k, v, start, window, sinks)
+    for t in range(T):
+        p = start + t
+        vis = [j for j in range(p + 1) if j < sinks or j > p - window]
+        assert len(vis) == sinks + window
+        for h in range(nq):
+            g = h // (nq // nkv)
+            sc = [math.fsum(q[t, h, d] * float(k[g, j, d]) for d in range(hd)) / math.sqrt(hd) for j in vis]
+            mx = max(sc)
+            e = [math.exp(x - mx) for x in sc]
+            z = math.fsum(e)
+            ref = [math.fsum(e[i] / z * float(v[g, j, d]) for i, j in enumerate(vis)) for d in range(hd)]
+            np.testing.assert_allclose(out[t, h], ref, rtol=1e-12, atol=1e-12)
+
+
+def test_ring_window_of_one_is_the_token_itself():
+    # closed form: a window of one position and no sinks gives o = v of the query's own position
+    rng = np.random.default_rng(12)
+    q = rng.standard_normal((5, 4, 8))
+    k = rng.standard_normal((2, 9, 8)).astype(np.float32)
+    v = rng.standard_normal((2, 9, 8)).astype(np.float32)
+    out = O.causal_gqa_attention(q, k, v, 4, window=1, sinks=0)
+    for t in range(5):
+        for h in range(4):
+            np.testing.assert_array_equal(out[t, h], v[h // 2, 4 + t].astype(np.float64))
+
+
+def test_ring_slot_mapping():
+    # sinks keep their slots, later positions cycle through the rest
+    s = _tiny(max_seq=32)
+    layers, _ = synth.model_inputs(s)
+    m = O.OracleModel(s, layers, ring_capacity=6, sink_count=2)
+    assert [m.ring_slot(p) for p in range(12)] == [0, 1, 2, 3, 4, 5, 2, 3, 4, 5, 2, 3]
+    with pytest.raises(ValueError):
+        O.OracleModel(s, layers, ring_capacity=4, sink_count=4)
+
+
+def test_ring_wide_enough_equals_linear():
+    # a ring that never wraps changes nothing (bit-identical)
+    s = _tiny(max_seq=40)
+    layers, _ = synth.model_inputs(s)
+    x = synth.hidden_input(16, s.hidden)
+    lin, _ = O.OracleModel(s, layers).prefill(x, [16], False, False)
+    for R, S in ((16, 0), (20, 3)):
+        ring, _ = O.OracleModel(s, layers, ring_capacity=R, sink_count=S).prefill(x, [16], False, False)
+        np.testing.assert_array_equal(ring, lin)
+
+
+def test_ring_one_shot_equals_chunked_equals_physical_ring_decode():
+    # The batched form masks a linear history; the per-token form reads a physical ring of
+    # ring_capacity slots. Both must agree, chunked or not, and the ring must matter.
+    s = _tiny(max_seq=48)
+    layers, _ = synth.model_inputs(s)
+    x = synth.hidden_input(24, s.hidden)
+    kw = dict(ring_capacity=10, sink_count=2)
+    a = O.OracleModel(s, layers, **kw)
+    one, _ = a.prefill(x, [24], False, False)
+    chunked, _ = O.OracleModel(s, layers, **kw).prefill(x, [5, 7, 12], False, False)
+    d = O.OracleModel(s, layers, **kw)
+    dec = O.decode_prompt(d, x)
+    assert O.rel_l2(chunked, one) <= 1e-6
+    assert O.rel_l2(dec, one) <= 1e-6
+    lin, _ = O.OracleModel(s, layers).prefill(x, [24], False, False)
+    assert O.rel_l2(one, lin) > 1e-3
+    for l in range(s.n_layers):  # what the batched model's history implies for the ring slots
+        k, v = a.ring_cache(l)
+        np.testing.assert_allclose(k, d.ring_k[l], rtol=1e-5, atol=1e-6)
+        np.testing.assert_allclose(v, d.ring_v[l], rtol=1e-5, atol=1e-6)
