@@ -273,7 +273,12 @@ pf_status pf_op_dequant(int32_t wfmt, const void* packed_dev, int64_t N, int64_t
  * pf_gemm_scratch_bytes(M, N, max_ctas) bytes, owned by the caller, required for every
  * epilogue): its trailing per-tile counters must be zero before the first call, and each
  * call that completes leaves them zero; after PF_ERR_DEVICE_TIMEOUT zero them again.
- * Calls sharing one scratch must not overlap in time (same stream, or ordered). */
+ * Calls sharing one scratch must not overlap in time (same stream, or ordered).
+ * The kernel depends on M: M > 64 the persistent tcgen05 GEMM described above; 8 < M <= 64
+ * the same partition with the weight rows as the MMA's M side; M <= 8 a warp-level MMA
+ * GEMV that ignores max_ctas and the scratch (residual and store forms add with f32
+ * atomics, the store form after zeroing out). The results agree to the GEMM tolerances:
+ * all three use f16 operands with f32 accumulation. */
 size_t pf_gemm_scratch_bytes(int32_t M, int32_t N, int32_t max_ctas);
 pf_status pf_op_gemm(int32_t wfmt, int32_t epilogue, const uint16_t* a_f16_dev,
                      const void* packed_dev, int32_t M, int32_t N, int32_t K, void* out_dev,
