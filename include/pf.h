@@ -50,7 +50,7 @@ typedef enum {
   PF_ERR_TOKEN_OUT_OF_VOCAB = 5, /* token < 0 or >= vocab ([P3]) */
   PF_ERR_KV_CAPACITY = 6,        /* start_pos + M > max_seq */
   PF_ERR_LOGITS = 7,             /* logits requested but no LM head / buffer */
-  PF_ERR_UNSUPPORTED = 8,        /* a mode this build refuses by name */
+  PF_ERR_UNSUPPORTED = 8,        /* a mode the library does not implement */
   PF_ERR_CUDA = 9,               /* a CUDA runtime call failed */
   PF_ERR_DEVICE_TIMEOUT = 10,    /* a kernel's bounded wait expired (see status word) */
   PF_ERR_WORKSPACE = 11          /* workspace too small / not initialised */

@@ -59,7 +59,7 @@ class ModelShape:
         return (self.n_q_heads + 2 * self.n_kv_heads) * self.head_dim
 
 
-# Workloads (sizes and distributions as the task's five configurations state them).
+# Workloads: the five configurations' sizes and value distributions.
 TINY = ModelShape(hidden=256, intermediate=768, n_q_heads=4, n_kv_heads=2, head_dim=64,
                   n_layers=1, vocab=0, rope_theta=1e6, eps=1e-6, final_eps=1e-6,
                   qk_norm=True, wfmt=Q1, kv_dtype=KV_F32, max_seq=64)
