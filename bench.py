@@ -13,10 +13,17 @@ e2e: the same through pf_prefill_tokens_host with pinned host tokens in and the 
 logits out, copies inside the timed region.
 roofline: the kernel class with the most device time (per-launch CUDA events in a
 profiled pass of the same steps) against the measured peak.
+roofline_all: every kernel class of the step against its own roof (HBM bytes or tensor
+FLOPs per launch, from the algorithmic work of the method, over the class's average
+in-step launch time).
+int4_layer: the Llama-3-8B-shaped INT4-affine layer over a cache already holding 8192
+positions, at chunks of M = 1, 4, 16, 64 and 512 tokens (the small-M crossover): weight
+GB/s for M <= 64, tensor TFLOP/s at M = 512.
 cpu_baseline: the CPU oracle on a bounded sample (the first layers of the same prompt).
 
-N > 1 (torchrun): independent replicas, one prompt per GPU ("replicas only": the path
-does not shard), value = all ranks' tokens / the slowest rank's time.
+N > 1: independent replicas, one prompt per GPU ("replicas only": the path does not
+shard), value = all ranks' tokens / the slowest rank's time. `--gpus N` outside torchrun
+re-launches itself under torch.distributed.run with N processes.
 """
 import argparse
 import json
@@ -341,20 +348,37 @@ def oracle_sample(layers_sample: int, tokens_sample: int, seed: int, emb_rows):
 
 
 def run_reference(args):
+    """The oracle as it stands on the host cores. Each step times layer 0 of the workload on
+    the first chunk (start 0) and on the last chunk (start 1536, attention over 2048 keys;
+    the layer-0 cache of the chunks between is filled once before timing); the attention
+    cost grows linearly with the chunk's start, so the mean of the first and last chunk is
+    the mean over all four. tokens/s = 2048 / (mean chunk time x 4 chunks x 36 layers)."""
     ws, rank, _ = dist_setup("gloo")
     if rank != 0:
         return
-    import numpy as np  # noqa: F401
+    import dataclasses
+
+    from oracle import prefill_oracle as O
+    from quantized_transformer_prefill_q1_gb300 import synth
     cores = os.cpu_count()
-    samples = []
     emb = sample_embedding_rows(args.seed)
+    s = dataclasses.replace(synth.QWEN3_8B_STACK, n_layers=1)
+    model = O.OracleModel(s, [synth.layer_weights(synth.QWEN3_8B_STACK, 0, args.seed)], None)
+    for c in range(3):  # the layer-0 cache of chunks 0..2 (untimed set-up)
+        model.layer_forward(0, emb[c * CHUNK:(c + 1) * CHUNK], c * CHUNK)
+    last = (PROMPT // CHUNK - 1) * CHUNK
+    samples = []
     for i in range(args.warmup + args.steps):
-        dt, tps = oracle_sample(1, CHUNK, args.seed, emb)
+        t0 = time.perf_counter()
+        model.layer_forward(0, emb[:CHUNK], 0)
+        model.layer_forward(0, emb[last:last + CHUNK], last)
+        dt = time.perf_counter() - t0
         if i >= args.warmup:
-            samples.append((dt, tps))
-    dt = statistics.median(s[0] for s in samples)
-    tps = statistics.median(s[1] for s in samples)
-    sample = "layer 0 of 36, first 512-token chunk; tokens/s extrapolated x36 layers x4 chunks"
+            samples.append(dt)
+    dt = statistics.median(samples)
+    tps = PROMPT / (dt / 2 * (PROMPT // CHUNK) * 36)
+    sample = ("layer 0 of 36 on the first and the last 512-token chunk (starts 0 and 1536) per "
+              "step; tokens/s extrapolated to 4 chunks x 36 layers; LM head not sampled")
     line = {"impl": "reference", "metric": METRIC, "value": tps, "unit": "tokens/s",
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak",
@@ -378,6 +402,127 @@ def gemm_flops(cls, shape, m):
 def attention_flops_per_prompt(shape):
     # QK^T + PV over causal positions: 4 * nq * hd * (p + 1) per query row
     return sum(4 * shape.n_q_heads * shape.head_dim * (p + 1) for p in range(PROMPT))
+
+
+def class_work(shape, chunk):
+    """Algorithmic work per launch of each kernel class at one chunk of `chunk` rows:
+    ("hbm", bytes) or ("tensor", flops). Bytes are what the method must move (inputs read
+    once, outputs written once); attention is the per-launch average over the prompt."""
+    H, hd = shape.hidden, shape.head_dim
+    nq, nkv = shape.n_q_heads, shape.n_kv_heads
+    m = chunk
+    n_att = PROMPT // CHUNK
+    att = attention_flops_per_prompt(shape) / n_att
+    lm_bytes = (shape.vocab + 255) // 256 * 256 * H // 8 + (shape.vocab + 255) // 256 * 256 * (H // 128) * 2
+    return {
+        "rmsnorm": ("hbm", m * (4 * H + 2 * H) + 4 * H),
+        "qk_rope_kv": ("hbm", m * ((nq + 2 * nkv) * hd * 4 + nq * hd * 2 + 2 * nkv * hd * 2 + hd * 4)),
+        "attention": ("tensor", att),
+        "gemm_qkv": ("tensor", gemm_flops("gemm_qkv", shape, m)),
+        "gemm_o": ("tensor", gemm_flops("gemm_o", shape, m)),
+        "gemm_gate_up": ("tensor", gemm_flops("gemm_gate_up", shape, m)),
+        "gemm_down": ("tensor", gemm_flops("gemm_down", shape, m)),
+        "embed": ("hbm", m * H * 4 * 2),
+        "lm_head": ("hbm", lm_bytes + H * 4 * 2 + shape.vocab * 4),
+    }
+
+
+def roofline_all(prof, steps, shape, peaks, peak_src):
+    """Per kernel class: algorithmic work per launch / average launch time (profiled pass,
+    per-launch CUDA events) against the HBM or tensor peak."""
+    work = class_work(shape, CHUNK)
+    out = {}
+    for cls, (ms, n) in prof.items():
+        if not n or cls not in work:
+            continue
+        bound, w = work[cls]
+        us = ms / n * 1e3
+        if bound == "hbm":
+            ach, peak, unit = w / (us * 1e-6) / 1e9, peaks["hbm_gbs"], "GB/s"
+        else:
+            ach = w / (us * 1e-6) / 1e12
+            peak, unit = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]), "TFLOP/s"
+        out[cls] = {"bound": bound, "achieved": round(ach, 1), "peak": peak, "unit": unit,
+                    "frac": round(ach / peak, 4), "avg_launch_us": round(us, 2),
+                    "launches_per_step": n / steps,
+                    ("bytes_per_launch" if bound == "hbm" else "flops_per_launch"): w}
+    out["_note"] = (f"peaks {peak_src}: hbm_gbs for bytes, bf16_tflops_sustained for flops; "
+                    "launch times from per-launch CUDA events without graph replay, so each "
+                    "includes its launch gap")
+    return out
+
+
+INT4_MS = (1, 4, 16, 64, 512)
+INT4_FILLED = 8192
+
+
+def int4_layer_measure(pf, synth, torch, peaks, reps=20, seed=0):
+    """The Llama-3-8B-shaped INT4-affine layer (hidden 4096, intermediate 14336, 32/8 heads)
+    over a bf16 cache already holding positions 0..8191, one chunk of M tokens at start 8192
+    through pf_layer_forward (graph replayed). Each timed launch follows a 256 MB read that
+    evicts L2, so weights and cache come from HBM. Weight bytes = the packed INT4 weights;
+    KV bytes = the cache rows the attention reads."""
+    import numpy as np
+    s = synth.LLAMA3_8B_INT4_LAYER
+    layers, _ = synth.model_inputs(s, seed=seed)
+    dm = pf.DeviceModel(s, layers, max_chunk=max(INT4_MS))
+    sess = pf.Session(dm)
+    kvp = synth.kv_prefill_bf16_bits(1, s.n_kv_heads, INT4_FILLED, s.head_dim, seed=seed)
+    sess.k[:, :, :INT4_FILLED].view(torch.int16).copy_(torch.from_numpy(kvp["k"].view(np.int16)).cuda())
+    sess.v[:, :, :INT4_FILLED].view(torch.int16).copy_(torch.from_numpy(kvp["v"].view(np.int16)).cuda())
+    del kvp
+    wbytes = sum(t.numel() for t in dm.keep if t.dtype == torch.uint8)
+    nweights = (s.qkv_rows * s.hidden + s.hidden * s.n_q_heads * s.head_dim
+                + 2 * s.intermediate * s.hidden + s.hidden * s.intermediate)
+    flush = torch.ones(64 << 20, dtype=torch.float32, device="cuda")
+    peak_t = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
+    rows = {}
+    for m in INT4_MS:
+        x0 = torch.from_numpy(synth.hidden_input(m, s.hidden, seed=seed)).cuda()
+        x = x0.clone()
+
+        def run():
+            sess.layer_forward(0, x, INT4_FILLED)
+        for _ in range(3):
+            x.copy_(x0)
+            run()
+        torch.cuda.synchronize()
+        tot = 0.0
+        for _ in range(reps):
+            x.copy_(x0)
+            flush.sum()
+            torch.cuda._sleep(400_000)  # the host enqueues while the GPU is busy
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            run()
+            e1.record()
+            e1.synchronize()
+            tot += e0.elapsed_time(e1)
+        us = tot / reps * 1e3
+        kv_bytes = 2 * s.n_kv_heads * (INT4_FILLED + m) * s.head_dim * 2
+        att_flops = sum(4 * s.n_q_heads * s.head_dim * (p + 1) for p in range(INT4_FILLED, INT4_FILLED + m))
+        flops = 2 * m * nweights + att_flops
+        r = {"us_per_layer": round(us, 2), "tokens_per_s": round(m / (us * 1e-6), 1),
+             "weight_GBps": round(wbytes / (us * 1e-6) / 1e9, 1),
+             "weight_plus_kv_GBps": round((wbytes + kv_bytes) / (us * 1e-6) / 1e9, 1),
+             "tflops": round(flops / (us * 1e-6) / 1e12, 2)}
+        if m <= 64:
+            r.update({"bound": "hbm", "frac": round((wbytes + kv_bytes) / (us * 1e-6) / 1e9 / peaks["hbm_gbs"], 4)})
+        else:
+            r.update({"bound": "tensor", "frac": round(flops / (us * 1e-6) / 1e12 / peak_t, 4)})
+        # per kernel class of the same call (per-launch events, no graph replay)
+        sess.set_profile(True)
+        sess.profile_read()
+        x.copy_(x0)
+        run()
+        prof = sess.profile_read()
+        sess.set_profile(False)
+        r["profiled_us"] = {k: round(v[0] * 1e3, 2) for k, v in prof.items() if v[1]}
+        rows[str(m)] = r
+    sess.close()
+    return {"workload": "llama-3-8b-shaped INT4-affine layer (H 4096, I 14336, 32/8 heads, hd 128, "
+                        "no QK-norm, theta 5e5), bf16 cache holding 8192 positions, chunk at start 8192",
+            "weight_bytes": wbytes, "l2": "256 MB read before each timed launch", "by_m": rows}
 
 
 def run_ours(args):
@@ -477,6 +622,9 @@ def run_ours(args):
                                                                  "gemm_down")) * shape.n_layers * (PROMPT // CHUNK)
     breakdown = {k: {"ms_per_step": round(v[0], 4), "launches_per_step": v[1]} for k, v in per_step.items()}
 
+    roof_all = roofline_all(prof, args.profile_steps, shape, peaks, peak_src)
+    int4 = int4_layer_measure(pf, synth, torch, peaks, seed=args.seed) if args.layers == 36 else None
+
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         dt, tps = oracle_sample(2, PROMPT, args.seed, emb_rows)
@@ -492,9 +640,11 @@ def run_ours(args):
                 "config": {"workload": WORKLOAD if args.layers == 36 else WORKLOAD + f" [DEV: {args.layers} layers]",
                            "prompt_tokens": PROMPT, "chunk": CHUNK, "layers": args.layers,
                            "parallelism": f"replicas x{ws}",
-                           "l2": "inputs larger than L2: 1.0 GB packed layer weights + 87.5 MB LM "
-                                 "head + 2.49 GB embedding touched per step"},
-                "e2e": e2e, "gpu_launches": launches, "roofline": roof,
+                           "l2": "inputs larger than L2: 0.98 GB of packed layer weights, 87.5 MB "
+                                 "of LM head and 0.3 GB of KV cache read per step (the 2048 "
+                                 "gathered embedding rows are 32 MB)"},
+                "e2e": e2e, "gpu_launches": launches, "roofline": roof, "roofline_all": roof_all,
+                "int4_layer": int4,
                 "gemm_tflops_profiled": gemm_flops_step / (gemm_ms / 1e3) / 1e12 if gemm_ms else None,
                 "attention_tflops_profiled": attention_flops_per_prompt(shape) * shape.n_layers /
                 (per_step["attention"][0] / 1e3) / 1e12 if per_step["attention"][0] else None,
@@ -505,8 +655,23 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+def respawn_under_torchrun(n):
+    """`bench.py --gpus N` started directly: start N ranks (one per GPU) with
+    torch.distributed.run on this node and exit with its status."""
+    import socket
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        port = sk.getsockname()[1]
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={n}",
+           "--master-addr", "127.0.0.1", "--master-port", str(port), os.path.abspath(__file__),
+           *sys.argv[1:]]
+    raise SystemExit(subprocess.call(cmd))
+
+
 def main():
     args = parse()
+    if args.gpus > 1 and "WORLD_SIZE" not in os.environ and not args.case:
+        respawn_under_torchrun(args.gpus)
     if args.case:
         bad = [c for c in args.case.split(",") if c not in CASES]
         if bad:

@@ -290,9 +290,10 @@ pf_status pf_op_gemm(int32_t wfmt, int32_t epilogue, const uint16_t* a_f16_dev,
  * one fixed 4 MiB + 64 KiB array inside the library, which every GPU that loads the library
  * keeps until the process exits. The pages have no counterpart of this call. It runs at
  * most 16 CTAs (slower than pf_op_gemm on large shapes) and rejects with PF_ERR_SHAPE an
- * output of more than 16384 tiles of 128 x 256. The first call on a device looks the
- * array's device address up (cudaGetSymbolAddress) and should come before any stream
- * capture; each call clears the tile counters it uses on `stream`. Every call on a device
+ * output of more than 16384 tiles of 128 x 256. Each call looks the array's device address
+ * up (cudaGetSymbolAddress) on the current device; the first call on a device may load the
+ * library's device code and should come before any stream capture. Each call clears the
+ * tile counters it uses on `stream`. Every call on a device
  * shares the array: calls that overlap on the GPU (other streams, other threads) race and
  * corrupt each other's results. Allocates nothing; arguments otherwise as pf_op_gemm. */
 pf_status pf_op_gemm_static_scratch(int32_t wfmt, int32_t epilogue, const uint16_t* a_f16_dev,

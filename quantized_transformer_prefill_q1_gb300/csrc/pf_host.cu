@@ -914,23 +914,14 @@ constexpr size_t STATIC_GEMM_BYTES =
     static_cast<size_t>(2) * STATIC_GEMM_CTAS * 128 * 256 * sizeof(float) + STATIC_GEMM_TILES * sizeof(int);
 static __device__ __align__(256) unsigned char g_static_gemm_scratch[STATIC_GEMM_BYTES];
 
-constexpr int MAX_DEVICES = 64;
-std::mutex g_static_gemm_mu;
-void* g_static_gemm_ptr[MAX_DEVICES] = {};
-
 // Device address of the array on the current device (host code cannot use the symbol
-// itself: on the host it names a stand-in, not device memory). Looked up once per device.
+// itself: on the host it names a stand-in, not device memory). Looked up on every call:
+// the lookup is cheap once the module is loaded, and an address kept from an earlier call
+// could be stale after cudaDeviceReset or a new primary context reloads the module.
 pf_status static_gemm_scratch(void** out) {
-  int dev = 0;
-  PF_CUDA(cudaGetDevice(&dev), "cudaGetDevice");
-  if (dev < 0 || dev >= MAX_DEVICES) return fail(PF_ERR_INVALID_ARG, "device %d out of range", dev);
-  std::lock_guard<std::mutex> lock(g_static_gemm_mu);
-  if (!g_static_gemm_ptr[dev]) {
-    void* p = nullptr;
-    PF_CUDA(cudaGetSymbolAddress(&p, g_static_gemm_scratch), "cudaGetSymbolAddress");
-    g_static_gemm_ptr[dev] = p;
-  }
-  *out = g_static_gemm_ptr[dev];
+  void* p = nullptr;
+  PF_CUDA(cudaGetSymbolAddress(&p, g_static_gemm_scratch), "cudaGetSymbolAddress");
+  *out = p;
   return PF_OK;
 }
 }  // namespace

@@ -276,6 +276,62 @@ def test_validation_errors():
         m.forward_chunk(np.zeros((17, s.hidden), np.float32), 0, False)
 
 
+# ----------------------------------------------------------------------------- embedding / head
+def test_embed_rows_exact_without_scale():
+    # The embedding is a plain row gather at scale 1.0 (turbospark-runtime 0.3.0
+    # families/llama/prefill.rs, the chunk function's embedding step; no sqrt(hidden)
+    # factor). Rows planted with known values (each row's entries encode its own id) come
+    # back bit for bit, first and last id included, repeated ids included, in token order.
+    # Catches: a sqrt(H) scale, an off-by-one id, a transposed table, an f16 round trip.
+    H, V = 256, 37
+    s = _tiny(vocab=V)
+    table = (np.arange(V, dtype=np.float32)[:, None] * np.float32(1000.0)
+             + np.arange(H, dtype=np.float32)[None, :] * np.float32(0.125))
+    table[V - 1] = np.float32(1.0) + np.float32(2.0 ** -20)  # not representable in f16
+    m = O.OracleModel(s, synth.model_inputs(s)[0], {"embed": table})
+    toks = np.array([0, V - 1, 5, 5, 36, 1], np.int32)
+    got = m.embed(toks)
+    assert got.dtype == np.float32 and got.shape == (6, H)
+    for i, t in enumerate(toks):
+        np.testing.assert_array_equal(got[i], table[t])
+    assert got[0, 1] == np.float32(0.125) and got[2, 0] == np.float32(5000.0)
+    assert got[1, 0] == np.float32(1.0) + np.float32(2.0 ** -20)
+
+
+def test_head_uses_the_final_eps():
+    # The tail normalises the last row with the final norm's own eps (metal_prefill.rs,
+    # encode_full_forward_prefill: final_norm_eps, separate from the layers' eps), then
+    # applies the LM head. A row of small magnitude makes the two eps values give clearly
+    # different results; the expected logits are formed in pure Python (bit extraction,
+    # math.fsum), a different route from the oracle's numpy code.
+    # Catches: the layer eps used in the tail, the norm weight skipped, the wrong row.
+    H, V = 256, 5
+    s = _tiny(vocab=V, eps=1e-6, final_eps=1e-2)
+    rng = np.random.default_rng(11)
+    lm = synth.q1_weight(rng, V, H)
+    fn = (1.0 + 0.1 * rng.standard_normal(H)).astype(np.float32)
+    x = (0.05 * rng.standard_normal(H)).astype(np.float32)
+    m = O.OracleModel(s, synth.model_inputs(s)[0], {"final_norm": fn, "lm_head": lm})
+    got = m.head(x)
+
+    def expect(eps):
+        ms = math.fsum(float(v) * float(v) for v in x) / H
+        y = [np.float32(float(x[k]) / math.sqrt(ms + eps) * float(fn[k])) for k in range(H)]
+        out = []
+        for n in range(V):
+            terms = []
+            for k in range(H):
+                bit = (int(lm["bits"][n, k // 8]) >> (k % 8)) & 1
+                sc = float(lm["scales"][n, k // 128])
+                terms.append((sc if bit else -sc) * float(y[k]))
+            out.append(math.fsum(terms))
+        return np.array(out)
+
+    np.testing.assert_allclose(got, expect(1e-2), rtol=1e-6, atol=1e-7)
+    wrong = expect(1e-6)
+    assert np.max(np.abs(wrong - expect(1e-2))) > 100 * np.max(np.abs(got - expect(1e-2))) + 1e-3
+
+
 # ----------------------------------------------------------------------------- greedy tail
 def test_argmax_first_special_cases_and_library():
     # Catches: the last (not first) of equal maxima, NaN winning or poisoning the row, an
