@@ -68,6 +68,9 @@ def parse():
                         + ", ".join(CASES))
     p.add_argument("--reps", type=int, default=3)
     p.add_argument("--ctas", type=int, default=0, help="GEMM cases: most persistent CTAs (0 = the library's choice)")
+    p.add_argument("--split", type=int, default=1, help="attention case: split-KV parts (1 = one pass)")
+    p.add_argument("--start", type=int, default=None,
+                   help="attention case: first query position (default: the prompt's last M positions)")
     p.add_argument("--m", default=None,
                    help="comma list of chunk tokens for the int4_* (Llama-3-8B-shaped INT4 layer, default 1) "
                         "and gemm_* (Qwen3-8B-shaped Q1 layer, default 512) cases")
@@ -144,13 +147,21 @@ def run_case(args):
                 flops = 2 * M * n * k
                 wbytes = w.numel()
             elif case == "attention":
-                start = PROMPT - CHUNK
+                start = PROMPT - M if args.start is None else args.start
+                seq = max(s.max_seq, start + M)
+                acfg = pf.make_config(s, max(M, CHUNK), n_layers=1, max_seq=seq)
                 q = torch.randn((M, s.n_q_heads, s.head_dim), device="cuda").to(torch.bfloat16)
-                kc = torch.randn((1, s.n_kv_heads, s.max_seq, s.head_dim), device="cuda").to(torch.bfloat16)
+                kc = torch.randn((1, s.n_kv_heads, seq, s.head_dim), device="cuda").to(torch.bfloat16)
                 vc = torch.randn_like(kc)
                 out = torch.empty((M, s.n_q_heads * s.head_dim), dtype=torch.float16, device="cuda")
-                fn = lambda: pf.pf_op_attention(cfg, q, kc, vc, 0, start, M, out)  # noqa: E731
+                if args.split > 1:
+                    ascr = torch.empty(pf.pf_attention_scratch_bytes(acfg, M, args.split), dtype=torch.uint8,
+                                       device="cuda")
+                    fn = lambda: pf.pf_op_attention_split(acfg, q, kc, vc, 0, start, M, args.split, ascr, out)  # noqa: E731
+                else:
+                    fn = lambda: pf.pf_op_attention(acfg, q, kc, vc, 0, start, M, out)  # noqa: E731
                 flops = sum(4 * s.n_q_heads * s.head_dim * (p + 1) for p in range(start, start + M))
+                wbytes = 2 * s.n_kv_heads * (start + M) * s.head_dim * 2  # K and V rows read
             elif case == "rmsnorm":
                 x = torch.randn((M, H), device="cuda")
                 wv = torch.ones(H, device="cuda")
@@ -176,6 +187,8 @@ def run_case(args):
             us = timed(fn, args.reps)
             line = {"case": case, "m": M, "us_per_launch": us, "ctas": args.ctas,
                     "l2": "256 MB read before each launch"}
+            if case == "attention":
+                line.update({"start": start, "split": args.split})
             if wbytes:
                 line.update({"weight_bytes": wbytes, "weight_GBps": wbytes / us / 1e3})
             if flops:

@@ -74,8 +74,16 @@ typedef struct {
   int32_t qk_norm;       /* 1: per-head RMSNorm of Q and K before RoPE */
   int32_t wfmt;          /* pf_wformat */
   int32_t kv_dtype;      /* pf_kvdtype */
-  int32_t max_seq;       /* KV capacity (positions) */
+  int32_t max_seq;       /* largest position + 1 (RoPE table); the linear cache's capacity */
   int32_t max_chunk;     /* largest micro-batch the workspace is sized for (<= 8192) */
+  /* Ring / sink KV cache ([P3] batch-attention contract fields ring_capacity, sink_count):
+   * 0 = linear cache of max_seq slots. R > 0 = a cache of R slots per (layer, kv head):
+   * positions 0 .. S-1 (S = sink_count, 0 <= S < R) keep slots 0 .. S-1, a later position p
+   * goes to slot S + (p - S) mod (R - S), and the query at p attends to the S sinks and the
+   * R - S most recent positions up to p (RoPE stays at absolute positions). Needs a 16-bit
+   * cache. */
+  int32_t ring_capacity;
+  int32_t sink_count;
 } pf_config;
 
 /* One layer's weights ([P1] LayerWeightRefs), all device pointers. Packed tensors
@@ -105,7 +113,7 @@ typedef struct pf_session pf_session; /* opaque */
 /* ------------------------------------------------------------------ misc */
 const char* pf_last_error(void);      /* thread-local, never NULL */
 const char* pf_status_name(int status);
-int32_t pf_abi_version(void);         /* bumps on any ABI change */
+int32_t pf_abi_version(void);         /* bumps on any ABI change (2: ring fields) */
 
 /* ------------------------------------------------------------------ packing
  * Canonical host formats (the pages name "Q1 block bytes" and an "AoS -> SoA"
@@ -130,7 +138,8 @@ pf_status pf_pack_weights_host(int32_t wfmt, const uint8_t* codes_host,
 
 /* ------------------------------------------------------------------ sizes */
 size_t pf_kv_bytes(const pf_config* cfg);        /* bytes of ONE of K / V:
-                                                    n_layers*nkv*max_seq*hd*elem */
+                                                    n_layers*nkv*slots*hd*elem, slots =
+                                                    ring_capacity (ring) or max_seq */
 size_t pf_workspace_bytes(const pf_config* cfg); /* activations for max_chunk rows,
                                                     RoPE table, status words */
 /* Validates a configuration; PF_OK or the reason it is not supported. Host only. */
@@ -146,8 +155,8 @@ pf_status pf_validate_chunk(const pf_config* cfg, int32_t kv_position,
 
 /* ------------------------------------------------------------------ sessions
  * A session binds a model, a KV cache (K and V buffers of pf_kv_bytes each, layout
- * [n_layers][nkv][max_seq][hd] of the cache element type, [P2] GpuKvCache) and a
- * workspace. Creation computes the RoPE table cos/sin(p * theta^(-2i/hd)) on the
+ * [n_layers][nkv][slots][hd] of the cache element type, [P2] GpuKvCache; slots = max_seq
+ * positions, or ring_capacity ring slots) and a workspace. Creation computes the RoPE table cos/sin(p * theta^(-2i/hd)) on the
  * host in double precision ([P1] PrefillBuffers cos_buf/sin_buf are host-made too),
  * copies it into the workspace and clears the status words; it synchronises the
  * stream. The KV position starts at 0. The model struct and its layer array are
@@ -303,7 +312,8 @@ pf_status pf_op_gemm_static_scratch(int32_t wfmt, int32_t epilogue, const uint16
  * fused_qk_rope / fused_kv_store; [P2] dispatch_fused_qk_norm_rope): from qkv f32
  * [M, (nq+2nkv) hd], writes q_dev [M, nq, hd] (bf16 when kv_dtype is bf16, else f16)
  * and the K (post-RoPE) / V slots of `layer` at positions start_pos.. in the caches.
- * rope_dev: table from pf_rope_table_host ([max_seq][hd/2] of (cos, sin) f32). */
+ * rope_dev: table from pf_rope_table_host ([max_seq][hd/2] of (cos, sin) f32). Linear
+ * caches only (PF_ERR_UNSUPPORTED for a ring configuration). */
 pf_status pf_op_qk_norm_rope_kv(const pf_config* cfg, const float* qkv_dev,
                                 const float* q_norm_dev, const float* k_norm_dev,
                                 const float* rope_dev, int32_t layer, int32_t start_pos,
@@ -311,10 +321,22 @@ pf_status pf_op_qk_norm_rope_kv(const pf_config* cfg, const float* qkv_dev,
                                 void* v_cache_dev, void* stream);
 /* Causal GQA attention ([P1] section 3 scores/softmax/weighted sum, batched; [P3]
  * encode_attention_decode_batch): query rows at positions start_pos.., keys 0..pos of
- * `layer`'s cache; out f16 [M, nq hd]. */
+ * `layer`'s cache; out f16 [M, nq hd]. Linear caches only (a ring configuration returns
+ * PF_ERR_UNSUPPORTED: its keys come from the session's chunk buffers). */
 pf_status pf_op_attention(const pf_config* cfg, const void* q_dev, const void* k_cache_dev,
                           const void* v_cache_dev, int32_t layer, int32_t start_pos,
                           int32_t M, uint16_t* out_f16_dev, void* stream);
+/* The same with the keys cut into n_split contiguous parts (1..64), one CTA each, whose
+ * unnormalised partial results (O sums, running max and sum per row) go to scratch_dev
+ * (device, 16-B aligned, caller-owned, at least pf_attention_scratch_bytes(cfg, M, n_split)
+ * bytes) and are merged by a second kernel: the split-KV form the sessions use when a
+ * chunk's CTAs fill less than half of the GPU (decode, small chunks). 16-bit linear caches
+ * only; the same result as pf_op_attention up to the order of the f32 additions. */
+size_t pf_attention_scratch_bytes(const pf_config* cfg, int32_t M, int32_t n_split);
+pf_status pf_op_attention_split(const pf_config* cfg, const void* q_dev, const void* k_cache_dev,
+                                const void* v_cache_dev, int32_t layer, int32_t start_pos,
+                                int32_t M, int32_t n_split, void* scratch_dev, size_t scratch_bytes,
+                                uint16_t* out_f16_dev, void* stream);
 /* Embedding rows ([P3] encode_embed_any, scale 1.0): x[t] = E[tokens[t]] (device ids).
  * An id outside [0, vocab) yields a zero row and PF_ERR_TOKEN_OUT_OF_VOCAB in
  * *status_dev (if not NULL). */

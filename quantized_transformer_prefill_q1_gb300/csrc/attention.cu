@@ -333,15 +333,15 @@ cudaError_t prepare_attention_kernels() {
 
 // Routes 16-bit caches to the tcgen05 kernel (attention_tc.cu); f32 caches stage K/V
 // through registers into the m16n8k16 kernel above.
-cudaError_t launch_attention(const pf_config& c, const void* q, const void* k_cache,
-                             const void* v_cache, int layer, const int* start_dev, int start_host,
-                             int M, void* out, int* status, cudaStream_t stream) {
-  if (attention_tc_supported(c))
-    return launch_attention_tc(c, q, k_cache, v_cache, layer, start_dev, start_host, M, out, status,
-                               stream);
+cudaError_t launch_attention(const AttnArgs& a, cudaStream_t stream) {
+  const pf_config& c = *a.c;
+  if (attention_tc_supported(c)) return launch_attention_tc(a, stream);
+  if (c.ring_capacity > 0 || a.n_split > 1) return cudaErrorInvalidValue;  // tensor-core kernel only
   if (c.head_dim == 128)
-    return dispatch_kv<128>(c, q, k_cache, v_cache, layer, start_dev, start_host, M, out, stream);
-  return dispatch_kv<64>(c, q, k_cache, v_cache, layer, start_dev, start_host, M, out, stream);
+    return dispatch_kv<128>(c, a.q, a.k_cache, a.v_cache, a.layer, a.start_dev, a.start_host, a.M,
+                            a.out, stream);
+  return dispatch_kv<64>(c, a.q, a.k_cache, a.v_cache, a.layer, a.start_dev, a.start_host, a.M, a.out,
+                         stream);
 }
 
 }  // namespace pf

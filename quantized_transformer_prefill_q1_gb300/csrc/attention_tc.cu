@@ -4,30 +4,40 @@
 // The method: oxibonsai-kernels metal_prefill.rs `encode_layer_prefill` section 3 (for
 // each query position, scores q.k_j * inv_sqrt_hd over the seq_len = pos + 1 cached keys
 // of its kv head h / heads_per_group, softmax, weighted sum of V), batched over the chunk
-// as in turbospark-runtime prefill.rs `encode_attention_decode_batch`.
+// as in turbospark-runtime prefill.rs `encode_attention_decode_batch`. With a ring cache
+// (the batch-attention contract's ring_capacity R and sink_count S on the same page) the
+// query at position p sees the S sink positions and the R - S most recent positions up to p.
 //
 // One CTA = one kv head and 128 query rows (128/G tokens x the G query heads that share
 // the kv head; row = token * G + head-in-group), so every row reads the same K/V tiles.
-// The probabilities P stay in tensor memory as the A operand of the PV product:
-//   warp 0      TMA: the Q tile once (3-D map over q[M][nq][hd]), then 128-key K and V tiles
-//               straight from the cache [layer][kvh][pos][hd] into two 3-stage rings; a K
-//               stage is free again once its QK^T is done, so K runs a tile ahead of V;
+// The keys the CTA's rows may see form a list of 128-key tiles (KeyTiles below): a linear
+// cache gives one run of positions 0 .. last; a ring cache gives the history sinks, the
+// history window (in ring slots, wrapping once) and the chunk's own keys (read from the chunk
+// buffers the QK-norm / RoPE kernel wrote, since the chunk's later tokens may overwrite ring
+// slots its earlier tokens still need). With n_split > 1 the tile list is cut into n_split
+// contiguous parts, one CTA each (split-KV, for chunks too small to fill the GPU); each part
+// writes its unnormalised O, running max and sum, and attn_combine_kernel merges them.
+//
+// Warp roles:
+//   warp 0      TMA: the Q tile once (3-D map over q[M][nq][hd]), then the K and V tiles
+//               into two 3-stage rings; a K stage is free again once its QK^T is done, so
+//               K runs a tile ahead of V;
 //   warp 1      TMEM (512 columns: three S buffers of 128 and O) and the MMAs, issued by
 //               the whole warp with one elected lane: S_0, S_1, then per tile
 //               O += P_j V_j (P from TMEM over S_j's columns, V used MN-major as it lies in
-//               the cache) followed by S_{j+2} = Q K_{j+2}^T, so the scores of the next
-//               tile are ready before the softmax reaches it;
+//               the cache) followed by S_{j+2} = Q K_{j+2}^T;
 //   warps 2..9  softmax, two threads per query row: warp w reads TMEM lane quarter w % 4
 //               and takes key columns [0, 64) (warps 2..5) or [64, 128) (warps 6..9) of
-//               each tile. Per tile: read S_j,
-//               causal mask (key > pos: -inf), row max combined with the partner thread
-//               through shared memory, online softmax in the exp2 domain, P_j (bf16/f16)
-//               back into TMEM; the running max is raised only when a tile's max exceeds it
-//               by more than 2^8 (then O is rescaled in TMEM), so probabilities stay <= 256
-//               and f32 accumulation is exact enough; final O / l to f16.
+//               each tile. Per tile: read S_j, mask keys the row may not see, row max
+//               combined with the partner thread through shared memory, online softmax in
+//               the exp2 domain, P_j (bf16/f16) back into TMEM; the running max is raised
+//               only when a tile's max exceeds it by more than 2^8 (then O is rescaled in
+//               TMEM), so probabilities stay <= 256; final O / l to f16 (or the partials).
 // Every wait is bounded; a timeout aborts the CTA and records PF_ERR_DEVICE_TIMEOUT.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+
+#include <algorithm>
 
 #include "ptx.cuh"
 
@@ -41,6 +51,7 @@ constexpr int THREADS = 320;     // warp 0 TMA, warp 1 MMA, warps 2..9 softmax
 constexpr int SM_THREADS = 256;  // softmax threads: two per query row
 constexpr int HK = TK / 2;       // keys per softmax thread and tile
 constexpr int NSB = 3;           // S / P buffers in TMEM
+constexpr int MAX_SPLIT = 64;
 constexpr float RESCALE_LOG2 = 8.0f;
 // TMEM columns: S buffers b at b TK (P_j over the first TK/2 columns of its buffer), O at 3 TK
 constexpr uint32_t COL_O = NSB * TK;
@@ -52,6 +63,89 @@ struct ASmem {
   static constexpr int RED = 2 * TQ * 4;  // partner exchange: [half][row] f32
   static constexpr int BYTES = 1024 + Q + 2 * KS * KV + RED + 256;
   static_assert(BYTES <= 232448, "attention shared memory");
+};
+
+// One run of consecutive key positions held in consecutive rows of one tensor.
+struct KeyRange {
+  int src;   // 0: the cache, 1: the chunk buffers
+  int row0;  // first row (slot / chunk row) of the run within its (layer, kv head)
+  int pos0;  // position of row0
+  int len;   // keys in the run
+};
+
+struct KeyTile {
+  int src, row, pos0, nvalid;
+};
+
+// The 128-key tiles a CTA's query rows (tokens t0 .. t1-1 of the chunk at `start`) may see.
+struct KeyTiles {
+  KeyRange r[4];
+  int nt[4];
+  int total;
+
+  __device__ __forceinline__ void finish() {
+    total = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      nt[i] = r[i].len > 0 ? (r[i].len + TK - 1) / TK : 0;
+      total += nt[i];
+    }
+  }
+  // linear cache: positions 0 .. start + t1 - 1 at rows = positions
+  __device__ __forceinline__ void init_linear(int start, int t1) {
+    r[0] = {0, 0, 0, start + t1};
+    r[1] = r[2] = r[3] = {0, 0, 0, 0};
+    finish();
+  }
+  // ring cache of R slots, S sinks, window W = R - S
+  __device__ __forceinline__ void init_ring(int start, int t0, int t1, int S, int W, int R) {
+    r[0] = {0, 0, 0, min(S, start)};  // history sinks: slot = position
+    const int wa = max(S, start + t0 - W + 1);  // oldest history key in any row's window
+    const int wlen = max(0, start - wa);
+    const int slot = wlen > 0 ? S + (wa - S) % W : S;
+    const int l1 = min(wlen, R - slot);  // up to the ring's end, then from slot S on
+    r[1] = {0, slot, wa, l1};
+    r[2] = {0, S, wa + l1, wlen - l1};
+    const int c0 = start < S ? 0 : max(0, t0 - W + 1);  // the chunk's own keys
+    r[3] = {1, c0, start + c0, t1 - c0};
+    finish();
+  }
+  // tile j of the list (selects with constant indices keep the ranges in registers)
+  __device__ __forceinline__ KeyTile at(int j) const {
+    KeyRange x = r[0];
+    if (j >= nt[0]) {
+      j -= nt[0];
+      x = r[1];
+      if (j >= nt[1]) {
+        j -= nt[1];
+        x = r[2];
+        if (j >= nt[2]) {
+          j -= nt[2];
+          x = r[3];
+        }
+      }
+    }
+    KeyTile t;
+    t.src = x.src;
+    t.row = x.row0 + j * TK;
+    t.pos0 = x.pos0 + j * TK;
+    t.nvalid = min(TK, x.len - j * TK);
+    return t;
+  }
+};
+
+struct AttnKParams {
+  int M, nq, nkv, layer;
+  int cache_rows;  // rows per (layer, kv head) in the cache: max_seq, or R for a ring
+  int chunk_rows;  // rows per kv head in the chunk buffers (ring mode)
+  int ring_R, ring_S;
+  const int* start_dev;
+  int start_host;
+  float scale_log2;
+  int n_split;
+  __half* out;
+  float* partial;
+  int* status;
 };
 
 __device__ __forceinline__ void mbar_wait_drain_a(uint32_t bar, uint32_t parity) {
@@ -92,6 +186,18 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
+// Bits [0, n) set (n clamped to [0, 64]).
+__device__ __forceinline__ uint64_t low_bits(int n) {
+  return n <= 0 ? 0ull : (n >= 64 ? ~0ull : (1ull << n) - 1ull);
+}
+
+// Visibility of one thread's 64 key columns to its query row: column e is visible when
+// e < nvalid (inside the tile's run), e < lim (at or before the row's position), and not in
+// [a, b) (a ring's keys older than the row's window that are not sinks).
+__device__ __forceinline__ uint64_t visible_cols(int nvalid, int lim, int a, int b) {
+  return low_bits(min(nvalid, lim)) & ~(low_bits(b) & ~low_bits(a));
+}
+
 template <int BF16>
 __device__ __forceinline__ uint32_t pack_pair(float a, float b) {
   if (BF16) {
@@ -106,9 +212,8 @@ __device__ __forceinline__ uint32_t pack_pair(float a, float b) {
 template <int HD, int BF16>
 __global__ void __launch_bounds__(THREADS, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                   const __grid_constant__ CUtensorMap tm_v, int M, int nq, int nkv, int max_seq, int layer,
-                   const int* __restrict__ start_dev, int start_host, float scale_log2,
-                   __half* __restrict__ out, int* __restrict__ status) {
+                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_kc,
+                   const __grid_constant__ CUtensorMap tm_vc, const AttnKParams P) {
   using L = ASmem<HD>;
   constexpr int NH = HD / 64;  // 64-wide (128-B) swizzle regions along head_dim
   extern __shared__ uint8_t smem_raw[];
@@ -141,16 +246,34 @@ __global__ void __launch_bounds__(THREADS, 1)
   griddep_launch_dependents();
   griddep_wait();  // the start position and q / cache come from earlier kernels
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int G = nq / nkv;
+  const int M = P.M, nq = P.nq;
+  const int G = nq / P.nkv;
   const int BT = TQ / G;  // tokens per CTA
   const int n_tt = (M + BT - 1) / BT;
   const int tt = n_tt - 1 - static_cast<int>(blockIdx.x);  // longest rows first
   const int kvh = blockIdx.y;
+  const int split = blockIdx.z;
   const int t0 = tt * BT;
-  const int start = start_dev ? *start_dev : start_host;
-  const int kv_len = start + min(t0 + BT, M);
-  const int n_tiles = (kv_len + TK - 1) / TK;
-  const int row0 = (layer * nkv + kvh) * max_seq;
+  const int t1 = min(t0 + BT, M);
+  const int start = P.start_dev ? *P.start_dev : P.start_host;
+  const bool ring = P.ring_R > 0;
+  const int S = P.ring_S, W = P.ring_R - P.ring_S;
+  KeyTiles kt;
+  if (ring)
+    kt.init_ring(start, t0, t1, S, W, P.ring_R);
+  else
+    kt.init_linear(start, t1);
+  // this CTA's part of the tile list
+  const int jb = static_cast<int>(static_cast<long long>(kt.total) * split / P.n_split);
+  const int nt = static_cast<int>(static_cast<long long>(kt.total) * (split + 1) / P.n_split) - jb;
+  const int crow0 = (P.layer * P.nkv + kvh) * P.cache_rows;  // (layer, kv head) in the cache
+  const int brow0 = kvh * P.chunk_rows;                      // kv head in the chunk buffers
+  const int first_pos = start + t0, last_pos = start + t1 - 1;
+  // whether some key of tile `t` is hidden from some query row of the CTA
+  auto needs_mask = [&](const KeyTile& t) {
+    if (t.nvalid < TK || t.pos0 + TK - 1 > first_pos) return true;
+    return ring && t.pos0 + TK - 1 >= S && t.pos0 <= last_pos - W;
+  };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < KS; ++s) {
@@ -182,7 +305,19 @@ __global__ void __launch_bounds__(THREADS, 1)
   const uint32_t tmem = *tmem_slot;
   const uint32_t tmem_o = tmem + COL_O;
 
-  if (warp == 0) {
+  if (nt == 0) {
+    // an empty part of a split list: its rows contribute nothing (max -inf, sum 0)
+    if (warp >= 2 && threadIdx.x - 64 < TQ) {
+      const int r = threadIdx.x - 64;
+      const int t = t0 + r / G;
+      if (t < M) {
+        float* ml = P.partial + static_cast<size_t>(P.n_split) * M * nq * HD;
+        const size_t row = (static_cast<size_t>(split) * M + t) * nq + kvh * G + r % G;
+        ml[2 * row] = -INFINITY;
+        ml[2 * row + 1] = 0.f;
+      }
+    }
+  } else if (warp == 0) {
     // ------------------------------------------------------------------ TMA producer
     if (lane == 0) {
       mbar_arrive_expect_tx(q_full, L::Q);
@@ -191,16 +326,18 @@ __global__ void __launch_bounds__(THREADS, 1)
       // K_i, then V_{i-1}: K runs one tile ahead of V
       int k_issued = 0, v_issued = 0;
       bool ok = true;
-      for (int i = 0; i <= n_tiles && ok; ++i) {
-        if (i < n_tiles) {
+      for (int i = 0; i <= nt && ok; ++i) {
+        if (i < nt) {
           const int s = i % KS;
           if (!mbar_wait(k_empty(s), ((i / KS) & 1) ^ 1, abort_flag)) {
             ok = false;
             break;
           }
+          const KeyTile kt_i = kt.at(jb + i);
+          const CUtensorMap* mk = kt_i.src ? &tm_kc : &tm_k;
+          const int row = (kt_i.src ? brow0 : crow0) + kt_i.row;
           mbar_arrive_expect_tx(k_full(s), L::KV);
-          for (int h = 0; h < NH; ++h)
-            tma_load_2d(k_tile(s) + h * (TK * 128), &tm_k, h * 64, row0 + i * TK, k_full(s));
+          for (int h = 0; h < NH; ++h) tma_load_2d(k_tile(s) + h * (TK * 128), mk, h * 64, row, k_full(s));
           ++k_issued;
         }
         if (i >= 1) {
@@ -209,9 +346,11 @@ __global__ void __launch_bounds__(THREADS, 1)
             ok = false;
             break;
           }
+          const KeyTile kt_v = kt.at(jb + jv);
+          const CUtensorMap* mv = kt_v.src ? &tm_vc : &tm_v;
+          const int row = (kt_v.src ? brow0 : crow0) + kt_v.row;
           mbar_arrive_expect_tx(v_full(s), L::KV);
-          for (int h = 0; h < NH; ++h)
-            tma_load_2d(v_tile(s) + h * (TK * 128), &tm_v, h * 64, row0 + jv * TK, v_full(s));
+          for (int h = 0; h < NH; ++h) tma_load_2d(v_tile(s) + h * (TK * 128), mv, h * 64, row, v_full(s));
           ++v_issued;
         }
       }
@@ -247,8 +386,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     };
     bool ok = __all_sync(0xffffffffu, mbar_wait(q_full, 0, abort_flag));
     if (ok) ok = issue_s(0);
-    if (ok && n_tiles > 1) ok = issue_s(1);
-    for (int j = 0; j < n_tiles && ok; ++j) {
+    if (ok && nt > 1) ok = issue_s(1);
+    for (int j = 0; j < nt && ok; ++j) {
       // O += P_j V_j, P from TMEM over S_j's columns
       const int sb = j % NSB, vs = j % KS;
       if (!__all_sync(0xffffffffu, mbar_wait(p_full(sb), (j / NSB) & 1, abort_flag) &&
@@ -265,7 +404,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       umma_commit_warp(s_empty(sb));  // P_j consumed: S buffer reusable
       umma_commit_warp(v_empty(vs));
       umma_commit_warp(o_done);
-      if (j + 2 < n_tiles) ok = issue_s(j + 2);
+      if (j + 2 < nt) ok = issue_s(j + 2);
     }
     if (ok) {
       umma_commit_warp(o_final);
@@ -287,8 +426,9 @@ __global__ void __launch_bounds__(THREADS, 1)
     // tcgen05.ld / tcgen05.st are warp-collective: every branch around them is warp-uniform.
     // The 256 softmax threads meet at named barrier 1 twice per tile; a failed wait is
     // carried to the next barrier-and, where all of them stop together.
-    for (int j = 0; j < n_tiles; ++j) {
+    for (int j = 0; j < nt; ++j) {
       const int s = j % NSB;
+      const KeyTile tl = kt.at(jb + j);
       const bool got = mbar_wait(s_full(s), (j / NSB) & 1, abort_flag);
       if (!named_bar_and_a(1, SM_THREADS, got && !failed)) {
         ok = false;
@@ -296,25 +436,28 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
       tc_fence_after();
       const uint32_t sbuf = tmem + lane_off + s * TK;
-      const int kbase = j * TK + half * HK;  // first key of this thread's columns
       uint32_t v[HK];
 #pragma unroll
       for (int c = 0; c < HK / 32; ++c)
         tmem_ld_32x32b_x32(sbuf + half * HK + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(v + 32 * c));
       tmem_ld_wait();
-      // a tile wholly at or below the CTA's first position needs no causal mask
-      const bool diag = j * TK + TK - 1 > start + t0;
+      // key column e of this thread holds position kp0 + e; keys this row may not see (outside the tile's run, after the row's position, or, in
+      // a ring, older than its window and not a sink) become -inf scores in place, so one
+      // code path follows: they add nothing to the max and get probability ex2(-inf) = 0
+      if (needs_mask(tl)) {
+        const int kp0 = tl.pos0 + half * HK;  // position of this thread's first key column
+        const uint64_t vis = visible_cols(tl.nvalid - half * HK, pos - kp0 + 1,
+                                          ring ? S - kp0 : 0, ring ? pos - W + 1 - kp0 : 0);
+        const uint32_t lo = static_cast<uint32_t>(vis), hi = static_cast<uint32_t>(vis >> 32);
+#pragma unroll
+        for (int e = 0; e < HK; ++e)
+          if (!(((e < 32 ? lo : hi) >> (e & 31)) & 1u)) v[e] = 0xff800000u;  // -inf
+      }
       float mp[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) mp[i] = -INFINITY;
-      if (diag) {
 #pragma unroll
-        for (int e = 0; e < HK; ++e)
-          if (kbase + e <= pos) mp[e & 7] = fmaxf(mp[e & 7], __uint_as_float(v[e]));
-      } else {
-#pragma unroll
-        for (int e = 0; e < HK; ++e) mp[e & 7] = fmaxf(mp[e & 7], __uint_as_float(v[e]));
-      }
+      for (int e = 0; e < HK; ++e) mp[e & 7] = fmaxf(mp[e & 7], __uint_as_float(v[e]));
       float mraw = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
                          fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7])));
       red[half * TQ + r] = mraw;
@@ -323,13 +466,14 @@ __global__ void __launch_bounds__(THREADS, 1)
       named_bar_sync_a(1, SM_THREADS);
       tc_fence_after();
       mraw = fmaxf(mraw, red[(1 - half) * TQ + r]);  // the row's max over all 128 keys
-      const float mx = mraw * scale_log2;  // scale > 0 keeps the order
+      const float mx = mraw * P.scale_log2;  // scale > 0 keeps the order; -inf stays
       const bool need = j > 0 && mx > m + RESCALE_LOG2;
       if (j == 0) {
-        m = mx;  // key 0 is visible to every row, so this is finite
+        m = mx;  // -inf when no key of the first tile is visible to the row
       } else if (__any_sync(0xffffffffu, need)) {
         // some row of this warp raises its max: the warp rescales its half of those O rows,
-        // the rows that keep their max with alpha = 1 (the partner warp decides the same)
+        // the rows that keep their max with alpha = 1 (the partner warp decides the same);
+        // a row whose max was -inf has O = 0 and l = 0, and alpha = 0 keeps them so
         const float alpha = need ? exp2f(m - mx) : 1.0f;
         l *= alpha;
         // O holds P_0..P_{j-1} V: wait for PV_{j-1}, then scale it in place
@@ -350,27 +494,26 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         if (need) m = mx;
       }
-      const float neg_m = -m;
+      // a row that has seen no key yet (max -inf) has only -inf scores: any finite offset
+      // keeps ex2 at 0 (-inf - -inf would be NaN)
+      const float neg_m = m == -INFINITY ? 0.f : -m;
+      const float sl2 = P.scale_log2;
       float rsp[4] = {0.f, 0.f, 0.f, 0.f};  // independent partial row sums
       uint32_t pk[HK / 2];                  // this thread's 64 probabilities, packed in pairs
 #pragma unroll
       for (int x = 0; x < HK; x += 2) {
-        float p0 = ex2_approx(fmaf(__uint_as_float(v[x]), scale_log2, neg_m));
-        float p1 = ex2_approx(fmaf(__uint_as_float(v[x + 1]), scale_log2, neg_m));
-        if (diag) {
-          p0 = (kbase + x <= pos) ? p0 : 0.f;
-          p1 = (kbase + x + 1 <= pos) ? p1 : 0.f;
-        }
+        const float p0 = ex2_approx(fmaf(__uint_as_float(v[x]), sl2, neg_m));
+        const float p1 = ex2_approx(fmaf(__uint_as_float(v[x + 1]), sl2, neg_m));
         rsp[(x >> 1) & 3] += p0 + p1;
         pk[x >> 1] = pack_pair<BF16>(p0, p1);
       }
       l += (rsp[0] + rsp[1]) + (rsp[2] + rsp[3]);
       // P_j over the first TK/2 columns of S buffer s: keys 2c, 2c+1 in column c
       tmem_st_32x32b_x32(sbuf + half * (HK / 2), pk);
-      if (j == n_tiles - 1 && j * TK + r >= kv_len) {
-        // key row r of this tile lies past the cache's filled range: zero its V row (once
-        // the tile has landed) so a zero probability never meets a stale NaN / Inf in the
-        // PV product
+      if (r >= tl.nvalid) {
+        // key row r of this tile lies outside its run (another head's slots, a stale or
+        // unwritten row, or past the tensor): zero its V row once the tile has landed, so a
+        // zero probability never meets a NaN / Inf in the PV product
         const int vs = j % KS;
         if (!mbar_wait(v_full(vs), (j / KS) & 1, abort_flag)) failed = true;
         for (int h = half; h < NH; h += 2)
@@ -388,26 +531,43 @@ __global__ void __launch_bounds__(THREADS, 1)
     named_bar_sync_a(1, SM_THREADS);
     if (all_ok) {
       tc_fence_after();
-      const float inv = 1.f / (l + red[(1 - half) * TQ + r]);
+      const float l_row = l + red[(1 - half) * TQ + r];
       const int t = t0 + t_loc;
       const int h = kvh * G + h_loc;
+      const bool partial = P.n_split > 1;
+      const float inv = partial ? 1.f : 1.f / l_row;
+      if (partial && half == 0 && t < M) {
+        float* ml = P.partial + static_cast<size_t>(P.n_split) * M * nq * HD;
+        const size_t row = (static_cast<size_t>(split) * M + t) * nq + h;
+        ml[2 * row] = m;
+        ml[2 * row + 1] = l_row;
+      }
 #pragma unroll 1
       for (int c = half * (HD / 64); c < (half + 1) * (HD / 64); ++c) {
         uint32_t v[32];
         tmem_ld_32x32b_x32(tmem_o + lane_off + 32 * c, v);
         tmem_ld_wait();
         if (t < M) {
-          uint4* dst = reinterpret_cast<uint4*>(out + (static_cast<size_t>(t) * nq + h) * HD + 32 * c);
+          if (partial) {
+            float4* dst = reinterpret_cast<float4*>(
+                P.partial + ((static_cast<size_t>(split) * M + t) * nq + h) * HD + 32 * c);
 #pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) {
-            uint32_t w[4];
+            for (int q4 = 0; q4 < 8; ++q4)
+              dst[q4] = make_float4(__uint_as_float(v[4 * q4]), __uint_as_float(v[4 * q4 + 1]),
+                                    __uint_as_float(v[4 * q4 + 2]), __uint_as_float(v[4 * q4 + 3]));
+          } else {
+            uint4* dst = reinterpret_cast<uint4*>(P.out + (static_cast<size_t>(t) * nq + h) * HD + 32 * c);
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const __half2 hv = __floats2half2_rn(__uint_as_float(v[8 * q4 + 2 * e]) * inv,
-                                                   __uint_as_float(v[8 * q4 + 2 * e + 1]) * inv);
-              w[e] = *reinterpret_cast<const uint32_t*>(&hv);
+            for (int q4 = 0; q4 < 4; ++q4) {
+              uint32_t w[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const __half2 hv = __floats2half2_rn(__uint_as_float(v[8 * q4 + 2 * e]) * inv,
+                                                     __uint_as_float(v[8 * q4 + 2 * e + 1]) * inv);
+                w[e] = *reinterpret_cast<const uint32_t*>(&hv);
+              }
+              dst[q4] = make_uint4(w[0], w[1], w[2], w[3]);
             }
-            dst[q4] = make_uint4(w[0], w[1], w[2], w[3]);
           }
         }
       }
@@ -421,32 +581,99 @@ __global__ void __launch_bounds__(THREADS, 1)
     __syncwarp();  // lane 0 ran the MMA loop: reconverge before the collective dealloc
     tmem_dealloc(tmem, 512);
   }
-  if (threadIdx.x == 0 && *abort_flag && status != nullptr) atomicCAS(status, 0, PF_ERR_DEVICE_TIMEOUT);
+  if (threadIdx.x == 0 && *abort_flag && P.status != nullptr) atomicCAS(P.status, 0, PF_ERR_DEVICE_TIMEOUT);
+}
+
+// Merges the n_split partial results of each (token, head) row: with m* the largest of the
+// parts' running maxima, O = sum_s 2^(m_s - m*) O_s / sum_s 2^(m_s - m*) l_s (the parts keep
+// O_s and l_s relative to their own m_s, in the exp2 domain). Parts that saw no key of the
+// row (m_s = -inf) are skipped. One warp per row.
+template <int HD>
+__global__ void __launch_bounds__(256) attn_combine_kernel(const float* __restrict__ part, int rows,
+                                                           int n_split, __half* __restrict__ out) {
+  griddep_launch_dependents();
+  griddep_wait();
+  const int row = blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= rows) return;
+  constexpr int PER = HD / 32;
+  const float* ml = part + static_cast<size_t>(n_split) * rows * HD;
+  float mstar = -INFINITY;
+  for (int s = 0; s < n_split; ++s) mstar = fmaxf(mstar, ml[2 * (static_cast<size_t>(s) * rows + row)]);
+  float acc[PER];
+#pragma unroll
+  for (int i = 0; i < PER; ++i) acc[i] = 0.f;
+  float lsum = 0.f;
+  for (int s = 0; s < n_split; ++s) {
+    const size_t sr = static_cast<size_t>(s) * rows + row;
+    const float ms = ml[2 * sr];
+    if (ms == -INFINITY) continue;
+    const float w = exp2f(ms - mstar);
+    lsum += w * ml[2 * sr + 1];
+    const float* o = part + sr * HD + lane * PER;
+#pragma unroll
+    for (int i = 0; i < PER; ++i) acc[i] += w * o[i];
+  }
+  const float inv = 1.f / lsum;
+  __half* dst = out + static_cast<size_t>(row) * HD + lane * PER;
+#pragma unroll
+  for (int i = 0; i < PER; i += 2) *reinterpret_cast<__half2*>(dst + i) = __floats2half2_rn(acc[i] * inv, acc[i + 1] * inv);
 }
 
 template <int HD, int BF16>
-cudaError_t launch_tc(const pf_config& c, const void* q, const void* kc, const void* vc, int layer,
-                      const int* start_dev, int start_host, int M, void* out, int* status,
-                      cudaStream_t st) {
+cudaError_t launch_tc(const AttnArgs& a, cudaStream_t st) {
+  const pf_config& c = *a.c;
   const int G = c.n_q_heads / c.n_kv_heads;
   const int BT = TQ / G;
-  const uint64_t rows = static_cast<uint64_t>(c.n_layers) * c.n_kv_heads * c.max_seq;
-  CUtensorMap tq, tk, tv;
+  const bool ring = c.ring_capacity > 0;
+  const int cache_rows = ring ? c.ring_capacity : c.max_seq;
+  const uint64_t rows = static_cast<uint64_t>(c.n_layers) * c.n_kv_heads * cache_rows;
+  CUtensorMap tq, tk, tv, tkc, tvc;
   const uint64_t qd[3] = {static_cast<uint64_t>(HD), static_cast<uint64_t>(c.n_q_heads),
-                          static_cast<uint64_t>(M)};
+                          static_cast<uint64_t>(a.M)};
   const uint64_t qs[2] = {static_cast<uint64_t>(HD) * 2, static_cast<uint64_t>(c.n_q_heads) * HD * 2};
   const uint32_t qb[3] = {64, static_cast<uint32_t>(G), static_cast<uint32_t>(BT)};
   const uint64_t kd[2] = {static_cast<uint64_t>(HD), rows};
   const uint64_t ks[1] = {static_cast<uint64_t>(HD) * 2};
   const uint32_t kb[2] = {64, static_cast<uint32_t>(TK)};
-  if (!encode_tmap_16(&tq, BF16, 3, q, qd, qs, qb) || !encode_tmap_16(&tk, BF16, 2, kc, kd, ks, kb) ||
-      !encode_tmap_16(&tv, BF16, 2, vc, kd, ks, kb))
+  if (!encode_tmap_16(&tq, BF16, 3, a.q, qd, qs, qb) || !encode_tmap_16(&tk, BF16, 2, a.k_cache, kd, ks, kb) ||
+      !encode_tmap_16(&tv, BF16, 2, a.v_cache, kd, ks, kb))
     return cudaErrorInvalidValue;
-  dim3 grid((M + BT - 1) / BT, c.n_kv_heads);
-  const float scale_log2 = 1.4426950408889634f / sqrtf(static_cast<float>(HD));
-  return launch_pdl(attn_tc_kernel<HD, BF16>, grid, dim3(THREADS), ASmem<HD>::BYTES, st, tq, tk, tv,
-                    M, c.n_q_heads, c.n_kv_heads, c.max_seq, layer, start_dev, start_host,
-                    scale_log2, reinterpret_cast<__half*>(out), status);
+  if (ring) {
+    const uint64_t cd[2] = {static_cast<uint64_t>(HD), static_cast<uint64_t>(c.n_kv_heads) * a.chunk_rows};
+    if (!a.k_chunk || !a.v_chunk || !encode_tmap_16(&tkc, BF16, 2, a.k_chunk, cd, ks, kb) ||
+        !encode_tmap_16(&tvc, BF16, 2, a.v_chunk, cd, ks, kb))
+      return cudaErrorInvalidValue;
+  } else {
+    tkc = tk;
+    tvc = tv;
+  }
+  const int n_split = std::max(1, std::min(a.n_split, MAX_SPLIT));
+  if (n_split > 1 && !a.partial) return cudaErrorInvalidValue;
+  AttnKParams p;
+  p.M = a.M;
+  p.nq = c.n_q_heads;
+  p.nkv = c.n_kv_heads;
+  p.layer = a.layer;
+  p.cache_rows = cache_rows;
+  p.chunk_rows = a.chunk_rows;
+  p.ring_R = ring ? c.ring_capacity : 0;
+  p.ring_S = ring ? c.sink_count : 0;
+  p.start_dev = a.start_dev;
+  p.start_host = a.start_host;
+  p.scale_log2 = 1.4426950408889634f / sqrtf(static_cast<float>(HD));
+  p.n_split = n_split;
+  p.out = reinterpret_cast<__half*>(a.out);
+  p.partial = a.partial;
+  p.status = a.status;
+  dim3 grid((a.M + BT - 1) / BT, c.n_kv_heads, n_split);
+  cudaError_t e = launch_pdl(attn_tc_kernel<HD, BF16>, grid, dim3(THREADS), ASmem<HD>::BYTES, st, tq, tk,
+                             tv, tkc, tvc, p);
+  if (e != cudaSuccess || n_split == 1) return e;
+  const int rows_out = a.M * c.n_q_heads;
+  return launch_pdl(attn_combine_kernel<HD>, dim3((rows_out + 7) / 8), dim3(256), 0, st,
+                    static_cast<const float*>(a.partial), rows_out, n_split,
+                    reinterpret_cast<__half*>(a.out));
 }
 
 template <int HD, int BF16>
@@ -463,6 +690,33 @@ bool attention_tc_supported(const pf_config& c) {
          (c.head_dim == 128 || c.head_dim == 64) && G >= 1 && TQ % G == 0;
 }
 
+int attention_splits(const pf_config& c, int M, int sms) {
+  if (!attention_tc_supported(c) || M <= 0) return 1;
+  const int BT = TQ / (c.n_q_heads / c.n_kv_heads);
+  const int ctas = (M + BT - 1) / BT * c.n_kv_heads;
+  if (2 * ctas > sms) return 1;  // at least half of the SMs busy without splitting
+  return std::max(1, std::min(MAX_SPLIT, sms / ctas));
+}
+
+size_t attention_partial_bytes(const pf_config& c, int M, int n_split) {
+  if (n_split <= 1) return 0;
+  return static_cast<size_t>(n_split) * M * c.n_q_heads * (c.head_dim + 2) * sizeof(float);
+}
+
+size_t attention_partial_bytes_max(const pf_config& c, int max_sms) {
+  if (!attention_tc_supported(c)) return 0;
+  const int BT = TQ / (c.n_q_heads / c.n_kv_heads);
+  size_t best = 0;
+  for (int nqt = 1; nqt <= (c.max_chunk + BT - 1) / BT; ++nqt) {
+    const int M = std::min(nqt * BT, c.max_chunk);
+    int worst = 1;
+    for (int sms = 1; sms <= max_sms; ++sms) worst = std::max(worst, attention_splits(c, M, sms));
+    best = std::max(best, attention_partial_bytes(c, M, worst));
+    if (2 * nqt * c.n_kv_heads > max_sms) break;  // no split at this size or beyond
+  }
+  return best;
+}
+
 cudaError_t prepare_attention_tc_kernels() {
   cudaError_t e = cudaSuccess, r;
   if ((r = set_attr_tc<128, 1>()) != cudaSuccess) e = r;
@@ -472,15 +726,11 @@ cudaError_t prepare_attention_tc_kernels() {
   return e;
 }
 
-cudaError_t launch_attention_tc(const pf_config& c, const void* q, const void* k_cache,
-                                const void* v_cache, int layer, const int* start_dev, int start_host,
-                                int M, void* out, int* status, cudaStream_t stream) {
+cudaError_t launch_attention_tc(const AttnArgs& a, cudaStream_t stream) {
+  const pf_config& c = *a.c;
   const bool bf = c.kv_dtype == PF_KV_BF16;
-  if (c.head_dim == 128)
-    return bf ? launch_tc<128, 1>(c, q, k_cache, v_cache, layer, start_dev, start_host, M, out, status, stream)
-              : launch_tc<128, 0>(c, q, k_cache, v_cache, layer, start_dev, start_host, M, out, status, stream);
-  return bf ? launch_tc<64, 1>(c, q, k_cache, v_cache, layer, start_dev, start_host, M, out, status, stream)
-            : launch_tc<64, 0>(c, q, k_cache, v_cache, layer, start_dev, start_host, M, out, status, stream);
+  if (c.head_dim == 128) return bf ? launch_tc<128, 1>(a, stream) : launch_tc<128, 0>(a, stream);
+  return bf ? launch_tc<64, 1>(a, stream) : launch_tc<64, 0>(a, stream);
 }
 
 }  // namespace pf

@@ -505,7 +505,7 @@ template <int WFMT, int EPI>
 cudaError_t launch_t(const GemmArgs& g, const CUtensorMap& ta, const CUtensorMap& to, int num_sms,
                      cudaStream_t stream) {
   constexpr int smem = smem_bytes<WFMT>();
-  Plan p;
+  Plan p{};
   p.n_mt = (g.M + BM - 1) / BM;
   p.n_nt = static_cast<int>(padded_rows(g.N) / TILE_N);
   p.kbt = g.K / BK;
@@ -516,7 +516,8 @@ cudaError_t launch_t(const GemmArgs& g, const CUtensorMap& ta, const CUtensorMap
   const int tiles = p.n_mt * p.n_nt;
   if (EPI != EPI_RESID_ADD && tiles < p.ctas && 2 * tiles >= p.ctas) p.ctas = tiles;
   float* scratch = reinterpret_cast<float*>(g.scratch);
-  int* counters = reinterpret_cast<int*>(scratch + static_cast<size_t>(2) * g.max_ctas * SLOT_FLOATS);
+  int* counters =
+      scratch ? reinterpret_cast<int*>(scratch + static_cast<size_t>(2) * g.max_ctas * SLOT_FLOATS) : nullptr;
   return launch_pdl(gemm_q_kernel<WFMT, EPI>, dim3(p.ctas), dim3(NUM_THREADS), smem, stream, ta, to,
                     g.w, g.M, g.N, g.K, p, scratch, counters, g.status);
 }

@@ -377,7 +377,7 @@ cudaError_t launch_s(const GemmArgs& g, int num_sms, cudaStream_t stream) {
   const uint64_t strides[2] = {static_cast<uint64_t>(g.K) * 2, 128};
   const uint32_t box[3] = {64, static_cast<uint32_t>(NT), 2};
   if (!encode_tmap_16(&tx, 0, 3, g.a, dims, strides, box)) return cudaErrorInvalidValue;
-  Plan p;
+  Plan p{};
   p.n_mt = 1;
   p.n_nt = static_cast<int>(padded_rows(g.N) / TT);
   p.kbt = g.K / GROUP;

@@ -139,11 +139,13 @@ __device__ __forceinline__ void store4<__nv_bfloat16>(__nv_bfloat16* dst, float 
 // when enabled, then rotate-half RoPE at position start + t from the (cos, sin) table;
 // Q goes to q_out [M, nq, hd], K to the cache slot [layer, kvh, pos, :], and V is copied
 // unchanged to its slot. Cache layout of metal_full_layer.rs `GpuKvCache`:
-// [n_layers][nkv][max_seq][hd].
+// [n_layers][nkv][max_seq][hd]: K/V row (kv_layer * nkv + kvh) * kv_rows + start + t
+// (kv_by_pos = 1); a ring cache's chunk buffers take row kvh * kv_rows + t (kv_layer = 0,
+// kv_by_pos = 0) and the ring slots are filled after the attention (ring_store_kernel).
 template <int HD, typename QT, typename KT>
 __global__ void __launch_bounds__(256) qk_norm_rope_kv_kernel(
     const float* __restrict__ qkv, const float* __restrict__ qn, const float* __restrict__ kn,
-    const float* __restrict__ rope, int M, int nq, int nkv, int max_seq, int layer,
+    const float* __restrict__ rope, int M, int nq, int nkv, int kv_rows, int kv_layer, int kv_by_pos,
     const int* __restrict__ start_dev, int start_host, float eps, int qk_norm,
     QT* __restrict__ q_out, KT* __restrict__ kc, KT* __restrict__ vc) {
   constexpr int HALF = HD / 2;
@@ -185,8 +187,9 @@ __global__ void __launch_bounds__(256) qk_norm_rope_kv_kernel(
 #pragma unroll
   for (int o = LPH / 2; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
   if (!valid) return;
+  const int kv_row = kv_by_pos ? pos : t;
   if (is_v) {  // V head: straight to the cache
-    KT* dst = vc + ((static_cast<size_t>(layer) * nkv + (j - nq - nkv)) * max_seq + pos) * HD;
+    KT* dst = vc + ((static_cast<size_t>(kv_layer) * nkv + (j - nq - nkv)) * kv_rows + kv_row) * HD;
     store4<KT>(dst + 4 * l, a.x, a.y, a.z, a.w);
     store4<KT>(dst + HALF + 4 * l, b.x, b.y, b.z, b.w);
     return;
@@ -205,9 +208,40 @@ __global__ void __launch_bounds__(256) qk_norm_rope_kv_kernel(
     store4<QT>(dst + 4 * l, ra0, ra1, ra2, ra3);
     store4<QT>(dst + HALF + 4 * l, rb0, rb1, rb2, rb3);
   } else {
-    KT* dst = kc + ((static_cast<size_t>(layer) * nkv + (j - nq)) * max_seq + pos) * HD;
+    KT* dst = kc + ((static_cast<size_t>(kv_layer) * nkv + (j - nq)) * kv_rows + kv_row) * HD;
     store4<KT>(dst + 4 * l, ra0, ra1, ra2, ra3);
     store4<KT>(dst + HALF + 4 * l, rb0, rb1, rb2, rb3);
+  }
+}
+
+// ------------------------------------------------------------------ ring / sink KV store
+// The ring cache of the batch-attention contract (turbospark-runtime prefill.rs:
+// ring_capacity R, sink_count S): position p keeps slot p when p < S, otherwise slot
+// S + (p - S) mod (R - S). After the chunk's attention (which read the chunk's own keys from
+// the chunk buffers), the rows a ring keeps are copied in: the sinks among the chunk's
+// positions and its last R - S positions (earlier ones would be overwritten within the chunk
+// anyway, so no two copies hit one slot). One warp per (token, kv head), `words` 32-bit words
+// per row.
+__global__ void __launch_bounds__(256) ring_store_kernel(
+    const uint32_t* __restrict__ kb, const uint32_t* __restrict__ vb, int chunk_rows, int M,
+    int nkv, int words, int layer, int R, int S, const int* __restrict__ start_dev, int start_host,
+    uint32_t* __restrict__ kc, uint32_t* __restrict__ vc) {
+  griddep_launch_dependents();
+  griddep_wait();
+  const int item = blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (item >= M * nkv) return;
+  const int t = item / nkv, kvh = item - (item / nkv) * nkv;
+  const int start = start_dev ? *start_dev : start_host;
+  const int p = start + t;
+  const int W = R - S;
+  if (p >= S && p < start + M - W) return;  // overwritten by a later position of this chunk
+  const int slot = p < S ? p : S + (p - S) % W;
+  const size_t src = (static_cast<size_t>(kvh) * chunk_rows + t) * words;
+  const size_t dst = ((static_cast<size_t>(layer) * nkv + kvh) * R + slot) * words;
+  for (int w = lane; w < words; w += 32) {
+    kc[dst + w] = kb[src + w];
+    vc[dst + w] = vb[src + w];
   }
 }
 
@@ -438,48 +472,65 @@ cudaError_t launch_rmsnorm(const float* x, const float* w, float eps, int M, int
   return launch_pdl(rmsnorm_kernel, dim3(M), dim3(threads), 0, stream, x, w, eps, H, yh);
 }
 
+struct QkDst {
+  int kv_layer, kv_rows, kv_by_pos;
+};
+
 template <int HD, typename QT, typename KT>
 static void qk_launch(const pf_config& c, const float* qkv, const float* qn, const float* kn,
-                      const float* rope, int layer, const int* start_dev, int start_host, int M,
+                      const float* rope, QkDst d, const int* start_dev, int start_host, int M,
                       void* q, void* kc, void* vc, cudaStream_t stream) {
   const int heads = c.n_q_heads + 2 * c.n_kv_heads;
   constexpr int HPW = 32 / (HD / 8);
   const long long warps = (static_cast<long long>(M) * heads + HPW - 1) / HPW;
   const int blocks = static_cast<int>((warps * 32 + 255) / 256);
   launch_pdl(qk_norm_rope_kv_kernel<HD, QT, KT>, dim3(blocks), dim3(256), 0, stream, qkv, qn, kn,
-             rope, M, c.n_q_heads, c.n_kv_heads, c.max_seq, layer, start_dev, start_host, c.eps,
-             c.qk_norm, reinterpret_cast<QT*>(q), reinterpret_cast<KT*>(kc),
+             rope, M, c.n_q_heads, c.n_kv_heads, d.kv_rows, d.kv_layer, d.kv_by_pos, start_dev,
+             start_host, c.eps, c.qk_norm, reinterpret_cast<QT*>(q), reinterpret_cast<KT*>(kc),
              reinterpret_cast<KT*>(vc));
 }
 
 template <int HD>
 static void qk_dispatch_kv(const pf_config& c, const float* qkv, const float* qn, const float* kn,
-                           const float* rope, int layer, const int* sd, int sh, int M, void* q,
+                           const float* rope, QkDst d, const int* sd, int sh, int M, void* q,
                            void* kc, void* vc, cudaStream_t st) {
   switch (c.kv_dtype) {
     case PF_KV_BF16:
-      qk_launch<HD, __nv_bfloat16, __nv_bfloat16>(c, qkv, qn, kn, rope, layer, sd, sh, M, q, kc, vc, st);
+      qk_launch<HD, __nv_bfloat16, __nv_bfloat16>(c, qkv, qn, kn, rope, d, sd, sh, M, q, kc, vc, st);
       break;
     case PF_KV_F16:
-      qk_launch<HD, __half, __half>(c, qkv, qn, kn, rope, layer, sd, sh, M, q, kc, vc, st);
+      qk_launch<HD, __half, __half>(c, qkv, qn, kn, rope, d, sd, sh, M, q, kc, vc, st);
       break;
     default:
-      qk_launch<HD, __half, float>(c, qkv, qn, kn, rope, layer, sd, sh, M, q, kc, vc, st);
+      qk_launch<HD, __half, float>(c, qkv, qn, kn, rope, d, sd, sh, M, q, kc, vc, st);
       break;
   }
 }
 
 cudaError_t launch_qk_norm_rope_kv(const pf_config& c, const float* qkv, const float* q_norm,
-                                   const float* k_norm, const float* rope, int layer,
-                                   const int* start_dev, int start_host, int M, void* q_out,
-                                   void* k_cache, void* v_cache, cudaStream_t stream) {
+                                   const float* k_norm, const float* rope, int kv_layer, int kv_rows,
+                                   int kv_by_pos, const int* start_dev, int start_host, int M,
+                                   void* q_out, void* k_dst, void* v_dst, cudaStream_t stream) {
+  const QkDst d{kv_layer, kv_rows, kv_by_pos};
   if (c.head_dim == 128)
-    qk_dispatch_kv<128>(c, qkv, q_norm, k_norm, rope, layer, start_dev, start_host, M, q_out,
-                        k_cache, v_cache, stream);
+    qk_dispatch_kv<128>(c, qkv, q_norm, k_norm, rope, d, start_dev, start_host, M, q_out, k_dst,
+                        v_dst, stream);
   else
-    qk_dispatch_kv<64>(c, qkv, q_norm, k_norm, rope, layer, start_dev, start_host, M, q_out,
-                       k_cache, v_cache, stream);
+    qk_dispatch_kv<64>(c, qkv, q_norm, k_norm, rope, d, start_dev, start_host, M, q_out, k_dst,
+                       v_dst, stream);
   return cudaGetLastError();
+}
+
+cudaError_t launch_ring_store(const pf_config& c, const void* k_chunk, const void* v_chunk,
+                              int chunk_rows, int layer, const int* start_dev, int start_host, int M,
+                              void* k_cache, void* v_cache, cudaStream_t stream) {
+  const int words = c.head_dim * (c.kv_dtype == PF_KV_F32 ? 4 : 2) / 4;
+  const int rows = M * c.n_kv_heads;
+  return launch_pdl(ring_store_kernel, dim3((rows + 7) / 8), dim3(256), 0, stream,
+                    static_cast<const uint32_t*>(k_chunk), static_cast<const uint32_t*>(v_chunk),
+                    chunk_rows, M, c.n_kv_heads, words, layer, c.ring_capacity, c.sink_count,
+                    start_dev, start_host, static_cast<uint32_t*>(k_cache),
+                    static_cast<uint32_t*>(v_cache));
 }
 
 cudaError_t launch_embed(const float* E, const int* tokens, int M, int H, int vocab, float* x,

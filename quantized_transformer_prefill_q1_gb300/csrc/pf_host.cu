@@ -49,7 +49,10 @@ size_t kv_elem_bytes(int kv_dtype) { return kv_dtype == PF_KV_F32 ? 4 : 2; }
 
 // ------------------------------------------------------------------ workspace layout
 struct WsLayout {
-  size_t status, params, tokens, x, y, qkv, q, attn, act, logits, gemm, gemm_bytes, rope, total;
+  size_t status, params, tokens, x, y, qkv, q, attn, act, logits, gemm, gemm_bytes, rope;
+  size_t kchunk, vchunk;          // ring mode: the chunk's K / V rows [nkv][max_chunk][hd]
+  size_t attn_part, attn_part_bytes;  // split-KV partial results
+  size_t total;
 };
 
 WsLayout ws_layout(const pf_config& c) {
@@ -78,6 +81,11 @@ WsLayout ws_layout(const pf_config& c) {
   L.gemm_bytes = gemm_scratch_bytes(c.max_chunk, widest, GEMM_MAX_CTAS);
   L.gemm = take(L.gemm_bytes);
   L.rope = take(static_cast<size_t>(c.max_seq) * (hd / 2) * 2 * 4);
+  const size_t chunk_kv = c.ring_capacity > 0 ? C * c.n_kv_heads * hd * kv_elem_bytes(c.kv_dtype) : 0;
+  L.kchunk = take(chunk_kv);
+  L.vchunk = take(chunk_kv);
+  L.attn_part_bytes = attention_partial_bytes_max(c, GEMM_MAX_CTAS);
+  L.attn_part = take(L.attn_part_bytes);
   L.total = o;
   return L;
 }
@@ -233,6 +241,16 @@ pf_status check_cfg(const pf_config* c) {
   if (c->max_chunk <= 0 || c->max_chunk > 8192) return fail(PF_ERR_SHAPE, "max_chunk %d: 1..8192", c->max_chunk);
   if (!(c->eps >= 0.f) || !(c->final_eps >= 0.f) || !(c->rope_theta > 0.f))
     return fail(PF_ERR_INVALID_ARG, "eps / rope_theta");
+  if (c->ring_capacity < 0) return fail(PF_ERR_SHAPE, "ring_capacity %d", c->ring_capacity);
+  if (c->ring_capacity > 0) {
+    if (c->sink_count < 0 || c->sink_count >= c->ring_capacity)
+      return fail(PF_ERR_SHAPE, "ring cache: need 0 <= sink_count (%d) < ring_capacity (%d)", c->sink_count,
+                  c->ring_capacity);
+    if (!attention_tc_supported(*c))
+      return fail(PF_ERR_UNSUPPORTED, "ring cache: needs a 16-bit cache (bf16 / f16) and a GQA group dividing 128");
+  } else if (c->sink_count != 0) {
+    return fail(PF_ERR_SHAPE, "sink_count %d without a ring cache", c->sink_count);
+  }
   return PF_OK;
 }
 
@@ -306,14 +324,37 @@ pf_status enqueue_layer(pf_session* s, int l, float* x, int M, cudaStream_t st) 
                   [&] { return launch_rmsnorm(x, w.attn_norm, c.eps, M, H, y, st); }));
   // 2. fused QKV projection
   PF_TRY(enqueue_gemm(s, PF_K_GEMM_QKV, c.wfmt, EPI_STORE_F32, y, w.qkv, M, qkv_rows, H, qkv, st));
-  // 3. QK-norm + RoPE + KV store, then causal GQA attention over cache + chunk
+  // 3. QK-norm + RoPE + KV store, then causal GQA attention over cache + chunk. A ring cache
+  //    takes the chunk's K / V in the chunk buffers first (its later tokens may overwrite
+  //    slots its earlier tokens still see) and into the ring after the attention.
+  const bool ring = c.ring_capacity > 0;
+  void* kc = ring ? wsp<void>(s, s->L.kchunk) : s->k;
+  void* vc = ring ? wsp<void>(s, s->L.vchunk) : s->v;
   PF_TRY(launch_k(s, PF_K_QK_ROPE_KV, st, "qk_norm_rope_kv", [&] {
-    return launch_qk_norm_rope_kv(c, qkv, w.q_norm, w.k_norm, wsp<float>(s, s->L.rope), l,
-                                  start_dev, 0, M, q, s->k, s->v, st);
+    return launch_qk_norm_rope_kv(c, qkv, w.q_norm, w.k_norm, wsp<float>(s, s->L.rope), ring ? 0 : l,
+                                  ring ? c.max_chunk : c.max_seq, ring ? 0 : 1, start_dev, 0, M, q, kc,
+                                  vc, st);
   }));
-  PF_TRY(launch_k(s, PF_K_ATTENTION, st, "attention", [&] {
-    return launch_attention(c, q, s->k, s->v, l, start_dev, 0, M, attn, wsp<int>(s, s->L.status), st);
-  }));
+  AttnArgs aa{};
+  aa.c = &c;
+  aa.q = q;
+  aa.k_cache = s->k;
+  aa.v_cache = s->v;
+  aa.k_chunk = ring ? kc : nullptr;
+  aa.v_chunk = ring ? vc : nullptr;
+  aa.chunk_rows = c.max_chunk;
+  aa.layer = l;
+  aa.start_dev = start_dev;
+  aa.M = M;
+  aa.out = attn;
+  aa.n_split = attention_splits(c, M, std::min(s->sms, GEMM_MAX_CTAS));
+  aa.partial = wsp<float>(s, s->L.attn_part);
+  aa.status = wsp<int>(s, s->L.status);
+  PF_TRY(launch_k(s, PF_K_ATTENTION, st, "attention", [&] { return launch_attention(aa, st); }));
+  if (ring)
+    PF_TRY(launch_k(s, PF_K_QK_ROPE_KV, st, "ring store", [&] {
+      return launch_ring_store(c, kc, vc, c.max_chunk, l, start_dev, 0, M, s->k, s->v, st);
+    }));
   // 4. O projection + residual
   PF_TRY(enqueue_gemm(s, PF_K_GEMM_O, c.wfmt, EPI_RESID_ADD, attn, w.o_proj, M, H,
                       c.n_q_heads * hd, x, st));
@@ -427,7 +468,7 @@ const char* pf_status_name(int st) {
   }
 }
 
-int32_t pf_abi_version(void) { return 1; }
+int32_t pf_abi_version(void) { return 2; }
 
 size_t pf_packed_bytes(int32_t wfmt, int64_t N, int64_t K) {
   if ((wfmt != PF_W_Q1_G128 && wfmt != PF_W_INT4_AFFINE_G128) || N <= 0 || K <= 0 || K % GROUP)
@@ -522,7 +563,8 @@ pf_status pf_pack_weights_host(int32_t wfmt, const uint8_t* codes, const uint16_
 
 size_t pf_kv_bytes(const pf_config* c) {
   if (check_cfg(c) != PF_OK) return 0;
-  return static_cast<size_t>(c->n_layers) * c->n_kv_heads * c->max_seq * c->head_dim *
+  const int slots = c->ring_capacity > 0 ? c->ring_capacity : c->max_seq;
+  return static_cast<size_t>(c->n_layers) * c->n_kv_heads * slots * c->head_dim *
          kv_elem_bytes(c->kv_dtype);
 }
 
@@ -973,30 +1015,67 @@ pf_status pf_op_qk_norm_rope_kv(const pf_config* cfg, const float* qkv, const fl
                                 int32_t M, void* q, void* kc, void* vc, void* stream) {
   pf_status r = check_cfg(cfg);
   if (r != PF_OK) return r;
+  if (cfg->ring_capacity > 0) return fail(PF_ERR_UNSUPPORTED, "single-step KV store: linear caches only");
   if (!qkv || !rope || !q || !kc || !vc || (cfg->qk_norm && (!qn || !kn)))
     return fail(PF_ERR_INVALID_ARG, "NULL pointer");
   if (M <= 0 || layer < 0 || layer >= cfg->n_layers || start < 0 ||
       static_cast<int64_t>(start) + M > cfg->max_seq)
     return fail(PF_ERR_SHAPE, "M %d layer %d start %d", M, layer, start);
-  PF_CUDA(launch_qk_norm_rope_kv(*cfg, qkv, qn, kn, rope, layer, nullptr, start, M, q, kc, vc,
-                                 static_cast<cudaStream_t>(stream)),
+  PF_CUDA(launch_qk_norm_rope_kv(*cfg, qkv, qn, kn, rope, layer, cfg->max_seq, 1, nullptr, start, M, q,
+                                 kc, vc, static_cast<cudaStream_t>(stream)),
           "qk_norm_rope_kv");
+  return PF_OK;
+}
+
+static pf_status attention_op(const pf_config* cfg, const void* q, const void* kc, const void* vc,
+                              int32_t layer, int32_t start, int32_t M, int32_t n_split, void* scratch,
+                              size_t scratch_bytes, uint16_t* out, void* stream) {
+  pf_status r = check_cfg(cfg);
+  if (r != PF_OK) return r;
+  if (cfg->ring_capacity > 0) return fail(PF_ERR_UNSUPPORTED, "single-step attention: linear caches only");
+  if (!q || !kc || !vc || !out) return fail(PF_ERR_INVALID_ARG, "NULL pointer");
+  if (M <= 0 || layer < 0 || layer >= cfg->n_layers || start < 0 ||
+      static_cast<int64_t>(start) + M > cfg->max_seq)
+    return fail(PF_ERR_SHAPE, "M %d layer %d start %d", M, layer, start);
+  if (n_split > 1) {
+    if (!attention_tc_supported(*cfg)) return fail(PF_ERR_UNSUPPORTED, "split-KV attention needs a 16-bit cache");
+    if (n_split > 64) return fail(PF_ERR_INVALID_ARG, "n_split %d outside 1..64", n_split);
+    const size_t need = attention_partial_bytes(*cfg, M, n_split);
+    if (!scratch || scratch_bytes < need)
+      return fail(PF_ERR_WORKSPACE, "attention scratch %zu bytes, need %zu", scratch_bytes, need);
+    if (reinterpret_cast<uintptr_t>(scratch) & 15) return fail(PF_ERR_INVALID_ARG, "scratch must be 16-B aligned");
+  }
+  prepare_all();
+  AttnArgs a{};
+  a.c = cfg;
+  a.q = q;
+  a.k_cache = kc;
+  a.v_cache = vc;
+  a.layer = layer;
+  a.start_host = start;
+  a.M = M;
+  a.out = out;
+  a.n_split = n_split < 1 ? 1 : n_split;
+  a.partial = static_cast<float*>(scratch);
+  PF_CUDA(launch_attention(a, static_cast<cudaStream_t>(stream)), "attention");
   return PF_OK;
 }
 
 pf_status pf_op_attention(const pf_config* cfg, const void* q, const void* kc, const void* vc,
                           int32_t layer, int32_t start, int32_t M, uint16_t* out, void* stream) {
-  pf_status r = check_cfg(cfg);
-  if (r != PF_OK) return r;
-  if (!q || !kc || !vc || !out) return fail(PF_ERR_INVALID_ARG, "NULL pointer");
-  if (M <= 0 || layer < 0 || layer >= cfg->n_layers || start < 0 ||
-      static_cast<int64_t>(start) + M > cfg->max_seq)
-    return fail(PF_ERR_SHAPE, "M %d layer %d start %d", M, layer, start);
-  prepare_all();
-  PF_CUDA(launch_attention(*cfg, q, kc, vc, layer, nullptr, start, M, out, nullptr,
-                           static_cast<cudaStream_t>(stream)),
-          "attention");
-  return PF_OK;
+  return attention_op(cfg, q, kc, vc, layer, start, M, 1, nullptr, 0, out, stream);
+}
+
+size_t pf_attention_scratch_bytes(const pf_config* cfg, int32_t M, int32_t n_split) {
+  if (check_cfg(cfg) != PF_OK || M <= 0 || n_split < 1 || n_split > 64) return 0;
+  return attention_partial_bytes(*cfg, M, n_split);
+}
+
+pf_status pf_op_attention_split(const pf_config* cfg, const void* q, const void* kc, const void* vc,
+                                int32_t layer, int32_t start, int32_t M, int32_t n_split, void* scratch,
+                                size_t scratch_bytes, uint16_t* out, void* stream) {
+  if (n_split < 1) return fail(PF_ERR_INVALID_ARG, "n_split %d outside 1..64", n_split);
+  return attention_op(cfg, q, kc, vc, layer, start, M, n_split, scratch, scratch_bytes, out, stream);
 }
 
 pf_status pf_op_embed(const float* E, const int32_t* tokens, int32_t M, int32_t H, int32_t vocab,

@@ -85,13 +85,47 @@ cudaError_t launch_rmsnorm(const float* x, const float* w, float eps, int M, int
                            cudaStream_t stream);
 cudaError_t launch_dequant(int wfmt, const uint8_t* packed, int64_t N, int64_t K, void* w_f16,
                            cudaStream_t stream);
+// K and V go to row (kv_layer * nkv + kvh) * kv_rows + (kv_by_pos ? start + t : t) of
+// k_dst / v_dst: the cache slot of position start + t (kv_layer = layer, kv_rows = max_seq,
+// kv_by_pos = 1) or row t of the ring mode's chunk buffers (0, chunk rows, 0).
 cudaError_t launch_qk_norm_rope_kv(const pf_config& c, const float* qkv, const float* q_norm,
-                                   const float* k_norm, const float* rope, int layer,
-                                   const int* start_dev, int start_host, int M, void* q_out,
-                                   void* k_cache, void* v_cache, cudaStream_t stream);
-cudaError_t launch_attention(const pf_config& c, const void* q, const void* k_cache,
-                             const void* v_cache, int layer, const int* start_dev, int start_host,
-                             int M, void* out_f16, int* status, cudaStream_t stream);
+                                   const float* k_norm, const float* rope, int kv_layer, int kv_rows,
+                                   int kv_by_pos, const int* start_dev, int start_host, int M,
+                                   void* q_out, void* k_dst, void* v_dst, cudaStream_t stream);
+// Keys an attention launch reads. A linear cache holds position p of (layer, kv head) at row
+// (layer * nkv + kvh) * max_seq + p. A ring cache (ring_capacity R > 0, sink_count S) holds
+// position p at slot p (p < S) or S + (p - S) mod (R - S), row (layer * nkv + kvh) * R + slot;
+// the chunk's own keys are then read from the chunk buffers [nkv][chunk_rows][hd] that the
+// QK-norm / RoPE kernel wrote, and stored into the ring after the attention (launch_ring_store).
+struct AttnArgs {
+  const pf_config* c;
+  const void* q;        // [M][nq][hd] (bf16 for a bf16 cache, else f16)
+  const void* k_cache;
+  const void* v_cache;
+  const void* k_chunk;  // ring mode only
+  const void* v_chunk;
+  int chunk_rows;
+  int layer;
+  const int* start_dev;  // start position in device memory, or NULL to use start_host
+  int start_host;
+  int M;
+  void* out;            // f16 [M][nq * hd]
+  int n_split;          // key-tile parts (split-KV); 1 = none
+  float* partial;       // n_split > 1: attention_partial_bytes(c, M, n_split) bytes
+  int* status;
+};
+cudaError_t launch_attention(const AttnArgs& a, cudaStream_t stream);
+// Split-KV parts for a chunk of M rows on `sms` SMs (1 unless the chunk's CTAs fill less
+// than half of the SMs; only the tensor-core kernel splits).
+int attention_splits(const pf_config& c, int M, int sms);
+size_t attention_partial_bytes(const pf_config& c, int M, int n_split);
+// the largest partial buffer any M <= max_chunk needs on a GPU of at most max_sms SMs
+size_t attention_partial_bytes_max(const pf_config& c, int max_sms);
+// Ring cache: stores the chunk's K/V rows (chunk buffers) into the ring slots of `layer`
+// that the chunk's positions keep (sinks, and the last R - S positions).
+cudaError_t launch_ring_store(const pf_config& c, const void* k_chunk, const void* v_chunk,
+                              int chunk_rows, int layer, const int* start_dev, int start_host, int M,
+                              void* k_cache, void* v_cache, cudaStream_t stream);
 cudaError_t launch_embed(const float* E, const int* tokens, int M, int H, int vocab, float* x,
                          int* status, cudaStream_t stream);
 cudaError_t launch_lm_head(int wfmt, const float* x_row, const float* norm_w, float eps,
@@ -130,9 +164,7 @@ bool encode_tmap_out_2d(CUtensorMap* map, bool f32, const void* base, uint64_t i
                         uint32_t box_inner, uint32_t box_outer, int swizzle_bytes);
 bool attention_tc_supported(const pf_config& c);
 cudaError_t prepare_attention_tc_kernels();
-cudaError_t launch_attention_tc(const pf_config& c, const void* q, const void* k_cache,
-                                const void* v_cache, int layer, const int* start_dev, int start_host,
-                                int M, void* out, int* status, cudaStream_t stream);
+cudaError_t launch_attention_tc(const AttnArgs& a, cudaStream_t stream);
 cudaError_t prepare_gemm_kernels();
 cudaError_t prepare_attention_kernels();
 

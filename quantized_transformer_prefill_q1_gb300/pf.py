@@ -44,7 +44,8 @@ class pf_config(ctypes.Structure):
                 ("eps", ctypes.c_float), ("final_eps", ctypes.c_float),
                 ("qk_norm", ctypes.c_int32), ("wfmt", ctypes.c_int32),
                 ("kv_dtype", ctypes.c_int32), ("max_seq", ctypes.c_int32),
-                ("max_chunk", ctypes.c_int32)]
+                ("max_chunk", ctypes.c_int32), ("ring_capacity", ctypes.c_int32),
+                ("sink_count", ctypes.c_int32)]
 
 
 class pf_layer_weights(ctypes.Structure):
@@ -96,6 +97,9 @@ _SIGS = {
     "pf_op_qk_norm_rope_kv": ([ctypes.POINTER(pf_config), _VP, _VP, _VP, _VP, _I32, _I32, _I32,
                                _VP, _VP, _VP, _VP], _I32),
     "pf_op_attention": ([ctypes.POINTER(pf_config), _VP, _VP, _VP, _I32, _I32, _I32, _VP, _VP], _I32),
+    "pf_attention_scratch_bytes": ([ctypes.POINTER(pf_config), _I32, _I32], _SZ),
+    "pf_op_attention_split": ([ctypes.POINTER(pf_config), _VP, _VP, _VP, _I32, _I32, _I32, _I32, _VP, _SZ,
+                               _VP, _VP], _I32),
     "pf_op_embed": ([_VP, _VP, _I32, _I32, _I32, _VP, _VP, _VP], _I32),
     "pf_op_lm_head": ([_I32, _VP, _VP, _F, _VP, _I32, _I32, _VP, _VP], _I32),
     "pf_op_argmax": ([_VP, _I32, _I32, _I64, _VP, _VP], _I32),
@@ -150,7 +154,7 @@ def _stream(stream=None) -> Optional[int]:
 
 # ------------------------------------------------------------------ host-side calls
 def make_config(shape, max_chunk: int, n_layers: Optional[int] = None, max_seq: Optional[int] = None,
-                vocab: Optional[int] = None) -> pf_config:
+                vocab: Optional[int] = None, ring_capacity: int = 0, sink_count: int = 0) -> pf_config:
     return pf_config(hidden=shape.hidden, intermediate=shape.intermediate,
                      n_q_heads=shape.n_q_heads, n_kv_heads=shape.n_kv_heads,
                      head_dim=shape.head_dim,
@@ -159,7 +163,8 @@ def make_config(shape, max_chunk: int, n_layers: Optional[int] = None, max_seq: 
                      rope_theta=shape.rope_theta, eps=shape.eps, final_eps=shape.final_eps,
                      qk_norm=int(shape.qk_norm), wfmt=_WFMT[shape.wfmt],
                      kv_dtype=_KVDT[shape.kv_dtype],
-                     max_seq=shape.max_seq if max_seq is None else max_seq, max_chunk=max_chunk)
+                     max_seq=shape.max_seq if max_seq is None else max_seq, max_chunk=max_chunk,
+                     ring_capacity=ring_capacity, sink_count=sink_count)
 
 
 def pf_packed_bytes(wfmt: int, n: int, k: int) -> int:
@@ -236,6 +241,16 @@ def pf_op_attention(cfg, q, kc, vc, layer, start, m, out, stream=None):
                                 _ptr(out), _stream(stream)))
 
 
+def pf_attention_scratch_bytes(cfg, m, n_split):
+    return lib().pf_attention_scratch_bytes(ctypes.byref(cfg), m, n_split)
+
+
+def pf_op_attention_split(cfg, q, kc, vc, layer, start, m, n_split, scratch, out, stream=None):
+    check(lib().pf_op_attention_split(ctypes.byref(cfg), _ptr(q), _ptr(kc), _ptr(vc), layer, start, m,
+                                      n_split, _ptr(scratch), scratch.numel() * scratch.element_size(),
+                                      _ptr(out), _stream(stream)))
+
+
 def pf_op_argmax(x, rows, n, ld, out, stream=None):
     check(lib().pf_op_argmax(_ptr(x), rows, n, ld, _ptr(out), _stream(stream)))
 
@@ -264,7 +279,8 @@ class DeviceModel:
     torch tensors and fills a ``pf_model`` pointing at them."""
 
     def __init__(self, shape, layers: Sequence[Dict], extra: Optional[Dict] = None,
-                 max_chunk: int = 512, device: str = "cuda", max_seq: Optional[int] = None):
+                 max_chunk: int = 512, device: str = "cuda", max_seq: Optional[int] = None,
+                 ring_capacity: int = 0, sink_count: int = 0):
         import torch
         self.shape = shape
         self.keep: List = []
@@ -280,7 +296,8 @@ class DeviceModel:
 
         n = len(layers)
         self.cfg = make_config(shape, max_chunk, n_layers=n, max_seq=max_seq,
-                               vocab=shape.vocab if "lm_head" in extra else 0)
+                               vocab=shape.vocab if "lm_head" in extra else 0,
+                               ring_capacity=ring_capacity, sink_count=sink_count)
         self.layer_arr = (pf_layer_weights * n)()
         for i, w in enumerate(layers):
             lw = self.layer_arr[i]
@@ -312,13 +329,15 @@ class Session:
         self.dm = dm
         c = dm.cfg
         dt = getattr(torch, _KV_TORCH[c.kv_dtype])
-        shape = (c.n_layers, c.n_kv_heads, c.max_seq, c.head_dim)
+        slots = c.ring_capacity if c.ring_capacity > 0 else c.max_seq
+        shape = (c.n_layers, c.n_kv_heads, slots, c.head_dim)
         self.k = torch.empty(shape, dtype=dt, device="cuda")
         self.v = torch.empty(shape, dtype=dt, device="cuda")
         if kv_fill_bits is not None:  # sentinel bit pattern in every slot
             ib = torch.int32 if c.kv_dtype == KV_F32 else torch.int16
             self.k.view(ib).fill_(kv_fill_bits)
             self.v.view(ib).fill_(kv_fill_bits)
+        check(lib().pf_config_check(ctypes.byref(c)))
         wsb = lib().pf_workspace_bytes(ctypes.byref(c))
         if wsb == 0:
             raise PfError(2, lib().pf_last_error().decode())

@@ -1,6 +1,8 @@
 """Step-level parity: each libpf kernel (through the C ABI) against the CPU oracle on the
 same seeded inputs. Integer / byte / index work is compared bit-exactly; floating point
 within the tolerance stated (and derived) at each test."""
+import dataclasses
+
 import numpy as np
 import pytest
 
@@ -252,6 +254,58 @@ def test_attention_vs_oracle(shape, m, start, qscale):
     got = out.float().cpu().numpy().reshape(m, nq, hd)
     assert np.all(np.isfinite(got))
     assert rel_l2(got, ref) <= 5e-3
+
+
+@pytest.mark.parametrize("shape,m,start,n_split,qscale", [
+    (synth.LLAMA3_8B_INT4_LAYER, 1, 8192, 19, 1), (synth.LLAMA3_8B_INT4_LAYER, 1, 8192, 19, 8),
+    (synth.LLAMA3_8B_INT4_LAYER, 16, 8192, 9, 1), (synth.LLAMA3_8B_INT4_LAYER, 64, 5000, 4, 1),
+    # more parts than key tiles: most parts are empty and must not disturb the merge
+    (synth.QWEN3_8B_LAYER, 7, 100, 64, 1), (synth.QWEN3_8B_LAYER, 512, 0, 2, 1),
+    (dataclasses.replace(synth.TINY, kv_dtype="bf16"), 9, 40, 3, 1),
+])
+def test_attention_split_vs_oracle(shape, m, start, n_split, qscale):
+    # split-KV: the key tiles cut into n_split parts whose partial results are merged by a
+    # second kernel; the same result as the one-pass kernel up to f32 addition order
+    s = shape
+    nq, nkv, hd = s.n_q_heads, s.n_kv_heads, s.head_dim
+    cfg = pf.make_config(s, max_chunk=max(m, 16))
+    rng = synth.rng_for(18, m, start)
+    L = start + m
+    tdt = torch.bfloat16
+    q = torch.from_numpy(qscale * rng.standard_normal((m, nq, hd)).astype(np.float32)).to(tdt).cuda()
+    kc = torch.full((1, nkv, s.max_seq, hd), float("nan"), dtype=tdt, device="cuda")
+    vc = torch.full_like(kc, float("nan"))
+    kc[0, :, :L] = torch.from_numpy(rng.standard_normal((nkv, L, hd)).astype(np.float32)).to(tdt).cuda()
+    vc[0, :, :L] = torch.from_numpy(rng.standard_normal((nkv, L, hd)).astype(np.float32)).to(tdt).cuda()
+    nbytes = pf.pf_attention_scratch_bytes(cfg, m, n_split)
+    assert nbytes == n_split * m * nq * (hd + 2) * 4
+    scratch = torch.full((nbytes,), 0xFF, dtype=torch.uint8, device="cuda")  # NaN-filled partials
+    out = torch.full((m, nq * hd), float("nan"), dtype=torch.float16, device="cuda")
+    pf.pf_op_attention_split(cfg, q, kc, vc, 0, start, m, n_split, scratch, out)
+    one = torch.full_like(out, float("nan"))
+    pf.pf_op_attention(cfg, q, kc, vc, 0, start, m, one)
+    torch.cuda.synchronize()
+    ref = O.causal_gqa_attention(q.float().cpu().numpy(), kc[0].float().cpu().numpy(),
+                                 vc[0].float().cpu().numpy(), start)
+    got = out.float().cpu().numpy().reshape(m, nq, hd)
+    assert np.all(np.isfinite(got))
+    assert rel_l2(got, ref) <= 5e-3
+    assert rel_l2(got, one.float().cpu().numpy().reshape(m, nq, hd)) <= 5e-3
+
+
+def test_attention_split_rejects_bad_arguments():
+    s = synth.QWEN3_8B_LAYER
+    cfg = pf.make_config(s, max_chunk=16)
+    q = torch.zeros((4, s.n_q_heads, s.head_dim), dtype=torch.bfloat16, device="cuda")
+    kc = torch.zeros((1, s.n_kv_heads, s.max_seq, s.head_dim), dtype=torch.bfloat16, device="cuda")
+    out = torch.zeros((4, s.n_q_heads * s.head_dim), dtype=torch.float16, device="cuda")
+    small = torch.zeros(16, dtype=torch.uint8, device="cuda")
+    with pytest.raises(pf.PfError) as e:
+        pf.pf_op_attention_split(cfg, q, kc, kc, 0, 0, 4, 8, small, out)
+    assert e.value.status == 11  # PF_ERR_WORKSPACE
+    with pytest.raises(pf.PfError) as e:
+        pf.pf_op_attention_split(cfg, q, kc, kc, 0, 0, 4, 65, small, out)
+    assert e.value.status == 1
 
 
 # ----------------------------------------------------------------------------- embed / head

@@ -12,7 +12,8 @@ Checked element by element:
     oracle's only by the f16 GEMM operand rounding (about 2^-12 relative) and the two sides'
     rounding to bf16: every element within 1e-3 of its slot's largest magnitude plus one
     bf16 ulp of the oracle's value. Deeper layers carry the accumulated f16 / bf16 error of
-    the layers before them: relative L2 <= 2e-2 per slot, the per-layer hidden-state bound.
+    the layers before them: relative L2 <= 2e-2 over the layer's sampled slots (the per-layer
+    hidden-state bound), and <= 4e-2 for any single slot of 128 values.
 """
 import json
 import os
@@ -101,6 +102,8 @@ def test_full_stack_kv_slots_match_the_oracle(stack_run, name):
     ref = gold[name + "_slots"].astype(np.float64)
     assert got.shape == ref.shape
     for i, layer in enumerate(gold["kv_layers"]):
+        if layer != 0:
+            assert rel_l2(got[i], ref[i]) <= TOL, (name, int(layer))
         for h in range(ref.shape[1]):
             for j, pos in enumerate(gold["kv_positions"]):
                 g, r = got[i, h, j], ref[i, h, j]
@@ -108,4 +111,4 @@ def test_full_stack_kv_slots_match_the_oracle(stack_run, name):
                     bound = 1e-3 * np.abs(r).max() + bf16_ulp(r)
                     assert np.all(np.abs(g - r) <= bound), (name, int(layer), h, int(pos))
                 else:
-                    assert rel_l2(g, r) <= TOL, (name, int(layer), h, int(pos))
+                    assert rel_l2(g, r) <= 2 * TOL, (name, int(layer), h, int(pos))

@@ -143,6 +143,35 @@ def test_config_check(lib):
     assert lib.pf_workspace_bytes(ctypes.byref(good)) > 0
 
 
+def test_ring_config_check_and_sizes(lib):
+    # the ring / sink cache (turbospark-runtime prefill.rs batch-attention contract:
+    # ring_capacity, sink_count): 0 <= S < R, a 16-bit cache, and K/V of R slots per head
+    import dataclasses
+    s = synth.QWEN3_8B_LAYER
+    ring = pf.make_config(s, 512, ring_capacity=1024, sink_count=4)
+    assert lib.pf_config_check(ctypes.byref(ring)) == 0
+    assert lib.pf_kv_bytes(ctypes.byref(ring)) == 1 * 8 * 1024 * 128 * 2
+    linear = pf.make_config(s, 512)
+    # the ring adds the chunk's K / V rows to the workspace: 2 x 8 heads x 512 rows x 128 x 2 B
+    extra = lib.pf_workspace_bytes(ctypes.byref(ring)) - lib.pf_workspace_bytes(ctypes.byref(linear))
+    assert extra >= 2 * 8 * 512 * 128 * 2
+    for R, S, want in ((1024, 1024, 2), (1024, -1, 2), (0, 3, 2), (-5, 0, 2)):
+        bad = pf.make_config(s, 512, ring_capacity=R, sink_count=S)
+        assert lib.pf_config_check(ctypes.byref(bad)) == want, (R, S)
+    f32 = pf.make_config(dataclasses.replace(s, kv_dtype="f32"), 512, ring_capacity=64, sink_count=0)
+    assert lib.pf_config_check(ctypes.byref(f32)) == 8  # PF_ERR_UNSUPPORTED
+    assert lib.pf_abi_version() == 2
+
+
+def test_attention_scratch_bytes(lib):
+    s = synth.QWEN3_8B_LAYER
+    c = pf.make_config(s, 512)
+    assert lib.pf_attention_scratch_bytes(ctypes.byref(c), 16, 9) == 9 * 16 * 32 * (128 + 2) * 4
+    assert lib.pf_attention_scratch_bytes(ctypes.byref(c), 16, 1) == 0
+    assert lib.pf_attention_scratch_bytes(ctypes.byref(c), 16, 65) == 0
+    assert lib.pf_attention_scratch_bytes(ctypes.byref(c), 0, 2) == 0
+
+
 def test_rope_table_matches_definition(lib):
     t = pf.pf_rope_table_host(1e6, 128, 64)
     p, i = 37, 5
