@@ -14,13 +14,17 @@ cache stores values rounded to the cache's element type (f32, bf16 or f16) —
 storing into a typed cache is part of the method (the pages' cache is f16:
 metal_full_layer.rs, ``GpuKvCache``; the workloads here use f32 and bf16).
 
-Step order follows oxibonsai-kernels metal_prefill.rs ``encode_layer_prefill``
-(sections 1-7) and ``encode_full_forward_prefill`` (tail); the chunk loop follows
-turbospark-runtime families/llama/prefill.rs ``prefill_chunk_real_llama_dense``.
-The per-token decode restatement follows metal_full_layer.rs ``encode_layer_into``.
+The method, as the pages state it: a decoder layer of seven steps (pre-attention RMSNorm,
+fused QKV projection, per-head QK-norm + RoPE + KV store and causal GQA attention, O
+projection with the residual add, FFN RMSNorm, gate+up with SwiGLU, down projection with
+the residual add; oxibonsai-kernels 0.1.1 metal_prefill.rs, the prefill layer encoder,
+sections 1-7), a tail of final RMSNorm and LM head on the last position (the same page's
+full-forward prefill), and chunks of a prompt at consecutive start positions over one KV
+cache (turbospark-runtime 0.3.0 families/llama/prefill.rs, the dense chunk function). The
+per-token form below is the decode layer of oxibonsai-kernels 0.1.0 metal_full_layer.rs,
+written independently of the batched form.
 
-Where the pages are silent, each function states the reading it takes (numbered
-A1-A19 throughout this package's notes).
+Where the pages are silent, each function states in words the reading it takes.
 
 Parity status: every function below is pinned by ``tests/test_oracle_pins.py``
 except the composition of a full stack's logits, which has no worked example on
@@ -44,7 +48,7 @@ GROUP = 128
 def dequant_q1(bits: np.ndarray, scales: np.ndarray) -> np.ndarray:
     """Q1 weight -> float64 [N, K].
 
-    Reading A1/A2 (the pages name "Q1 block bytes" only — metal_full_layer.rs,
+    Reading taken (the pages name "Q1 block bytes" only — metal_full_layer.rs,
     ``FullForwardLayerParams``): bit j (LSB first) of byte b of row n is k = 8b+j;
     a set bit means +s, a clear bit -s; s is the f16 scale of group k // 128.
     """
@@ -59,7 +63,7 @@ def dequant_q1(bits: np.ndarray, scales: np.ndarray) -> np.ndarray:
 def dequant_int4(codes: np.ndarray, scales: np.ndarray, zeros: np.ndarray) -> np.ndarray:
     """INT4-affine weight -> float64 [N, K]: w = s * (q - z) per 128-group.
 
-    Reading A3 (turbospark-runtime prefill.rs only names an "INT4-affine" M-row
+    Reading taken (turbospark-runtime prefill.rs only names an "INT4-affine" M-row
     GEMM): q is the uint4 code (low nibble = even k), s and z the group's f16
     scale and zero point. Evaluated exactly in float64.
     """
@@ -86,7 +90,7 @@ def dequant(w: Dict) -> np.ndarray:
 def rmsnorm(x: np.ndarray, w: np.ndarray, eps: float) -> np.ndarray:
     """y_i = w_i * x_i / sqrt(mean_j(x_j^2) + eps) over the last axis, in float64.
 
-    Reading A6 (the kernel bodies behind ``dispatch_batched_rmsnorm`` /
+    Reading taken (the kernel bodies behind ``dispatch_batched_rmsnorm`` /
     ``rmsnorm_weighted_v2`` in metal_prefill.rs are not printed): the weight
     multiplies as-is (no implicit 1 + w).
     """
@@ -96,7 +100,8 @@ def rmsnorm(x: np.ndarray, w: np.ndarray, eps: float) -> np.ndarray:
 
 
 def rope_inv_freq(head_dim: int, theta: float) -> np.ndarray:
-    """inv_freq_i = theta^(-2i/head_dim), i = 0 .. head_dim/2 - 1 (reading A4)."""
+    """inv_freq_i = theta^(-2i/head_dim), i = 0 .. head_dim/2 - 1 (the standard RoPE ladder;
+    the pages only build per-position cos / sin tables)."""
     i = np.arange(head_dim // 2, dtype=np.float64)
     return np.power(float(theta), -2.0 * i / head_dim)
 
@@ -107,7 +112,7 @@ def rope_angles(positions: np.ndarray, head_dim: int, theta: float) -> np.ndarra
 
 
 def apply_rope(v: np.ndarray, angles: np.ndarray) -> np.ndarray:
-    """Rotate-half RoPE (reading A4: pair i is (i, i + hd/2)).
+    """Rotate-half RoPE (the pages do not state the pairing; reading: pair i is (i, i + hd/2)).
 
     v: [..., T, heads, hd]; angles: [T, hd/2]. out_a = a cos - b sin,
     out_b = b cos + a sin, where a = v[..., :hd/2], b = v[..., hd/2:].
@@ -131,7 +136,8 @@ def silu(g: np.ndarray) -> np.ndarray:
 def round_to_cache(x: np.ndarray, kv_dtype: str) -> np.ndarray:
     """Value stored in a KV cache of element type kv_dtype, returned as float32.
 
-    Round-to-nearest-even from float32 (reading A11). bf16 keeps the top 16 bits
+    Round-to-nearest-even from float32 (the storing rule is not printed; reading: IEEE
+    round to nearest even). bf16 keeps the top 16 bits
     of the float32 pattern after adding the RNE rounding bias.
     """
     x32 = np.asarray(x, dtype=np.float32)
@@ -153,13 +159,15 @@ def causal_gqa_attention(q: np.ndarray, k_cache: np.ndarray, v_cache: np.ndarray
 
     q: [T, nq, hd] (float64 or float32); k_cache, v_cache: [nkv, >=start+T, hd] holding
     the cache for this layer by absolute position. Query at position p sees keys 0..p
-    inclusive (reading A9: ``seq_len = pos + 1`` in metal_prefill.rs
+    inclusive (``seq_len = pos + 1`` in metal_prefill.rs
     ``encode_layer_prefill`` section 3). Scores use 1/sqrt(hd) (``inv_sqrt_hd``); q head h
-    reads kv head h // (nq/nkv) (``heads_per_group``, reading A7). Softmax subtracts the
+    reads kv head h // (nq/nkv) (``heads_per_group``: consecutive q heads share a kv head).
+    Softmax subtracts the
     row max and is evaluated in float64. Returns float64 [T, nq, hd].
 
     With a ring cache (turbospark-runtime prefill.rs ``BatchAttentionInputContract``:
-    ``ring_capacity``, ``sink_count``; reading A19) the query at p sees only the first
+    ``ring_capacity``, ``sink_count``; the contract only names them, and the reading taken
+    is the usual sliding window with attention sinks) the query at p sees only the first
     ``sinks`` positions and the ``window`` most recent positions up to p.
     """
     T, nq, hd = q.shape
@@ -264,12 +272,13 @@ class OracleModel:
             raise ValueError("chunk exceeds KV capacity")
         # 1. pre-attention RMSNorm
         y = rmsnorm(x, w["attn_norm"], s.eps).astype(np.float32)
-        # 2. fused QKV projection: rows Q | K | V, head-major (reading A10)
+        # 2. fused QKV projection: rows Q | K | V, head-major (the offsets the page uses)
         qkv = (y.astype(np.float64) @ w["qkv_w"].T).astype(np.float32)
         q = qkv[:, : nq * hd].reshape(T, nq, hd)
         k = qkv[:, nq * hd: (nq + nkv) * hd].reshape(T, nkv, hd)
         v = qkv[:, (nq + nkv) * hd:].reshape(T, nkv, hd)
-        # 3a. per-head QK RMSNorm over head_dim, same eps as the layer (reading A5)
+        # 3a. per-head QK RMSNorm over head_dim, same eps as the layer (the page passes the
+        #     layer eps to its fused QK-norm)
         if s.qk_norm:
             q = rmsnorm(q, w["q_norm"], s.eps).astype(np.float32)
             k = rmsnorm(k, w["k_norm"], s.eps).astype(np.float32)
@@ -297,7 +306,7 @@ class OracleModel:
         x = (x.astype(np.float64) + act.astype(np.float64) @ w["down_w"].T).astype(np.float32)
         return x
 
-    # ---- the ring cache's slots (reading A19) -----------------------------------------
+    # ---- the ring cache's slots (sinks first, then a cycle over the remaining slots) -----
     def ring_slot(self, p: int) -> int:
         """Slot of absolute position p in a ring cache of ring_capacity slots: the first
         sink_count positions keep slots 0 .. sink_count-1; later positions cycle through
@@ -337,7 +346,7 @@ class OracleModel:
         return logits, argmax_first(logits)
 
     def embed(self, tokens: np.ndarray) -> np.ndarray:
-        """x[t] = E[token_t] with no sqrt(hidden) scale (reading A13; turbospark-runtime
+        """x[t] = E[token_t] with no sqrt(hidden) scale (turbospark-runtime
         prefill.rs embeds each token at scale 1.0)."""
         tokens = np.asarray(tokens)
         if tokens.size and (tokens.min() < 0 or tokens.max() >= self.shape.vocab):
@@ -493,7 +502,8 @@ def decode_prompt(model: OracleModel, x: np.ndarray, start: int = 0) -> np.ndarr
 def argmax_first(logits: np.ndarray) -> np.ndarray:
     """Greedy selection (oxibonsai-kernels metal_prefill.rs: the argmax of the logits on
     the GPU, one token id per position). Per row of the last axis: the index of the largest
-    value; ties go to the lowest index (reading A15, the pages do not print the kernel);
+    value; ties go to the lowest index (the pages do not print the kernel; reading: the
+    first maximum);
     NaN is never chosen and a row without a number gives 0. Written out row by row."""
     x = np.asarray(logits, dtype=np.float64)
     rows = x.reshape(-1, x.shape[-1])
