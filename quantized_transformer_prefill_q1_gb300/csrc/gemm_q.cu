@@ -92,6 +92,9 @@ constexpr int smem_bytes() {
          NUM_EPI_WARPS * STG_BYTES + 256 /*barriers and flags*/;
 }
 static_assert(smem_bytes<PF_W_Q1_G128>() <= 232448, "Q1 GEMM shared memory");
+static_assert(ring_bytes<PF_W_Q1_G128>() >= NUM_EPI_WARPS * (BN / 32) * STG_BYTES &&
+                  ring_bytes<PF_W_INT4_AFFINE_G128>() >= NUM_EPI_WARPS * (BN / 32) * STG_BYTES,
+              "the last segment's epilogue stages every chunk in the operand ring");
 static_assert(smem_bytes<PF_W_INT4_AFFINE_G128>() <= 232448, "INT4 GEMM shared memory");
 
 // Bounded wait that ignores the abort flag (used while draining after an abort).
@@ -335,24 +338,30 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int q = warp & 3;           // TMEM lane quarter this warp may read
     const int et = threadIdx.x - 64;  // 0..127
     const uint32_t stg = stg0 + q * STG_BYTES;
-    // hands the staging tile (after its 32 x 32 values were written) to TMA
-    auto stage_out = [&](int x, int y) {
+    // hands a staging tile (after its 32 x 32 values were written) to TMA
+    auto stage_out = [&](uint32_t buf, int x, int y) {
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) {
         if (EPI == EPI_RESID_ADD)
-          tma_reduce_add_2d(&tmap_out, stg, x, y);
+          tma_reduce_add_2d(&tmap_out, buf, x, y);
         else
-          tma_store_2d(&tmap_out, stg, x, y);
+          tma_store_2d(&tmap_out, buf, x, y);
         bulk_commit();
       }
     };
-    // the previous TMA store has finished reading the staging tile
-    auto stage_free = [&]() {
-      if (lane == 0) bulk_wait_read0();
-      __syncwarp();
-    };
     for (int k = 0; k < rg.n; ++k) {
+      // The last segment's epilogue runs after the main loop has ended, when the operand ring
+      // is idle (its last MMA has completed): each 32-column chunk then gets a 4 KB buffer of
+      // its own there, so no chunk waits for the TMA read of the one before. Earlier segments
+      // share this warp's staging tile and wait for it.
+      const bool last = k == rg.n - 1;
+      auto stage_buf = [&](int c) {
+        if (last) return a_st + static_cast<uint32_t>(q * (BN / 32) + c) * STG_BYTES;
+        if (lane == 0) bulk_wait_read0();  // the previous TMA store has read the tile
+        __syncwarp();
+        return stg;
+      };
       const Segment sg = rg.at(plan, k);
       const int b = k & 1;
       const uint32_t use = static_cast<uint32_t>(k >> 1);
@@ -373,9 +382,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           uint32_t v[32];
           tmem_ld_32x32b_x32(tb + 32 * c, v);
           tmem_ld_wait();
-          stage_free();
-          stage_f32(stg, lane, v);
-          stage_out(sg.nt * BN + 32 * c, row0);
+          const uint32_t buf = stage_buf(c);
+          stage_f32(buf, lane, v);
+          stage_out(buf, sg.nt * BN + 32 * c, row0);
         }
       } else {
         // ---- a tile split across CTAs: hand the partial off, or finish the tile if last.
@@ -455,7 +464,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               add_partials(g, 4 * h + q2);
               add_partials(u, 4 * h + 2 + q2);
             }
-            stage_free();
+            const uint32_t buf = stage_buf(c);
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
               uint32_t pk[4];
@@ -467,9 +476,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     silu_mul(__uint_as_float(g[x + 1]), __uint_as_float(u[x + 1])));
                 pk[e] = *reinterpret_cast<const uint32_t*>(&hv);
               }
-              st_shared_v4(stg + lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4), pk[0], pk[1], pk[2], pk[3]);
+              st_shared_v4(buf + lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4), pk[0], pk[1], pk[2], pk[3]);
             }
-            stage_out(sg.nt * 128 + 64 * h + 32 * q2, row0);
+            stage_out(buf, sg.nt * 128 + 64 * h + 32 * q2, row0);
           }
         } else if (finish) {
 #pragma unroll 1
@@ -478,9 +487,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             tmem_ld_32x32b_x32(tb + 32 * c, v);
             tmem_ld_wait();
             if (!sg.whole && valid) add_partials(v, c);
-            stage_free();
-            stage_f32(stg, lane, v);
-            stage_out(sg.nt * BN + 32 * c, row0);
+            const uint32_t buf = stage_buf(c);
+            stage_f32(buf, lane, v);
+            stage_out(buf, sg.nt * BN + 32 * c, row0);
           }
         }
       }
