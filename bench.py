@@ -376,7 +376,9 @@ def run_reference(args):
     cores = os.cpu_count()
     emb = sample_embedding_rows(args.seed)
     s = dataclasses.replace(synth.QWEN3_8B_STACK, n_layers=1)
-    model = O.OracleModel(s, [synth.layer_weights(synth.QWEN3_8B_STACK, 0, args.seed)], None)
+    # as the 36-layer run uses it: each chunk's layer step dequantises that layer's weights
+    model = O.OracleModel(s, [synth.layer_weights(synth.QWEN3_8B_STACK, 0, args.seed)], None,
+                          cache_dequant=False)
     for c in range(3):  # the layer-0 cache of chunks 0..2 (untimed set-up)
         model.layer_forward(0, emb[c * CHUNK:(c + 1) * CHUNK], c * CHUNK)
     last = (PROMPT // CHUNK - 1) * CHUNK
