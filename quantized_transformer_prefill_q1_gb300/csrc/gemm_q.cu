@@ -105,7 +105,11 @@ __device__ __forceinline__ void mbar_wait_drain(uint32_t bar, uint32_t parity) {
   }
 }
 
-__device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.0f + __expf(-g)) * u; }
+// silu(g) * u = g / (1 + e^-g) * u. The exponent is capped at 80 so the denominator stays
+// below 2^126, where the fast division is within 2 ulp; for g < -80 the result is ~1e-33 * u.
+__device__ __forceinline__ float silu_mul(float g, float u) {
+  return __fdividef(g, 1.0f + __expf(fminf(-g, 80.0f))) * u;
+}
 
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
                                              uint32_t d) {
@@ -561,14 +565,18 @@ cudaError_t prepare_gemm_kernels() {
   return e;
 }
 
+bool gemm_store_accumulates(int wfmt, int M) { return M > gemv_max_m(wfmt) && M > SMALL_M_MAX; }
+
 cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t stream) {
   if (g.M <= gemv_max_m(g.wfmt)) return launch_gemv(g, stream);
   if (g.M <= SMALL_M_MAX) return launch_gemm_small(g, stream);
-  if (g.epilogue == EPI_STORE_F32 && g.max_ctas >= 0) {
-    // zero the output and accumulate every CTA's share by TMA reduce-add (no partial
+  if (g.epilogue == EPI_STORE_F32) {
+    // accumulate every CTA's share into a zeroed output by TMA reduce-add (no partial
     // hand-off, all SMs busy), as the residual form does
-    cudaError_t e = cudaMemsetAsync(g.out, 0, static_cast<size_t>(g.M) * g.N * sizeof(float), stream);
-    if (e != cudaSuccess) return e;
+    if (!g.out_zeroed) {
+      cudaError_t e = cudaMemsetAsync(g.out, 0, static_cast<size_t>(g.M) * g.N * sizeof(float), stream);
+      if (e != cudaSuccess) return e;
+    }
     GemmArgs r = g;
     r.epilogue = EPI_RESID_ADD;
     return launch_gemm(r, stream);

@@ -81,7 +81,11 @@ __device__ __forceinline__ bool bar_and_s(int id, int threads, bool pred) {
       : "memory");
   return r != 0;
 }
-__device__ __forceinline__ float silu_mul_s(float g, float u) { return g / (1.0f + __expf(-g)) * u; }
+// silu(g) * u = g / (1 + e^-g) * u. The exponent is capped at 80 so the denominator stays
+// below 2^126, where the fast division is within 2 ulp; for g < -80 the result is ~1e-33 * u.
+__device__ __forceinline__ float silu_mul_s(float g, float u) {
+  return __fdividef(g, 1.0f + __expf(fminf(-g, 80.0f))) * u;
+}
 
 template <int WFMT, int EPI, int NT>
 __global__ void __launch_bounds__(THREADS_S, 1)

@@ -182,7 +182,11 @@ struct Frag<PF_W_INT4_AFFINE_G128> {
   }
 };
 
-__device__ __forceinline__ float silu_mul_v(float g, float u) { return g / (1.0f + __expf(-g)) * u; }
+// silu(g) * u = g / (1 + e^-g) * u. The exponent is capped at 80 so the denominator stays
+// below 2^126, where the fast division is within 2 ulp; for g < -80 the result is ~1e-33 * u.
+__device__ __forceinline__ float silu_mul_v(float g, float u) {
+  return __fdividef(g, 1.0f + __expf(fminf(-g, 80.0f))) * u;
+}
 
 // Unit u = (16-row tile t, group g). Tile t covers, for SwiGLU, gate rows 8q .. 8q+7 and the
 // matching up rows of 128-row packed group b = t / 8 (q = t % 8: source rows 128 (b % 2) + 8q

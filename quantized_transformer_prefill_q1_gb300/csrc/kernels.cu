@@ -31,17 +31,28 @@ __device__ __forceinline__ float block_sum(float v, float* red) {
   return warp_sum(t);
 }
 
+// Row `row` of an optional f32 buffer [rows, 4 zero4] set to zero (a store-form GEMM that
+// follows accumulates its output there by reduce-add): issued with the norm, so the GEMM needs
+// no memset of its own between the two kernels.
+__device__ __forceinline__ void zero_row(float4* __restrict__ zero, int zero4, int row) {
+  if (zero == nullptr) return;
+  float4* z = zero + static_cast<size_t>(row) * zero4;
+  for (int i = threadIdx.x; i < zero4; i += blockDim.x) __stcg(z + i, make_float4(0.f, 0.f, 0.f, 0.f));
+}
+
 // ------------------------------------------------------------------ RMSNorm
 // oxibonsai-kernels metal_prefill.rs `encode_layer_prefill` sections 1 and 5
 // (`dispatch_batched_rmsnorm`): y[m, :] = x[m, :] * w / sqrt(mean(x[m, :]^2) + eps),
 // f32 in, f16 out (the next GEMM's operand). One CTA per row, 128-bit loads.
 __global__ void __launch_bounds__(256) rmsnorm_kernel(const float* __restrict__ x,
                                                       const float* __restrict__ w, float eps,
-                                                      int H, __half* __restrict__ y) {
+                                                      int H, __half* __restrict__ y,
+                                                      float4* __restrict__ zero, int zero4) {
   __shared__ float red[32];
   griddep_launch_dependents();
   griddep_wait();
   const int row = blockIdx.x;
+  zero_row(zero, zero4, row);
   const float4* xr = reinterpret_cast<const float4*>(x + static_cast<size_t>(row) * H);
   const float4* w4 = reinterpret_cast<const float4*>(w);
   __half2* yr = reinterpret_cast<__half2*>(y + static_cast<size_t>(row) * H);
@@ -66,7 +77,8 @@ __global__ void __launch_bounds__(256) rmsnorm_kernel(const float* __restrict__ 
 template <int NV>
 __global__ void __launch_bounds__(128) rmsnorm_reg_kernel(const float* __restrict__ x,
                                                           const float* __restrict__ w, float eps,
-                                                          int H, __half* __restrict__ y) {
+                                                          int H, __half* __restrict__ y,
+                                                          float4* __restrict__ zero, int zero4) {
   __shared__ float red[4];
   griddep_launch_dependents();
   // the norm weights never depend on the previous kernel: load them while it finishes
@@ -78,12 +90,12 @@ __global__ void __launch_bounds__(128) rmsnorm_reg_kernel(const float* __restric
   const int row = blockIdx.x;
   const float4* xr = reinterpret_cast<const float4*>(x + static_cast<size_t>(row) * H);
   float4 v[NV];
+#pragma unroll
+  for (int i = 0; i < NV; ++i) v[i] = xr[threadIdx.x + 128 * i];
+  zero_row(zero, zero4, row);
   float ss = 0.f;
 #pragma unroll
-  for (int i = 0; i < NV; ++i) {
-    v[i] = xr[threadIdx.x + 128 * i];
-    ss += v[i].x * v[i].x + v[i].y * v[i].y + v[i].z * v[i].z + v[i].w * v[i].w;
-  }
+  for (int i = 0; i < NV; ++i) ss += v[i].x * v[i].x + v[i].y * v[i].y + v[i].z * v[i].z + v[i].w * v[i].w;
   ss = warp_sum(ss);
   if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
   __syncthreads();
@@ -456,20 +468,27 @@ __global__ void wait_selftest_kernel(int* status, long long limit_ns, int arrive
 }  // namespace
 
 cudaError_t launch_rmsnorm(const float* x, const float* w, float eps, int M, int H, void* y,
-                           cudaStream_t stream) {
+                           cudaStream_t stream, float* zero, int zero_cols) {
   __half* yh = reinterpret_cast<__half*>(y);
+  if (zero != nullptr && (zero_cols % 4 != 0 || reinterpret_cast<uintptr_t>(zero) % 16 != 0))
+    return cudaErrorInvalidValue;
+  float4* z4 = reinterpret_cast<float4*>(zero);
+  const int zero4 = zero_cols / 4;
+  auto reg = [&](auto kernel) {
+    return launch_pdl(kernel, dim3(M), dim3(128), 0, stream, x, w, eps, H, yh, z4, zero4);
+  };
   if (H % 512 == 0) {
     switch (H / 512) {
-      case 1: return launch_pdl(rmsnorm_reg_kernel<1>, dim3(M), dim3(128), 0, stream, x, w, eps, H, yh);
-      case 2: return launch_pdl(rmsnorm_reg_kernel<2>, dim3(M), dim3(128), 0, stream, x, w, eps, H, yh);
-      case 4: return launch_pdl(rmsnorm_reg_kernel<4>, dim3(M), dim3(128), 0, stream, x, w, eps, H, yh);
-      case 8: return launch_pdl(rmsnorm_reg_kernel<8>, dim3(M), dim3(128), 0, stream, x, w, eps, H, yh);
-      case 16: return launch_pdl(rmsnorm_reg_kernel<16>, dim3(M), dim3(128), 0, stream, x, w, eps, H, yh);
+      case 1: return reg(rmsnorm_reg_kernel<1>);
+      case 2: return reg(rmsnorm_reg_kernel<2>);
+      case 4: return reg(rmsnorm_reg_kernel<4>);
+      case 8: return reg(rmsnorm_reg_kernel<8>);
+      case 16: return reg(rmsnorm_reg_kernel<16>);
       default: break;
     }
   }
   const int threads = H / 4 >= 256 ? 256 : ((H / 4 + 31) / 32) * 32;
-  return launch_pdl(rmsnorm_kernel, dim3(M), dim3(threads), 0, stream, x, w, eps, H, yh);
+  return launch_pdl(rmsnorm_kernel, dim3(M), dim3(threads), 0, stream, x, w, eps, H, yh, z4, zero4);
 }
 
 struct QkDst {

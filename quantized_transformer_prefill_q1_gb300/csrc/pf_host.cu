@@ -291,8 +291,9 @@ pf_status launch_k(pf_session* s, int cls, cudaStream_t st, const char* what, Ca
   } while (0)
 
 pf_status enqueue_gemm(pf_session* s, int cls, int wfmt, int epi, const void* a, const void* w,
-                       int M, int N, int K, void* out, cudaStream_t st) {
+                       int M, int N, int K, void* out, cudaStream_t st, bool out_zeroed = false) {
   GemmArgs g{};
+  g.out_zeroed = out_zeroed;
   g.wfmt = wfmt;
   g.epilogue = epi;
   g.a = a;
@@ -319,11 +320,15 @@ pf_status enqueue_layer(pf_session* s, int l, float* x, int M, cudaStream_t st) 
   void* q = wsp<void>(s, s->L.q);
   void* attn = wsp<void>(s, s->L.attn);
   void* act = wsp<void>(s, s->L.act);
-  // 1. pre-attention RMSNorm
-  PF_TRY(launch_k(s, PF_K_RMSNORM, st, "rmsnorm",
-                  [&] { return launch_rmsnorm(x, w.attn_norm, c.eps, M, H, y, st); }));
+  // 1. pre-attention RMSNorm; where the QKV GEMM accumulates into a zeroed output, the norm's
+  //    CTAs zero it (one qkv row each), so no memset breaks the launch chain
+  const bool zero_qkv = gemm_store_accumulates(c.wfmt, M);
+  PF_TRY(launch_k(s, PF_K_RMSNORM, st, "rmsnorm", [&] {
+    return launch_rmsnorm(x, w.attn_norm, c.eps, M, H, y, st, zero_qkv ? qkv : nullptr, qkv_rows);
+  }));
   // 2. fused QKV projection
-  PF_TRY(enqueue_gemm(s, PF_K_GEMM_QKV, c.wfmt, EPI_STORE_F32, y, w.qkv, M, qkv_rows, H, qkv, st));
+  PF_TRY(enqueue_gemm(s, PF_K_GEMM_QKV, c.wfmt, EPI_STORE_F32, y, w.qkv, M, qkv_rows, H, qkv, st,
+                      zero_qkv));
   // 3. QK-norm + RoPE + KV store, then causal GQA attention over cache + chunk. A ring cache
   //    takes the chunk's K / V in the chunk buffers first (its later tokens may overwrite
   //    slots its earlier tokens still see) and into the ring after the attention.

@@ -62,8 +62,13 @@ struct GemmArgs {
   int max_ctas;         // 1..GEMM_MAX_CTAS; the scratch layout depends on it
   void* scratch;        // gemm_scratch_bytes(M, N, max_ctas); its counters zero before the launch
   int* status;          // may be NULL
+  bool out_zeroed;      // store form: the caller has set out to zero (gemm_store_accumulates)
 };
 cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t stream);
+// Whether launch_gemm's store form at this M accumulates into a zeroed output (TMA
+// reduce-add from every CTA's share). It zeroes the output itself first unless
+// GemmArgs::out_zeroed says the caller already has.
+bool gemm_store_accumulates(int wfmt, int M);
 // M <= SMALL_M_MAX: the weight rows are the MMA's M side (gemm_small.cu); launch_gemm routes
 cudaError_t launch_gemm_small(const GemmArgs& g, cudaStream_t stream);
 cudaError_t prepare_gemm_small_kernels();
@@ -81,8 +86,10 @@ bool encode_tmap_f16_2d(CUtensorMap* map, const void* base, uint64_t inner, uint
 constexpr int GEMM_MAX_CTAS = 160;
 size_t gemm_scratch_bytes(int M, int N, int max_ctas);
 
+// y_f16 [M, H] = RMSNorm of x [M, H]; with `zero` (16-B aligned, zero_cols % 4 == 0) each
+// row's CTA also sets row m of the f32 buffer zero [M, zero_cols] to 0.
 cudaError_t launch_rmsnorm(const float* x, const float* w, float eps, int M, int H, void* y_f16,
-                           cudaStream_t stream);
+                           cudaStream_t stream, float* zero = nullptr, int zero_cols = 0);
 cudaError_t launch_dequant(int wfmt, const uint8_t* packed, int64_t N, int64_t K, void* w_f16,
                            cudaStream_t stream);
 // K and V go to row (kv_layer * nkv + kvh) * kv_rows + (kv_by_pos ? start + t : t) of
