@@ -171,12 +171,32 @@ __device__ __forceinline__ void stage_f32(uint32_t stg, int r, const uint32_t (&
                  v[4 * j + 3]);
 }
 
+// SwiGLU chunk of one epilogue warp: silu(g) * u of 32 rows x 32 columns, f16 in the 64-B
+// swizzle of the output box (row r at r * 64, unit j at (j ^ ((r / 2) % 4)) * 16).
+__device__ __forceinline__ void stage_swiglu(uint32_t buf, int r, const uint32_t (&g)[32],
+                                             const uint32_t (&u)[32]) {
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    uint32_t pk[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int x = 8 * j + 2 * e;
+      const __half2 hv =
+          __floats2half2_rn(silu_mul(__uint_as_float(g[x]), __uint_as_float(u[x])),
+                            silu_mul(__uint_as_float(g[x + 1]), __uint_as_float(u[x + 1])));
+      pk[e] = *reinterpret_cast<const uint32_t*>(&hv);
+    }
+    st_shared_v4(buf + r * 64 + ((j ^ ((r >> 1) & 3)) << 4), pk[0], pk[1], pk[2], pk[3]);
+  }
+}
+
 template <int WFMT, int EPI>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_q_kernel(const __grid_constant__ CUtensorMap tmap_a,
                   const __grid_constant__ CUtensorMap tmap_out, const uint8_t* __restrict__ wpk,
                   int M, int N, int K, Plan plan, float* __restrict__ scratch,
-                  int* __restrict__ counters, int* __restrict__ status) {
+                  int* __restrict__ counters, int* __restrict__ status,
+                  float4* __restrict__ side_zero, long long side_zero4) {
   using F = Fmt<WFMT>;
   constexpr int S = F::STAGES;
   extern __shared__ uint8_t smem_raw[];
@@ -341,6 +361,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     griddep_wait();  // out / scratch / counters are shared with the previous kernels
     const int q = warp & 3;           // TMEM lane quarter this warp may read
     const int et = threadIdx.x - 64;  // 0..127
+    if (side_zero != nullptr) {
+      // idle until the first accumulator is ready: clear this CTA's share of the buffer a
+      // later kernel accumulates into
+      const long long per = (side_zero4 + gridDim.x - 1) / gridDim.x;
+      const long long z1 = min(side_zero4, per * (blockIdx.x + 1));
+      for (long long i = per * blockIdx.x + et; i < z1; i += EPI_THREADS)
+        __stcg(side_zero + i, make_float4(0.f, 0.f, 0.f, 0.f));
+    }
     const uint32_t stg = stg0 + q * STG_BYTES;
     // hands a staging tile (after its 32 x 32 values were written) to TMA
     auto stage_out = [&](uint32_t buf, int x, int y) {
@@ -454,9 +482,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         };
 
         if (finish && EPI == EPI_SWIGLU) {
-          // each 128 columns of the tile: 64 gate columns, then the 64 matching up columns;
-          // out f16 32 x 32 staged in the 64-B swizzle (row r at r * 64, unit j at
-          // (j ^ ((r / 2) % 4)) * 16)
+          // each 128 columns of the tile: 64 gate columns, then the 64 matching up columns
 #pragma unroll 1
           for (int c = 0; c < 4; ++c) {
             const int h = c >> 1, q2 = c & 1;
@@ -469,19 +495,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               add_partials(u, 4 * h + 2 + q2);
             }
             const uint32_t buf = stage_buf(c);
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              uint32_t pk[4];
-#pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const int x = 8 * j + 2 * e;
-                const __half2 hv = __floats2half2_rn(
-                    silu_mul(__uint_as_float(g[x]), __uint_as_float(u[x])),
-                    silu_mul(__uint_as_float(g[x + 1]), __uint_as_float(u[x + 1])));
-                pk[e] = *reinterpret_cast<const uint32_t*>(&hv);
-              }
-              st_shared_v4(buf + lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4), pk[0], pk[1], pk[2], pk[3]);
-            }
+            stage_swiglu(buf, lane, g, u);
             stage_out(buf, sg.nt * 128 + 64 * h + 32 * q2, row0);
           }
         } else if (finish) {
@@ -532,7 +546,8 @@ cudaError_t launch_t(const GemmArgs& g, const CUtensorMap& ta, const CUtensorMap
   int* counters =
       scratch ? reinterpret_cast<int*>(scratch + static_cast<size_t>(2) * g.max_ctas * SLOT_FLOATS) : nullptr;
   return launch_pdl(gemm_q_kernel<WFMT, EPI>, dim3(p.ctas), dim3(NUM_THREADS), smem, stream, ta, to,
-                    g.w, g.M, g.N, g.K, p, scratch, counters, g.status);
+                    g.w, g.M, g.N, g.K, p, scratch, counters, g.status,
+                    reinterpret_cast<float4*>(g.side_zero), static_cast<long long>(g.side_zero_bytes / 16));
 }
 
 }  // namespace
@@ -568,6 +583,10 @@ cudaError_t prepare_gemm_kernels() {
 bool gemm_store_accumulates(int wfmt, int M) { return M > gemv_max_m(wfmt) && M > SMALL_M_MAX; }
 
 cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t stream) {
+  if (g.side_zero != nullptr && (g.M <= SMALL_M_MAX || g.M <= gemv_max_m(g.wfmt) ||
+                                 g.side_zero_bytes % 16 != 0 ||
+                                 reinterpret_cast<uintptr_t>(g.side_zero) % 16 != 0))
+    return cudaErrorInvalidValue;
   if (g.M <= gemv_max_m(g.wfmt)) return launch_gemv(g, stream);
   if (g.M <= SMALL_M_MAX) return launch_gemm_small(g, stream);
   if (g.epilogue == EPI_STORE_F32) {

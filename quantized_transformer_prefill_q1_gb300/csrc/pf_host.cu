@@ -291,9 +291,12 @@ pf_status launch_k(pf_session* s, int cls, cudaStream_t st, const char* what, Ca
   } while (0)
 
 pf_status enqueue_gemm(pf_session* s, int cls, int wfmt, int epi, const void* a, const void* w,
-                       int M, int N, int K, void* out, cudaStream_t st, bool out_zeroed = false) {
+                       int M, int N, int K, void* out, cudaStream_t st, bool out_zeroed = false,
+                       void* side_zero = nullptr, size_t side_zero_bytes = 0) {
   GemmArgs g{};
   g.out_zeroed = out_zeroed;
+  g.side_zero = side_zero;
+  g.side_zero_bytes = side_zero_bytes;
   g.wfmt = wfmt;
   g.epilogue = epi;
   g.a = a;
@@ -308,8 +311,12 @@ pf_status enqueue_gemm(pf_session* s, int cls, int wfmt, int epi, const void* a,
   return launch_k(s, cls, st, "gemm launch", [&] { return launch_gemm(g, st); });
 }
 
-// metal_prefill.rs encode_layer_prefill, sections 1-7, on x [M, H] (in place).
-pf_status enqueue_layer(pf_session* s, int l, float* x, int M, cudaStream_t st) {
+// metal_prefill.rs encode_layer_prefill, sections 1-7, on x [M, H] (in place). Where the
+// QKV GEMM accumulates into a zeroed qkv buffer (gemm_store_accumulates), `qkv_zeroed` says
+// an earlier kernel has zeroed it already, and `zero_next_qkv` has this layer's gate_up GEMM
+// zero it for the next layer (its epilogue warps are idle during the main loop).
+pf_status enqueue_layer(pf_session* s, int l, float* x, int M, cudaStream_t st, bool qkv_zeroed,
+                        bool zero_next_qkv) {
   const pf_config& c = s->model.cfg;
   const pf_layer_weights& w = s->layers[l];
   const int H = c.hidden, I = c.intermediate, hd = c.head_dim;
@@ -322,13 +329,14 @@ pf_status enqueue_layer(pf_session* s, int l, float* x, int M, cudaStream_t st) 
   void* act = wsp<void>(s, s->L.act);
   // 1. pre-attention RMSNorm; where the QKV GEMM accumulates into a zeroed output, the norm's
   //    CTAs zero it (one qkv row each), so no memset breaks the launch chain
-  const bool zero_qkv = gemm_store_accumulates(c.wfmt, M);
+  const bool accum = gemm_store_accumulates(c.wfmt, M);
+  const bool zero_qkv = accum && !qkv_zeroed;
   PF_TRY(launch_k(s, PF_K_RMSNORM, st, "rmsnorm", [&] {
     return launch_rmsnorm(x, w.attn_norm, c.eps, M, H, y, st, zero_qkv ? qkv : nullptr, qkv_rows);
   }));
   // 2. fused QKV projection
   PF_TRY(enqueue_gemm(s, PF_K_GEMM_QKV, c.wfmt, EPI_STORE_F32, y, w.qkv, M, qkv_rows, H, qkv, st,
-                      zero_qkv));
+                      accum));
   // 3. QK-norm + RoPE + KV store, then causal GQA attention over cache + chunk. A ring cache
   //    takes the chunk's K / V in the chunk buffers first (its later tokens may overwrite
   //    slots its earlier tokens still see) and into the ring after the attention.
@@ -367,7 +375,10 @@ pf_status enqueue_layer(pf_session* s, int l, float* x, int M, cudaStream_t st) 
   PF_TRY(launch_k(s, PF_K_RMSNORM, st, "rmsnorm",
                   [&] { return launch_rmsnorm(x, w.ffn_norm, c.eps, M, H, y, st); }));
   // 6. gate_up + SwiGLU
-  PF_TRY(enqueue_gemm(s, PF_K_GEMM_GATE_UP, c.wfmt, EPI_SWIGLU, y, w.gate_up, M, 2 * I, H, act, st));
+  const bool zero_next = accum && zero_next_qkv;
+  PF_TRY(enqueue_gemm(s, PF_K_GEMM_GATE_UP, c.wfmt, EPI_SWIGLU, y, w.gate_up, M, 2 * I, H, act, st,
+                      false, zero_next ? qkv : nullptr,
+                      zero_next ? static_cast<size_t>(M) * qkv_rows * sizeof(float) : 0));
   // 7. down projection + residual
   PF_TRY(enqueue_gemm(s, PF_K_GEMM_DOWN, c.wfmt, EPI_RESID_ADD, act, w.down, M, H, I, x, st));
   return PF_OK;
@@ -382,7 +393,7 @@ pf_status enqueue_chunk(pf_session* s, float* x, int M, const int* tokens_dev, f
       return launch_embed(s->model.embed, tokens_dev, M, c.hidden, c.vocab, x,
                           wsp<int>(s, s->L.status), st);
     }));
-  for (int l = 0; l < c.n_layers; ++l) PF_TRY(enqueue_layer(s, l, x, M, st));
+  for (int l = 0; l < c.n_layers; ++l) PF_TRY(enqueue_layer(s, l, x, M, st, l > 0, l + 1 < c.n_layers));
   if (logits)
     PF_TRY(launch_k(s, PF_K_LM_HEAD, st, "lm_head", [&] {
       return launch_lm_head(c.wfmt, x + static_cast<size_t>(M - 1) * c.hidden, s->model.final_norm,
@@ -868,7 +879,7 @@ pf_status pf_layer_forward(pf_session* s, int32_t layer, float* x_dev, int32_t M
   if (r != PF_OK) return r;
   GraphKey key{M, x_dev, nullptr, nullptr, layer};
   return run_maybe_graph(s, key, st,
-                         [&](cudaStream_t rs) { return enqueue_layer(s, layer, x_dev, M, rs); });
+                         [&](cudaStream_t rs) { return enqueue_layer(s, layer, x_dev, M, rs, false, false); });
 }
 
 pf_status pf_prefill_tokens_host(pf_session* s, const int32_t* tokens_host, int32_t M, int32_t start_pos,

@@ -63,6 +63,10 @@ struct GemmArgs {
   void* scratch;        // gemm_scratch_bytes(M, N, max_ctas); its counters zero before the launch
   int* status;          // may be NULL
   bool out_zeroed;      // store form: the caller has set out to zero (gemm_store_accumulates)
+  // optional (M > SMALL_M_MAX only): a buffer that the CTAs' epilogue warps set to zero while
+  // the main loop runs (the accumulator of a later store-form GEMM); 16-B aligned and sized
+  void* side_zero;
+  size_t side_zero_bytes;
 };
 cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t stream);
 // Whether launch_gemm's store form at this M accumulates into a zeroed output (TMA
