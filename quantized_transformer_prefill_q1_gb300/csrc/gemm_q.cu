@@ -34,6 +34,7 @@
 #include <cuda_fp16.h>
 
 #include <algorithm>
+#include <cstdlib>
 
 #include "dequant.cuh"
 #include "ptx.cuh"
@@ -55,7 +56,6 @@ constexpr int EPI_THREADS = NUM_EPI_WARPS * 32;
 constexpr int NUM_THREADS = 32 * (2 + NUM_EPI_WARPS + NUM_DQ_WARPS);  // 448
 constexpr int FIRST_DQ_WARP = 2 + NUM_EPI_WARPS;
 constexpr int A_STAGE = BM * BK * 2;  // 16 KB
-constexpr int B_STAGE = BN * BK * 2;  // 32 KB
 constexpr int STG_BYTES = 32 * 32 * 4;  // per epilogue warp: 32 rows x 32 f32
 constexpr int TMEM_COLS = 512;          // two accumulators of 256 f32 columns
 constexpr size_t SLOT_FLOATS = static_cast<size_t>(BM) * BN;  // one partial tile
@@ -82,20 +82,30 @@ struct Fmt<PF_W_INT4_AFFINE_G128> {
   static constexpr int STAGES = 3;
 };
 
-template <int WFMT>
-constexpr int ring_bytes() {
-  return Fmt<WFMT>::STAGES * (A_STAGE + B_STAGE + Fmt<WFMT>::P_STAGE);
-}
-template <int WFMT>
-constexpr int smem_bytes() {
-  return 1024 /*alignment*/ + (ring_bytes<WFMT>() + 1023) / 1024 * 1024 +
-         NUM_EPI_WARPS * STG_BYTES + 256 /*barriers and flags*/;
-}
-static_assert(smem_bytes<PF_W_Q1_G128>() <= 232448, "Q1 GEMM shared memory");
-static_assert(ring_bytes<PF_W_Q1_G128>() >= NUM_EPI_WARPS * (BN / 32) * STG_BYTES &&
-                  ring_bytes<PF_W_INT4_AFFINE_G128>() >= NUM_EPI_WARPS * (BN / 32) * STG_BYTES,
-              "the last segment's epilogue stages every chunk in the operand ring");
-static_assert(smem_bytes<PF_W_INT4_AFFINE_G128>() <= 232448, "INT4 GEMM shared memory");
+// One CTA per tile (PAIR = false): 128 tokens x 256 weight rows, the CTA dequantises all
+// 256 rows. A CTA pair (PAIR = true, cta_group::2): 256 tokens x 256 weight rows per pair,
+// each CTA loads 128 token rows and dequantises 128 weight rows (its half of B), so a CTA
+// moves about two thirds of the shared-memory bytes per k-block (A 16 KB + B half 16 KB read
+// by the MMA, 16 KB of dequantised B written, instead of 16 + 32 + 32 KB), and the smaller
+// stages allow a deeper ring.
+template <int WFMT, bool PAIR>
+struct Cfg {
+  using F = Fmt<WFMT>;
+  static constexpr int B_ROWS = PAIR ? BN / 2 : BN;  // weight rows dequantised per CTA
+  static constexpr int TILE_M = PAIR ? 2 * BM : BM;  // tokens per tile
+  static constexpr int B_STAGE = B_ROWS * BK * 2;
+  // packed bytes per stage: the rows' codes of one 64-wide k-block, then their scales
+  // (and zeros)
+  static constexpr int P_STAGE = PAIR ? B_ROWS * (WFMT == PF_W_Q1_G128 ? 8 + 2 : 32 + 4) : F::P_STAGE;
+  static constexpr int STAGES = PAIR ? (WFMT == PF_W_Q1_G128 ? 6 : 5) : F::STAGES;
+  static constexpr int RING = STAGES * (A_STAGE + B_STAGE + P_STAGE);
+  static constexpr int SMEM = 1024 /*alignment*/ + (RING + 1023) / 1024 * 1024 + NUM_EPI_WARPS * STG_BYTES +
+                              256 /*barriers and flags*/;
+  static_assert(SMEM <= 232448, "GEMM shared memory");
+  static_assert(RING >= NUM_EPI_WARPS * (BN / 32) * STG_BYTES,
+                "the last segment's epilogue stages every chunk in the operand ring");
+  static_assert(P_STAGE % 16 == 0 && B_STAGE % 1024 == 0, "stage alignment");
+};
 
 // Bounded wait that ignores the abort flag (used while draining after an abort).
 __device__ __forceinline__ void mbar_wait_drain(uint32_t bar, uint32_t parity) {
@@ -162,6 +172,30 @@ __device__ __forceinline__ void dequant_row_smem(const uint8_t* p, int r, uint32
   }
 }
 
+// Pair form: thread (row r of the CTA's 128 weight rows, k half h) -> 4 16-B chunks of the
+// 128 x 64 B half tile (same swizzled layout). Stage layout: codes [128 rows][8 (Q1) or 32
+// (INT4) bytes], then scales [128] (and INT4 zeros [128]) as f16.
+template <int WFMT>
+__device__ __forceinline__ void dequant_half_row_pair(const uint8_t* p, int r, int h, uint32_t b_tile) {
+  const uint32_t row_base = b_tile + (r >> 3) * 1024 + (r & 7) * 128;
+  uint32_t w[16];
+  if (WFMT == PF_W_Q1_G128) {
+    const uint32_t Z = reinterpret_cast<const uint32_t*>(p + r * 8)[h];
+    const uint32_t s16 = reinterpret_cast<const uint16_t*>(p + (BN / 2) * 8)[r];
+    dq_q1_32(Z, s16 | (s16 << 16), w);
+  } else {
+    const uint4 q = reinterpret_cast<const uint4*>(p + r * 32)[h];
+    const uint16_t s16 = reinterpret_cast<const uint16_t*>(p + (BN / 2) * 32)[r];
+    const uint16_t z16 = reinterpret_cast<const uint16_t*>(p + (BN / 2) * 34)[r];
+    dq_i4_32(q, __half2half2(__ushort_as_half(s16)), __half2half2(__ushort_as_half(z16)), w);
+  }
+#pragma unroll
+  for (int c4 = 0; c4 < 4; ++c4) {
+    const int c = 4 * h + c4;
+    st_shared_v4(row_base + ((c ^ (r & 7)) << 4), w[4 * c4], w[4 * c4 + 1], w[4 * c4 + 2], w[4 * c4 + 3]);
+  }
+}
+
 // Staging tile of one epilogue warp, f32 32 x 32 in the TMA 128-B swizzle: row r at
 // r * 128, 16-B unit j at (j ^ (r % 8)) * 16 (a warp's store of unit j hits all banks).
 __device__ __forceinline__ void stage_f32(uint32_t stg, int r, const uint32_t (&v)[32]) {
@@ -190,7 +224,7 @@ __device__ __forceinline__ void stage_swiglu(uint32_t buf, int r, const uint32_t
   }
 }
 
-template <int WFMT, int EPI>
+template <int WFMT, int EPI, bool PAIR>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_q_kernel(const __grid_constant__ CUtensorMap tmap_a,
                   const __grid_constant__ CUtensorMap tmap_out, const uint8_t* __restrict__ wpk,
@@ -198,7 +232,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                   int* __restrict__ counters, int* __restrict__ status,
                   float4* __restrict__ side_zero, long long side_zero4) {
   using F = Fmt<WFMT>;
-  constexpr int S = F::STAGES;
+  using C = Cfg<WFMT, PAIR>;
+  constexpr int S = C::STAGES;
+  constexpr int B_STAGE = C::B_STAGE;
+  constexpr int P_STAGE = C::P_STAGE;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -207,7 +244,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const uint32_t b_st = a_st + S * A_STAGE;
   const uint32_t p_st = b_st + S * B_STAGE;
   const uint8_t* p_gen = gbase + (p_st - base);
-  const uint32_t stg0 = base + (ring_bytes<WFMT>() + 1023) / 1024 * 1024;
+  const uint32_t stg0 = base + (C::RING + 1023) / 1024 * 1024;
   const uint32_t bar0 = stg0 + NUM_EPI_WARPS * STG_BYTES;
   // barriers: full[S], bfull[S], empty[S], acc_full[2], acc_empty[2], drain; then flags
   auto full = [&](int s) { return bar0 + 8u * s; };
@@ -222,17 +259,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  // pair form: `rank` 0 issues the MMAs; the plan's unit is the pair
+  const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
+  const int unit = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
   griddep_launch_dependents();
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(full(s), 1);
-      mbar_init(bfull(s), DQ_THREADS);
+      // pair: one arrival per dequantising warp of both CTAs, on the even CTA's barrier
+      mbar_init(bfull(s), PAIR ? 2 * NUM_DQ_WARPS : DQ_THREADS);
       mbar_init(empty(s), 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(acc_full(b), 1);
-      mbar_init(acc_empty(b), EPI_THREADS);
+      mbar_init(acc_empty(b), PAIR ? 2 * NUM_EPI_WARPS : EPI_THREADS);
     }
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
@@ -241,18 +282,42 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   }
   if (warp == 1) {
     __syncwarp();
-    tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
-    tmem_relinquish();
+    if (PAIR) {
+      tmem_alloc_pair(smem_u32(tmem_slot), TMEM_COLS);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
-  __syncthreads();
+  if (PAIR)
+    cluster_sync_all();  // both CTAs' barriers exist before either arrives on the other's
+  else
+    __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   // Only the activation tiles and the epilogue's global accesses depend on the previous
   // kernel in the stream (griddep_wait below); the packed weights do not, so the producer
   // issues the first stages' weight copies before waiting for it.
   const int G = K / GROUP;
-  const Range rg(plan, blockIdx.x);
+  const Range rg(plan, unit);
+  const int a_row = static_cast<int>(rank) * BM;  // this CTA's first token row of a tile
+  // the stage's packed copies: pair CTAs take their 128 weight rows' codes and scales (zeros)
+  auto load_packed = [&](int s, const uint8_t* chunk, int kb) {
+    const uint32_t dst = p_st + s * P_STAGE;
+    if (!PAIR) {
+      bulk_load(dst, chunk + (kb & 1) * F::HALF, F::HALF, full(s));
+      bulk_load(dst + F::HALF, chunk + F::META_OFF, F::META, full(s));
+    } else {
+      constexpr int CODE = WFMT == PF_W_Q1_G128 ? 8 : 32;  // bytes per row and k-block
+      const uint8_t* half = chunk + (kb & 1) * F::HALF;
+      bulk_load(dst, half + rank * (BN / 2) * CODE, (BN / 2) * CODE, full(s));
+      bulk_load(dst + (BN / 2) * CODE, chunk + F::META_OFF + rank * BN, BN, full(s));
+      if (WFMT != PF_W_Q1_G128)
+        bulk_load(dst + (BN / 2) * (CODE + 2), chunk + F::META_OFF + 2 * BN + rank * BN, BN, full(s));
+    }
+  };
 
   if (warp == 0) {
     // ---------------------------------------------------------------- TMA producer
@@ -264,16 +329,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           const int kb = sg.kb0 + i;
           const uint8_t* chunk =
               wpk + (static_cast<size_t>(sg.nt) * G + (kb >> 1)) * static_cast<size_t>(F::CHUNK);
-          mbar_arrive_expect_tx(full(pre), A_STAGE + F::P_STAGE);
-          bulk_load(p_st + pre * F::P_STAGE, chunk + (kb & 1) * F::HALF, F::HALF, full(pre));
-          bulk_load(p_st + pre * F::P_STAGE + F::HALF, chunk + F::META_OFF, F::META, full(pre));
+          mbar_arrive_expect_tx(full(pre), A_STAGE + P_STAGE);
+          load_packed(pre, chunk, kb);
         }
       }
       griddep_wait();  // the activations come from the previous kernel
       for (int k = 0, j = 0; k < rg.n && j < pre; ++k) {
         const Segment sg = rg.at(plan, k);
         for (int i = 0; i < sg.nkb && j < pre; ++i, ++j)
-          tma_load_2d(a_st + j * A_STAGE, &tmap_a, (sg.kb0 + i) * BK, sg.mt * BM, full(j));
+          tma_load_2d(a_st + j * A_STAGE, &tmap_a, (sg.kb0 + i) * BK, sg.mt * C::TILE_M + a_row, full(j));
       }
       int it = 0;
       bool ok = true;
@@ -290,10 +354,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           const int kb = sg.kb0 + i;
           const uint8_t* chunk =
               wpk + (static_cast<size_t>(sg.nt) * G + (kb >> 1)) * static_cast<size_t>(F::CHUNK);
-          mbar_arrive_expect_tx(full(s), A_STAGE + F::P_STAGE);
-          tma_load_2d(a_st + s * A_STAGE, &tmap_a, kb * BK, sg.mt * BM, full(s));
-          bulk_load(p_st + s * F::P_STAGE, chunk + (kb & 1) * F::HALF, F::HALF, full(s));
-          bulk_load(p_st + s * F::P_STAGE + F::HALF, chunk + F::META_OFF, F::META, full(s));
+          mbar_arrive_expect_tx(full(s), A_STAGE + P_STAGE);
+          tma_load_2d(a_st + s * A_STAGE, &tmap_a, kb * BK, sg.mt * C::TILE_M + a_row, full(s));
+          load_packed(s, chunk, kb);
         }
       }
       if (!ok) {  // let copies already in flight land before shared memory is released
@@ -303,11 +366,25 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA issuer
     // The whole warp runs the loop (uniform control flow and operands); one elected lane
-    // issues each MMA / commit. Wait outcomes are made warp-uniform by vote.
-    constexpr uint32_t idesc = idesc_f16(BM, BN, 0);
+    // issues each MMA / commit. Wait outcomes are made warp-uniform by vote. In a pair only
+    // the even CTA issues: its bfull / acc_empty barriers count both CTAs' arrivals, and
+    // its commits arrive on the same barrier in both CTAs.
+    constexpr uint32_t idesc = idesc_f16(C::TILE_M, BN, 0);
+    auto mma = [&](uint32_t d, uint64_t ad, uint64_t bd, uint32_t acc) {
+      if (PAIR)
+        umma_pair_f16_ss_warp(d, ad, bd, idesc, acc);
+      else
+        umma_f16_ss_warp(d, ad, bd, idesc, acc);
+    };
+    auto commit = [&](uint32_t bar) {
+      if (PAIR)
+        umma_pair_commit_warp(bar, 3);
+      else
+        umma_commit_warp(bar);
+    };
     int it = 0;
     bool ok = true;
-    for (int k = 0; k < rg.n && ok; ++k) {
+    for (int k = 0; k < (PAIR && rank != 0 ? 0 : rg.n) && ok; ++k) {
       const Segment sg = rg.at(plan, k);
       const int b = k & 1;
       const uint32_t use = static_cast<uint32_t>(k >> 1);
@@ -320,6 +397,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       for (int i = 0; i < sg.nkb; ++i, ++it) {
         const int s = it % S;
         const uint32_t ph = (it / S) & 1;
+        // (the dequantisers arrive on bfull after their own stage's copies landed)
         ok = __all_sync(0xffffffffu,
                         mbar_wait(bfull(s), ph, abort_flag) && mbar_wait(full(s), ph, abort_flag));
         if (!ok) break;
@@ -327,19 +405,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const uint64_t ad = sdesc_kmajor_sw128(a_st + s * A_STAGE);
         const uint64_t bd = sdesc_kmajor_sw128(b_st + s * B_STAGE);
 #pragma unroll
-        for (int kk = 0; kk < BK / 16; ++kk)
-          umma_f16_ss_warp(d_tmem, ad + 2 * kk, bd + 2 * kk, idesc, (i | kk) != 0);
-        umma_commit_warp(empty(s));
+        for (int kk = 0; kk < BK / 16; ++kk) mma(d_tmem, ad + 2 * kk, bd + 2 * kk, (i | kk) != 0);
+        commit(empty(s));
       }
-      if (ok) umma_commit_warp(acc_full(b));
+      if (ok) commit(acc_full(b));
     }
     if (!ok) {
-      umma_commit_warp(drain_bar);  // wait for any MMA still reading shared memory / TMEM
+      commit(drain_bar);  // wait for any MMA still reading shared memory / TMEM
       mbar_wait_drain(drain_bar, 0);
     }
   } else if (warp >= FIRST_DQ_WARP) {
     // ---------------------------------------------------------------- dequantisers
-    const int d = threadIdx.x - FIRST_DQ_WARP * 32;  // weight row of the tile
+    const int d = threadIdx.x - FIRST_DQ_WARP * 32;  // weight row of the tile (pair: row + 128 half)
     int it = 0;
     bool ok = true;
     for (int k = 0; k < rg.n && ok; ++k) {
@@ -351,9 +428,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           ok = false;
           break;
         }
-        dequant_row_smem<WFMT>(p_gen + s * F::P_STAGE, d, b_st + s * B_STAGE);
-        fence_proxy_async_smem();
-        mbar_arrive(bfull(s));
+        if (PAIR) {
+          dequant_half_row_pair<WFMT>(p_gen + s * P_STAGE, d & (BN / 2 - 1), d / (BN / 2), b_st + s * B_STAGE);
+          fence_proxy_async_smem();  // this CTA's shared memory, read by the pair's MMA
+          __syncwarp();
+          if (lane == 0) {
+            if (rank == 0)
+              mbar_arrive(bfull(s));
+            else
+              mbar_arrive_cta(bfull(s), 0);
+          }
+        } else {
+          dequant_row_smem<WFMT>(p_gen + s * P_STAGE, d, b_st + s * B_STAGE);
+          fence_proxy_async_smem();
+          mbar_arrive(bfull(s));
+        }
       }
     }
   } else {
@@ -402,7 +491,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const bool got = mbar_wait(acc_full(b), use & 1, abort_flag);
       if (!named_bar_and(1, EPI_THREADS, got)) break;
       tc_fence_after();
-      const int row0 = sg.mt * BM + 32 * q;  // first row of this warp's quarter
+      const int row0 = sg.mt * C::TILE_M + a_row + 32 * q;  // first row of this warp's quarter
       const int lrow = 32 * q + lane;        // row within the tile
       const bool valid = row0 + lane < M;
       const uint32_t tb = tmem_base + b * BN + (static_cast<uint32_t>(32 * q) << 16);
@@ -428,10 +517,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           c_lo = plan.owner(static_cast<long long>(sg.tile) * plan.kbt);
           c_hi = plan.owner(static_cast<long long>(sg.tile + 1) * plan.kbt - 1);
           const int others = c_hi - c_lo;  // contributors besides this CTA
-          const int slot = plan.slot(blockIdx.x, sg.tile);
+          const int slot = plan.slot(unit, sg.tile);
+          // a pair tile's two row halves are finished independently, one counter each
+          int* ctr = counters + (PAIR ? 2 * sg.tile + static_cast<int>(rank) : sg.tile);
           volatile int* flag = flags + 2 * slot;  // each slot serves one segment only
           // if every other contributor has arrived already, finish without storing
-          if (et == 0) flag[0] = ld_acquire_gpu(counters + sg.tile) == others ? 1 : 0;
+          if (et == 0) flag[0] = ld_acquire_gpu(ctr) == others ? 1 : 0;
           named_bar_sync(1, EPI_THREADS);
           finish = flag[0] != 0;
           if (!finish) {
@@ -452,21 +543,22 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
             __threadfence();
             named_bar_sync(1, EPI_THREADS);
-            if (et == 0) flag[1] = atomicAdd(counters + sg.tile, 1) == others ? 1 : 0;
+            if (et == 0) flag[1] = atomicAdd(ctr, 1) == others ? 1 : 0;
             named_bar_sync(1, EPI_THREADS);
             finish = flag[1] != 0;
           }
           if (finish) {
-            if (et == 0) counters[sg.tile] = 0;  // every contributor is in: ready for reuse
+            if (et == 0) *ctr = 0;  // every contributor is in: ready for reuse
             __threadfence();
           }
         }
         // adds the other contributors' partials of 32-column chunk `chunk` of this row to v
         auto add_partials = [&](uint32_t (&v)[32], int chunk) {
           for (int c = c_lo; c <= c_hi; ++c) {
-            if (c == static_cast<int>(blockIdx.x)) continue;
+            if (c == unit) continue;
+            const int cta = PAIR ? 2 * c + static_cast<int>(rank) : c;  // same row half
             const float4* src = reinterpret_cast<const float4*>(scratch) +
-                                (static_cast<size_t>(c) * 2 + plan.slot(c, sg.tile)) * (SLOT_FLOATS / 4) +
+                                (static_cast<size_t>(cta) * 2 + plan.slot(c, sg.tile)) * (SLOT_FLOATS / 4) +
                                 lrow;
             float4 x[8];
 #pragma unroll
@@ -512,42 +604,99 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
       }
       tc_fence_before();
-      mbar_arrive(acc_empty(b));
+      if (PAIR) {
+        __syncwarp();
+        if (lane == 0) {
+          if (rank == 0)
+            mbar_arrive(acc_empty(b));
+          else
+            mbar_arrive_cta(acc_empty(b), 0);
+        }
+      } else {
+        mbar_arrive(acc_empty(b));
+      }
     }
     if (lane == 0) bulk_wait0();  // TMA writes complete before the CTA retires
     __syncwarp();
   }
 
   tc_fence_before();
-  __syncthreads();
+  // a pair's CTAs stay until both are done: the even CTA's MMAs read the odd one's shared
+  // memory, and the odd one arrives on the even one's barriers
+  __syncwarp();
+  if (PAIR)
+    cluster_sync_all();
+  else
+    __syncthreads();
   if (warp == 1) {
     tc_fence_after();
     __syncwarp();  // reconverge before the collective dealloc
-    tmem_dealloc(tmem_base, TMEM_COLS);
+    if (PAIR)
+      tmem_dealloc_pair(tmem_base, TMEM_COLS);
+    else
+      tmem_dealloc(tmem_base, TMEM_COLS);
   }
   if (threadIdx.x == 0 && *abort_flag && status != nullptr) atomicCAS(status, 0, PF_ERR_DEVICE_TIMEOUT);
 }
 
-template <int WFMT, int EPI>
+template <int WFMT, int EPI, bool PAIR>
 cudaError_t launch_t(const GemmArgs& g, const CUtensorMap& ta, const CUtensorMap& to, int num_sms,
                      cudaStream_t stream) {
-  constexpr int smem = smem_bytes<WFMT>();
+  using C = Cfg<WFMT, PAIR>;
   Plan p{};
-  p.n_mt = (g.M + BM - 1) / BM;
+  p.n_mt = (g.M + C::TILE_M - 1) / C::TILE_M;
   p.n_nt = static_cast<int>(padded_rows(g.N) / TILE_N);
   p.kbt = g.K / BK;
   p.total = static_cast<long long>(p.n_mt) * p.n_nt * p.kbt;
-  p.ctas = static_cast<int>(std::min<long long>(std::min(g.max_ctas, num_sms), p.total));
-  // store / SwiGLU epilogues: a tile split between CTAs costs a partial hand-off, so when
-  // the tiles alone fill at least half of the CTAs, run one whole tile per CTA instead
+  // the plan's units: CTAs, or CTA pairs (no more pairs than can be resident at once)
+  int units = std::min(g.max_ctas, num_sms) / (PAIR ? 2 : 1);
+  if (PAIR) {
+    static const int resident = [] {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(2);
+      cfg.blockDim = dim3(NUM_THREADS);
+      cfg.dynamicSmemBytes = C::SMEM;
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = 2;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      int n = 0;
+      if (cudaOccupancyMaxActiveClusters(&n, gemm_q_kernel<WFMT, EPI, true>, &cfg) != cudaSuccess) {
+        (void)cudaGetLastError();
+        n = 0;
+      }
+      return n;
+    }();
+    if (resident > 0) units = std::min(units, resident);
+  }
+  p.ctas = static_cast<int>(std::min<long long>(units, p.total));
+  // store / SwiGLU epilogues: a tile split between units costs a partial hand-off, so when
+  // the tiles alone fill at least half of the units, run one whole tile per unit instead
   const int tiles = p.n_mt * p.n_nt;
   if (EPI != EPI_RESID_ADD && tiles < p.ctas && 2 * tiles >= p.ctas) p.ctas = tiles;
   float* scratch = reinterpret_cast<float*>(g.scratch);
   int* counters =
       scratch ? reinterpret_cast<int*>(scratch + static_cast<size_t>(2) * g.max_ctas * SLOT_FLOATS) : nullptr;
-  return launch_pdl(gemm_q_kernel<WFMT, EPI>, dim3(p.ctas), dim3(NUM_THREADS), smem, stream, ta, to,
-                    g.w, g.M, g.N, g.K, p, scratch, counters, g.status,
-                    reinterpret_cast<float4*>(g.side_zero), static_cast<long long>(g.side_zero_bytes / 16));
+  float4* zero = reinterpret_cast<float4*>(g.side_zero);
+  const long long zero4 = static_cast<long long>(g.side_zero_bytes / 16);
+  if (PAIR)
+    return launch_pdl_pairs(gemm_q_kernel<WFMT, EPI, true>, dim3(2 * p.ctas), dim3(NUM_THREADS), C::SMEM,
+                            stream, ta, to, g.w, g.M, g.N, g.K, p, scratch, counters, g.status, zero, zero4);
+  return launch_pdl(gemm_q_kernel<WFMT, EPI, false>, dim3(p.ctas), dim3(NUM_THREADS), C::SMEM, stream, ta,
+                    to, g.w, g.M, g.N, g.K, p, scratch, counters, g.status, zero, zero4);
+}
+
+// CTA pairs for more than one 128-token block (PF_GEMM_PAIRS=0 in the environment turns
+// them off, to compare the two forms).
+bool use_pairs(const GemmArgs& g, int sms) {
+  static const bool enabled = [] {
+    const char* e = getenv("PF_GEMM_PAIRS");
+    return e == nullptr || atoi(e) != 0;
+  }();
+  return enabled && g.M > BM && std::min(g.max_ctas, sms) >= 2;
 }
 
 }  // namespace
@@ -557,26 +706,30 @@ cudaError_t launch_t(const GemmArgs& g, const CUtensorMap& ta, const CUtensorMap
 // begins and ends inside at most two tiles), then one arrival counter per output tile, which
 // must be zero before the first launch (every launch that completes leaves them zero).
 size_t gemm_scratch_bytes(int M, int N, int max_ctas) {
-  // one counter per 128 x 256 tile (the small-M kernel's 256-row tiles are fewer)
-  const size_t tiles = static_cast<size_t>((M + BM - 1) / BM) * (padded_rows(N) / TILE_N);
+  // one counter per 128 x 256 tile, or two per 256 x 256 pair tile (one per row half); the
+  // small-M kernel's 256-row tiles are fewer
+  const size_t nt = static_cast<size_t>(padded_rows(N) / TILE_N);
+  const size_t tiles = std::max<size_t>((M + BM - 1) / BM, 2 * ((M + 2 * BM - 1) / (2 * BM))) * nt;
   return static_cast<size_t>(2) * max_ctas * SLOT_FLOATS * sizeof(float) + tiles * sizeof(int);
 }
 
-template <int WFMT, int EPI>
+template <int WFMT, int EPI, bool PAIR>
 cudaError_t set_smem_attr() {
-  return cudaFuncSetAttribute(gemm_q_kernel<WFMT, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              smem_bytes<WFMT>());
+  return cudaFuncSetAttribute(gemm_q_kernel<WFMT, EPI, PAIR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              Cfg<WFMT, PAIR>::SMEM);
 }
 
 cudaError_t prepare_gemm_kernels() {
   cudaError_t e = cudaSuccess;
   cudaError_t r;
-  if ((r = set_smem_attr<PF_W_Q1_G128, EPI_STORE_F32>()) != cudaSuccess) e = r;
-  if ((r = set_smem_attr<PF_W_Q1_G128, EPI_RESID_ADD>()) != cudaSuccess) e = r;
-  if ((r = set_smem_attr<PF_W_Q1_G128, EPI_SWIGLU>()) != cudaSuccess) e = r;
-  if ((r = set_smem_attr<PF_W_INT4_AFFINE_G128, EPI_STORE_F32>()) != cudaSuccess) e = r;
-  if ((r = set_smem_attr<PF_W_INT4_AFFINE_G128, EPI_RESID_ADD>()) != cudaSuccess) e = r;
-  if ((r = set_smem_attr<PF_W_INT4_AFFINE_G128, EPI_SWIGLU>()) != cudaSuccess) e = r;
+  if ((r = set_smem_attr<PF_W_Q1_G128, EPI_RESID_ADD, false>()) != cudaSuccess) e = r;
+  if ((r = set_smem_attr<PF_W_Q1_G128, EPI_SWIGLU, false>()) != cudaSuccess) e = r;
+  if ((r = set_smem_attr<PF_W_INT4_AFFINE_G128, EPI_RESID_ADD, false>()) != cudaSuccess) e = r;
+  if ((r = set_smem_attr<PF_W_INT4_AFFINE_G128, EPI_SWIGLU, false>()) != cudaSuccess) e = r;
+  if ((r = set_smem_attr<PF_W_Q1_G128, EPI_RESID_ADD, true>()) != cudaSuccess) e = r;
+  if ((r = set_smem_attr<PF_W_Q1_G128, EPI_SWIGLU, true>()) != cudaSuccess) e = r;
+  if ((r = set_smem_attr<PF_W_INT4_AFFINE_G128, EPI_RESID_ADD, true>()) != cudaSuccess) e = r;
+  if ((r = set_smem_attr<PF_W_INT4_AFFINE_G128, EPI_SWIGLU, true>()) != cudaSuccess) e = r;
   return e;
 }
 
@@ -609,20 +762,20 @@ cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t stream) {
                           static_cast<uint64_t>(g.M), 32, 32, swiglu ? 64 : 128))
     return cudaErrorInvalidValue;
   static int sms = device_sm_count();
-  if (g.wfmt == PF_W_Q1_G128) {
-    switch (g.epilogue) {
-      case EPI_STORE_F32: return launch_t<PF_W_Q1_G128, EPI_STORE_F32>(g, ta, to, sms, stream);
-      case EPI_RESID_ADD: return launch_t<PF_W_Q1_G128, EPI_RESID_ADD>(g, ta, to, sms, stream);
-      case EPI_SWIGLU: return launch_t<PF_W_Q1_G128, EPI_SWIGLU>(g, ta, to, sms, stream);
-    }
-  } else {
-    switch (g.epilogue) {
-      case EPI_STORE_F32: return launch_t<PF_W_INT4_AFFINE_G128, EPI_STORE_F32>(g, ta, to, sms, stream);
-      case EPI_RESID_ADD: return launch_t<PF_W_INT4_AFFINE_G128, EPI_RESID_ADD>(g, ta, to, sms, stream);
-      case EPI_SWIGLU: return launch_t<PF_W_INT4_AFFINE_G128, EPI_SWIGLU>(g, ta, to, sms, stream);
-    }
+  const bool pair = use_pairs(g, sms);
+  const bool q1 = g.wfmt == PF_W_Q1_G128;
+  constexpr int Q1 = PF_W_Q1_G128, I4 = PF_W_INT4_AFFINE_G128;
+  if (swiglu) {
+    if (q1) return pair ? launch_t<Q1, EPI_SWIGLU, true>(g, ta, to, sms, stream)
+                        : launch_t<Q1, EPI_SWIGLU, false>(g, ta, to, sms, stream);
+    return pair ? launch_t<I4, EPI_SWIGLU, true>(g, ta, to, sms, stream)
+                : launch_t<I4, EPI_SWIGLU, false>(g, ta, to, sms, stream);
   }
-  return cudaErrorInvalidValue;
+  if (g.epilogue != EPI_RESID_ADD) return cudaErrorInvalidValue;
+  if (q1) return pair ? launch_t<Q1, EPI_RESID_ADD, true>(g, ta, to, sms, stream)
+                      : launch_t<Q1, EPI_RESID_ADD, false>(g, ta, to, sms, stream);
+  return pair ? launch_t<I4, EPI_RESID_ADD, true>(g, ta, to, sms, stream)
+              : launch_t<I4, EPI_RESID_ADD, false>(g, ta, to, sms, stream);
 }
 
 }  // namespace pf

@@ -994,7 +994,9 @@ pf_status pf_op_gemm_static_scratch(int32_t wfmt, int32_t epi, const uint16_t* a
   if (epi == EPI_SWIGLU && N % 256) return fail(PF_ERR_SHAPE, "SwiGLU needs N = 2I with I %% 128 == 0");
   if ((reinterpret_cast<uintptr_t>(a) & 15) || (reinterpret_cast<uintptr_t>(out) & 15))
     return fail(PF_ERR_INVALID_ARG, "a and out must be 16-B aligned");
-  const size_t tiles = static_cast<size_t>((M + 127) / 128) * static_cast<size_t>((N + 255) / 256);
+  // arrival counters: one per 128 x 256 tile, or two per 256 x 256 tile of a CTA pair
+  const size_t tiles = std::max<size_t>((M + 127) / 128, 2 * ((M + 255) / 256)) *
+                       static_cast<size_t>((N + 255) / 256);
   if (tiles > STATIC_GEMM_TILES)
     return fail(PF_ERR_SHAPE,
                 "M %d x N %d is %zu output tiles of 128 x 256; the static GEMM scratch holds at most %zu",

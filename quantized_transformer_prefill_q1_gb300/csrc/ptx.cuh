@@ -226,6 +226,65 @@ __device__ __forceinline__ void tmem_ld_wait() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+// ------------------------------------------------------------------ CTA pairs
+// A cluster of two CTAs on two SMs shares one MMA (cta_group::2): TMEM is allocated in both
+// by both (same address), the even CTA issues M = 256 MMAs whose A rows and B columns are
+// split between the two CTAs' shared memory (each holds 128 rows of A and N/2 rows of B at
+// the same offsets), D rows 0..127 land in the even CTA's TMEM and 128..255 in the odd one's,
+// and a commit can arrive on the same barrier in both CTAs.
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// Every thread of every CTA of the cluster; release / acquire at cluster scope.
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// Arrive on the barrier at shared offset `bar` of cluster CTA `rank` (the instruction's
+// default release semantics). Used by the odd CTA of a pair to tell the even one that its
+// dequantised operand tile (written, then fenced to the async proxy, in its own shared memory,
+// where the pair's MMA reads it) or its TMEM reads are done; a release at cluster scope
+// measured ~0.7 us per arrive, slower than the stage it guards.
+__device__ __forceinline__ void mbar_arrive_cta(uint32_t bar, uint32_t rank) {
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(bar), "r"(rank));
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(remote) : "memory");
+}
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
+               "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish_pair() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+// Warp-collective pair MMA (one elected lane issues), kind::f16, A and B from shared memory.
+__device__ __forceinline__ void umma_pair_f16_ss_warp(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                                      uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// Arrive (once per CTA in `mask`) on the barrier at offset `bar` of those CTAs when the pair
+// MMAs issued so far complete.
+__device__ __forceinline__ void umma_pair_commit_warp(uint32_t bar, uint16_t mask) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;\n\t}" ::"r"(bar),
+      "h"(mask)
+      : "memory");
+}
+
 // Shared-memory matrix descriptor for a K-major operand tile written in the 128-byte
 // swizzle layout (rows of 64 16-bit elements = 128 B; 8-row atoms of 1024 B stacked
 // along M/N; 16-B chunk c of row r stored at chunk c ^ (r % 8)). The tile base must be

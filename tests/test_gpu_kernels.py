@@ -88,8 +88,9 @@ GEMM_CASES = [
 
 
 def assert_counters_zero(scratch, m, n):
-    """Every launch that completes leaves the per-tile arrival counters zero."""
-    tiles = -(-m // 128) * -(-n // 256)
+    """Every launch that completes leaves the per-tile arrival counters zero (one per
+    128 x 256 tile, or two per 256 x 256 tile of a CTA pair)."""
+    tiles = max(-(-m // 128), 2 * -(-m // 256)) * -(-n // 256)
     counters = scratch[scratch.numel() - 4 * tiles:].view(torch.int32)
     assert int(counters.abs().sum()) == 0
 
