@@ -46,11 +46,11 @@ PROMPT, CHUNK = 2048, 512
 # kernel class; None when no capture matches the kernel as it now stands.
 # gate_up: dram__bytes_read.sum + dram__bytes_write.sum of one --set full capture of
 # `bench.py --case gemm_gate_up` (M 512, N 24576, K 4096)
-NCU_TRAFFIC = {"gemm_gate_up": 18408704 + 427520}
+NCU_TRAFFIC = {"gemm_gate_up": 18405888 + 673536}
 
 
 CASES = ["gemm_gate_up", "gemm_qkv", "gemm_down", "gemm_o", "attention", "rmsnorm", "qk_rope_kv", "lm_head",
-         "int4_gate_up", "int4_qkv", "int4_o", "int4_down", "decode"]
+         "int4_gate_up", "int4_qkv", "int4_o", "int4_down", "decode", "timeline"]
 
 
 def parse():
@@ -75,6 +75,86 @@ def parse():
                    help="comma list of chunk tokens for the int4_* (Llama-3-8B-shaped INT4 layer, default 1) "
                         "and gemm_* (Qwen3-8B-shaped Q1 layer, default 512) cases")
     return p.parse_args()
+
+
+def timeline_classes(names):
+    """Labels the launches of one prompt (a list of kernel names in launch order) with their
+    role in the layer: the two RMSNorms and the residual-form GEMMs are told apart by what
+    precedes them."""
+    labels, norm, after = [], 0, None
+    for n in names:
+        if n == "rmsnorm_reg" or n == "rmsnorm":
+            norm += 1
+            labels.append("rmsnorm_attn" if norm % 2 == 1 else "rmsnorm_ffn")
+            after = "qkv" if norm % 2 == 1 else None
+        elif n.startswith("gemm") and n.endswith("resid"):
+            labels.append("gemm_" + (after or "?"))
+        elif n.startswith("gemm") and n.endswith("swiglu"):
+            labels.append("gemm_gate_up")
+            after = "down"
+        elif n.startswith("attention"):
+            labels.append("attention")
+            after = "o"
+        else:
+            labels.append(n)
+    return labels
+
+
+def run_timeline(args, pf, synth):
+    """One 2048-token prompt of the workload (graphs replayed, as in the timed steps) with
+    the per-CTA kernel timeline on. Launches are the runs of equal kernel id in start order
+    (with programmatic launch a kernel's CTAs all start before the next kernel's first). Per
+    launch: `crit` = its last CTA's end minus the previous launch's last end, so the crits
+    add up to the prompt's time; `gap` = its first CTA's start minus the previous launch's
+    last end (negative: started early under programmatic launch); `spread` = last minus
+    first CTA end. Prints one JSON line with the mean of each per layer class."""
+    import numpy as np
+    import torch
+    shape = synth.QWEN3_8B_STACK
+    layers, extra = synth.model_inputs(shape, seed=args.seed)
+    dm = pf.DeviceModel(shape, layers, extra, max_chunk=CHUNK)
+    del layers, extra
+    sess = pf.Session(dm)
+    tok = torch.from_numpy(synth.tokens(PROMPT, shape.vocab, seed=args.seed)).cuda()
+    logits = torch.empty(shape.vocab, dtype=torch.float32, device="cuda")
+
+    def step():
+        sess.set_position(0)
+        sess.prefill_chunk_dev(tok, 0, logits)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    sess.sync()
+    cap = 1 << 20
+    buf = torch.zeros(4 + 4 * cap, dtype=torch.int64, device="cuda")
+    pf.pf_timeline_set(buf, cap)
+    step()
+    sess.sync()
+    torch.cuda.synchronize()
+    pf.pf_timeline_set(None, 0)
+    rec = pf.timeline_records(buf)
+    ids = rec["kernel"]
+    cut = np.flatnonzero(np.diff(ids) != 0) + 1
+    bounds = list(zip(np.concatenate([[0], cut]), np.concatenate([cut, [len(ids)]])))
+    names = [pf.pf_timeline_kernel_name(int(ids[a])) for a, _ in bounds]
+    labels = timeline_classes(names)
+    prev, per = int(rec["start_ns"].min()), {}
+    for (a, z), lab in zip(bounds, labels):
+        st, en = rec["start_ns"][a:z], rec["end_ns"][a:z]
+        e1 = int(en.max())
+        d = per.setdefault(lab, [])
+        d.append((e1 - prev, int(st.min()) - prev, e1 - int(st.min()), e1 - int(en.min()), z - a))
+        prev = max(prev, e1)
+    total_ns = prev - int(rec["start_ns"].min())
+    out = {"case": "timeline", "workload": WORKLOAD, "records": int(len(rec)), "launches": len(bounds),
+           "prompt_us": total_ns / 1e3, "classes": {}}
+    for lab, d in per.items():
+        x = np.array(d, dtype=np.float64)
+        out["classes"][lab] = {"launches": len(d), "crit_us": round(x[:, 0].mean() / 1e3, 2),
+                               "span_us": round(x[:, 2].mean() / 1e3, 2), "gap_us": round(x[:, 1].mean() / 1e3, 2),
+                               "end_spread_us": round(x[:, 3].mean() / 1e3, 2),
+                               "ctas": int(x[:, 4].mean()), "crit_ms_per_prompt": round(x[:, 0].sum() / 1e6, 3)}
+    print(json.dumps(out))
 
 
 def run_case(args):
@@ -117,6 +197,9 @@ def run_case(args):
     for case in args.case.split(","):
         if case == "decode":
             run_decode(args, pf, synth, dev)
+            continue
+        if case == "timeline":
+            run_timeline(args, pf, synth)
             continue
         for M in (ms or [1 if case.startswith("int4") else CHUNK]):
             rng = synth.rng_for(99)

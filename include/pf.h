@@ -194,6 +194,22 @@ pf_status pf_session_profile_read(pf_session* s, void* stream, double* ms_out,
  * kernel node they run). */
 int64_t pf_session_kernel_launches(const pf_session* s);
 
+/* Kernel timeline, per CTA: the CUDA analogue of the GPU start / end stamps the pages take
+ * per command buffer ([P2] OXIBONSAI_PROFILE_GPU, GPUStartTime / GPUEndTime). While a buffer
+ * is set, each CTA of every libpf kernel (graph replays included, any session or op) appends
+ * one record when its first thread leaves the kernel:
+ *   buffer[0]              records appended so far (may exceed `capacity`: those are dropped)
+ *   buffer[1]              capacity (written here)
+ *   buffer[4 + 4 i + 0]    %globaltimer (ns) when the CTA's first thread started
+ *   buffer[4 + 4 i + 1]    %globaltimer (ns) when it left the kernel
+ *   buffer[4 + 4 i + 2]    kernel id << 48 | SM id << 32 | linear CTA index (low 32 bits)
+ * `buffer`: DEVICE memory of 4 + 4 * capacity uint64 words, owned by the caller; its first
+ * word is zeroed here. NULL stops recording. Synchronous: call with no libpf work in flight.
+ * Errors: PF_ERR_INVALID_ARG (capacity <= 0 with a buffer), PF_ERR_CUDA. */
+pf_status pf_timeline_set(uint64_t* buffer, int64_t capacity);
+/* Name of a timeline kernel id ("gemm_pair_swiglu", "attention_tc", ...); NULL if unknown. */
+const char* pf_timeline_kernel_name(int32_t id);
+
 /* ------------------------------------------------------------------ the path
  * pf_prefill_chunk — [P3] prefill_chunk(tokens, start_position, logits): embeds M
  * token ids (HOST array, checked against vocab on the host before any launch), runs

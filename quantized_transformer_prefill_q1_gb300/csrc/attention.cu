@@ -121,6 +121,7 @@ __global__ void __launch_bounds__(THREADS) attention_kernel(
     const T* __restrict__ q, const KT* __restrict__ kc, const KT* __restrict__ vc, int M, int nq,
     int nkv, int max_seq, int layer, const int* __restrict__ start_dev, int start_host,
     float scale_log2, __half* __restrict__ out) {
+  PF_TIMELINE(TL_ATTENTION_F32);
   extern __shared__ __align__(128) uint8_t sm[];
   uint8_t* Qs = sm;
   uint8_t* Ks = Qs + BR * HD * 2;
@@ -345,3 +346,5 @@ cudaError_t launch_attention(const AttnArgs& a, cudaStream_t stream) {
 }
 
 }  // namespace pf
+
+PF_TIMELINE_SETTER(attention)

@@ -214,6 +214,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_kc,
                    const __grid_constant__ CUtensorMap tm_vc, const AttnKParams P) {
+  PF_TIMELINE(TL_ATTENTION_TC);
   using L = ASmem<HD>;
   constexpr int NH = HD / 64;  // 64-wide (128-B) swizzle regions along head_dim
   extern __shared__ uint8_t smem_raw[];
@@ -591,6 +592,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 template <int HD>
 __global__ void __launch_bounds__(256) attn_combine_kernel(const float* __restrict__ part, int rows,
                                                            int n_split, __half* __restrict__ out) {
+  PF_TIMELINE(TL_ATTN_COMBINE);
   griddep_launch_dependents();
   griddep_wait();
   const int row = blockIdx.x * 8 + (threadIdx.x >> 5);
@@ -734,3 +736,5 @@ cudaError_t launch_attention_tc(const AttnArgs& a, cudaStream_t stream) {
 }
 
 }  // namespace pf
+
+PF_TIMELINE_SETTER(attention_tc)

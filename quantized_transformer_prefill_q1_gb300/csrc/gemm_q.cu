@@ -231,6 +231,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                   int M, int N, int K, Plan plan, float* __restrict__ scratch,
                   int* __restrict__ counters, int* __restrict__ status,
                   float4* __restrict__ side_zero, long long side_zero4) {
+  PF_TIMELINE(TL_GEMM + EPI + (PAIR ? 3 : 0));
   using F = Fmt<WFMT>;
   using C = Cfg<WFMT, PAIR>;
   constexpr int S = C::STAGES;
@@ -779,3 +780,5 @@ cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t stream) {
 }
 
 }  // namespace pf
+
+PF_TIMELINE_SETTER(gemm_q)

@@ -93,6 +93,7 @@ __global__ void __launch_bounds__(THREADS_S, 1)
                       int M, int N, int K, void* __restrict__ out, Plan plan,
                       float* __restrict__ scratch, int* __restrict__ counters,
                       int* __restrict__ status) {
+  PF_TIMELINE(TL_GEMM_SMALL + EPI);
   using F = SF<WFMT>;
   using L = SL<WFMT, NT>;
   constexpr int S = L::S;
@@ -456,3 +457,5 @@ cudaError_t launch_gemm_small(const GemmArgs& g, cudaStream_t stream) {
 }
 
 }  // namespace pf
+
+PF_TIMELINE_SETTER(gemm_small)

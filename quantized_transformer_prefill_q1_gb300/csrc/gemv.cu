@@ -209,6 +209,7 @@ template <int WFMT, int EPI>
 __global__ void __launch_bounds__(THREADS_V)
     gemv_kernel(const __half* a, const uint8_t* __restrict__ wpk, int M, int N, int K,
                 void* __restrict__ out, long long units, int warps) {
+  PF_TIMELINE(TL_GEMV + EPI);
   using S = ST<WFMT>;
   constexpr int DS = S::DS;
   constexpr size_t P = WFMT == PF_W_Q1_G128 ? Q1_CHUNK_BYTES : I4_CHUNK_BYTES;
@@ -417,3 +418,5 @@ cudaError_t launch_gemv(const GemmArgs& g, cudaStream_t stream) {
 }
 
 }  // namespace pf
+
+PF_TIMELINE_SETTER(gemv)

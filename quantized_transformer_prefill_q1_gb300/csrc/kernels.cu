@@ -48,6 +48,7 @@ __global__ void __launch_bounds__(256) rmsnorm_kernel(const float* __restrict__ 
                                                       const float* __restrict__ w, float eps,
                                                       int H, __half* __restrict__ y,
                                                       float4* __restrict__ zero, int zero4) {
+  PF_TIMELINE(TL_RMSNORM);
   __shared__ float red[32];
   griddep_launch_dependents();
   griddep_wait();
@@ -79,6 +80,7 @@ __global__ void __launch_bounds__(128) rmsnorm_reg_kernel(const float* __restric
                                                           const float* __restrict__ w, float eps,
                                                           int H, __half* __restrict__ y,
                                                           float4* __restrict__ zero, int zero4) {
+  PF_TIMELINE(TL_RMSNORM_REG);
   __shared__ float red[4];
   griddep_launch_dependents();
   // the norm weights never depend on the previous kernel: load them while it finishes
@@ -160,6 +162,7 @@ __global__ void __launch_bounds__(256) qk_norm_rope_kv_kernel(
     const float* __restrict__ rope, int M, int nq, int nkv, int kv_rows, int kv_layer, int kv_by_pos,
     const int* __restrict__ start_dev, int start_host, float eps, int qk_norm,
     QT* __restrict__ q_out, KT* __restrict__ kc, KT* __restrict__ vc) {
+  PF_TIMELINE(TL_QK_ROPE_KV);
   constexpr int HALF = HD / 2;
   constexpr int LPH = HALF / 4;   // lanes per head
   constexpr int HPW = 32 / LPH;   // heads per warp
@@ -238,6 +241,7 @@ __global__ void __launch_bounds__(256) ring_store_kernel(
     const uint32_t* __restrict__ kb, const uint32_t* __restrict__ vb, int chunk_rows, int M,
     int nkv, int words, int layer, int R, int S, const int* __restrict__ start_dev, int start_host,
     uint32_t* __restrict__ kc, uint32_t* __restrict__ vc) {
+  PF_TIMELINE(TL_RING_STORE);
   griddep_launch_dependents();
   griddep_wait();
   const int item = blockIdx.x * 8 + (threadIdx.x >> 5);
@@ -264,6 +268,7 @@ __global__ void __launch_bounds__(256) embed_kernel(const float* __restrict__ E,
                                                     const int* __restrict__ tokens, int H,
                                                     int vocab, float* __restrict__ x,
                                                     int* __restrict__ status) {
+  PF_TIMELINE(TL_EMBED);
   griddep_launch_dependents();
   griddep_wait();
   const int t = blockIdx.x;
@@ -288,6 +293,7 @@ __global__ void __launch_bounds__(256) lm_head_kernel(const float* __restrict__ 
                                                       const float* __restrict__ nw, float eps,
                                                       const uint8_t* __restrict__ W, int vocab,
                                                       int H, float* __restrict__ logits) {
+  PF_TIMELINE(TL_LM_HEAD);
   extern __shared__ float ys[];  // [H] normalised row, then [H/128] group sums
   __shared__ float red[32];
   griddep_launch_dependents();
@@ -369,6 +375,7 @@ __global__ void __launch_bounds__(256) lm_head_kernel(const float* __restrict__ 
 template <int WFMT>
 __global__ void __launch_bounds__(256) dequant_kernel(const uint8_t* __restrict__ W, int64_t N,
                                                       int64_t K, __half* __restrict__ w) {
+  PF_TIMELINE(TL_DEQUANT);
   const int G = static_cast<int>(K / GROUP);
   const int64_t n = static_cast<int64_t>(blockIdx.x) * 256 + threadIdx.x;  // packed row
   const int run = blockIdx.y;                                             // 32-k run
@@ -393,6 +400,7 @@ __global__ void __launch_bounds__(256) dequant_kernel(const uint8_t* __restrict_
 }
 
 __global__ void set_int_kernel(int* dst, int v) {
+  PF_TIMELINE(TL_SET_INT);
   griddep_launch_dependents();
   griddep_wait(); *dst = v; }
 
@@ -409,6 +417,7 @@ __device__ __forceinline__ void argmax_take(float v, int i, float& best, int& bi
 }
 __global__ void __launch_bounds__(1024) argmax_rows_kernel(const float* __restrict__ x, int n,
                                                            long long ld, int* __restrict__ out) {
+  PF_TIMELINE(TL_ARGMAX);
   __shared__ float wb[32];
   __shared__ int wi[32];
   griddep_launch_dependents();
@@ -447,6 +456,7 @@ __global__ void __launch_bounds__(1024) argmax_rows_kernel(const float* __restri
 // arrival; with `arrive` set a thread provides it, otherwise nothing ever does and the
 // wait must give up after limit_ns and record PF_ERR_DEVICE_TIMEOUT.
 __global__ void wait_selftest_kernel(int* status, long long limit_ns, int arrive) {
+  PF_TIMELINE(TL_WAIT_SELFTEST);
   griddep_launch_dependents();
   griddep_wait();
   __shared__ __align__(8) uint64_t bar;
@@ -585,6 +595,7 @@ __global__ void __launch_bounds__(512) lm_head_q1_kernel(const float* __restrict
                                                          const float* __restrict__ nw, float eps,
                                                          const uint8_t* __restrict__ W, int vocab,
                                                          int H, float* __restrict__ logits) {
+  PF_TIMELINE(TL_LM_HEAD_Q1);
   // [H/32 words][8 nibbles][16 values] (each word's table 512-B aligned), then y [H], then [256]
   extern __shared__ __align__(1024) float lut[];
   __shared__ float red[32];
@@ -714,3 +725,5 @@ cudaError_t launch_wait_selftest(int* status, long long limit_ns, int arrive, cu
 }
 
 }  // namespace pf
+
+PF_TIMELINE_SETTER(kernels)

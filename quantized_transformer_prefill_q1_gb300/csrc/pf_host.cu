@@ -707,6 +707,42 @@ pf_status pf_session_set_profile(pf_session* s, int32_t enable) {
   return PF_OK;
 }
 
+pf_status pf_timeline_set(uint64_t* buffer, int64_t capacity) {
+  if (buffer != nullptr && capacity <= 0) return fail(PF_ERR_INVALID_ARG, "timeline capacity %lld", (long long)capacity);
+  unsigned long long* b = reinterpret_cast<unsigned long long*>(buffer);
+  if (b != nullptr) {
+    const unsigned long long hdr[4] = {0ull, static_cast<unsigned long long>(capacity), 0ull, 0ull};
+    PF_CUDA(cudaMemcpy(b, hdr, sizeof(hdr), cudaMemcpyHostToDevice), "timeline header");
+  }
+  PF_CUDA(timeline_set_kernels(b), "timeline");
+  PF_CUDA(timeline_set_gemm_q(b), "timeline");
+  PF_CUDA(timeline_set_gemm_small(b), "timeline");
+  PF_CUDA(timeline_set_gemv(b), "timeline");
+  PF_CUDA(timeline_set_attention(b), "timeline");
+  PF_CUDA(timeline_set_attention_tc(b), "timeline");
+  return PF_OK;
+}
+
+const char* pf_timeline_kernel_name(int32_t id) {
+  static const std::vector<std::string> names = [] {
+    std::vector<std::string> n(64);
+    const char* fixed[15] = {"", "rmsnorm", "rmsnorm_reg", "qk_norm_rope_kv", "ring_store", "embed",
+                             "lm_head", "dequant", "set_int", "argmax_rows", "wait_selftest", "lm_head_q1",
+                             "attention_f32", "attention_tc", "attn_combine"};
+    for (int i = 1; i < 15; ++i) n[i] = fixed[i];
+    const char* epi[3] = {"store", "resid", "swiglu"};
+    for (int e = 0; e < 3; ++e) {
+      n[TL_GEMM + e] = std::string("gemm_") + epi[e];
+      n[TL_GEMM + 3 + e] = std::string("gemm_pair_") + epi[e];
+      n[TL_GEMM_SMALL + e] = std::string("gemm_small_") + epi[e];
+      n[TL_GEMV + e] = std::string("gemv_") + epi[e];
+    }
+    return n;
+  }();
+  if (id < 1 || id >= 64 || names[id].empty()) return nullptr;
+  return names[id].c_str();
+}
+
 pf_status pf_session_profile_read(pf_session* s, void* stream, double* ms_out, int64_t* launches_out) {
   if (!s || !ms_out || !launches_out) return fail(PF_ERR_INVALID_ARG, "NULL pointer");
   PF_CUDA(cudaStreamSynchronize(static_cast<cudaStream_t>(stream)), "stream sync");

@@ -185,6 +185,23 @@ inline cudaError_t launch_pdl_pairs(void (*kern)(KArgs...), dim3 grid, dim3 bloc
   return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
 }
 
+// Kernel timeline ids (timeline.cuh); names in pf_timeline_kernel_name.
+enum TimelineId : int {
+  TL_RMSNORM = 1, TL_RMSNORM_REG = 2, TL_QK_ROPE_KV = 3, TL_RING_STORE = 4, TL_EMBED = 5,
+  TL_LM_HEAD = 6, TL_DEQUANT = 7, TL_SET_INT = 8, TL_ARGMAX = 9, TL_WAIT_SELFTEST = 10,
+  TL_LM_HEAD_Q1 = 11, TL_ATTENTION_F32 = 12, TL_ATTENTION_TC = 13, TL_ATTN_COMBINE = 14,
+  TL_GEMM = 20,        // + epilogue (0 store, 1 residual, 2 SwiGLU) + 3 for the CTA-pair form
+  TL_GEMM_SMALL = 30,  // + epilogue
+  TL_GEMV = 40         // + epilogue
+};
+// Per translation unit: points its kernels' timeline buffer at `buf` (NULL: off).
+cudaError_t timeline_set_kernels(unsigned long long* buf);
+cudaError_t timeline_set_gemm_q(unsigned long long* buf);
+cudaError_t timeline_set_gemm_small(unsigned long long* buf);
+cudaError_t timeline_set_gemv(unsigned long long* buf);
+cudaError_t timeline_set_attention(unsigned long long* buf);
+cudaError_t timeline_set_attention_tc(unsigned long long* buf);
+
 int device_sm_count();
 // Tiled tensor map over a 16-bit (bf16 if `bf16`, else f16) array of `rank` dims
 // (innermost first), 128-B swizzle, zero fill out of bounds.

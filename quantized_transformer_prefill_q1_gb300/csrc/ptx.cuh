@@ -6,6 +6,7 @@
 #include <cuda_runtime.h>
 
 #include "pf_internal.h"
+#include "timeline.cuh"
 
 namespace pf {
 

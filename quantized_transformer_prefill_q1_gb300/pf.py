@@ -86,6 +86,8 @@ _SIGS = {
     "pf_session_profile_read": ([_VP, _VP, ctypes.POINTER(ctypes.c_double),
                                  ctypes.POINTER(ctypes.c_int64)], _I32),
     "pf_session_kernel_launches": ([_VP], ctypes.c_int64),
+    "pf_timeline_set": ([_VP, ctypes.c_int64], _I32),
+    "pf_timeline_kernel_name": ([_I32], ctypes.c_char_p),
     "pf_prefill_hidden": ([_VP, _VP, _I32, _I32, _VP, _VP], _I32),
     "pf_layer_forward": ([_VP, _I32, _VP, _I32, _I32, _VP], _I32),
     "pf_prefill_tokens_host": ([_VP, _VP, _I32, _I32, _VP, _VP], _I32),
@@ -274,6 +276,33 @@ def pf_selftest_bounded_wait(status, limit_ns: int, arrive: bool, stream=None):
 
 
 # ------------------------------------------------------------------ model + session
+def pf_timeline_set(buffer, capacity: int) -> None:
+    """Point every libpf kernel's per-CTA timeline at `buffer` (device int64/uint64 tensor
+    of 4 + 4 * capacity words), or stop recording with None."""
+    check(lib().pf_timeline_set(_ptr(buffer), int(capacity) if buffer is not None else 0))
+
+
+def pf_timeline_kernel_name(kernel_id: int) -> Optional[str]:
+    n = lib().pf_timeline_kernel_name(int(kernel_id))
+    return n.decode() if n is not None else None
+
+
+def timeline_records(buffer) -> np.ndarray:
+    """The records of a timeline buffer as a structured array (start_ns, end_ns, kernel,
+    sm, cta), sorted by start; records past the capacity were dropped by the device."""
+    b = buffer.cpu().numpy().view(np.uint64)
+    n = int(min(b[0], b[1]))
+    r = b[4:4 + 4 * n].reshape(n, 4)
+    out = np.zeros(n, dtype=[("start_ns", np.int64), ("end_ns", np.int64), ("kernel", np.int32),
+                             ("sm", np.int32), ("cta", np.int64)])
+    out["start_ns"] = r[:, 0].astype(np.int64)
+    out["end_ns"] = r[:, 1].astype(np.int64)
+    out["kernel"] = (r[:, 2] >> np.uint64(48)).astype(np.int32)
+    out["sm"] = ((r[:, 2] >> np.uint64(32)) & np.uint64(0xffff)).astype(np.int32)
+    out["cta"] = (r[:, 2] & np.uint64(0xffffffff)).astype(np.int64)
+    return np.sort(out, order="start_ns", kind="stable")
+
+
 class DeviceModel:
     """Uploads a stack's weights (packed once, on the host) into device memory owned by
     torch tensors and fills a ``pf_model`` pointing at them."""

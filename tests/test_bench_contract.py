@@ -22,3 +22,17 @@ def test_reference_arm_prints_one_contract_line():
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["value"] == d["value"]
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
     assert "workload" in d["config"]
+
+
+def test_timeline_labels_follow_the_layer_order():
+    """bench.py's timeline case names each launch by its place in the layer: the first
+    RMSNorm of a layer precedes the QKV GEMM, attention precedes the O GEMM, gate_up
+    precedes down."""
+    sys.path.insert(0, ROOT)
+    import bench
+    layer = ["rmsnorm_reg", "gemm_pair_resid", "qk_norm_rope_kv", "attention_tc", "gemm_pair_resid",
+             "rmsnorm_reg", "gemm_pair_swiglu", "gemm_pair_resid"]
+    got = bench.timeline_classes(["set_int", "embed"] + layer * 2 + ["lm_head_q1"])
+    one = ["rmsnorm_attn", "gemm_qkv", "qk_norm_rope_kv", "attention", "gemm_o", "rmsnorm_ffn", "gemm_gate_up",
+           "gemm_down"]
+    assert got == ["set_int", "embed"] + one * 2 + ["lm_head_q1"]
