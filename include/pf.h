@@ -48,7 +48,7 @@ typedef enum {
   PF_ERR_EMPTY_CHUNK = 3,        /* M == 0 ([P3] "empty chunk") */
   PF_ERR_NONSEQUENTIAL_START = 4,/* start_pos != KV position ([P3]) */
   PF_ERR_TOKEN_OUT_OF_VOCAB = 5, /* token < 0 or >= vocab ([P3]) */
-  PF_ERR_KV_CAPACITY = 6,        /* start_pos + M > max_seq */
+  PF_ERR_KV_CAPACITY = 6,        /* start_pos + M > max_seq, or a paged block unassigned */
   PF_ERR_LOGITS = 7,             /* logits requested but no LM head / buffer */
   PF_ERR_UNSUPPORTED = 8,        /* a mode the library does not implement */
   PF_ERR_CUDA = 9,               /* a CUDA runtime call failed */
@@ -84,7 +84,17 @@ typedef struct {
    * cache. */
   int32_t ring_capacity;
   int32_t sink_count;
+  /* Paged KV cache (the "paged" KV layout the target names beside the contiguous one): 0 =
+   * off. P > 0 = K and V each hold P blocks of PF_KV_BLOCK positions per (layer, kv head),
+   * slots = PF_KV_BLOCK * P, and the session's block table (pf_session_set_block_table) maps
+   * position block b = p / PF_KV_BLOCK to the physical block holding positions
+   * b * PF_KV_BLOCK .. +PF_KV_BLOCK-1 (same block for every layer and head). Sessions given
+   * the same K / V buffers and disjoint tables share one pool. Needs a 16-bit cache and no
+   * ring. */
+  int32_t kv_block_pool;
 } pf_config;
+
+#define PF_KV_BLOCK 128 /* positions per paged KV block: one attention key tile */
 
 /* One layer's weights ([P1] LayerWeightRefs), all device pointers. Packed tensors
  * come from pf_pack_weights_host (gate_up with interleave_gate_up = 1). */
@@ -113,7 +123,7 @@ typedef struct pf_session pf_session; /* opaque */
 /* ------------------------------------------------------------------ misc */
 const char* pf_last_error(void);      /* thread-local, never NULL */
 const char* pf_status_name(int status);
-int32_t pf_abi_version(void);         /* bumps on any ABI change (2: ring fields) */
+int32_t pf_abi_version(void);         /* bumps on any ABI change (2: ring fields, 3: kv_block_pool) */
 
 /* ------------------------------------------------------------------ packing
  * Canonical host formats (the pages name "Q1 block bytes" and an "AoS -> SoA"
@@ -139,7 +149,8 @@ pf_status pf_pack_weights_host(int32_t wfmt, const uint8_t* codes_host,
 /* ------------------------------------------------------------------ sizes */
 size_t pf_kv_bytes(const pf_config* cfg);        /* bytes of ONE of K / V:
                                                     n_layers*nkv*slots*hd*elem, slots =
-                                                    ring_capacity (ring) or max_seq */
+                                                    ring_capacity (ring), PF_KV_BLOCK *
+                                                    kv_block_pool (paged) or max_seq */
 size_t pf_workspace_bytes(const pf_config* cfg); /* activations for max_chunk rows,
                                                     RoPE table, status words */
 /* Validates a configuration; PF_OK or the reason it is not supported. Host only. */
@@ -190,6 +201,16 @@ typedef enum {
 pf_status pf_session_set_profile(pf_session* s, int32_t enable);
 pf_status pf_session_profile_read(pf_session* s, void* stream, double* ms_out,
                                   int64_t* launches_out);
+/* Paged caches: sets the session's block table from a HOST array of
+ * ceil(max_seq / PF_KV_BLOCK) entries; entry b is the physical block (0 .. kv_block_pool-1)
+ * of positions b * PF_KV_BLOCK .. +PF_KV_BLOCK-1, or -1 while unassigned. Assigned entries
+ * must be distinct. A chunk whose positions reach an unassigned block is refused
+ * (PF_ERR_KV_CAPACITY) before any launch. Copied to the workspace synchronously: call with
+ * none of the session's work in flight. New sessions start with every entry unassigned.
+ * Errors: PF_ERR_UNSUPPORTED (not a paged configuration), PF_ERR_SHAPE (wrong count, entry
+ * out of range, repeated block), PF_ERR_CUDA. */
+pf_status pf_session_set_block_table(pf_session* s, const int32_t* table_host, int32_t n_entries);
+
 /* Number of libpf kernels enqueued by this session so far (graph replays count every
  * kernel node they run). */
 int64_t pf_session_kernel_launches(const pf_session* s);

@@ -146,6 +146,7 @@ struct AttnKParams {
   __half* out;
   float* partial;
   int* status;
+  const int* blocks;  // paged cache: block table (position block -> physical block), else NULL
 };
 
 __device__ __forceinline__ void mbar_wait_drain_a(uint32_t bar, uint32_t parity) {
@@ -324,10 +325,18 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_arrive_expect_tx(q_full, L::Q);
       for (int h = 0; h < NH; ++h)
         tma_load_3d(q_s + h * (TQ * 128), &tm_q, h * 64, kvh * G, t0, q_full);
-      // K_i, then V_{i-1}: K runs one tile ahead of V
+      // K_i, then V_{i-1}: K runs one tile ahead of V. A paged cache's tiles are whole blocks
+      // (tile j of the list = position block j): its row comes from the block table, read a
+      // tile ahead so the load's latency hides behind the stage waits.
+      const bool paged = P.blocks != nullptr;
+      auto cache_row = [&](const KeyTile& t, int blk) {
+        return t.src ? brow0 + t.row : crow0 + (paged ? blk * TK : t.row);
+      };
+      int blk_cur = paged && nt > 0 ? P.blocks[kt.at(jb).pos0 / TK] : 0, blk_prev = 0;
       int k_issued = 0, v_issued = 0;
       bool ok = true;
       for (int i = 0; i <= nt && ok; ++i) {
+        const int blk_next = paged && i + 1 < nt ? P.blocks[kt.at(jb + i + 1).pos0 / TK] : 0;
         if (i < nt) {
           const int s = i % KS;
           if (!mbar_wait(k_empty(s), ((i / KS) & 1) ^ 1, abort_flag)) {
@@ -336,7 +345,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
           const KeyTile kt_i = kt.at(jb + i);
           const CUtensorMap* mk = kt_i.src ? &tm_kc : &tm_k;
-          const int row = (kt_i.src ? brow0 : crow0) + kt_i.row;
+          const int row = cache_row(kt_i, blk_cur);
           mbar_arrive_expect_tx(k_full(s), L::KV);
           for (int h = 0; h < NH; ++h) tma_load_2d(k_tile(s) + h * (TK * 128), mk, h * 64, row, k_full(s));
           ++k_issued;
@@ -349,11 +358,13 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
           const KeyTile kt_v = kt.at(jb + jv);
           const CUtensorMap* mv = kt_v.src ? &tm_vc : &tm_v;
-          const int row = (kt_v.src ? brow0 : crow0) + kt_v.row;
+          const int row = cache_row(kt_v, blk_prev);
           mbar_arrive_expect_tx(v_full(s), L::KV);
           for (int h = 0; h < NH; ++h) tma_load_2d(v_tile(s) + h * (TK * 128), mv, h * 64, row, v_full(s));
           ++v_issued;
         }
+        blk_prev = blk_cur;
+        blk_cur = blk_next;
       }
       if (*abort_flag) {  // let copies already in flight land before shared memory is released
         mbar_wait_drain_a(q_full, 0);
@@ -628,7 +639,7 @@ cudaError_t launch_tc(const AttnArgs& a, cudaStream_t st) {
   const int G = c.n_q_heads / c.n_kv_heads;
   const int BT = TQ / G;
   const bool ring = c.ring_capacity > 0;
-  const int cache_rows = ring ? c.ring_capacity : c.max_seq;
+  const int cache_rows = cache_slots(c);
   const uint64_t rows = static_cast<uint64_t>(c.n_layers) * c.n_kv_heads * cache_rows;
   CUtensorMap tq, tk, tv, tkc, tvc;
   const uint64_t qd[3] = {static_cast<uint64_t>(HD), static_cast<uint64_t>(c.n_q_heads),
@@ -668,6 +679,7 @@ cudaError_t launch_tc(const AttnArgs& a, cudaStream_t st) {
   p.out = reinterpret_cast<__half*>(a.out);
   p.partial = a.partial;
   p.status = a.status;
+  p.blocks = a.blocks;
   dim3 grid((a.M + BT - 1) / BT, c.n_kv_heads, n_split);
   cudaError_t e = launch_pdl(attn_tc_kernel<HD, BF16>, grid, dim3(THREADS), ASmem<HD>::BYTES, st, tq, tk,
                              tv, tkc, tvc, p);

@@ -281,26 +281,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     fence_barrier_init();
     fence_proxy_async_smem();
   }
-  if (warp == 1) {
-    __syncwarp();
-    if (PAIR) {
-      tmem_alloc_pair(smem_u32(tmem_slot), TMEM_COLS);
-      tmem_relinquish_pair();
-    } else {
-      tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
-      tmem_relinquish();
-    }
-  }
-  tc_fence_before();
-  if (PAIR)
-    cluster_sync_all();  // both CTAs' barriers exist before either arrives on the other's
-  else
-    __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem_base = *tmem_slot;
   // Only the activation tiles and the epilogue's global accesses depend on the previous
   // kernel in the stream (griddep_wait below); the packed weights do not, so the producer
-  // issues the first stages' weight copies before waiting for it.
+  // issues the first stages' weight copies right after its own barriers exist, before the
+  // TMEM allocation, the pair's cluster barrier and the wait.
   const int G = K / GROUP;
   const Range rg(plan, unit);
   const int a_row = static_cast<int>(rank) * BM;  // this CTA's first token row of a tile
@@ -319,21 +303,42 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         bulk_load(dst + (BN / 2) * (CODE + 2), chunk + F::META_OFF + 2 * BN + rank * BN, BN, full(s));
     }
   };
+  __syncthreads();  // this CTA's barriers are initialised
+  int pre = 0;      // (producer thread) stages whose weight copies are issued before the wait
+  if (threadIdx.x == 0) {
+    for (int k = 0; k < rg.n && pre < S; ++k) {
+      const Segment sg = rg.at(plan, k);
+      for (int i = 0; i < sg.nkb && pre < S; ++i, ++pre) {
+        const int kb = sg.kb0 + i;
+        const uint8_t* chunk =
+            wpk + (static_cast<size_t>(sg.nt) * G + (kb >> 1)) * static_cast<size_t>(F::CHUNK);
+        mbar_arrive_expect_tx(full(pre), A_STAGE + P_STAGE);
+        load_packed(pre, chunk, kb);
+      }
+    }
+  }
+  if (warp == 1) {
+    __syncwarp();
+    if (PAIR) {
+      tmem_alloc_pair(smem_u32(tmem_slot), TMEM_COLS);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+      tmem_relinquish();
+    }
+  }
+  tc_fence_before();
+  __syncwarp();
+  if (PAIR)
+    cluster_sync_all();  // both CTAs' barriers exist before either arrives on the other's
+  else
+    __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
 
   if (warp == 0) {
     // ---------------------------------------------------------------- TMA producer
     if (lane == 0) {
-      int pre = 0;            // stages whose weight copies are issued before the wait
-      for (int k = 0; k < rg.n && pre < S; ++k) {
-        const Segment sg = rg.at(plan, k);
-        for (int i = 0; i < sg.nkb && pre < S; ++i, ++pre) {
-          const int kb = sg.kb0 + i;
-          const uint8_t* chunk =
-              wpk + (static_cast<size_t>(sg.nt) * G + (kb >> 1)) * static_cast<size_t>(F::CHUNK);
-          mbar_arrive_expect_tx(full(pre), A_STAGE + P_STAGE);
-          load_packed(pre, chunk, kb);
-        }
-      }
       griddep_wait();  // the activations come from the previous kernel
       for (int k = 0, j = 0; k < rg.n && j < pre; ++k) {
         const Segment sg = rg.at(plan, k);

@@ -161,7 +161,7 @@ __global__ void __launch_bounds__(256) qk_norm_rope_kv_kernel(
     const float* __restrict__ qkv, const float* __restrict__ qn, const float* __restrict__ kn,
     const float* __restrict__ rope, int M, int nq, int nkv, int kv_rows, int kv_layer, int kv_by_pos,
     const int* __restrict__ start_dev, int start_host, float eps, int qk_norm,
-    QT* __restrict__ q_out, KT* __restrict__ kc, KT* __restrict__ vc) {
+    QT* __restrict__ q_out, KT* __restrict__ kc, KT* __restrict__ vc, const int* __restrict__ blocks) {
   PF_TIMELINE(TL_QK_ROPE_KV);
   constexpr int HALF = HD / 2;
   constexpr int LPH = HALF / 4;   // lanes per head
@@ -202,7 +202,8 @@ __global__ void __launch_bounds__(256) qk_norm_rope_kv_kernel(
 #pragma unroll
   for (int o = LPH / 2; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
   if (!valid) return;
-  const int kv_row = kv_by_pos ? pos : t;
+  // cache slot of the position; a paged cache goes through the block table
+  const int kv_row = !kv_by_pos ? t : (blocks ? blocks[pos / PF_KV_BLOCK] * PF_KV_BLOCK + pos % PF_KV_BLOCK : pos);
   if (is_v) {  // V head: straight to the cache
     KT* dst = vc + ((static_cast<size_t>(kv_layer) * nkv + (j - nq - nkv)) * kv_rows + kv_row) * HD;
     store4<KT>(dst + 4 * l, a.x, a.y, a.z, a.w);
@@ -503,6 +504,7 @@ cudaError_t launch_rmsnorm(const float* x, const float* w, float eps, int M, int
 
 struct QkDst {
   int kv_layer, kv_rows, kv_by_pos;
+  const int* blocks;  // paged cache: block table, else NULL
 };
 
 template <int HD, typename QT, typename KT>
@@ -516,7 +518,7 @@ static void qk_launch(const pf_config& c, const float* qkv, const float* qn, con
   launch_pdl(qk_norm_rope_kv_kernel<HD, QT, KT>, dim3(blocks), dim3(256), 0, stream, qkv, qn, kn,
              rope, M, c.n_q_heads, c.n_kv_heads, d.kv_rows, d.kv_layer, d.kv_by_pos, start_dev,
              start_host, c.eps, c.qk_norm, reinterpret_cast<QT*>(q), reinterpret_cast<KT*>(kc),
-             reinterpret_cast<KT*>(vc));
+             reinterpret_cast<KT*>(vc), d.blocks);
 }
 
 template <int HD>
@@ -539,8 +541,9 @@ static void qk_dispatch_kv(const pf_config& c, const float* qkv, const float* qn
 cudaError_t launch_qk_norm_rope_kv(const pf_config& c, const float* qkv, const float* q_norm,
                                    const float* k_norm, const float* rope, int kv_layer, int kv_rows,
                                    int kv_by_pos, const int* start_dev, int start_host, int M,
-                                   void* q_out, void* k_dst, void* v_dst, cudaStream_t stream) {
-  const QkDst d{kv_layer, kv_rows, kv_by_pos};
+                                   void* q_out, void* k_dst, void* v_dst, cudaStream_t stream,
+                                   const int* blocks) {
+  const QkDst d{kv_layer, kv_rows, kv_by_pos, blocks};
   if (c.head_dim == 128)
     qk_dispatch_kv<128>(c, qkv, q_norm, k_norm, rope, d, start_dev, start_host, M, q_out, k_dst,
                         v_dst, stream);

@@ -52,6 +52,7 @@ struct WsLayout {
   size_t status, params, tokens, x, y, qkv, q, attn, act, logits, gemm, gemm_bytes, rope;
   size_t kchunk, vchunk;          // ring mode: the chunk's K / V rows [nkv][max_chunk][hd]
   size_t attn_part, attn_part_bytes;  // split-KV partial results
+  size_t blocks;                      // paged cache: block table [block_table_entries] int32
   size_t total;
 };
 
@@ -86,6 +87,7 @@ WsLayout ws_layout(const pf_config& c) {
   L.vchunk = take(chunk_kv);
   L.attn_part_bytes = attention_partial_bytes_max(c, GEMM_MAX_CTAS);
   L.attn_part = take(L.attn_part_bytes);
+  L.blocks = take(c.kv_block_pool > 0 ? block_table_entries(c) * sizeof(int) : 0);
   L.total = o;
   return L;
 }
@@ -210,6 +212,7 @@ struct pf_session {
   std::vector<ProfRecord> prof;
   std::vector<cudaEvent_t> event_pool;
   cudaStream_t capture_stream = nullptr;
+  std::vector<int32_t> blocks;  // paged cache: host copy of the block table (-1 = unassigned)
 };
 
 namespace {
@@ -251,6 +254,24 @@ pf_status check_cfg(const pf_config* c) {
   } else if (c->sink_count != 0) {
     return fail(PF_ERR_SHAPE, "sink_count %d without a ring cache", c->sink_count);
   }
+  if (c->kv_block_pool < 0) return fail(PF_ERR_SHAPE, "kv_block_pool %d", c->kv_block_pool);
+  if (c->kv_block_pool > 0) {
+    if (c->ring_capacity > 0) return fail(PF_ERR_SHAPE, "a paged cache cannot also be a ring");
+    if (!attention_tc_supported(*c))
+      return fail(PF_ERR_UNSUPPORTED, "paged cache: needs a 16-bit cache (bf16 / f16) and a GQA group dividing 128");
+    if (static_cast<int64_t>(c->kv_block_pool) * PF_KV_BLOCK > (int64_t{1} << 30))
+      return fail(PF_ERR_SHAPE, "kv_block_pool %d too large", c->kv_block_pool);
+  }
+  return PF_OK;
+}
+
+// Paged caches: every position block of [0, end) has a physical block.
+pf_status check_blocks(const pf_session* s, int64_t end) {
+  if (s->model.cfg.kv_block_pool <= 0) return PF_OK;
+  for (int64_t b = 0; b * PF_KV_BLOCK < end; ++b)
+    if (b >= static_cast<int64_t>(s->blocks.size()) || s->blocks[b] < 0)
+      return fail(PF_ERR_KV_CAPACITY, "paged cache: position block %lld (positions %lld..) has no physical block",
+                  static_cast<long long>(b), static_cast<long long>(b * PF_KV_BLOCK));
   return PF_OK;
 }
 
@@ -341,12 +362,13 @@ pf_status enqueue_layer(pf_session* s, int l, float* x, int M, cudaStream_t st, 
   //    takes the chunk's K / V in the chunk buffers first (its later tokens may overwrite
   //    slots its earlier tokens still see) and into the ring after the attention.
   const bool ring = c.ring_capacity > 0;
+  const int* blocks = c.kv_block_pool > 0 ? wsp<int>(s, s->L.blocks) : nullptr;
   void* kc = ring ? wsp<void>(s, s->L.kchunk) : s->k;
   void* vc = ring ? wsp<void>(s, s->L.vchunk) : s->v;
   PF_TRY(launch_k(s, PF_K_QK_ROPE_KV, st, "qk_norm_rope_kv", [&] {
     return launch_qk_norm_rope_kv(c, qkv, w.q_norm, w.k_norm, wsp<float>(s, s->L.rope), ring ? 0 : l,
-                                  ring ? c.max_chunk : c.max_seq, ring ? 0 : 1, start_dev, 0, M, q, kc,
-                                  vc, st);
+                                  ring ? c.max_chunk : cache_slots(c), ring ? 0 : 1, start_dev, 0, M, q, kc,
+                                  vc, st, blocks);
   }));
   AttnArgs aa{};
   aa.c = &c;
@@ -363,6 +385,7 @@ pf_status enqueue_layer(pf_session* s, int l, float* x, int M, cudaStream_t st, 
   aa.n_split = attention_splits(c, M, std::min(s->sms, GEMM_MAX_CTAS));
   aa.partial = wsp<float>(s, s->L.attn_part);
   aa.status = wsp<int>(s, s->L.status);
+  aa.blocks = blocks;
   PF_TRY(launch_k(s, PF_K_ATTENTION, st, "attention", [&] { return launch_attention(aa, st); }));
   if (ring)
     PF_TRY(launch_k(s, PF_K_QK_ROPE_KV, st, "ring store", [&] {
@@ -484,7 +507,7 @@ const char* pf_status_name(int st) {
   }
 }
 
-int32_t pf_abi_version(void) { return 2; }
+int32_t pf_abi_version(void) { return 3; }
 
 size_t pf_packed_bytes(int32_t wfmt, int64_t N, int64_t K) {
   if ((wfmt != PF_W_Q1_G128 && wfmt != PF_W_INT4_AFFINE_G128) || N <= 0 || K <= 0 || K % GROUP)
@@ -579,7 +602,7 @@ pf_status pf_pack_weights_host(int32_t wfmt, const uint8_t* codes, const uint16_
 
 size_t pf_kv_bytes(const pf_config* c) {
   if (check_cfg(c) != PF_OK) return 0;
-  const int slots = c->ring_capacity > 0 ? c->ring_capacity : c->max_seq;
+  const int slots = cache_slots(*c);
   return static_cast<size_t>(c->n_layers) * c->n_kv_heads * slots * c->head_dim *
          kv_elem_bytes(c->kv_dtype);
 }
@@ -662,6 +685,10 @@ pf_status pf_session_create(const pf_model* model, void* k, void* v, void* ws, s
   cudaError_t e = cudaMemcpyAsync(s->ws + L.rope, rope.data(), rope.size() * 4, cudaMemcpyHostToDevice, st);
   if (e == cudaSuccess) e = cudaMemsetAsync(s->ws + L.status, 0, STATUS_WORDS * 4, st);
   if (e == cudaSuccess) e = cudaMemsetAsync(s->ws + L.gemm, 0, L.gemm_bytes, st);  // tile counters
+  if (c.kv_block_pool > 0) {  // every position block unassigned (-1)
+    s->blocks.assign(block_table_entries(c), -1);
+    if (e == cudaSuccess) e = cudaMemsetAsync(s->ws + L.blocks, 0xff, s->blocks.size() * sizeof(int), st);
+  }
   if (e == cudaSuccess) e = cudaStreamSynchronize(st);
   if (e != cudaSuccess) {
     delete s;
@@ -692,6 +719,27 @@ pf_status pf_session_set_position(pf_session* s, int32_t position) {
   if (position < 0 || position > s->model.cfg.max_seq)
     return fail(PF_ERR_KV_CAPACITY, "position %d outside [0, %d]", position, s->model.cfg.max_seq);
   s->position = position;
+  return PF_OK;
+}
+
+pf_status pf_session_set_block_table(pf_session* s, const int32_t* table, int32_t n) {
+  if (!s) return fail(PF_ERR_INVALID_ARG, "session is NULL");
+  const pf_config& c = s->model.cfg;
+  if (c.kv_block_pool <= 0) return fail(PF_ERR_UNSUPPORTED, "not a paged cache (kv_block_pool 0)");
+  if (!table) return fail(PF_ERR_INVALID_ARG, "table is NULL");
+  if (n != block_table_entries(c))
+    return fail(PF_ERR_SHAPE, "block table of %d entries; this configuration has %d", n, block_table_entries(c));
+  std::vector<char> used(c.kv_block_pool, 0);
+  for (int i = 0; i < n; ++i) {
+    if (table[i] == -1) continue;
+    if (table[i] < 0 || table[i] >= c.kv_block_pool)
+      return fail(PF_ERR_SHAPE, "block table entry %d = %d outside [0, %d) (or -1)", i, table[i], c.kv_block_pool);
+    if (used[table[i]]) return fail(PF_ERR_SHAPE, "block table entry %d repeats physical block %d", i, table[i]);
+    used[table[i]] = 1;
+  }
+  PF_CUDA(cudaMemcpy(s->ws + s->L.blocks, table, static_cast<size_t>(n) * sizeof(int), cudaMemcpyHostToDevice),
+          "block table upload");
+  s->blocks.assign(table, table + n);
   return PF_OK;
 }
 
@@ -803,6 +851,8 @@ static pf_status prefill_common(pf_session* s, const int32_t* tokens, bool token
   pf_status v = pf_validate_chunk(&c, s->position, tokens_on_device ? nullptr : tokens, M, start,
                                   logits != nullptr, has_head);
   if (v != PF_OK) return v;
+  v = check_blocks(s, static_cast<int64_t>(start) + M);
+  if (v != PF_OK) return v;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   int off = 0;
   while (off < M) {  // micro-batches of at most max_chunk rows; head on the last only
@@ -910,8 +960,10 @@ pf_status pf_layer_forward(pf_session* s, int32_t layer, float* x_dev, int32_t M
   if (!x_dev) return fail(PF_ERR_INVALID_ARG, "x is NULL");
   if (start_pos < 0 || static_cast<int64_t>(start_pos) + M > c.max_seq)
     return fail(PF_ERR_KV_CAPACITY, "chunk [%d, %d) exceeds KV capacity %d", start_pos, start_pos + M, c.max_seq);
+  pf_status r = check_blocks(s, static_cast<int64_t>(start_pos) + M);
+  if (r != PF_OK) return r;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  pf_status r = set_start(s, start_pos, st);
+  r = set_start(s, start_pos, st);
   if (r != PF_OK) return r;
   GraphKey key{M, x_dev, nullptr, nullptr, layer};
   return run_maybe_graph(s, key, st,
@@ -1069,7 +1121,8 @@ pf_status pf_op_qk_norm_rope_kv(const pf_config* cfg, const float* qkv, const fl
                                 int32_t M, void* q, void* kc, void* vc, void* stream) {
   pf_status r = check_cfg(cfg);
   if (r != PF_OK) return r;
-  if (cfg->ring_capacity > 0) return fail(PF_ERR_UNSUPPORTED, "single-step KV store: linear caches only");
+  if (cfg->ring_capacity > 0 || cfg->kv_block_pool > 0)
+    return fail(PF_ERR_UNSUPPORTED, "single-step KV store: linear caches only");
   if (!qkv || !rope || !q || !kc || !vc || (cfg->qk_norm && (!qn || !kn)))
     return fail(PF_ERR_INVALID_ARG, "NULL pointer");
   if (M <= 0 || layer < 0 || layer >= cfg->n_layers || start < 0 ||
@@ -1086,7 +1139,8 @@ static pf_status attention_op(const pf_config* cfg, const void* q, const void* k
                               size_t scratch_bytes, uint16_t* out, void* stream) {
   pf_status r = check_cfg(cfg);
   if (r != PF_OK) return r;
-  if (cfg->ring_capacity > 0) return fail(PF_ERR_UNSUPPORTED, "single-step attention: linear caches only");
+  if (cfg->ring_capacity > 0 || cfg->kv_block_pool > 0)
+    return fail(PF_ERR_UNSUPPORTED, "single-step attention: linear caches only");
   if (!q || !kc || !vc || !out) return fail(PF_ERR_INVALID_ARG, "NULL pointer");
   if (M <= 0 || layer < 0 || layer >= cfg->n_layers || start < 0 ||
       static_cast<int64_t>(start) + M > cfg->max_seq)

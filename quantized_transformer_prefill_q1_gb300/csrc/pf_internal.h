@@ -17,6 +17,13 @@
 namespace pf {
 
 // ------------------------------------------------------------------ packed weight layout
+// Cache slots per (layer, kv head): ring slots, paged blocks x PF_KV_BLOCK, or max_seq.
+inline int cache_slots(const pf_config& c) {
+  return c.ring_capacity > 0 ? c.ring_capacity : (c.kv_block_pool > 0 ? c.kv_block_pool * PF_KV_BLOCK : c.max_seq);
+}
+// Entries of a paged session's block table.
+inline int block_table_entries(const pf_config& c) { return (c.max_seq + PF_KV_BLOCK - 1) / PF_KV_BLOCK; }
+
 // Tiles of TILE_N = 256 rows x GROUP = 128 weights ("chunks"), chunk (t, g) at byte
 // offset (t * K/128 + g) * chunk_bytes. Inside a chunk, each half h (k in
 // [128g + 64h, 128g + 64h + 64)) of every row is contiguous so that one GEMM stage
@@ -96,13 +103,15 @@ cudaError_t launch_rmsnorm(const float* x, const float* w, float eps, int M, int
                            cudaStream_t stream, float* zero = nullptr, int zero_cols = 0);
 cudaError_t launch_dequant(int wfmt, const uint8_t* packed, int64_t N, int64_t K, void* w_f16,
                            cudaStream_t stream);
-// K and V go to row (kv_layer * nkv + kvh) * kv_rows + (kv_by_pos ? start + t : t) of
-// k_dst / v_dst: the cache slot of position start + t (kv_layer = layer, kv_rows = max_seq,
-// kv_by_pos = 1) or row t of the ring mode's chunk buffers (0, chunk rows, 0).
+// K and V go to row (kv_layer * nkv + kvh) * kv_rows + (kv_by_pos ? slot(start + t) : t) of
+// k_dst / v_dst: the cache slot of position p = start + t (kv_layer = layer, kv_rows = cache
+// slots, kv_by_pos = 1; slot(p) = p, or with a block table blocks[p / PF_KV_BLOCK] *
+// PF_KV_BLOCK + p % PF_KV_BLOCK) or row t of the ring mode's chunk buffers (0, chunk rows, 0).
 cudaError_t launch_qk_norm_rope_kv(const pf_config& c, const float* qkv, const float* q_norm,
                                    const float* k_norm, const float* rope, int kv_layer, int kv_rows,
                                    int kv_by_pos, const int* start_dev, int start_host, int M,
-                                   void* q_out, void* k_dst, void* v_dst, cudaStream_t stream);
+                                   void* q_out, void* k_dst, void* v_dst, cudaStream_t stream,
+                                   const int* blocks = nullptr);
 // Keys an attention launch reads. A linear cache holds position p of (layer, kv head) at row
 // (layer * nkv + kvh) * max_seq + p. A ring cache (ring_capacity R > 0, sink_count S) holds
 // position p at slot p (p < S) or S + (p - S) mod (R - S), row (layer * nkv + kvh) * R + slot;
@@ -124,6 +133,7 @@ struct AttnArgs {
   int n_split;          // key-tile parts (split-KV); 1 = none
   float* partial;       // n_split > 1: attention_partial_bytes(c, M, n_split) bytes
   int* status;
+  const int* blocks;    // paged cache: the block table (device), else NULL
 };
 cudaError_t launch_attention(const AttnArgs& a, cudaStream_t stream);
 // Split-KV parts for a chunk of M rows on `sms` SMs (1 unless the chunk's CTAs fill less

@@ -45,7 +45,9 @@ class pf_config(ctypes.Structure):
                 ("qk_norm", ctypes.c_int32), ("wfmt", ctypes.c_int32),
                 ("kv_dtype", ctypes.c_int32), ("max_seq", ctypes.c_int32),
                 ("max_chunk", ctypes.c_int32), ("ring_capacity", ctypes.c_int32),
-                ("sink_count", ctypes.c_int32)]
+                ("sink_count", ctypes.c_int32), ("kv_block_pool", ctypes.c_int32)]
+
+KV_BLOCK = 128  # PF_KV_BLOCK: positions per paged KV block
 
 
 class pf_layer_weights(ctypes.Structure):
@@ -76,6 +78,7 @@ _SIGS = {
     "pf_session_position": ([_VP], _I32),
     "pf_session_set_position": ([_VP, _I32], _I32),
     "pf_session_set_graphs": ([_VP, _I32], _I32),
+    "pf_session_set_block_table": ([_VP, _VP, _I32], _I32),
     "pf_session_sync": ([_VP, _VP], _I32),
     "pf_prefill_chunk": ([_VP, _VP, _I32, _I32, _VP, _VP], _I32),
     "pf_prefill_chunk_dev": ([_VP, _VP, _I32, _I32, _VP, _VP], _I32),
@@ -156,7 +159,8 @@ def _stream(stream=None) -> Optional[int]:
 
 # ------------------------------------------------------------------ host-side calls
 def make_config(shape, max_chunk: int, n_layers: Optional[int] = None, max_seq: Optional[int] = None,
-                vocab: Optional[int] = None, ring_capacity: int = 0, sink_count: int = 0) -> pf_config:
+                vocab: Optional[int] = None, ring_capacity: int = 0, sink_count: int = 0,
+                kv_block_pool: int = 0) -> pf_config:
     return pf_config(hidden=shape.hidden, intermediate=shape.intermediate,
                      n_q_heads=shape.n_q_heads, n_kv_heads=shape.n_kv_heads,
                      head_dim=shape.head_dim,
@@ -166,7 +170,7 @@ def make_config(shape, max_chunk: int, n_layers: Optional[int] = None, max_seq: 
                      qk_norm=int(shape.qk_norm), wfmt=_WFMT[shape.wfmt],
                      kv_dtype=_KVDT[shape.kv_dtype],
                      max_seq=shape.max_seq if max_seq is None else max_seq, max_chunk=max_chunk,
-                     ring_capacity=ring_capacity, sink_count=sink_count)
+                     ring_capacity=ring_capacity, sink_count=sink_count, kv_block_pool=kv_block_pool)
 
 
 def pf_packed_bytes(wfmt: int, n: int, k: int) -> int:
@@ -309,7 +313,7 @@ class DeviceModel:
 
     def __init__(self, shape, layers: Sequence[Dict], extra: Optional[Dict] = None,
                  max_chunk: int = 512, device: str = "cuda", max_seq: Optional[int] = None,
-                 ring_capacity: int = 0, sink_count: int = 0):
+                 ring_capacity: int = 0, sink_count: int = 0, kv_block_pool: int = 0):
         import torch
         self.shape = shape
         self.keep: List = []
@@ -326,7 +330,8 @@ class DeviceModel:
         n = len(layers)
         self.cfg = make_config(shape, max_chunk, n_layers=n, max_seq=max_seq,
                                vocab=shape.vocab if "lm_head" in extra else 0,
-                               ring_capacity=ring_capacity, sink_count=sink_count)
+                               ring_capacity=ring_capacity, sink_count=sink_count,
+                               kv_block_pool=kv_block_pool)
         self.layer_arr = (pf_layer_weights * n)()
         for i, w in enumerate(layers):
             lw = self.layer_arr[i]
@@ -353,15 +358,22 @@ class Session:
     """A pf_session with its KV cache and workspace allocated by torch (caller-owned)."""
 
     def __init__(self, dm: DeviceModel, stream=None, kv_fill_bits: Optional[int] = None,
-                 graphs: bool = True):
+                 graphs: bool = True, kv=None, block_table: Optional[Sequence[int]] = None):
+        """`kv`: an existing (k, v) pair to share (paged caches: one pool, disjoint block
+        tables); `block_table`: a paged session's table (default: position block b in
+        physical block b, when the pool has enough blocks)."""
         import torch
         self.dm = dm
         c = dm.cfg
         dt = getattr(torch, _KV_TORCH[c.kv_dtype])
-        slots = c.ring_capacity if c.ring_capacity > 0 else c.max_seq
+        slots = c.ring_capacity if c.ring_capacity > 0 else (
+            c.kv_block_pool * KV_BLOCK if c.kv_block_pool > 0 else c.max_seq)
         shape = (c.n_layers, c.n_kv_heads, slots, c.head_dim)
-        self.k = torch.empty(shape, dtype=dt, device="cuda")
-        self.v = torch.empty(shape, dtype=dt, device="cuda")
+        if kv is not None:
+            self.k, self.v = kv
+        else:
+            self.k = torch.empty(shape, dtype=dt, device="cuda")
+            self.v = torch.empty(shape, dtype=dt, device="cuda")
         if kv_fill_bits is not None:  # sentinel bit pattern in every slot
             ib = torch.int32 if c.kv_dtype == KV_F32 else torch.int16
             self.k.view(ib).fill_(kv_fill_bits)
@@ -376,6 +388,16 @@ class Session:
                                       _ptr(self.ws), wsb, _stream(stream), ctypes.byref(h)))
         self.h = h
         check(lib().pf_session_set_graphs(self.h, int(graphs)))
+        if c.kv_block_pool > 0:
+            n = -(-c.max_seq // KV_BLOCK)
+            if block_table is None and c.kv_block_pool >= n:
+                block_table = range(n)
+            if block_table is not None:
+                self.set_block_table(block_table)
+
+    def set_block_table(self, table: Sequence[int]) -> None:
+        t = np.ascontiguousarray(np.asarray(table, dtype=np.int32))
+        check(lib().pf_session_set_block_table(self.h, _ptr(t), len(t)))
 
     @property
     def position(self) -> int:

@@ -160,7 +160,25 @@ def test_ring_config_check_and_sizes(lib):
         assert lib.pf_config_check(ctypes.byref(bad)) == want, (R, S)
     f32 = pf.make_config(dataclasses.replace(s, kv_dtype="f32"), 512, ring_capacity=64, sink_count=0)
     assert lib.pf_config_check(ctypes.byref(f32)) == 8  # PF_ERR_UNSUPPORTED
-    assert lib.pf_abi_version() == 2
+    assert lib.pf_abi_version() == 3
+
+
+def test_paged_config_check_and_sizes(lib):
+    # paged cache: P blocks of PF_KV_BLOCK = 128 positions per (layer, kv head); a 16-bit cache,
+    # not combined with a ring; K/V hold 128 P slots; the workspace gains the block table
+    import dataclasses
+    s = synth.QWEN3_8B_LAYER  # max_seq 4096: 32 position blocks
+    paged = pf.make_config(s, 512, kv_block_pool=40)
+    assert lib.pf_config_check(ctypes.byref(paged)) == 0
+    assert lib.pf_kv_bytes(ctypes.byref(paged)) == 1 * 8 * (40 * 128) * 128 * 2
+    linear = pf.make_config(s, 512)
+    extra = lib.pf_workspace_bytes(ctypes.byref(paged)) - lib.pf_workspace_bytes(ctypes.byref(linear))
+    assert 32 * 4 <= extra <= 32 * 4 + 256
+    assert lib.pf_config_check(ctypes.byref(pf.make_config(s, 512, kv_block_pool=-1))) == 2  # PF_ERR_SHAPE
+    both = pf.make_config(s, 512, kv_block_pool=8, ring_capacity=1024, sink_count=4)
+    assert lib.pf_config_check(ctypes.byref(both)) == 2
+    f32 = pf.make_config(dataclasses.replace(s, kv_dtype="f32"), 512, kv_block_pool=8)
+    assert lib.pf_config_check(ctypes.byref(f32)) == 8  # PF_ERR_UNSUPPORTED
 
 
 def test_attention_scratch_bytes(lib):
