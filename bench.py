@@ -100,14 +100,42 @@ def timeline_classes(names):
     return labels
 
 
+def timeline_prompt(pf, torch, step, cap=1 << 20):
+    """Runs `step` once with the per-CTA kernel timeline on and returns (prompt us, launches,
+    {class: [(crit, gap, span, end spread, ctas) per launch, ns]}). Launches are the runs of
+    equal kernel id in start order (with programmatic launch a kernel's CTAs all start before
+    the next kernel's first); `crit` = a launch's last CTA end minus the previous launch's
+    last end, so the crits add up to the prompt."""
+    import numpy as np
+    buf = torch.zeros(4 + 4 * cap, dtype=torch.int64, device="cuda")
+    pf.pf_timeline_set(buf, cap)
+    step()
+    torch.cuda.synchronize()
+    pf.pf_timeline_set(None, 0)
+    rec = pf.timeline_records(buf)
+    ids = rec["kernel"]
+    cut = np.flatnonzero(np.diff(ids) != 0) + 1
+    bounds = list(zip(np.concatenate([[0], cut]), np.concatenate([cut, [len(ids)]])))
+    names = [pf.pf_timeline_kernel_name(int(ids[a])) for a, _ in bounds]
+    labels = timeline_classes(names)
+    t_first = int(rec["start_ns"].min())
+    prev, per = t_first, {}
+    for (a, z), lab in zip(bounds, labels):
+        st, en = rec["start_ns"][a:z], rec["end_ns"][a:z]
+        e1 = int(en.max())
+        per.setdefault(lab, []).append((e1 - prev, int(st.min()) - prev, e1 - int(st.min()), e1 - int(en.min()),
+                                        int(z - a)))
+        prev = max(prev, e1)
+    return (prev - t_first) / 1e3, len(bounds), per
+
+
 def run_timeline(args, pf, synth):
     """One 2048-token prompt of the workload (graphs replayed, as in the timed steps) with
-    the per-CTA kernel timeline on. Launches are the runs of equal kernel id in start order
-    (with programmatic launch a kernel's CTAs all start before the next kernel's first). Per
-    launch: `crit` = its last CTA's end minus the previous launch's last end, so the crits
-    add up to the prompt's time; `gap` = its first CTA's start minus the previous launch's
-    last end (negative: started early under programmatic launch); `spread` = last minus
-    first CTA end. Prints one JSON line with the mean of each per layer class."""
+    the per-CTA kernel timeline on. Per launch: `crit` = its last CTA's end minus the
+    previous launch's last end, so the crits add up to the prompt's time; `gap` = its first
+    CTA's start minus the previous launch's last end (negative: started early under
+    programmatic launch); `spread` = last minus first CTA end. Prints one JSON line with the
+    mean of each per layer class."""
     import numpy as np
     import torch
     shape = synth.QWEN3_8B_STACK
@@ -125,29 +153,9 @@ def run_timeline(args, pf, synth):
     for _ in range(max(3, args.warmup)):
         step()
     sess.sync()
-    cap = 1 << 20
-    buf = torch.zeros(4 + 4 * cap, dtype=torch.int64, device="cuda")
-    pf.pf_timeline_set(buf, cap)
-    step()
-    sess.sync()
-    torch.cuda.synchronize()
-    pf.pf_timeline_set(None, 0)
-    rec = pf.timeline_records(buf)
-    ids = rec["kernel"]
-    cut = np.flatnonzero(np.diff(ids) != 0) + 1
-    bounds = list(zip(np.concatenate([[0], cut]), np.concatenate([cut, [len(ids)]])))
-    names = [pf.pf_timeline_kernel_name(int(ids[a])) for a, _ in bounds]
-    labels = timeline_classes(names)
-    prev, per = int(rec["start_ns"].min()), {}
-    for (a, z), lab in zip(bounds, labels):
-        st, en = rec["start_ns"][a:z], rec["end_ns"][a:z]
-        e1 = int(en.max())
-        d = per.setdefault(lab, [])
-        d.append((e1 - prev, int(st.min()) - prev, e1 - int(st.min()), e1 - int(en.min()), z - a))
-        prev = max(prev, e1)
-    total_ns = prev - int(rec["start_ns"].min())
-    out = {"case": "timeline", "workload": WORKLOAD, "records": int(len(rec)), "launches": len(bounds),
-           "prompt_us": total_ns / 1e3, "classes": {}}
+    prompt_us, launches, per = timeline_prompt(pf, torch, step)
+    out = {"case": "timeline", "workload": WORKLOAD, "launches": launches, "prompt_us": prompt_us,
+           "classes": {}}
     for lab, d in per.items():
         x = np.array(d, dtype=np.float64)
         out["classes"][lab] = {"launches": len(d), "crit_us": round(x[:, 0].mean() / 1e3, 2),
@@ -155,6 +163,40 @@ def run_timeline(args, pf, synth):
                                "end_spread_us": round(x[:, 3].mean() / 1e3, 2),
                                "ctas": int(x[:, 4].mean()), "crit_ms_per_prompt": round(x[:, 0].sum() / 1e6, 3)}
     print(json.dumps(out))
+
+
+# timeline layer classes -> the kernel classes of class_work
+TIMELINE_TO_CLASS = {"rmsnorm_attn": "rmsnorm", "rmsnorm_ffn": "rmsnorm", "gemm_qkv": "gemm_qkv",
+                     "qk_norm_rope_kv": "qk_rope_kv", "attention": "attention", "gemm_o": "gemm_o",
+                     "gemm_gate_up": "gemm_gate_up", "gemm_down": "gemm_down", "embed": "embed",
+                     "lm_head_q1": "lm_head"}
+
+
+def roofline_step(per, shape, peaks):
+    """Per kernel class: algorithmic work per launch / mean time the launch adds to the
+    graph-replayed prompt (its critical-path share from the kernel timeline), against the
+    HBM or tensor peak: what each kernel costs the step, its dependency waits included."""
+    import numpy as np
+    work = class_work(shape, CHUNK)
+    crit = {}
+    for lab, d in per.items():
+        cls = TIMELINE_TO_CLASS.get(lab)
+        if cls:
+            crit.setdefault(cls, []).extend(x[0] for x in d)
+    out = {}
+    for cls, v in crit.items():
+        bound, w = work[cls]
+        us = float(np.mean(v)) / 1e3
+        if bound == "hbm":
+            ach, peak, unit = w / (us * 1e-6) / 1e9, peaks["hbm_gbs"], "GB/s"
+        else:
+            ach = w / (us * 1e-6) / 1e12
+            peak, unit = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]), "TFLOP/s"
+        out[cls] = {"bound": bound, "achieved": round(ach, 1), "peak": peak, "unit": unit,
+                    "frac": round(ach / peak, 4), "crit_us": round(us, 2)}
+    out["_note"] = ("time = a launch's critical-path share in the graph-replayed prompt (per-CTA kernel "
+                    "timeline: its last CTA end minus the previous launch's last end)")
+    return out
 
 
 def run_case(args):
@@ -721,6 +763,9 @@ def run_ours(args):
     breakdown = {k: {"ms_per_step": round(v[0], 4), "launches_per_step": v[1]} for k, v in per_step.items()}
 
     roof_all = roofline_all(prof, args.profile_steps, shape, peaks, peak_src)
+    # the same classes from one timeline-recorded prompt (graphs replayed, as timed)
+    _, _, tl_per = timeline_prompt(pf, torch, step)
+    roof_step = roofline_step(tl_per, shape, peaks)
     int4 = int4_layer_measure(pf, synth, torch, peaks, seed=args.seed) if args.layers == 36 else None
 
     cpu = None
@@ -742,6 +787,7 @@ def run_ours(args):
                                  "of LM head and 0.3 GB of KV cache read per step (the 2048 "
                                  "gathered embedding rows are 32 MB)"},
                 "e2e": e2e, "gpu_launches": launches, "roofline": roof, "roofline_all": roof_all,
+                "roofline_step": roof_step,
                 "int4_layer": int4,
                 "gemm_tflops_profiled": gemm_flops_step / (gemm_ms / 1e3) / 1e12 if gemm_ms else None,
                 "attention_tflops_profiled": attention_flops_per_prompt(shape) * shape.n_layers /

@@ -246,37 +246,9 @@ __global__ void __launch_bounds__(THREADS, 1)
   auto v_tile = [&](int s) { return v_s + s * L::KV; };
 
   griddep_launch_dependents();
-  griddep_wait();  // the start position and q / cache come from earlier kernels
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int M = P.M, nq = P.nq;
-  const int G = nq / P.nkv;
-  const int BT = TQ / G;  // tokens per CTA
-  const int n_tt = (M + BT - 1) / BT;
-  const int tt = n_tt - 1 - static_cast<int>(blockIdx.x);  // longest rows first
-  const int kvh = blockIdx.y;
-  const int split = blockIdx.z;
-  const int t0 = tt * BT;
-  const int t1 = min(t0 + BT, M);
-  const int start = P.start_dev ? *P.start_dev : P.start_host;
-  const bool ring = P.ring_R > 0;
-  const int S = P.ring_S, W = P.ring_R - P.ring_S;
-  KeyTiles kt;
-  if (ring)
-    kt.init_ring(start, t0, t1, S, W, P.ring_R);
-  else
-    kt.init_linear(start, t1);
-  // this CTA's part of the tile list
-  const int jb = static_cast<int>(static_cast<long long>(kt.total) * split / P.n_split);
-  const int nt = static_cast<int>(static_cast<long long>(kt.total) * (split + 1) / P.n_split) - jb;
-  const int crow0 = (P.layer * P.nkv + kvh) * P.cache_rows;  // (layer, kv head) in the cache
-  const int brow0 = kvh * P.chunk_rows;                      // kv head in the chunk buffers
-  const int first_pos = start + t0, last_pos = start + t1 - 1;
-  // whether some key of tile `t` is hidden from some query row of the CTA
-  auto needs_mask = [&](const KeyTile& t) {
-    if (t.nvalid < TK || t.pos0 + TK - 1 > first_pos) return true;
-    return ring && t.pos0 + TK - 1 >= S && t.pos0 <= last_pos - W;
-  };
-
+  // barriers and the TMEM allocation need nothing from earlier kernels: set them up while the
+  // previous kernel finishes
   if (threadIdx.x == 0) {
     for (int s = 0; s < KS; ++s) {
       mbar_init(k_full(s), 1);
@@ -306,6 +278,36 @@ __global__ void __launch_bounds__(THREADS, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const uint32_t tmem_o = tmem + COL_O;
+  griddep_wait();  // the start position and q / cache come from earlier kernels
+  const int M = P.M, nq = P.nq;
+  const int G = nq / P.nkv;
+  const int BT = TQ / G;  // tokens per CTA
+  const int n_tt = (M + BT - 1) / BT;
+  const int tt = n_tt - 1 - static_cast<int>(blockIdx.x);  // longest rows first
+  const int kvh = blockIdx.y;
+  const int split = blockIdx.z;
+  const int t0 = tt * BT;
+  const int t1 = min(t0 + BT, M);
+  const int start = P.start_dev ? *P.start_dev : P.start_host;
+  const bool ring = P.ring_R > 0;
+  const int S = P.ring_S, W = P.ring_R - P.ring_S;
+  KeyTiles kt;
+  if (ring)
+    kt.init_ring(start, t0, t1, S, W, P.ring_R);
+  else
+    kt.init_linear(start, t1);
+  // this CTA's part of the tile list
+  const int jb = static_cast<int>(static_cast<long long>(kt.total) * split / P.n_split);
+  const int nt = static_cast<int>(static_cast<long long>(kt.total) * (split + 1) / P.n_split) - jb;
+  const int crow0 = (P.layer * P.nkv + kvh) * P.cache_rows;  // (layer, kv head) in the cache
+  const int brow0 = kvh * P.chunk_rows;                      // kv head in the chunk buffers
+  const int first_pos = start + t0, last_pos = start + t1 - 1;
+  // whether some key of tile `t` is hidden from some query row of the CTA
+  auto needs_mask = [&](const KeyTile& t) {
+    if (t.nvalid < TK || t.pos0 + TK - 1 > first_pos) return true;
+    return ring && t.pos0 + TK - 1 >= S && t.pos0 <= last_pos - W;
+  };
+
 
   if (nt == 0) {
     // an empty part of a split list: its rows contribute nothing (max -inf, sum 0)

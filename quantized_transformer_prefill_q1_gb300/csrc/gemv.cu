@@ -135,29 +135,32 @@ struct Frag;
 template <>
 struct Frag<PF_W_Q1_G128> {
   uint32_t z[2][2];  // [half][row g, g + 8]
-  float s[2];
+  uint32_t s2[2];    // the rows' f16 scales in both halves
   __device__ __forceinline__ void read(uint32_t st, int gq, int c) {
 #pragma unroll
     for (int h = 0; h < 2; ++h)
 #pragma unroll
       for (int i = 0; i < 2; ++i) z[h][i] = lds32(st + h * 128 + i * 64 + gq * 8 + (c >> 1) * 4);
 #pragma unroll
-    for (int i = 0; i < 2; ++i) s[i] = h2f(lds16(st + ST<PF_W_Q1_G128>::SC + i * 16 + gq * 2));
+    for (int i = 0; i < 2; ++i) {
+      const uint32_t b = lds16(st + ST<PF_W_Q1_G128>::SC + i * 16 + gq * 2);
+      s2[i] = b | (b << 16);
+    }
   }
+  // +-scale, as the tensor-core path's dequantiser forms it
   __device__ __forceinline__ void a(int h, int ks, int c, uint32_t (&f)[4]) const {
     const int i0 = 8 * (c & 1) + 2 * ks;
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
-      f[i] = ((z[h][i] << i0) & 0x80008000u) | 0x3C003C00u;
-      f[2 + i] = ((z[h][i] << (i0 + 1)) & 0x80008000u) | 0x3C003C00u;
+      f[i] = ((z[h][i] << i0) & 0x80008000u) ^ s2[i];
+      f[2 + i] = ((z[h][i] << (i0 + 1)) & 0x80008000u) ^ s2[i];
     }
   }
 };
 template <>
 struct Frag<PF_W_INT4_AFFINE_G128> {
   uint2 q[2][2];
-  uint32_t zp[2];
-  float s[2];
+  __half2 z2[2], s2[2];
   __device__ __forceinline__ void read(uint32_t st, int gq, int c) {
 #pragma unroll
     for (int h = 0; h < 2; ++h)
@@ -165,19 +168,21 @@ struct Frag<PF_W_INT4_AFFINE_G128> {
       for (int i = 0; i < 2; ++i) q[h][i] = lds64(st + h * 512 + i * 256 + gq * 32 + c * 8);
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
-      s[i] = h2f(lds16(st + ST<PF_W_INT4_AFFINE_G128>::SC + i * 16 + gq * 2));
-      zp[i] = lds16(st + ST<PF_W_INT4_AFFINE_G128>::ZP + i * 16 + gq * 2);
+      const uint32_t sb = lds16(st + ST<PF_W_INT4_AFFINE_G128>::SC + i * 16 + gq * 2);
+      const uint32_t zb = lds16(st + ST<PF_W_INT4_AFFINE_G128>::ZP + i * 16 + gq * 2);
+      s2[i] = u2h(sb | (sb << 16));
+      z2[i] = u2h(zb | (zb << 16));
     }
   }
+  // f16(f16(q - z) * s), as the tensor-core path's dequantiser forms it
   __device__ __forceinline__ void a(int h, int ks, int c, uint32_t (&f)[4]) const {
     const __half2 k1024 = u2h(0x64006400u), k16th = u2h(0x2C002C00u), km64 = u2h(0xD400D400u);
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
       uint32_t W = (ks >> 1) ? q[h][i].y : q[h][i].x;
       if (ks & 1) W >>= 8;
-      const __half2 z2 = u2h(zp[i] | (zp[i] << 16));
-      f[i] = h2u(__hsub2(__hsub2(u2h((W & 0x000F000Fu) | 0x64006400u), k1024), z2));
-      f[2 + i] = h2u(__hsub2(__hfma2(u2h((W & 0x00F000F0u) | 0x64006400u), k16th, km64), z2));
+      f[i] = h2u(__hmul2(__hsub2(__hsub2(u2h((W & 0x000F000Fu) | 0x64006400u), k1024), z2[i]), s2[i]));
+      f[2 + i] = h2u(__hmul2(__hsub2(__hfma2(u2h((W & 0x00F000F0u) | 0x64006400u), k16th, km64), z2[i]), s2[i]));
     }
   }
 };
@@ -205,52 +210,58 @@ __device__ __forceinline__ void tile_rows(int t, int& tile256, int& roA, int& ro
   }
 }
 
-template <int WFMT, int EPI>
+template <int WFMT, int EPI, int GS>
 __global__ void __launch_bounds__(THREADS_V)
     gemv_kernel(const __half* a, const uint8_t* __restrict__ wpk, int M, int N, int K,
                 void* __restrict__ out, long long units, int warps) {
   PF_TIMELINE(TL_GEMV + EPI);
   using S = ST<WFMT>;
-  constexpr int DS = S::DS;
+  constexpr int DS = S::DS / GS;     // stages in flight per warp
+  constexpr int SB = GS * S::BYTES;  // a stage: GS consecutive groups of one 16-row tile
   constexpr size_t P = WFMT == PF_W_Q1_G128 ? Q1_CHUNK_BYTES : I4_CHUNK_BYTES;
+  static_assert(DS >= 2, "ring depth");
   extern __shared__ __align__(16) uint8_t gv_smem[];
-  __shared__ float part[WARPS_V / 2][32][4];  // SwiGLU: the odd-group half of a tile's sums
+  __shared__ float part[WARPS_V / 2][32][4];  // SwiGLU: the odd-stage half of a tile's sums
   griddep_launch_dependents();
   const int G = K / GROUP;
+  const int GG = G / GS;  // stages per tile
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gq = lane >> 2, c = lane & 3;
   const bool tok = gq < M;  // this lane's B column (token gq) exists
   const int gw = blockIdx.x * WARPS_V + warp;
-  // This warp's units as a cursor (t, g) stepping by `gs`: SwiGLU tiles are split between two
-  // warps of the CTA by group parity (warp 2i + p takes groups p, p + 2, ... of tile
-  // 2 blockIdx + i); otherwise an equal contiguous range of (tile, group) units.
+  // This warp's units (tile, stage) as a cursor (t, g) stepping by `gs`: SwiGLU tiles are
+  // split between two warps of the CTA by stage parity (warp 2i + p takes stages p, p + 2, ...
+  // of tile 2 blockIdx + i); otherwise an equal contiguous range of units.
   int t0, g0, gs, n;
   if (EPI == EPI_SWIGLU) {
     t0 = gw >> 1;
     g0 = gw & 1;
     gs = 2;
-    n = t0 < warps ? (G - g0 + 1) >> 1 : 0;
+    n = t0 < warps ? (GG - g0 + 1) >> 1 : 0;
   } else {
     const long long u0 = gw < warps ? units * gw / warps : 0;
     const long long u1 = gw < warps ? units * (gw + 1) / warps : 0;
-    t0 = static_cast<int>(u0 / G);
-    g0 = static_cast<int>(u0 - static_cast<long long>(t0) * G);
+    t0 = static_cast<int>(u0 / GG);
+    g0 = static_cast<int>(u0 - static_cast<long long>(t0) * GG);
     gs = 1;
     n = static_cast<int>(u1 - u0);
   }
-  const uint32_t ring = smem_u32(gv_smem) + static_cast<uint32_t>(warp * DS * S::BYTES);
+  const uint32_t ring = smem_u32(gv_smem) + static_cast<uint32_t>(warp * DS * SB);
 
   int ti = t0, gi = g0, si = 0;  // issue cursor and its stage
   auto issue_next = [&]() {
     int tile256, roA, roB;
     tile_rows<EPI>(ti, tile256, roA, roB);
-    const uint8_t* ch = wpk + (static_cast<size_t>(tile256) * G + gi) * P;
-    const uint32_t st = ring + static_cast<uint32_t>(si * S::BYTES);
-    if (WFMT == PF_W_Q1_G128) issue_q1(st, ch, roA, roB, lane);
-    else issue_i4(st, ch, roA, roB, lane);
+    const uint8_t* ch = wpk + (static_cast<size_t>(tile256) * G + gi * GS) * P;
+    const uint32_t st = ring + static_cast<uint32_t>(si * SB);
+#pragma unroll
+    for (int q = 0; q < GS; ++q) {
+      if (WFMT == PF_W_Q1_G128) issue_q1(st + q * S::BYTES, ch + q * P, roA, roB, lane);
+      else issue_i4(st + q * S::BYTES, ch + q * P, roA, roB, lane);
+    }
     gi += gs;
-    if (gi >= G) {
-      gi -= G;
+    if (gi >= GG) {
+      gi -= GG;
       ++ti;
     }
     si = si + 1 == DS ? 0 : si + 1;
@@ -265,85 +276,90 @@ __global__ void __launch_bounds__(THREADS_V)
 
   int tc = t0, gc = g0, sc = 0;  // compute cursor
   const __half* xbase = a + static_cast<size_t>(tok ? gq : 0) * K + 16 * c;
-  uint4 xn[4] = {};  // the next unit's 16 activations of each half (token gq)
+  uint4 xn[4] = {};  // the next group's 16 activations of each half (token gq)
   auto load_x = [&](int g, uint4 (&x)[4]) {
 #pragma unroll
     for (int e = 0; e < 4; ++e)
       x[e] = tok ? ld_act16(xbase + g * GROUP + 64 * (e >> 1) + 8 * (e & 1)) : make_uint4(0u, 0u, 0u, 0u);
   };
-  if (n > 0) load_x(gc, xn);
-  float acc[4] = {0.f, 0.f, 0.f, 0.f};  // (row g, token 2c), (g, 2c+1), (g+8, 2c), (g+8, 2c+1)
+  if (n > 0) load_x(gc * GS, xn);
+  // four independent MMA chains (half, k-step parity), accumulated over a segment's groups
+  // (the scales are inside the A fragments): (row g, token 2c), (g, 2c+1), (g+8, 2c), (g+8, 2c+1)
+  float d[4][4] = {};
   bool seg_first = true;
   int seg_g0 = 0;
 #pragma unroll 1
   for (int j = 0; j < n; ++j) {
     if (j + DS - 1 < n) issue_next();
     cp_commit();
-    uint4 xc[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) xc[e] = xn[e];
     int tn = tc, gn = gc + gs;
-    if (gn >= G) {
-      gn -= G;
+    if (gn >= GG) {
+      gn -= GG;
       ++tn;
     }
-    if (j + 1 < n) load_x(gn, xn);
-    cp_wait<DS - 1>();  // this lane's copies of unit j have landed
+    cp_wait<DS - 1>();  // this lane's copies of stage j have landed
     __syncwarp();       // and every other lane's
     if (seg_first) {
       seg_g0 = gc;
       seg_first = false;
     }
-    Frag<WFMT> fr;
-    fr.read(ring + static_cast<uint32_t>(sc * S::BYTES), gq, c);
-    float d[4][4] = {};  // four independent chains: (half, k-step parity)
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
+    for (int q = 0; q < GS; ++q) {
+      uint4 xc[4];
 #pragma unroll
-      for (int ks = 0; ks < 4; ++ks) {
-        uint32_t af[4];
-        fr.a(h, ks, c, af);
-        const uint4& xv = xc[2 * h + (ks >> 1)];
-        mma16816(af, (ks & 1) ? xv.z : xv.x, (ks & 1) ? xv.w : xv.y, d[2 * h + (ks & 1)]);
+      for (int e = 0; e < 4; ++e) xc[e] = xn[e];
+      // the next group's activations: the next in this stage, else the next stage's first
+      if (q + 1 < GS) load_x(gc * GS + q + 1, xn);
+      else if (j + 1 < n) load_x(gn * GS, xn);
+      Frag<WFMT> fr;
+      fr.read(ring + static_cast<uint32_t>(sc * SB + q * S::BYTES), gq, c);
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks) {
+          uint32_t af[4];
+          fr.a(h, ks, c, af);
+          const uint4& xv = xc[2 * h + (ks >> 1)];
+          mma16816(af, (ks & 1) ? xv.z : xv.x, (ks & 1) ? xv.w : xv.y, d[2 * h + (ks & 1)]);
+        }
       }
     }
     __syncwarp();  // the stage is read: it may be refilled
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const float v = (d[0][i] + d[1][i]) + (d[2][i] + d[3][i]);
-      acc[i] = fmaf(fr.s[i >> 1], v, acc[i]);
-    }
-    const bool tile_end = EPI == EPI_SWIGLU ? j == n - 1 : (gc == G - 1 || j == n - 1);
+    const bool tile_end = EPI == EPI_SWIGLU ? j == n - 1 : (gc == GG - 1 || j == n - 1);
     const int t = tc;
     const int g = gc;
     tc = tn;
     gc = gn;
     sc = sc + 1 == DS ? 0 : sc + 1;
-    if (!tile_end) continue;
-    // ---- end of a segment of tile t: its share (acc[2i + e]: MMA row g + 8i, token 2c + e)
-    if (EPI != EPI_SWIGLU) {
-      const bool whole = seg_g0 == 0 && g == G - 1;
-      float* o = reinterpret_cast<float*>(out);
+    if (!tile_end || EPI == EPI_SWIGLU) continue;
+    // ---- end of a segment of tile t: its share (MMA row g + 8i, token 2c + e)
+    const bool whole = seg_g0 == 0 && g == GG - 1;
+    float* o = reinterpret_cast<float*>(out);
 #pragma unroll
-      for (int i = 0; i < 2; ++i) {
-        const int row = 16 * t + gq + 8 * i;
-        if (row >= N) continue;
+    for (int i = 0; i < 2; ++i) {
+      const int row = 16 * t + gq + 8 * i;
 #pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int m = 2 * c + e;
-          if (m >= M) continue;
-          float* p = o + static_cast<size_t>(m) * N + row;
-          if (whole) *p += acc[2 * i + e];  // no other warp has this tile
-          else atomicAdd(p, acc[2 * i + e]);
-        }
+      for (int e = 0; e < 2; ++e) {
+        const int m = 2 * c + e;
+        const float v = (d[0][2 * i + e] + d[1][2 * i + e]) + (d[2][2 * i + e] + d[3][2 * i + e]);
+        if (row >= N || m >= M) continue;
+        float* p = o + static_cast<size_t>(m) * N + row;
+        if (whole) *p += v;  // no other warp has this tile
+        else atomicAdd(p, v);
       }
-      acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
-      seg_first = true;
     }
+#pragma unroll
+    for (int x = 0; x < 4; ++x)
+#pragma unroll
+      for (int y = 0; y < 4; ++y) d[x][y] = 0.f;
+    seg_first = true;
   }
   if (EPI == EPI_SWIGLU) {
-    // the odd-group warp hands its sums to the even-group warp of the same tile, which forms
+    // the odd-stage warp hands its sums to the even-stage warp of the same tile, which forms
     // silu(gate) * up: MMA rows g are gate rows, g + 8 their up rows
+    float acc[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) acc[i] = (d[0][i] + d[1][i]) + (d[2][i] + d[3][i]);
     const int pair = warp >> 1;
     if (warp & 1) {
 #pragma unroll
@@ -351,8 +367,10 @@ __global__ void __launch_bounds__(THREADS_V)
     }
     __syncthreads();
     if (!(warp & 1) && n > 0) {
+      if (GG > 1) {
 #pragma unroll
-      for (int i = 0; i < 4; ++i) acc[i] += part[pair][lane][i];
+        for (int i = 0; i < 4; ++i) acc[i] += part[pair][lane][i];
+      }
       const int col = 8 * t0 + gq;
       __half* o = reinterpret_cast<__half*>(out);
 #pragma unroll
@@ -366,13 +384,13 @@ __global__ void __launch_bounds__(THREADS_V)
   cp_wait<0>();
 }
 
-template <int WFMT, int EPI>
-cudaError_t launch_v(const GemmArgs& g, cudaStream_t stream) {
-  constexpr int smem = WARPS_V * ST<WFMT>::DS * ST<WFMT>::BYTES;
+template <int WFMT, int EPI, int GS>
+cudaError_t launch_vg(const GemmArgs& g, cudaStream_t stream) {
+  constexpr int smem = WARPS_V * (ST<WFMT>::DS / GS) * GS * ST<WFMT>::BYTES;
   static_assert(smem <= 48 * 1024, "GEMV stages");
   static const int warps_max = [] {
     int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gemv_kernel<WFMT, EPI>, THREADS_V, smem) !=
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gemv_kernel<WFMT, EPI, GS>, THREADS_V, smem) !=
             cudaSuccess ||
         per_sm < 1)
       per_sm = 1;
@@ -380,7 +398,7 @@ cudaError_t launch_v(const GemmArgs& g, cudaStream_t stream) {
   }();
   const int G = g.K / GROUP;
   const long long tiles = EPI == EPI_SWIGLU ? g.N / 16 : padded_rows(g.N) / 16;
-  const long long units = tiles * G;
+  const long long units = tiles * (G / GS);
   // SwiGLU: two warps per tile (gate and up rows meet in the CTA); `warps` counts tiles there.
   // Otherwise equal ranges of units, one per warp.
   int warps, ctas;
@@ -391,8 +409,17 @@ cudaError_t launch_v(const GemmArgs& g, cudaStream_t stream) {
     warps = static_cast<int>(std::min<long long>(units, warps_max));
     ctas = (warps + WARPS_V - 1) / WARPS_V;
   }
-  return launch_pdl(gemv_kernel<WFMT, EPI>, dim3(ctas), dim3(THREADS_V), smem, stream,
+  return launch_pdl(gemv_kernel<WFMT, EPI, GS>, dim3(ctas), dim3(THREADS_V), smem, stream,
                     reinterpret_cast<const __half*>(g.a), g.w, g.M, g.N, g.K, g.out, units, warps);
+}
+
+// Groups per stage: 4 when the 128-wide groups of a row divide by 4, else 2, else 1.
+template <int WFMT, int EPI>
+cudaError_t launch_v(const GemmArgs& g, cudaStream_t stream) {
+  const int G = g.K / GROUP;
+  if (G % 4 == 0) return launch_vg<WFMT, EPI, 4>(g, stream);
+  if (G % 2 == 0) return launch_vg<WFMT, EPI, 2>(g, stream);
+  return launch_vg<WFMT, EPI, 1>(g, stream);
 }
 
 template <int WFMT>
