@@ -214,7 +214,8 @@ template <int HD, int BF16>
 __global__ void __launch_bounds__(THREADS, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_kc,
-                   const __grid_constant__ CUtensorMap tm_vc, const AttnKParams P) {
+                   const __grid_constant__ CUtensorMap tm_vc, const __grid_constant__ CUtensorMap tm_o,
+                   const AttnKParams P) {
   PF_TIMELINE(TL_ATTENTION_TC);
   using L = ASmem<HD>;
   constexpr int NH = HD / 64;  // 64-wide (128-B) swizzle regions along head_dim
@@ -569,20 +570,33 @@ __global__ void __launch_bounds__(THREADS, 1)
             for (int q4 = 0; q4 < 8; ++q4)
               dst[q4] = make_float4(__uint_as_float(v[4 * q4]), __uint_as_float(v[4 * q4 + 1]),
                                     __uint_as_float(v[4 * q4 + 2]), __uint_as_float(v[4 * q4 + 3]));
-          } else {
-            uint4* dst = reinterpret_cast<uint4*>(P.out + (static_cast<size_t>(t) * nq + h) * HD + 32 * c);
-#pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
-              uint32_t w[4];
-#pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const __half2 hv = __floats2half2_rn(__uint_as_float(v[8 * q4 + 2 * e]) * inv,
-                                                     __uint_as_float(v[8 * q4 + 2 * e + 1]) * inv);
-                w[e] = *reinterpret_cast<const uint32_t*>(&hv);
-              }
-              dst[q4] = make_uint4(w[0], w[1], w[2], w[3]);
-            }
           }
+        }
+        if (!partial) {
+          // O / l as f16 into the idle K ring, in the layout of the output's TMA box: box
+          // b = c / 2 (64 head-dim columns) at k_s + b * 16 KB, row r at r * 128 B, 16-B unit
+          // j at (j ^ (r % 8)) * 16 (128-B swizzle); rows past M are clipped by the store
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) {
+            uint32_t w[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const __half2 hv = __floats2half2_rn(__uint_as_float(v[8 * q4 + 2 * e]) * inv,
+                                                   __uint_as_float(v[8 * q4 + 2 * e + 1]) * inv);
+              w[e] = *reinterpret_cast<const uint32_t*>(&hv);
+            }
+            const int j = (c & 1) * 4 + q4;
+            st_shared_v4a(k_s + (c >> 1) * (TQ * 128) + r * 128 + ((j ^ (r & 7)) << 4), w[0], w[1], w[2], w[3]);
+          }
+        }
+      }
+      if (!partial) {
+        fence_proxy_async_smem();
+        named_bar_sync_a(1, SM_THREADS);
+        if (threadIdx.x == 64) {  // one thread stores the tile: NH boxes of 64 x G x BT
+          for (int b = 0; b < NH; ++b) tma_store_3d(&tm_o, k_s + b * (TQ * 128), 64 * b, kvh * G, t0);
+          bulk_commit();
+          bulk_wait0();  // complete before the CTA retires
         }
       }
     }
@@ -651,6 +665,8 @@ cudaError_t launch_tc(const AttnArgs& a, cudaStream_t st) {
   const uint64_t kd[2] = {static_cast<uint64_t>(HD), rows};
   const uint64_t ks[1] = {static_cast<uint64_t>(HD) * 2};
   const uint32_t kb[2] = {64, static_cast<uint32_t>(TK)};
+  CUtensorMap to;  // the f16 output [M][nq][hd], boxes like Q's
+  if (!encode_tmap_16(&to, 0, 3, a.out, qd, qs, qb)) return cudaErrorInvalidValue;
   if (!encode_tmap_16(&tq, BF16, 3, a.q, qd, qs, qb) || !encode_tmap_16(&tk, BF16, 2, a.k_cache, kd, ks, kb) ||
       !encode_tmap_16(&tv, BF16, 2, a.v_cache, kd, ks, kb))
     return cudaErrorInvalidValue;
@@ -684,7 +700,7 @@ cudaError_t launch_tc(const AttnArgs& a, cudaStream_t st) {
   p.blocks = a.blocks;
   dim3 grid((a.M + BT - 1) / BT, c.n_kv_heads, n_split);
   cudaError_t e = launch_pdl(attn_tc_kernel<HD, BF16>, grid, dim3(THREADS), ASmem<HD>::BYTES, st, tq, tk,
-                             tv, tkc, tvc, p);
+                             tv, tkc, tvc, to, p);
   if (e != cudaSuccess || n_split == 1) return e;
   const int rows_out = a.M * c.n_q_heads;
   return launch_pdl(attn_combine_kernel<HD>, dim3((rows_out + 7) / 8), dim3(256), 0, st,

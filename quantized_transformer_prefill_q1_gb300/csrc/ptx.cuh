@@ -324,6 +324,16 @@ __host__ __device__ constexpr uint32_t idesc_f16(int M, int N, int ab_bf16, int 
          | (static_cast<uint32_t>(M >> 4) << 24);   // M / 16
 }
 
+// 3-D tiled TMA store shared -> global (bulk async-group completion), coordinates innermost
+// first; the shared source must have been written before a fence_proxy_async_smem().
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t src, int x, int y, int z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+          reinterpret_cast<uint64_t>(map)),
+      "r"(src), "r"(x), "r"(y), "r"(z)
+      : "memory");
+}
+
 // 3-D tiled TMA load (coordinates innermost first).
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int x, int y, int z,
                                             uint32_t bar) {
