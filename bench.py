@@ -79,24 +79,25 @@ def parse():
 
 def timeline_classes(names):
     """Labels the launches of one prompt (a list of kernel names in launch order) with their
-    role in the layer: the two RMSNorms and the residual-form GEMMs are told apart by what
-    precedes them."""
-    labels, norm, after = [], 0, None
+    role in the layer: the two RMSNorms by their order, a residual-form GEMM by the major
+    step before it (attention: the O projection, gate_up: down, else the QKV projection,
+    whose launch carries the attention RMSNorm as a prologue when no norm kernel runs)."""
+    labels, norm, prev = [], 0, None
     for n in names:
-        if n == "rmsnorm_reg" or n == "rmsnorm":
+        if n in ("rmsnorm_reg", "rmsnorm"):
             norm += 1
-            labels.append("rmsnorm_attn" if norm % 2 == 1 else "rmsnorm_ffn")
-            after = "qkv" if norm % 2 == 1 else None
+            lab = "rmsnorm_attn" if norm % 2 == 1 else "rmsnorm_ffn"
         elif n.startswith("gemm") and n.endswith("resid"):
-            labels.append("gemm_" + (after or "?"))
+            lab = {"attention": "gemm_o", "gemm_gate_up": "gemm_down"}.get(prev, "gemm_qkv")
         elif n.startswith("gemm") and n.endswith("swiglu"):
-            labels.append("gemm_gate_up")
-            after = "down"
+            lab = "gemm_gate_up"
         elif n.startswith("attention"):
-            labels.append("attention")
-            after = "o"
+            lab = "attention"
         else:
-            labels.append(n)
+            lab = n
+        labels.append(lab)
+        if n not in ("ring_store", "attn_combine"):
+            prev = lab
     return labels
 
 

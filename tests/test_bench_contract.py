@@ -36,3 +36,9 @@ def test_timeline_labels_follow_the_layer_order():
     one = ["rmsnorm_attn", "gemm_qkv", "qk_norm_rope_kv", "attention", "gemm_o", "rmsnorm_ffn", "gemm_gate_up",
            "gemm_down"]
     assert got == ["set_int", "embed"] + one * 2 + ["lm_head_q1"]
+    # with the norms as the GEMMs' prologues (no norm kernels), and a ring store after attention
+    fused = ["gemm_pair_resid", "qk_norm_rope_kv", "attention_tc", "ring_store", "gemm_pair_resid",
+             "gemm_pair_swiglu", "gemm_pair_resid"]
+    got = bench.timeline_classes(["embed"] + fused * 2)
+    one = ["gemm_qkv", "qk_norm_rope_kv", "attention", "ring_store", "gemm_o", "gemm_gate_up", "gemm_down"]
+    assert got == ["embed"] + one * 2
