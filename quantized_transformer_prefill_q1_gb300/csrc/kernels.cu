@@ -114,6 +114,7 @@ __global__ void __launch_bounds__(128) rmsnorm_reg_kernel(const float* __restric
 }
 
 // ------------------------------------------------------------------ QK-norm + RoPE + KV
+constexpr int QK_SLOTS = 4;  // head groups per warp in qk_norm_rope_kv_kernel
 template <typename T>
 __device__ __forceinline__ T to_elem(float v);
 template <>
@@ -157,7 +158,7 @@ __device__ __forceinline__ void store4<__nv_bfloat16>(__nv_bfloat16* dst, float 
 // (kv_by_pos = 1); a ring cache's chunk buffers take row kvh * kv_rows + t (kv_layer = 0,
 // kv_by_pos = 0) and the ring slots are filled after the attention (ring_store_kernel).
 template <int HD, typename QT, typename KT>
-__global__ void __launch_bounds__(256) qk_norm_rope_kv_kernel(
+__global__ void __launch_bounds__(256, 3) qk_norm_rope_kv_kernel(
     const float* __restrict__ qkv, const float* __restrict__ qn, const float* __restrict__ kn,
     const float* __restrict__ rope, int M, int nq, int nkv, int kv_rows, int kv_layer, int kv_by_pos,
     const int* __restrict__ start_dev, int start_host, float eps, int qk_norm,
@@ -165,68 +166,71 @@ __global__ void __launch_bounds__(256) qk_norm_rope_kv_kernel(
   PF_TIMELINE(TL_QK_ROPE_KV);
   constexpr int HALF = HD / 2;
   constexpr int LPH = HALF / 4;   // lanes per head
-  constexpr int HPW = 32 / LPH;   // heads per warp
+  constexpr int HPW = 32 / LPH;   // heads per warp and slot
   griddep_launch_dependents();
   const int heads = nq + 2 * nkv;
   const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   const int l = lane % LPH;
-  const int gh = gw * HPW + lane / LPH;  // (token, head) index
-  const int t = gh / heads;
-  const int j = gh - t * heads;
-  const bool valid = t < M;
-  const bool is_q = j < nq, is_v = j >= nq + nkv;
-  // the norm weights never depend on the previous kernel: load them while it finishes
-  float4 wa = make_float4(1.f, 1.f, 1.f, 1.f), wb = wa;
-  if (qk_norm && valid && !is_v) {
-    wa = reinterpret_cast<const float4*>(is_q ? qn : kn)[l];
-    wb = reinterpret_cast<const float4*>(is_q ? qn : kn)[LPH + l];
-  }
   griddep_wait();
   const int start = start_dev ? *start_dev : start_host;
-  const int pos = start + t;
-  // the head's values and its (cos, sin) of pairs 4l .. 4l+3 in one round trip
-  float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a, c01 = a, c23 = a;
-  if (valid) {
-    const float4* src = reinterpret_cast<const float4*>(qkv + (static_cast<size_t>(t) * heads + j) * HD);
-    a = src[l];
-    b = src[LPH + l];
-    if (!is_v) {
-      const float4* cs = reinterpret_cast<const float4*>(rope + (static_cast<size_t>(pos) * HALF + 4 * l) * 2);
-      c01 = cs[0];
-      c23 = cs[1];
+  // QK_SLOTS groups of HPW (token, head) pairs per warp: every slot's head values are loaded
+  // before any is used, so a launch is one round trip per thread and fits the GPU in one wave
+  // (the (cos, sin) rows and norm weights, shared by the heads of a token / kind, come after)
+  float4 A[QK_SLOTS], B[QK_SLOTS];
+#pragma unroll
+  for (int s = 0; s < QK_SLOTS; ++s) {
+    const int gh = (gw * QK_SLOTS + s) * HPW + lane / LPH;  // (token, head) index
+    const int t = gh / heads, j = gh - t * heads;
+    A[s] = B[s] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (t < M) {
+      const float4* src = reinterpret_cast<const float4*>(qkv + (static_cast<size_t>(t) * heads + j) * HD);
+      A[s] = src[l];
+      B[s] = src[LPH + l];
     }
   }
-  // per-head sum of squares over the LPH lanes of the group (every lane takes part)
-  float ss = a.x * a.x + a.y * a.y + a.z * a.z + a.w * a.w + b.x * b.x + b.y * b.y + b.z * b.z + b.w * b.w;
 #pragma unroll
-  for (int o = LPH / 2; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-  if (!valid) return;
-  // cache slot of the position; a paged cache goes through the block table
-  const int kv_row = !kv_by_pos ? t : (blocks ? blocks[pos / PF_KV_BLOCK] * PF_KV_BLOCK + pos % PF_KV_BLOCK : pos);
-  if (is_v) {  // V head: straight to the cache
-    KT* dst = vc + ((static_cast<size_t>(kv_layer) * nkv + (j - nq - nkv)) * kv_rows + kv_row) * HD;
-    store4<KT>(dst + 4 * l, a.x, a.y, a.z, a.w);
-    store4<KT>(dst + HALF + 4 * l, b.x, b.y, b.z, b.w);
-    return;
-  }
-  if (qk_norm) {
-    const float r = rsqrtf(ss / static_cast<float>(HD) + eps);
-    a = make_float4(a.x * r * wa.x, a.y * r * wa.y, a.z * r * wa.z, a.w * r * wa.w);
-    b = make_float4(b.x * r * wb.x, b.y * r * wb.y, b.z * r * wb.z, b.w * r * wb.w);
-  }
-  const float ra0 = a.x * c01.x - b.x * c01.y, rb0 = b.x * c01.x + a.x * c01.y;
-  const float ra1 = a.y * c01.z - b.y * c01.w, rb1 = b.y * c01.z + a.y * c01.w;
-  const float ra2 = a.z * c23.x - b.z * c23.y, rb2 = b.z * c23.x + a.z * c23.y;
-  const float ra3 = a.w * c23.z - b.w * c23.w, rb3 = b.w * c23.z + a.w * c23.w;
-  if (is_q) {
-    QT* dst = q_out + (static_cast<size_t>(t) * nq + j) * HD;
-    store4<QT>(dst + 4 * l, ra0, ra1, ra2, ra3);
-    store4<QT>(dst + HALF + 4 * l, rb0, rb1, rb2, rb3);
-  } else {
-    KT* dst = kc + ((static_cast<size_t>(kv_layer) * nkv + (j - nq)) * kv_rows + kv_row) * HD;
-    store4<KT>(dst + 4 * l, ra0, ra1, ra2, ra3);
-    store4<KT>(dst + HALF + 4 * l, rb0, rb1, rb2, rb3);
+  for (int s = 0; s < QK_SLOTS; ++s) {
+    const int gh = (gw * QK_SLOTS + s) * HPW + lane / LPH;
+    const int t = gh / heads, j = gh - t * heads;
+    const bool is_q = j < nq, is_v = j >= nq + nkv;
+    float4 a = A[s], b = B[s];
+    // per-head sum of squares over the LPH lanes of the group (every lane takes part)
+    float ss = a.x * a.x + a.y * a.y + a.z * a.z + a.w * a.w + b.x * b.x + b.y * b.y + b.z * b.z + b.w * b.w;
+#pragma unroll
+    for (int o = LPH / 2; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    if (t >= M) continue;
+    const int pos = start + t;
+    // cache slot of the position; a paged cache goes through the block table
+    const int kv_row = !kv_by_pos ? t : (blocks ? blocks[pos / PF_KV_BLOCK] * PF_KV_BLOCK + pos % PF_KV_BLOCK : pos);
+    if (is_v) {  // V head: straight to the cache
+      KT* dst = vc + ((static_cast<size_t>(kv_layer) * nkv + (j - nq - nkv)) * kv_rows + kv_row) * HD;
+      store4<KT>(dst + 4 * l, a.x, a.y, a.z, a.w);
+      store4<KT>(dst + HALF + 4 * l, b.x, b.y, b.z, b.w);
+      continue;
+    }
+    const float4* cs = reinterpret_cast<const float4*>(rope + (static_cast<size_t>(pos) * HALF + 4 * l) * 2);
+    const float4 c01 = __ldg(cs), c23 = __ldg(cs + 1);
+    if (qk_norm) {  // the norm weights (the same for every head of a kind) come from L1
+      const float r = rsqrtf(ss / static_cast<float>(HD) + eps);
+      const float4* w4 = reinterpret_cast<const float4*>(is_q ? qn : kn);
+      const float4 wa = __ldg(w4 + l), wb = __ldg(w4 + LPH + l);
+      a = make_float4(a.x * r * wa.x, a.y * r * wa.y, a.z * r * wa.z, a.w * r * wa.w);
+      b = make_float4(b.x * r * wb.x, b.y * r * wb.y, b.z * r * wb.z, b.w * r * wb.w);
+    }
+    const float ra0 = a.x * c01.x - b.x * c01.y, rb0 = b.x * c01.x + a.x * c01.y;
+    const float ra1 = a.y * c01.z - b.y * c01.w, rb1 = b.y * c01.z + a.y * c01.w;
+    const float ra2 = a.z * c23.x - b.z * c23.y, rb2 = b.z * c23.x + a.z * c23.y;
+    const float ra3 = a.w * c23.z - b.w * c23.w, rb3 = b.w * c23.z + a.w * c23.w;
+    if (is_q) {
+      QT* dst = q_out + (static_cast<size_t>(t) * nq + j) * HD;
+      store4<QT>(dst + 4 * l, ra0, ra1, ra2, ra3);
+      store4<QT>(dst + HALF + 4 * l, rb0, rb1, rb2, rb3);
+    } else {
+      KT* dst = kc + ((static_cast<size_t>(kv_layer) * nkv + (j - nq)) * kv_rows + kv_row) * HD;
+      store4<KT>(dst + 4 * l, ra0, ra1, ra2, ra3);
+      store4<KT>(dst + HALF + 4 * l, rb0, rb1, rb2, rb3);
+    }
   }
 }
 
@@ -513,7 +517,7 @@ static void qk_launch(const pf_config& c, const float* qkv, const float* qn, con
                       void* q, void* kc, void* vc, cudaStream_t stream) {
   const int heads = c.n_q_heads + 2 * c.n_kv_heads;
   constexpr int HPW = 32 / (HD / 8);
-  const long long warps = (static_cast<long long>(M) * heads + HPW - 1) / HPW;
+  const long long warps = (static_cast<long long>(M) * heads + HPW * QK_SLOTS - 1) / (HPW * QK_SLOTS);
   const int blocks = static_cast<int>((warps * 32 + 255) / 256);
   launch_pdl(qk_norm_rope_kv_kernel<HD, QT, KT>, dim3(blocks), dim3(256), 0, stream, qkv, qn, kn,
              rope, M, c.n_q_heads, c.n_kv_heads, d.kv_rows, d.kv_layer, d.kv_by_pos, start_dev,
