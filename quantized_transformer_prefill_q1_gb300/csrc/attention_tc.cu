@@ -615,7 +615,10 @@ __global__ void __launch_bounds__(THREADS, 1)
 // Merges the n_split partial results of each (token, head) row: with m* the largest of the
 // parts' running maxima, O = sum_s 2^(m_s - m*) O_s / sum_s 2^(m_s - m*) l_s (the parts keep
 // O_s and l_s relative to their own m_s, in the exp2 domain). Parts that saw no key of the
-// row (m_s = -inf) are skipped. One warp per row.
+// row (m_s = -inf) wrote no O and are skipped. One warp per row: lane s reads part s's (m, l) (and s + 32), the
+// warp reduces m* and the weighted sum of l, then each lane accumulates its HD / 32 columns
+// over the parts with the weights broadcast from their lanes, loads issued eight parts at a
+// time.
 template <int HD>
 __global__ void __launch_bounds__(256) attn_combine_kernel(const float* __restrict__ part, int rows,
                                                            int n_split, __half* __restrict__ out) {
@@ -627,21 +630,46 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(const float* __restri
   if (row >= rows) return;
   constexpr int PER = HD / 32;
   const float* ml = part + static_cast<size_t>(n_split) * rows * HD;
-  float mstar = -INFINITY;
-  for (int s = 0; s < n_split; ++s) mstar = fmaxf(mstar, ml[2 * (static_cast<size_t>(s) * rows + row)]);
+  float m0 = -INFINITY, l0 = 0.f, m1 = -INFINITY, l1 = 0.f;  // parts lane and lane + 32
+  if (lane < n_split) {
+    const size_t sr = static_cast<size_t>(lane) * rows + row;
+    m0 = ml[2 * sr];
+    l0 = ml[2 * sr + 1];
+  }
+  if (lane + 32 < n_split) {
+    const size_t sr = static_cast<size_t>(lane + 32) * rows + row;
+    m1 = ml[2 * sr];
+    l1 = ml[2 * sr + 1];
+  }
+  float mstar = fmaxf(m0, m1);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mstar = fmaxf(mstar, __shfl_xor_sync(0xffffffffu, mstar, o));
+  const float w0 = m0 == -INFINITY ? 0.f : exp2f(m0 - mstar);
+  const float w1 = m1 == -INFINITY ? 0.f : exp2f(m1 - mstar);
+  float lsum = w0 * l0 + w1 * l1;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, o);
   float acc[PER];
 #pragma unroll
   for (int i = 0; i < PER; ++i) acc[i] = 0.f;
-  float lsum = 0.f;
-  for (int s = 0; s < n_split; ++s) {
-    const size_t sr = static_cast<size_t>(s) * rows + row;
-    const float ms = ml[2 * sr];
-    if (ms == -INFINITY) continue;
-    const float w = exp2f(ms - mstar);
-    lsum += w * ml[2 * sr + 1];
-    const float* o = part + sr * HD + lane * PER;
+  const float* o0 = part + static_cast<size_t>(row) * HD + lane * PER;
+  const size_t stride = static_cast<size_t>(rows) * HD;  // between parts
+  for (int s0 = 0; s0 < n_split; s0 += 8) {
+    float x[8][PER];
 #pragma unroll
-    for (int i = 0; i < PER; ++i) acc[i] += w * o[i];
+    for (int u = 0; u < 8; ++u) {
+      const int s = s0 + u;
+#pragma unroll
+      for (int i = 0; i < PER; ++i) x[u][i] = s < n_split ? o0[s * stride + i] : 0.f;
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int s = s0 + u;
+      const float w = __shfl_sync(0xffffffffu, s < 32 ? w0 : w1, s & 31);
+      if (w == 0.f) continue;  // a part that saw no key of the row wrote no O (warp-uniform)
+#pragma unroll
+      for (int i = 0; i < PER; ++i) acc[i] = fmaf(w, x[u][i], acc[i]);
+    }
   }
   const float inv = 1.f / lsum;
   __half* dst = out + static_cast<size_t>(row) * HD + lane * PER;

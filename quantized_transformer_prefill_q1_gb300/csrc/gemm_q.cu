@@ -739,7 +739,7 @@ cudaError_t prepare_gemm_kernels() {
   return e;
 }
 
-bool gemm_store_accumulates(int wfmt, int M) { return M > gemv_max_m(wfmt) && M > SMALL_M_MAX; }
+bool gemm_side_zero_supported(int wfmt, int M) { return M > gemv_max_m(wfmt) && M > SMALL_M_MAX; }
 
 cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t stream) {
   if (g.side_zero != nullptr && (g.M <= SMALL_M_MAX || g.M <= gemv_max_m(g.wfmt) ||

@@ -437,10 +437,12 @@ cudaError_t prepare_gemm_small_kernels() {
 cudaError_t launch_gemm_small(const GemmArgs& g, cudaStream_t stream) {
   static int sms = device_sm_count();
   if (g.epilogue == EPI_STORE_F32) {
-    // the output is small (M x N f32, M <= 64): zero it and accumulate every CTA's share
-    // like the residual form, instead of passing split tiles through scratch
-    cudaError_t e = cudaMemsetAsync(g.out, 0, static_cast<size_t>(g.M) * g.N * sizeof(float), stream);
-    if (e != cudaSuccess) return e;
+    // the output is small (M x N f32, M <= 64): zero it (unless the caller has) and accumulate
+    // every CTA's share like the residual form, instead of passing split tiles through scratch
+    if (!g.out_zeroed) {
+      cudaError_t e = cudaMemsetAsync(g.out, 0, static_cast<size_t>(g.M) * g.N * sizeof(float), stream);
+      if (e != cudaSuccess) return e;
+    }
     GemmArgs r = g;
     r.epilogue = EPI_RESID_ADD;
     return launch_gemm_small(r, stream);

@@ -435,8 +435,9 @@ int gemv_max_m(int wfmt) { return wfmt == PF_W_Q1_G128 ? GEMV_M_MAX_Q1 : GEMV_M_
 cudaError_t launch_gemv(const GemmArgs& g, cudaStream_t stream) {
   if (g.M < 1 || g.M > 8 || g.K % GROUP) return cudaErrorInvalidValue;
   if (g.epilogue == EPI_SWIGLU && g.N % 256) return cudaErrorInvalidValue;
-  if (g.epilogue == EPI_STORE_F32) {
-    // zero the M x N output and add every range's share, as the residual form does
+  if (g.epilogue == EPI_STORE_F32 && !g.out_zeroed) {
+    // zero the M x N output (unless the caller has) and add every range's share, as the
+    // residual form does
     cudaError_t e = cudaMemsetAsync(g.out, 0, static_cast<size_t>(g.M) * g.N * sizeof(float), stream);
     if (e != cudaSuccess) return e;
   }

@@ -350,14 +350,15 @@ pf_status enqueue_layer(pf_session* s, int l, float* x, int M, cudaStream_t st, 
   void* act = wsp<void>(s, s->L.act);
   // 1. pre-attention RMSNorm; where the QKV GEMM accumulates into a zeroed output, the norm's
   //    CTAs zero it (one qkv row each), so no memset breaks the launch chain
-  const bool accum = gemm_store_accumulates(c.wfmt, M);
-  const bool zero_qkv = accum && !qkv_zeroed;
+  //    Every GEMM path accumulates the QKV projection into a zeroed qkv: the previous layer's
+  //    gate_up GEMM zeroes it where it can (M > 64), this norm's CTAs otherwise
+  const bool side = gemm_side_zero_supported(c.wfmt, M);
+  const bool zero_qkv = !(qkv_zeroed && side);
   PF_TRY(launch_k(s, PF_K_RMSNORM, st, "rmsnorm", [&] {
     return launch_rmsnorm(x, w.attn_norm, c.eps, M, H, y, st, zero_qkv ? qkv : nullptr, qkv_rows);
   }));
   // 2. fused QKV projection
-  PF_TRY(enqueue_gemm(s, PF_K_GEMM_QKV, c.wfmt, EPI_STORE_F32, y, w.qkv, M, qkv_rows, H, qkv, st,
-                      accum));
+  PF_TRY(enqueue_gemm(s, PF_K_GEMM_QKV, c.wfmt, EPI_STORE_F32, y, w.qkv, M, qkv_rows, H, qkv, st, true));
   // 3. QK-norm + RoPE + KV store, then causal GQA attention over cache + chunk. A ring cache
   //    takes the chunk's K / V in the chunk buffers first (its later tokens may overwrite
   //    slots its earlier tokens still see) and into the ring after the attention.
@@ -398,7 +399,7 @@ pf_status enqueue_layer(pf_session* s, int l, float* x, int M, cudaStream_t st, 
   PF_TRY(launch_k(s, PF_K_RMSNORM, st, "rmsnorm",
                   [&] { return launch_rmsnorm(x, w.ffn_norm, c.eps, M, H, y, st); }));
   // 6. gate_up + SwiGLU
-  const bool zero_next = accum && zero_next_qkv;
+  const bool zero_next = side && zero_next_qkv;
   PF_TRY(enqueue_gemm(s, PF_K_GEMM_GATE_UP, c.wfmt, EPI_SWIGLU, y, w.gate_up, M, 2 * I, H, act, st,
                       false, zero_next ? qkv : nullptr,
                       zero_next ? static_cast<size_t>(M) * qkv_rows * sizeof(float) : 0));

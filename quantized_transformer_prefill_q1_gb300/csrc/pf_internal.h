@@ -69,17 +69,17 @@ struct GemmArgs {
   int max_ctas;         // 1..GEMM_MAX_CTAS; the scratch layout depends on it
   void* scratch;        // gemm_scratch_bytes(M, N, max_ctas); its counters zero before the launch
   int* status;          // may be NULL
-  bool out_zeroed;      // store form: the caller has set out to zero (gemm_store_accumulates)
+  bool out_zeroed;      // store form: the caller has set out to zero (every path accumulates
+                        // the store form into a zeroed output; without this flag it zeroes
+                        // it itself first)
   // optional (M > SMALL_M_MAX only): a buffer that the CTAs' epilogue warps set to zero while
   // the main loop runs (the accumulator of a later store-form GEMM); 16-B aligned and sized
   void* side_zero;
   size_t side_zero_bytes;
 };
 cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t stream);
-// Whether launch_gemm's store form at this M accumulates into a zeroed output (TMA
-// reduce-add from every CTA's share). It zeroes the output itself first unless
-// GemmArgs::out_zeroed says the caller already has.
-bool gemm_store_accumulates(int wfmt, int M);
+// Whether GemmArgs::side_zero is available at this M (the persistent tcgen05 GEMM).
+bool gemm_side_zero_supported(int wfmt, int M);
 // M <= SMALL_M_MAX: the weight rows are the MMA's M side (gemm_small.cu); launch_gemm routes
 cudaError_t launch_gemm_small(const GemmArgs& g, cudaStream_t stream);
 cudaError_t prepare_gemm_small_kernels();
