@@ -683,6 +683,12 @@ cudaError_t launch_t(const GemmArgs& g, const CUtensorMap& ta, const CUtensorMap
   // the tiles alone fill at least half of the units, run one whole tile per unit instead
   const int tiles = p.n_mt * p.n_nt;
   if (EPI != EPI_RESID_ADD && tiles < p.ctas && 2 * tiles >= p.ctas) p.ctas = tiles;
+  p.late0 = p.ctas;
+  p.dk = 0;
+  if (PAIR && g.late_units > 0 && g.late_kb > 0) {
+    p.late0 = std::max(0, p.ctas - g.late_units);
+    p.dk = static_cast<int>(std::min<long long>(g.late_kb, std::max<long long>(0, p.total / p.ctas - 1)));
+  }
   float* scratch = reinterpret_cast<float*>(g.scratch);
   int* counters =
       scratch ? reinterpret_cast<int*>(scratch + static_cast<size_t>(2) * g.max_ctas * SLOT_FLOATS) : nullptr;

@@ -391,6 +391,8 @@ cudaError_t launch_s(const GemmArgs& g, int num_sms, cudaStream_t stream) {
   // store / SwiGLU: a tile split between CTAs costs a partial hand-off, so when the tiles
   // alone fill at least half of the CTAs, run whole tiles (the residual form adds shares)
   if (EPI != EPI_RESID_ADD && p.n_nt < p.ctas && 2 * p.n_nt >= p.ctas) p.ctas = p.n_nt;
+  p.late0 = p.ctas;  // no skew
+  p.dk = 0;
   float* scratch = reinterpret_cast<float*>(g.scratch);
   int* counters = reinterpret_cast<int*>(scratch + static_cast<size_t>(2) * g.max_ctas * SLOT);
   return launch_pdl(gemm_small_kernel<WFMT, EPI, NT>, dim3(p.ctas), dim3(THREADS_S), SL<WFMT, NT>::BYTES,

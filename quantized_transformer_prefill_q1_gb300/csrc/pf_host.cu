@@ -329,11 +329,24 @@ pf_status enqueue_gemm(pf_session* s, int cls, int wfmt, int epi, const void* a,
   g.max_ctas = GEMM_MAX_CTAS;
   g.scratch = wsp<void>(s, s->L.gemm);
   g.status = wsp<int>(s, s->L.status);
+  // Stream-K skew of the layer GEMMs at full chunks: the CTAs launched last start on SMs that
+  // the previous kernel still holds, 1-2 us after the others (per-CTA timeline, 512-token
+  // chunks on GB300: the last ~26 of 76 pairs after an RMSNorm, a ramp over the last ~36 after
+  // attention, the last ~20 after gate_up), so those units take a few k-blocks fewer.
+  if (M >= 384) {
+    switch (cls) {
+      case PF_K_GEMM_QKV: g.late_units = 26; g.late_kb = 5; break;
+      case PF_K_GEMM_GATE_UP: g.late_units = 26; g.late_kb = 3; break;
+      case PF_K_GEMM_O: g.late_units = 36; g.late_kb = 3; break;
+      case PF_K_GEMM_DOWN: g.late_units = 20; g.late_kb = 4; break;
+      default: break;
+    }
+  }
   return launch_k(s, cls, st, "gemm launch", [&] { return launch_gemm(g, st); });
 }
 
 // metal_prefill.rs encode_layer_prefill, sections 1-7, on x [M, H] (in place). Where the
-// QKV GEMM accumulates into a zeroed qkv buffer (gemm_store_accumulates), `qkv_zeroed` says
+// QKV GEMM accumulates into a zeroed qkv buffer (gemm_side_zero_supported), `qkv_zeroed` says
 // an earlier kernel has zeroed it already, and `zero_next_qkv` has this layer's gate_up GEMM
 // zero it for the next layer (its epilogue warps are idle during the main loop).
 pf_status enqueue_layer(pf_session* s, int l, float* x, int M, cudaStream_t st, bool qkv_zeroed,

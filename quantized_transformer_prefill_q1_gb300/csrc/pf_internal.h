@@ -76,6 +76,10 @@ struct GemmArgs {
   // the main loop runs (the accumulator of a later store-form GEMM); 16-B aligned and sized
   void* side_zero;
   size_t side_zero_bytes;
+  // optional stream-K skew (CTA-pair form): the last `late_units` units take `late_kb`
+  // k-blocks fewer each, for CTAs that start late on SMs the previous kernel still holds
+  int late_units;
+  int late_kb;
 };
 cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t stream);
 // Whether GemmArgs::side_zero is available at this M (the persistent tcgen05 GEMM).

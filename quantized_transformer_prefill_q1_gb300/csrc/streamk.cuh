@@ -6,16 +6,26 @@
 namespace pf {
 namespace sk {
 
-// n_mt x n_nt tiles of kbt k-blocks each, `total` k-blocks in all; CTA c owns
-// [total c / ctas, total (c + 1) / ctas).
+// n_mt x n_nt tiles of kbt k-blocks each, `total` k-blocks in all, cut into `ctas` contiguous
+// ranges. Units [late0, ctas) start later than the others (the scheduler places the CTAs
+// launched last on SMs that the previous kernel still holds), so each of them takes dk
+// k-blocks fewer: the ranges are equal on a virtual list in which every late unit's range is
+// padded by dk k-blocks. dk = 0 gives CTA c [total c / ctas, total (c + 1) / ctas).
 struct Plan {
   int n_mt, n_nt, kbt;
   long long total;
   int ctas;
-  __device__ __forceinline__ long long begin(int c) const { return total * c / ctas; }
-  // CTA whose range holds k-block w
+  int late0, dk;  // dk <= total / ctas - 1 keeps every range non-empty
+  __device__ __forceinline__ long long begin(int c) const {
+    const long long vt = total + static_cast<long long>(ctas - late0) * dk;
+    return vt * c / ctas - static_cast<long long>(dk) * (c > late0 ? c - late0 : 0);
+  }
+  // unit whose range holds k-block w (the unskewed guess is off by a few units at most)
   __device__ __forceinline__ int owner(long long w) const {
-    return static_cast<int>(((w + 1) * ctas - 1) / total);
+    int c = static_cast<int>(((w + 1) * ctas - 1) / total);
+    while (c > 0 && begin(c) > w) --c;
+    while (c + 1 < ctas && begin(c + 1) <= w) ++c;
+    return c;
   }
   // scratch slot (0 or 1) of contributor c's partial for `tile`: 0 if c's range begins
   // inside the tile, 1 if it begins at or before the tile's start
@@ -30,10 +40,12 @@ struct Segment {
 };
 
 // The segments of one CTA's range in processing order: the partial first and last
-// segments (if any) come first, then the whole tiles in k order.
+// segments (if any) come first, the shorter of the two ahead (its epilogue then runs under
+// the longer one's main loop), then the whole tiles in k order.
 struct Range {
   long long b, e;
   int t0, n, first_part, last_part;
+  bool swap;  // the partial last segment runs first
   __device__ __forceinline__ Range(const Plan& p, int c) {
     b = p.begin(c);
     e = p.begin(c + 1);
@@ -43,9 +55,11 @@ struct Range {
     const long long s0_end = std::min<long long>(e, static_cast<long long>(t0 + 1) * p.kbt);
     first_part = (b == static_cast<long long>(t0) * p.kbt && s0_end - b == p.kbt) ? 0 : 1;
     last_part = (n > 1 && e != static_cast<long long>(t1 + 1) * p.kbt) ? 1 : 0;
+    swap = first_part && last_part && e - static_cast<long long>(t1) * p.kbt < s0_end - b;
   }
   __device__ __forceinline__ Segment at(const Plan& p, int k) const {
-    const int i = k < first_part ? 0 : (k < first_part + last_part ? n - 1 : k - last_part);
+    int i = k < first_part ? 0 : (k < first_part + last_part ? n - 1 : k - last_part);
+    if (swap && k < 2) i = k == 0 ? n - 1 : 0;
     Segment s;
     s.tile = t0 + i;
     const long long ts = static_cast<long long>(s.tile) * p.kbt;
