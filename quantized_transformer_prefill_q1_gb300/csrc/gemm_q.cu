@@ -304,6 +304,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
   };
   __syncthreads();  // this CTA's barriers are initialised
+  // Pair: the cluster barrier is split. Each thread arrives once its part of the set-up that
+  // the other CTA relies on is done (barriers above; warp 1: this CTA's share of the pair's
+  // TMEM) and waits only before its first access to the other CTA (dequantisers, MMA and
+  // epilogue warps before their loops; the producer, which never touches it, at the end).
+  if (PAIR && warp != 1) cluster_arrive_relaxed();
   int pre = 0;      // (producer thread) stages whose weight copies are issued before the wait
   if (threadIdx.x == 0) {
     for (int k = 0; k < rg.n && pre < S; ++k) {
@@ -322,19 +327,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (PAIR) {
       tmem_alloc_pair(smem_u32(tmem_slot), TMEM_COLS);
       tmem_relinquish_pair();
+      tc_fence_before();
+      cluster_arrive_release();
     } else {
       tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
       tmem_relinquish();
     }
   }
-  tc_fence_before();
-  __syncwarp();
-  if (PAIR)
-    cluster_sync_all();  // both CTAs' barriers exist before either arrives on the other's
-  else
-    __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem_base = *tmem_slot;
+  // the TMEM address, for the MMA and epilogue warps (warps 1 .. 1 + NUM_EPI_WARPS)
+  uint32_t tmem_base = 0;
+  if (warp >= 1 && warp <= NUM_EPI_WARPS + 1) {
+    tc_fence_before();
+    named_bar_sync(2, 32 * (NUM_EPI_WARPS + 1));
+    tc_fence_after();
+    tmem_base = *tmem_slot;
+  }
 
   if (warp == 0) {
     // ---------------------------------------------------------------- TMA producer
@@ -388,6 +395,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       else
         umma_commit_warp(bar);
     };
+    if (PAIR) cluster_wait();  // the other CTA's barriers and TMEM share exist
     int it = 0;
     bool ok = true;
     for (int k = 0; k < (PAIR && rank != 0 ? 0 : rg.n) && ok; ++k) {
@@ -423,6 +431,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   } else if (warp >= FIRST_DQ_WARP) {
     // ---------------------------------------------------------------- dequantisers
     const int d = threadIdx.x - FIRST_DQ_WARP * 32;  // weight row of the tile (pair: row + 128 half)
+    if (PAIR) cluster_wait();  // before the first arrival on the even CTA's barriers
     int it = 0;
     bool ok = true;
     for (int k = 0; k < rg.n && ok; ++k) {
@@ -464,6 +473,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       for (long long i = per * blockIdx.x + et; i < z1; i += EPI_THREADS)
         __stcg(side_zero + i, make_float4(0.f, 0.f, 0.f, 0.f));
     }
+    if (PAIR) cluster_wait();
     const uint32_t stg = stg0 + q * STG_BYTES;
     // hands a staging tile (after its 32 x 32 values were written) to TMA
     auto stage_out = [&](uint32_t buf, int x, int y) {
@@ -502,8 +512,25 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const bool valid = row0 + lane < M;
       const uint32_t tb = tmem_base + b * BN + (static_cast<uint32_t>(32 * q) << 16);
 
-      if (EPI == EPI_RESID_ADD) {
-        // out += this segment's partial sum, whole tile or not
+      if (EPI == EPI_RESID_ADD && last) {
+        // out += the last segment's partial sum, whole tile or not. Its chunks have buffers of
+        // their own, and the TMEM load of chunk c + 1 is in flight while chunk c is staged.
+        uint32_t va[32], vb[32];
+        tmem_ld_32x32b_x32(tb, va);
+        tmem_ld_wait();
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; c += 2) {
+          tmem_ld_32x32b_x32(tb + 32 * (c + 1), vb);
+          stage_f32(stage_buf(c), lane, va);
+          stage_out(stage_buf(c), sg.nt * BN + 32 * c, row0);
+          tmem_ld_wait();
+          if (c + 2 < BN / 32) tmem_ld_32x32b_x32(tb + 32 * (c + 2), va);
+          stage_f32(stage_buf(c + 1), lane, vb);
+          stage_out(stage_buf(c + 1), sg.nt * BN + 32 * (c + 1), row0);
+          tmem_ld_wait();
+        }
+      } else if (EPI == EPI_RESID_ADD) {
+        // out += this segment's partial sum, through the warp's staging tile
 #pragma unroll 1
         for (int c = 0; c < BN / 32; ++c) {
           uint32_t v[32];
@@ -622,18 +649,26 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         mbar_arrive(acc_empty(b));
       }
     }
+    // this CTA's TMEM reads and arrivals on the other CTA are done: arrive on the end barrier
+    // before the last TMA writes drain
+    tc_fence_before();
+    if (PAIR) cluster_arrive_release();
     if (lane == 0) bulk_wait0();  // TMA writes complete before the CTA retires
     __syncwarp();
   }
 
+  if (PAIR && warp == 0) cluster_wait();  // the producer's wait of the split start-up barrier
+  // A pair's CTAs stay until both are done with each other: the even CTA's MMAs read the odd
+  // one's shared memory and write its TMEM, the odd one arrives on the even one's barriers.
+  // The end barrier is split as well (the epilogue warps arrived above).
   tc_fence_before();
-  // a pair's CTAs stay until both are done: the even CTA's MMAs read the odd one's shared
-  // memory, and the odd one arrives on the even one's barriers
   __syncwarp();
-  if (PAIR)
-    cluster_sync_all();
-  else
+  if (PAIR) {
+    if (warp < 2 || warp >= FIRST_DQ_WARP) cluster_arrive_release();
+    cluster_wait();
+  } else {
     __syncthreads();
+  }
   if (warp == 1) {
     tc_fence_after();
     __syncwarp();  // reconverge before the collective dealloc

@@ -242,6 +242,18 @@ __device__ __forceinline__ uint32_t cluster_ctarank() {
 __device__ __forceinline__ void cluster_sync_all() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
+// Split form of the same barrier: every thread arrives once and waits once, in that order.
+// relaxed: nothing of this thread's to publish (barrier inits are published by
+// fence.mbarrier_init.release.cluster first)
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_arrive_release() {
+  asm volatile("barrier.cluster.arrive.release;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+  asm volatile("barrier.cluster.wait.acquire;" ::: "memory");
+}
 // Arrive on the barrier at shared offset `bar` of cluster CTA `rank` (the instruction's
 // default release semantics). Used by the odd CTA of a pair to tell the even one that its
 // dequantised operand tile (written, then fenced to the async proxy, in its own shared memory,
