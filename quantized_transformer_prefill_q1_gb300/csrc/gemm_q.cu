@@ -55,6 +55,7 @@ constexpr int DQ_THREADS = NUM_DQ_WARPS * 32;  // == BN: one weight row per thre
 constexpr int EPI_THREADS = NUM_EPI_WARPS * 32;
 constexpr int NUM_THREADS = 32 * (2 + NUM_EPI_WARPS + NUM_DQ_WARPS);  // 448
 constexpr int FIRST_DQ_WARP = 2 + NUM_EPI_WARPS;
+constexpr int LAST_THREADS = EPI_THREADS + DQ_THREADS;  // barrier 3: the last residual epilogue
 constexpr int A_STAGE = BM * BK * 2;  // 16 KB
 constexpr int STG_BYTES = 32 * 32 * 4;  // per epilogue warp: 32 rows x 32 f32
 constexpr int TMEM_COLS = 512;          // two accumulators of 256 f32 columns
@@ -334,14 +335,35 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       tmem_relinquish();
     }
   }
-  // the TMEM address, for the MMA and epilogue warps (warps 1 .. 1 + NUM_EPI_WARPS)
+  // the TMEM address, for every warp but the producer (the dequantisers share the residual
+  // form's last epilogue)
   uint32_t tmem_base = 0;
-  if (warp >= 1 && warp <= NUM_EPI_WARPS + 1) {
+  if (warp >= 1) {
     tc_fence_before();
-    named_bar_sync(2, 32 * (NUM_EPI_WARPS + 1));
+    named_bar_sync(2, NUM_THREADS - 32);
     tc_fence_after();
     tmem_base = *tmem_slot;
   }
+  // Residual form, last segment: its 8 chunks of 32 columns per TMEM lane quarter are drained
+  // by the quarter's epilogue warp (share 0) and its two dequantising warps (shares 1, 2),
+  // chunks share, share + 3, ... each into a 4 KB buffer of its own in the idle operand ring.
+  auto last_resid_chunks = [&](const Segment& sg, uint32_t tb, int row0, int share) {
+    const int q = warp & 3;
+#pragma unroll 1
+    for (int c = share; c < BN / 32; c += 3) {
+      uint32_t v[32];
+      tmem_ld_32x32b_x32(tb + 32 * c, v);
+      tmem_ld_wait();
+      const uint32_t buf = a_st + static_cast<uint32_t>(q * (BN / 32) + c) * STG_BYTES;
+      stage_f32(buf, lane, v);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        tma_reduce_add_2d(&tmap_out, buf, sg.nt * BN + 32 * c, row0);
+        bulk_commit();
+      }
+    }
+  };
 
   if (warp == 0) {
     // ---------------------------------------------------------------- TMA producer
@@ -460,6 +482,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
       }
     }
+    if (EPI == EPI_RESID_ADD && rg.n > 0) {
+      // the epilogue warps meet these warps on barrier 3 once the last accumulator is ready
+      if (named_bar_and(3, LAST_THREADS, ok)) {
+        tc_fence_after();
+        const int k = rg.n - 1;
+        const Segment sg = rg.at(plan, k);
+        const int q = warp & 3;
+        const int row0 = sg.mt * C::TILE_M + a_row + 32 * q;
+        last_resid_chunks(sg, tmem_base + (k & 1) * BN + (static_cast<uint32_t>(32 * q) << 16), row0,
+                          warp < FIRST_DQ_WARP + 4 ? 1 : 2);
+      }
+      tc_fence_before();
+      if (lane == 0) bulk_wait0();
+      __syncwarp();
+    }
   } else {
     // ---------------------------------------------------------------- epilogue (warps 2..5)
     griddep_wait();  // out / scratch / counters are shared with the previous kernels
@@ -487,6 +524,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         bulk_commit();
       }
     };
+    bool met_last = false;  // residual form: barrier 3 with the dequantising warps passed
     for (int k = 0; k < rg.n; ++k) {
       // The last segment's epilogue runs after the main loop has ended, when the operand ring
       // is idle (its last MMA has completed): each 32-column chunk then gets a 4 KB buffer of
@@ -513,22 +551,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const uint32_t tb = tmem_base + b * BN + (static_cast<uint32_t>(32 * q) << 16);
 
       if (EPI == EPI_RESID_ADD && last) {
-        // out += the last segment's partial sum, whole tile or not. Its chunks have buffers of
-        // their own, and the TMEM load of chunk c + 1 is in flight while chunk c is staged.
-        uint32_t va[32], vb[32];
-        tmem_ld_32x32b_x32(tb, va);
-        tmem_ld_wait();
-#pragma unroll 1
-        for (int c = 0; c < BN / 32; c += 2) {
-          tmem_ld_32x32b_x32(tb + 32 * (c + 1), vb);
-          stage_f32(stage_buf(c), lane, va);
-          stage_out(stage_buf(c), sg.nt * BN + 32 * c, row0);
-          tmem_ld_wait();
-          if (c + 2 < BN / 32) tmem_ld_32x32b_x32(tb + 32 * (c + 2), va);
-          stage_f32(stage_buf(c + 1), lane, vb);
-          stage_out(stage_buf(c + 1), sg.nt * BN + 32 * (c + 1), row0);
-          tmem_ld_wait();
-        }
+        // out += the last segment's partial sum (whole tile or not): this warp's share, after
+        // handing the rest to the dequantising warps
+        met_last = true;
+        named_bar_and(3, LAST_THREADS, true);
+        last_resid_chunks(sg, tb, row0, 0);
       } else if (EPI == EPI_RESID_ADD) {
         // out += this segment's partial sum, through the warp's staging tile
 #pragma unroll 1
@@ -649,6 +676,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         mbar_arrive(acc_empty(b));
       }
     }
+    if (EPI == EPI_RESID_ADD && rg.n > 0 && !met_last) named_bar_and(3, LAST_THREADS, false);
     // this CTA's TMEM reads and arrivals on the other CTA are done: arrive on the end barrier
     // before the last TMA writes drain
     tc_fence_before();
