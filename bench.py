@@ -46,7 +46,7 @@ PROMPT, CHUNK = 2048, 512
 # kernel class; None when no capture matches the kernel as it now stands.
 # gate_up: dram__bytes_read.sum + dram__bytes_write.sum of one --set full capture of
 # `bench.py --case gemm_gate_up` (M 512, N 24576, K 4096)
-NCU_TRAFFIC = {"gemm_gate_up": 18405888 + 673536}
+NCU_TRAFFIC = {"gemm_gate_up": 18454528 + 880896}
 
 
 CASES = ["gemm_gate_up", "gemm_qkv", "gemm_down", "gemm_o", "attention", "rmsnorm", "qk_rope_kv", "lm_head",
@@ -356,10 +356,24 @@ def run_decode(args, pf, synth, dev):
     prof = sess.profile_read()
     sess.set_profile(False)
     breakdown = {k: round(v[0] / 4 * 1e3, 2) for k, v in prof.items() if v[1]}
+    # one replayed token with the per-CTA kernel timeline: each kernel class's mean share of
+    # the token's critical path per launch
+    pos = [4 + steps + 4]
+
+    def one():
+        i = pos[0]
+        sess.decode_step(toks[CHUNK + i % 64:CHUNK + i % 64 + 1], logits)
+        pos[0] += 1
+
+    one()
+    sess.sync()
+    tl_us, _, per = timeline_prompt(pf, torch, one)
+    crit = {lab: round(float(np.mean([x[0] for x in d])) / 1e3, 2) for lab, d in per.items()}
     wbytes = shape.n_layers * 27.13e6 + 87.5e6  # packed layer weights + LM head read per step
     print(json.dumps({"case": "decode", "us_per_token": us, "tokens_per_s": 1e6 / us,
                       "weight_GBps": wbytes / us / 1e3, "kv_position_end": sess.position,
-                      "profiled_us_per_token": breakdown}),
+                      "profiled_us_per_token": breakdown, "timeline_us_per_token": round(tl_us, 1),
+                      "critical_path_us_per_launch": crit}),
           flush=True)
 
 
