@@ -366,9 +366,11 @@ pf_status pf_op_attention(const pf_config* cfg, const void* q_dev, const void* k
 /* The same with the keys cut into n_split contiguous parts (1..64), one CTA each, whose
  * unnormalised partial results (O sums, running max and sum per row) go to scratch_dev
  * (device, 16-B aligned, caller-owned, at least pf_attention_scratch_bytes(cfg, M, n_split)
- * bytes) and are merged by a second kernel: the split-KV form the sessions use when a
- * chunk's CTAs fill less than half of the GPU (decode, small chunks). 16-bit linear caches
- * only; the same result as pf_op_attention up to the order of the f32 additions. */
+ * bytes: a counter per kv head, which the call zeroes first, then the partials) and are
+ * merged by a second kernel, or for M <= 2 by the part that completes each kv head's count:
+ * the split-KV form the sessions use when a chunk's CTAs fill less than half of the GPU
+ * (decode, small chunks). 16-bit linear caches only; the same result as pf_op_attention up
+ * to the order of the f32 additions. */
 size_t pf_attention_scratch_bytes(const pf_config* cfg, int32_t M, int32_t n_split);
 pf_status pf_op_attention_split(const pf_config* cfg, const void* q_dev, const void* k_cache_dev,
                                 const void* v_cache_dev, int32_t layer, int32_t start_pos,

@@ -52,6 +52,9 @@ constexpr int SM_THREADS = 256;  // softmax threads: two per query row
 constexpr int HK = TK / 2;       // keys per softmax thread and tile
 constexpr int NSB = 3;           // S / P buffers in TMEM
 constexpr int MAX_SPLIT = 64;
+// split-KV chunks of at most 2 tokens merge inside the kernel: at most 8 rows per kv head
+// (G <= 4), one per softmax warp; more rows per warp lost to the separate merge kernel
+constexpr int MERGE_M_MAX = 2;
 constexpr float RESCALE_LOG2 = 8.0f;
 // TMEM columns: S buffers b at b TK (P_j over the first TK/2 columns of its buffer), O at 3 TK
 constexpr uint32_t COL_O = NSB * TK;
@@ -143,8 +146,10 @@ struct AttnKParams {
   int start_host;
   float scale_log2;
   int n_split;
+  int merge;  // split-KV with few rows (M <= MERGE_M_MAX): the last part to finish merges them
   __half* out;
   float* partial;
+  int* counters;  // merge: one arrival counter per kv head (such a chunk is one query tile)
   int* status;
   const int* blocks;  // paged cache: block table (position block -> physical block), else NULL
 };
@@ -208,6 +213,66 @@ __device__ __forceinline__ uint32_t pack_pair(float a, float b) {
     __half2 h = __floats2half2_rn(a, b);
     return *reinterpret_cast<uint32_t*>(&h);
   }
+}
+
+// Merges the n_split partial results of (token, head) row `row` (of `rows` per part): with
+// m* the largest of the parts' running maxima, O = sum_s 2^(m_s - m*) O_s / sum_s 2^(m_s - m*)
+// l_s (the parts keep O_s and l_s relative to their own m_s, in the exp2 domain). Parts that
+// saw no key of the row (m_s = -inf) wrote no O and are skipped. One warp per row: lane s
+// reads part s's (m, l) (and s + 32), the warp reduces m* and the weighted sum of l, then each
+// lane accumulates its HD / 32 columns over the parts with the weights broadcast from their
+// lanes, loads issued eight parts at a time (through L2: other CTAs of the same kernel may
+// have written them).
+template <int HD>
+__device__ __forceinline__ void merge_row(const float* part, int rows, int n_split, int row, int lane,
+                                          __half* out) {
+  constexpr int PER = HD / 32;
+  const float* ml = part + static_cast<size_t>(n_split) * rows * HD;
+  float m0 = -INFINITY, l0 = 0.f, m1 = -INFINITY, l1 = 0.f;  // parts lane and lane + 32
+  if (lane < n_split) {
+    const size_t sr = static_cast<size_t>(lane) * rows + row;
+    m0 = __ldcg(ml + 2 * sr);
+    l0 = __ldcg(ml + 2 * sr + 1);
+  }
+  if (lane + 32 < n_split) {
+    const size_t sr = static_cast<size_t>(lane + 32) * rows + row;
+    m1 = __ldcg(ml + 2 * sr);
+    l1 = __ldcg(ml + 2 * sr + 1);
+  }
+  float mstar = fmaxf(m0, m1);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mstar = fmaxf(mstar, __shfl_xor_sync(0xffffffffu, mstar, o));
+  const float w0 = m0 == -INFINITY ? 0.f : exp2f(m0 - mstar);
+  const float w1 = m1 == -INFINITY ? 0.f : exp2f(m1 - mstar);
+  float lsum = w0 * l0 + w1 * l1;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, o);
+  float acc[PER];
+#pragma unroll
+  for (int i = 0; i < PER; ++i) acc[i] = 0.f;
+  const float* o0 = part + static_cast<size_t>(row) * HD + lane * PER;
+  const size_t stride = static_cast<size_t>(rows) * HD;  // between parts
+  for (int s0 = 0; s0 < n_split; s0 += 8) {
+    float x[8][PER];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int s = s0 + u;
+#pragma unroll
+      for (int i = 0; i < PER; ++i) x[u][i] = s < n_split ? __ldcg(o0 + s * stride + i) : 0.f;
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int s = s0 + u;
+      const float w = __shfl_sync(0xffffffffu, s < 32 ? w0 : w1, s & 31);
+      if (w == 0.f) continue;  // a part that saw no key of the row wrote no O (warp-uniform)
+#pragma unroll
+      for (int i = 0; i < PER; ++i) acc[i] = fmaf(w, x[u][i], acc[i]);
+    }
+  }
+  const float inv = 1.f / lsum;
+  __half* dst = out + static_cast<size_t>(row) * HD + lane * PER;
+#pragma unroll
+  for (int i = 0; i < PER; i += 2) *reinterpret_cast<__half2*>(dst + i) = __floats2half2_rn(acc[i] * inv, acc[i + 1] * inv);
 }
 
 template <int HD, int BF16>
@@ -310,17 +375,41 @@ __global__ void __launch_bounds__(THREADS, 1)
   };
 
 
+  // Split-KV with few rows: every part's softmax threads (two per query row, the mapping of
+  // the softmax warps) count the part in once its partial rows are written; the part that
+  // completes the count merges all parts' rows of its (query tile, kv head) into the output
+  // and resets the counter (what attn_combine_kernel does otherwise, without its launch).
+  __shared__ int merge_last;
+  auto merge_tail = [&](bool wrote) {
+    int* ctr = P.counters + kvh;
+    __threadfence();  // this thread's partial rows are visible GPU-wide before the count
+    named_bar_sync_a(1, SM_THREADS);
+    if (threadIdx.x == 64) merge_last = (wrote && atomicAdd(ctr, 1) == P.n_split - 1) ? 1 : 0;
+    named_bar_sync_a(1, SM_THREADS);
+    if (!merge_last) return;
+    __threadfence();
+    // one softmax warp per row of this CTA that exists (t < M)
+    const int rows_cta = (t1 - t0) * G;
+    for (int rr = warp - 2; rr < rows_cta; rr += SM_THREADS / 32) {
+      const int t = t0 + rr / G, h = kvh * G + rr % G;
+      merge_row<HD>(P.partial, M * nq, P.n_split, t * nq + h, lane, P.out);
+    }
+    if (threadIdx.x == 64) *ctr = 0;  // every part is in: ready for the next launch
+  };
+
   if (nt == 0) {
     // an empty part of a split list: its rows contribute nothing (max -inf, sum 0)
-    if (warp >= 2 && threadIdx.x - 64 < TQ) {
-      const int r = threadIdx.x - 64;
+    if (warp >= 2) {
+      const int quarter = warp & 3, half = (warp - 2) >> 2;
+      const int r = 32 * quarter + lane;
       const int t = t0 + r / G;
-      if (t < M) {
+      if (half == 0 && t < M) {
         float* ml = P.partial + static_cast<size_t>(P.n_split) * M * nq * HD;
         const size_t row = (static_cast<size_t>(split) * M + t) * nq + kvh * G + r % G;
         ml[2 * row] = -INFINITY;
         ml[2 * row + 1] = 0.f;
       }
+      if (P.merge) merge_tail(true);
     }
   } else if (warp == 0) {
     // ------------------------------------------------------------------ TMA producer
@@ -600,6 +689,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
       }
     }
+    if (P.merge) merge_tail(all_ok);
   }
 
   tc_fence_before();
@@ -612,13 +702,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   if (threadIdx.x == 0 && *abort_flag && P.status != nullptr) atomicCAS(P.status, 0, PF_ERR_DEVICE_TIMEOUT);
 }
 
-// Merges the n_split partial results of each (token, head) row: with m* the largest of the
-// parts' running maxima, O = sum_s 2^(m_s - m*) O_s / sum_s 2^(m_s - m*) l_s (the parts keep
-// O_s and l_s relative to their own m_s, in the exp2 domain). Parts that saw no key of the
-// row (m_s = -inf) wrote no O and are skipped. One warp per row: lane s reads part s's (m, l) (and s + 32), the
-// warp reduces m* and the weighted sum of l, then each lane accumulates its HD / 32 columns
-// over the parts with the weights broadcast from their lanes, loads issued eight parts at a
-// time.
+// The merge of split-KV parts as its own kernel (chunks of more than 2 tokens): one warp per
+// (token, head) row.
 template <int HD>
 __global__ void __launch_bounds__(256) attn_combine_kernel(const float* __restrict__ part, int rows,
                                                            int n_split, __half* __restrict__ out) {
@@ -626,55 +711,8 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(const float* __restri
   griddep_launch_dependents();
   griddep_wait();
   const int row = blockIdx.x * 8 + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
   if (row >= rows) return;
-  constexpr int PER = HD / 32;
-  const float* ml = part + static_cast<size_t>(n_split) * rows * HD;
-  float m0 = -INFINITY, l0 = 0.f, m1 = -INFINITY, l1 = 0.f;  // parts lane and lane + 32
-  if (lane < n_split) {
-    const size_t sr = static_cast<size_t>(lane) * rows + row;
-    m0 = ml[2 * sr];
-    l0 = ml[2 * sr + 1];
-  }
-  if (lane + 32 < n_split) {
-    const size_t sr = static_cast<size_t>(lane + 32) * rows + row;
-    m1 = ml[2 * sr];
-    l1 = ml[2 * sr + 1];
-  }
-  float mstar = fmaxf(m0, m1);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) mstar = fmaxf(mstar, __shfl_xor_sync(0xffffffffu, mstar, o));
-  const float w0 = m0 == -INFINITY ? 0.f : exp2f(m0 - mstar);
-  const float w1 = m1 == -INFINITY ? 0.f : exp2f(m1 - mstar);
-  float lsum = w0 * l0 + w1 * l1;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, o);
-  float acc[PER];
-#pragma unroll
-  for (int i = 0; i < PER; ++i) acc[i] = 0.f;
-  const float* o0 = part + static_cast<size_t>(row) * HD + lane * PER;
-  const size_t stride = static_cast<size_t>(rows) * HD;  // between parts
-  for (int s0 = 0; s0 < n_split; s0 += 8) {
-    float x[8][PER];
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const int s = s0 + u;
-#pragma unroll
-      for (int i = 0; i < PER; ++i) x[u][i] = s < n_split ? o0[s * stride + i] : 0.f;
-    }
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const int s = s0 + u;
-      const float w = __shfl_sync(0xffffffffu, s < 32 ? w0 : w1, s & 31);
-      if (w == 0.f) continue;  // a part that saw no key of the row wrote no O (warp-uniform)
-#pragma unroll
-      for (int i = 0; i < PER; ++i) acc[i] = fmaf(w, x[u][i], acc[i]);
-    }
-  }
-  const float inv = 1.f / lsum;
-  __half* dst = out + static_cast<size_t>(row) * HD + lane * PER;
-#pragma unroll
-  for (int i = 0; i < PER; i += 2) *reinterpret_cast<__half2*>(dst + i) = __floats2half2_rn(acc[i] * inv, acc[i + 1] * inv);
+  merge_row<HD>(part, rows, n_split, row, threadIdx.x & 31, out);
 }
 
 template <int HD, int BF16>
@@ -722,17 +760,20 @@ cudaError_t launch_tc(const AttnArgs& a, cudaStream_t st) {
   p.start_host = a.start_host;
   p.scale_log2 = 1.4426950408889634f / sqrtf(static_cast<float>(HD));
   p.n_split = n_split;
+  p.merge = n_split > 1 && a.M <= MERGE_M_MAX && a.M * G <= SM_THREADS / 32;
   p.out = reinterpret_cast<__half*>(a.out);
-  p.partial = a.partial;
+  // the buffer: the arrival counters, then the partial O sums and (max, sum) per row
+  p.counters = reinterpret_cast<int*>(a.partial);
+  p.partial = a.partial ? a.partial + attention_counter_bytes(c) / sizeof(float) : nullptr;
   p.status = a.status;
   p.blocks = a.blocks;
   dim3 grid((a.M + BT - 1) / BT, c.n_kv_heads, n_split);
   cudaError_t e = launch_pdl(attn_tc_kernel<HD, BF16>, grid, dim3(THREADS), ASmem<HD>::BYTES, st, tq, tk,
                              tv, tkc, tvc, to, p);
-  if (e != cudaSuccess || n_split == 1) return e;
+  if (e != cudaSuccess || n_split == 1 || p.merge) return e;
   const int rows_out = a.M * c.n_q_heads;
   return launch_pdl(attn_combine_kernel<HD>, dim3((rows_out + 7) / 8), dim3(256), 0, st,
-                    static_cast<const float*>(a.partial), rows_out, n_split,
+                    static_cast<const float*>(p.partial), rows_out, n_split,
                     reinterpret_cast<__half*>(a.out));
 }
 
@@ -758,9 +799,14 @@ int attention_splits(const pf_config& c, int M, int sms) {
   return std::max(1, std::min(MAX_SPLIT, sms / ctas));
 }
 
+size_t attention_counter_bytes(const pf_config& c) {
+  return (static_cast<size_t>(c.n_kv_heads) * sizeof(int) + 15) / 16 * 16;
+}
+
 size_t attention_partial_bytes(const pf_config& c, int M, int n_split) {
   if (n_split <= 1) return 0;
-  return static_cast<size_t>(n_split) * M * c.n_q_heads * (c.head_dim + 2) * sizeof(float);
+  // the arrival counters, then the partial O sums and (max, sum) per row
+  return attention_counter_bytes(c) + static_cast<size_t>(n_split) * M * c.n_q_heads * (c.head_dim + 2) * sizeof(float);
 }
 
 size_t attention_partial_bytes_max(const pf_config& c, int max_sms) {

@@ -699,6 +699,8 @@ pf_status pf_session_create(const pf_model* model, void* k, void* v, void* ws, s
   cudaError_t e = cudaMemcpyAsync(s->ws + L.rope, rope.data(), rope.size() * 4, cudaMemcpyHostToDevice, st);
   if (e == cudaSuccess) e = cudaMemsetAsync(s->ws + L.status, 0, STATUS_WORDS * 4, st);
   if (e == cudaSuccess) e = cudaMemsetAsync(s->ws + L.gemm, 0, L.gemm_bytes, st);  // tile counters
+  if (e == cudaSuccess && L.attn_part_bytes)  // split-KV arrival counters
+    e = cudaMemsetAsync(s->ws + L.attn_part, 0, attention_counter_bytes(c), st);
   if (c.kv_block_pool > 0) {  // every position block unassigned (-1)
     s->blocks.assign(block_table_entries(c), -1);
     if (e == cudaSuccess) e = cudaMemsetAsync(s->ws + L.blocks, 0xff, s->blocks.size() * sizeof(int), st);
@@ -1179,6 +1181,9 @@ static pf_status attention_op(const pf_config* cfg, const void* q, const void* k
   a.out = out;
   a.n_split = n_split < 1 ? 1 : n_split;
   a.partial = static_cast<float*>(scratch);
+  if (n_split > 1)  // the caller's scratch: its arrival counters start at zero
+    PF_CUDA(cudaMemsetAsync(scratch, 0, attention_counter_bytes(*cfg), static_cast<cudaStream_t>(stream)),
+            "attention counters");
   PF_CUDA(launch_attention(a, static_cast<cudaStream_t>(stream)), "attention");
   return PF_OK;
 }

@@ -146,6 +146,10 @@ int attention_splits(const pf_config& c, int M, int sms);
 size_t attention_partial_bytes(const pf_config& c, int M, int n_split);
 // the largest partial buffer any M <= max_chunk needs on a GPU of at most max_sms SMs
 size_t attention_partial_bytes_max(const pf_config& c, int max_sms);
+// the arrival counters at the start of the partial buffer (one int per kv head, used when a
+// split chunk of at most 2 tokens merges its parts in the kernel); they must be zero before
+// the first launch, and every launch that completes leaves them zero
+size_t attention_counter_bytes(const pf_config& c);
 // Ring cache: stores the chunk's K/V rows (chunk buffers) into the ring slots of `layer`
 // that the chunk's positions keep (sinks, and the last R - S positions).
 cudaError_t launch_ring_store(const pf_config& c, const void* k_chunk, const void* v_chunk,

@@ -184,7 +184,8 @@ def test_paged_config_check_and_sizes(lib):
 def test_attention_scratch_bytes(lib):
     s = synth.QWEN3_8B_LAYER
     c = pf.make_config(s, 512)
-    assert lib.pf_attention_scratch_bytes(ctypes.byref(c), 16, 9) == 9 * 16 * 32 * (128 + 2) * 4
+    # 8 kv heads' arrival counters (32 B), then the partial O sums and (max, sum) per row
+    assert lib.pf_attention_scratch_bytes(ctypes.byref(c), 16, 9) == 32 + 9 * 16 * 32 * (128 + 2) * 4
     assert lib.pf_attention_scratch_bytes(ctypes.byref(c), 16, 1) == 0
     assert lib.pf_attention_scratch_bytes(ctypes.byref(c), 16, 65) == 0
     assert lib.pf_attention_scratch_bytes(ctypes.byref(c), 0, 2) == 0
