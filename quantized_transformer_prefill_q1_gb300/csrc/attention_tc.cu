@@ -38,6 +38,7 @@
 #include <cuda_fp16.h>
 
 #include <algorithm>
+#include <type_traits>
 
 #include "ptx.cuh"
 
@@ -221,13 +222,24 @@ __device__ __forceinline__ uint32_t pack_pair(float a, float b) {
 // saw no key of the row (m_s = -inf) wrote no O and are skipped. One warp per row: lane s
 // reads part s's (m, l) (and s + 32), the warp reduces m* and the weighted sum of l, then each
 // lane accumulates its HD / 32 columns over the parts with the weights broadcast from their
-// lanes, loads issued eight parts at a time (through L2: other CTAs of the same kernel may
-// have written them).
+// lanes, eight parts' loads in flight while the previous eight are added (through L2: other
+// CTAs of the same kernel may have written them).
 template <int HD>
 __device__ __forceinline__ void merge_row(const float* part, int rows, int n_split, int row, int lane,
                                           __half* out) {
   constexpr int PER = HD / 32;
+  // each lane's PER columns as one vector load per part (float4 for HD 128, float2 for 64)
+  using V = typename std::conditional<PER == 4, float4, float2>::type;
+  static_assert(PER == 4 || PER == 2, "head_dim 64 or 128");
   const float* ml = part + static_cast<size_t>(n_split) * rows * HD;
+  const V* o0 = reinterpret_cast<const V*>(part + static_cast<size_t>(row) * HD + lane * PER);
+  const size_t stride = static_cast<size_t>(rows) * HD / PER;  // between parts, in vectors
+  // parts s0 .. s0 + 7 of this lane's columns (zero past n_split)
+  auto load8 = [&](int s0, V (&x)[8]) {
+#pragma unroll
+    for (int u = 0; u < 8; ++u) x[u] = s0 + u < n_split ? __ldcg(o0 + (s0 + u) * stride) : V{};
+  };
+  // the parts' (m, l) and the first eight parts' rows are requested together: one round trip
   float m0 = -INFINITY, l0 = 0.f, m1 = -INFINITY, l1 = 0.f;  // parts lane and lane + 32
   if (lane < n_split) {
     const size_t sr = static_cast<size_t>(lane) * rows + row;
@@ -239,6 +251,8 @@ __device__ __forceinline__ void merge_row(const float* part, int rows, int n_spl
     m1 = __ldcg(ml + 2 * sr);
     l1 = __ldcg(ml + 2 * sr + 1);
   }
+  V xa[8], xb[8];
+  load8(0, xa);
   float mstar = fmaxf(m0, m1);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) mstar = fmaxf(mstar, __shfl_xor_sync(0xffffffffu, mstar, o));
@@ -250,24 +264,23 @@ __device__ __forceinline__ void merge_row(const float* part, int rows, int n_spl
   float acc[PER];
 #pragma unroll
   for (int i = 0; i < PER; ++i) acc[i] = 0.f;
-  const float* o0 = part + static_cast<size_t>(row) * HD + lane * PER;
-  const size_t stride = static_cast<size_t>(rows) * HD;  // between parts
-  for (int s0 = 0; s0 < n_split; s0 += 8) {
-    float x[8][PER];
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const int s = s0 + u;
-#pragma unroll
-      for (int i = 0; i < PER; ++i) x[u][i] = s < n_split ? __ldcg(o0 + s * stride + i) : 0.f;
-    }
+  auto add8 = [&](int s0, const V (&x)[8]) {
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
       const int s = s0 + u;
       const float w = __shfl_sync(0xffffffffu, s < 32 ? w0 : w1, s & 31);
       if (w == 0.f) continue;  // a part that saw no key of the row wrote no O (warp-uniform)
+      const float* xv = reinterpret_cast<const float*>(&x[u]);
 #pragma unroll
-      for (int i = 0; i < PER; ++i) acc[i] = fmaf(w, x[u][i], acc[i]);
+      for (int i = 0; i < PER; ++i) acc[i] = fmaf(w, xv[i], acc[i]);
     }
+  };
+  // two batches of eight parts in flight: the next batch's loads go out before this one adds
+  for (int s0 = 0; s0 < n_split; s0 += 16) {
+    if (s0 + 8 < n_split) load8(s0 + 8, xb);
+    add8(s0, xa);
+    if (s0 + 16 < n_split) load8(s0 + 16, xa);
+    if (s0 + 8 < n_split) add8(s0 + 8, xb);
   }
   const float inv = 1.f / lsum;
   __half* dst = out + static_cast<size_t>(row) * HD + lane * PER;
