@@ -20,8 +20,9 @@
 // (lane / 4, lane % 4) reads, per 64-wide half of a group, 8 bytes (INT4: codes
 // 16c .. 16c+15 of the half) or one sign word (Q1: elements 32 (c / 2) .. +31) of MMA rows g
 // and g + 8, and the 16 activations 16c .. 16c+15 of the half for token g. Per group the
-// accumulator is scaled by the row's scale (INT4: the codes enter as the f16 value q - z,
-// rounded like the tcgen05 path's dequantiser rounds it) and added to the row's total in f32.
+// accumulator is scaled by the row's scale (INT4: the codes enter as f16(q s - f16(z s)), whose
+// error against (q - z) s is of the order of the tcgen05 path's f16(f16(q - z) s): half an
+// ulp of z s against half an ulp of q - z, times s) and added to the row's total in f32.
 // Residual form: each range's share is added into out (an f32 atomic add where another warp
 // shares the tile); store form: out is zeroed first and added to the same way.
 #include <cuda_fp16.h>
@@ -128,7 +129,7 @@ __device__ __forceinline__ void issue_i4(uint32_t st, const uint8_t* ch, int roA
 // A fragment of k-step ks of half h from the stage at `st` (lane g = gq, c):
 // Q1: +-1.0 for pairs i0, i0 + 1 of sign word c / 2 (pair i keeps its negative flags at bits
 //     15 - i / 31 - i);
-// INT4: pairs 2 (ks % 2), 2 (ks % 2) + 1 of nibble word 2c + ks / 2, as the f16 values q - z
+// INT4: pairs 2 (ks % 2), 2 (ks % 2) + 1 of nibble word 2c + ks / 2, dequantised to f16
 //     ((1024 + q) and (1024 + 16 q) are exact f16 bit patterns).
 template <int WFMT>
 struct Frag;
@@ -160,7 +161,7 @@ struct Frag<PF_W_Q1_G128> {
 template <>
 struct Frag<PF_W_INT4_AFFINE_G128> {
   uint2 q[2][2];
-  __half2 z2[2], s2[2];
+  __half2 s2[2], nzs2[2];  // the rows' scale and -f16(z s), in both halves
   __device__ __forceinline__ void read(uint32_t st, int gq, int c) {
 #pragma unroll
     for (int h = 0; h < 2; ++h)
@@ -171,18 +172,20 @@ struct Frag<PF_W_INT4_AFFINE_G128> {
       const uint32_t sb = lds16(st + ST<PF_W_INT4_AFFINE_G128>::SC + i * 16 + gq * 2);
       const uint32_t zb = lds16(st + ST<PF_W_INT4_AFFINE_G128>::ZP + i * 16 + gq * 2);
       s2[i] = u2h(sb | (sb << 16));
-      z2[i] = u2h(zb | (zb << 16));
+      nzs2[i] = __hneg2(__hmul2(u2h(zb | (zb << 16)), s2[i]));
     }
   }
-  // f16(f16(q - z) * s), as the tensor-core path's dequantiser forms it
+  // f16(q s - f16(z s)): the code q comes out exact ((1024 + q) and (1024 + 16 q) are f16
+  // bit patterns), then one fused multiply-add per weight pair: two f16 operations per pair
+  // instead of the three of f16(f16(q - z) s)
   __device__ __forceinline__ void a(int h, int ks, int c, uint32_t (&f)[4]) const {
     const __half2 k1024 = u2h(0x64006400u), k16th = u2h(0x2C002C00u), km64 = u2h(0xD400D400u);
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
       uint32_t W = (ks >> 1) ? q[h][i].y : q[h][i].x;
       if (ks & 1) W >>= 8;
-      f[i] = h2u(__hmul2(__hsub2(__hsub2(u2h((W & 0x000F000Fu) | 0x64006400u), k1024), z2[i]), s2[i]));
-      f[2 + i] = h2u(__hmul2(__hsub2(__hfma2(u2h((W & 0x00F000F0u) | 0x64006400u), k16th, km64), z2[i]), s2[i]));
+      f[i] = h2u(__hfma2(__hsub2(u2h((W & 0x000F000Fu) | 0x64006400u), k1024), s2[i], nzs2[i]));
+      f[2 + i] = h2u(__hfma2(__hfma2(u2h((W & 0x00F000F0u) | 0x64006400u), k16th, km64), s2[i], nzs2[i]));
     }
   }
 };
