@@ -50,7 +50,7 @@ NCU_TRAFFIC = {"gemm_gate_up": 18454528 + 880896}
 
 
 CASES = ["gemm_gate_up", "gemm_qkv", "gemm_down", "gemm_o", "attention", "rmsnorm", "qk_rope_kv", "lm_head",
-         "int4_gate_up", "int4_qkv", "int4_o", "int4_down", "decode", "timeline"]
+         "int4_gate_up", "int4_qkv", "int4_o", "int4_down", "decode", "timeline", "int4_timeline"]
 
 
 def parse():
@@ -166,6 +166,37 @@ def run_timeline(args, pf, synth):
     print(json.dumps(out))
 
 
+def run_int4_timeline(args, pf, synth, ms):
+    """The Llama-3-8B-shaped INT4 layer over 8192 cached positions (as in `int4_layer`), one
+    chunk of each M at start 8192 with the per-CTA kernel timeline on, after a 256 MB read
+    that evicts L2. Prints one JSON line per M: each kernel class's mean share of the
+    layer's critical path per launch."""
+    import numpy as np
+    import torch
+    s = synth.LLAMA3_8B_INT4_LAYER
+    layers, _ = synth.model_inputs(s, seed=args.seed)
+    dm = pf.DeviceModel(s, layers, max_chunk=max(INT4_MS))
+    sess = pf.Session(dm)
+    kvp = synth.kv_prefill_bf16_bits(1, s.n_kv_heads, INT4_FILLED, s.head_dim, seed=args.seed)
+    sess.k[:, :, :INT4_FILLED].view(torch.int16).copy_(torch.from_numpy(kvp["k"].view(np.int16)).cuda())
+    sess.v[:, :, :INT4_FILLED].view(torch.int16).copy_(torch.from_numpy(kvp["v"].view(np.int16)).cuda())
+    del kvp
+    flush = torch.ones(64 << 20, dtype=torch.float32, device="cuda")
+    for m in ms:
+        x0 = torch.from_numpy(synth.hidden_input(m, s.hidden, seed=args.seed)).cuda()
+        x = x0.clone()
+        for _ in range(3):
+            x.copy_(x0)
+            sess.layer_forward(0, x, INT4_FILLED)
+        x.copy_(x0)
+        flush.sum()
+        torch.cuda.synchronize()
+        layer_us, launches, per = timeline_prompt(pf, torch, lambda: sess.layer_forward(0, x, INT4_FILLED))
+        crit = {lab: round(float(np.mean([d[0] for d in v])) / 1e3, 2) for lab, v in per.items()}
+        print(json.dumps({"case": "int4_timeline", "m": m, "layer_us": round(layer_us, 1),
+                          "launches": launches, "critical_path_us_per_launch": crit}), flush=True)
+
+
 # timeline layer classes -> the kernel classes of class_work
 TIMELINE_TO_CLASS = {"rmsnorm_attn": "rmsnorm", "rmsnorm_ffn": "rmsnorm", "gemm_qkv": "gemm_qkv",
                      "qk_norm_rope_kv": "qk_rope_kv", "attention": "attention", "gemm_o": "gemm_o",
@@ -243,6 +274,9 @@ def run_case(args):
             continue
         if case == "timeline":
             run_timeline(args, pf, synth)
+            continue
+        if case == "int4_timeline":
+            run_int4_timeline(args, pf, synth, ms or [1, 4, 16, 64])
             continue
         for M in (ms or [1 if case.startswith("int4") else CHUNK]):
             rng = synth.rng_for(99)
