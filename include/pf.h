@@ -345,6 +345,19 @@ pf_status pf_op_gemm(int32_t wfmt, int32_t epilogue, const uint16_t* a_f16_dev,
 pf_status pf_op_gemm_static_scratch(int32_t wfmt, int32_t epilogue, const uint16_t* a_f16_dev,
                                     const void* packed_dev, int32_t M, int32_t N, int32_t K,
                                     void* out_dev, int32_t* status_dev, void* stream);
+/* Host view of the stream-K partition the quantised GEMMs run (for tests and tools; no GPU
+ * work): n_mt x n_nt output tiles of kbt k-blocks cut into `ctas` contiguous ranges, the last
+ * late_units of them late_kb k-blocks shorter (0, 0: even ranges; the GEMM's own launches
+ * set these for the layer projections on CTA pairs). Fills begins[0 .. ctas] (k-block where
+ * each unit's range starts, begins[ctas] = the total) and, per unit, up to max_segs segments
+ * in the order the unit runs them as (tile, first k-block within the tile, k-blocks, scratch
+ * slot) in segs[unit][max_segs][4] (tile = -1 past the unit's last segment); when owners is
+ * not NULL, owners[i] = the unit whose range holds k-block w_query[i]. Returns PF_ERR_SHAPE
+ * for sizes out of range (any count < 1, ctas > the total, a unit with more than max_segs
+ * segments). */
+pf_status pf_streamk_plan_host(int32_t n_mt, int32_t n_nt, int32_t kbt, int32_t ctas, int32_t late_units,
+                               int32_t late_kb, int64_t* begins, int32_t* segs, int32_t max_segs,
+                               const int64_t* w_query, int32_t n_query, int32_t* owners);
 /* Fused per-head QK RMSNorm + RoPE + KV store ([P1] section 3 fused_qk_norm /
  * fused_qk_rope / fused_kv_store; [P2] dispatch_fused_qk_norm_rope): from qkv f32
  * [M, (nq+2nkv) hd], writes q_dev [M, nq, hd] (bf16 when kv_dtype is bf16, else f16)

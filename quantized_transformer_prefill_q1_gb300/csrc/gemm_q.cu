@@ -41,6 +41,18 @@
 #include "streamk.cuh"
 
 namespace pf {
+
+void streamk_skew(sk::Plan& p, int late_units, int late_kb) {
+  p.late0 = p.ctas;
+  p.dk = 0;
+  // (the late units are a minority of the units on the GPU the values were measured on; with
+  // fewer SMs the pattern is not known, and the plan stays even)
+  if (late_units > 0 && late_kb > 0 && 2 * late_units <= p.ctas) {
+    p.late0 = p.ctas - late_units;
+    p.dk = static_cast<int>(std::min<long long>(late_kb, std::max<long long>(0, p.total / p.ctas - 1)));
+  }
+}
+
 namespace {
 using sk::Plan;
 using sk::Range;
@@ -746,12 +758,7 @@ cudaError_t launch_t(const GemmArgs& g, const CUtensorMap& ta, const CUtensorMap
   // the tiles alone fill at least half of the units, run one whole tile per unit instead
   const int tiles = p.n_mt * p.n_nt;
   if (EPI != EPI_RESID_ADD && tiles < p.ctas && 2 * tiles >= p.ctas) p.ctas = tiles;
-  p.late0 = p.ctas;
-  p.dk = 0;
-  if (PAIR && g.late_units > 0 && g.late_kb > 0) {
-    p.late0 = std::max(0, p.ctas - g.late_units);
-    p.dk = static_cast<int>(std::min<long long>(g.late_kb, std::max<long long>(0, p.total / p.ctas - 1)));
-  }
+  streamk_skew(p, PAIR ? g.late_units : 0, g.late_kb);
   float* scratch = reinterpret_cast<float*>(g.scratch);
   int* counters =
       scratch ? reinterpret_cast<int*>(scratch + static_cast<size_t>(2) * g.max_ctas * SLOT_FLOATS) : nullptr;

@@ -17,6 +17,7 @@
 #include <vector>
 
 #include "pf_internal.h"
+#include "streamk.cuh"
 
 namespace pf {
 namespace {
@@ -1231,3 +1232,41 @@ pf_status pf_op_argmax(const float* x, int32_t rows, int32_t n, int64_t ld, int3
 }
 
 }  // extern "C"
+
+pf_status pf_streamk_plan_host(int32_t n_mt, int32_t n_nt, int32_t kbt, int32_t ctas, int32_t late_units,
+                               int32_t late_kb, int64_t* begins, int32_t* segs, int32_t max_segs,
+                               const int64_t* w_query, int32_t n_query, int32_t* owners) {
+  using namespace pf;
+  if (!begins || !segs) return fail(PF_ERR_INVALID_ARG, "NULL pointer");
+  if (n_mt < 1 || n_nt < 1 || kbt < 1 || ctas < 1 || max_segs < 1 || late_units < 0 || late_kb < 0)
+    return fail(PF_ERR_SHAPE, "plan sizes");
+  sk::Plan p{};
+  p.n_mt = n_mt;
+  p.n_nt = n_nt;
+  p.kbt = kbt;
+  p.total = static_cast<long long>(n_mt) * n_nt * kbt;
+  if (ctas > p.total) return fail(PF_ERR_SHAPE, "ctas %d > %lld k-blocks", ctas, p.total);
+  p.ctas = ctas;
+  streamk_skew(p, late_units, late_kb);
+  for (int c = 0; c <= ctas; ++c) begins[c] = p.begin(c);
+  for (int c = 0; c < ctas; ++c) {
+    const sk::Range rg(p, c);
+    if (rg.n > max_segs) return fail(PF_ERR_SHAPE, "unit %d has %d segments", c, rg.n);
+    for (int k = 0; k < max_segs; ++k) {
+      int32_t* o = segs + (static_cast<size_t>(c) * max_segs + k) * 4;
+      if (k >= rg.n) {
+        o[0] = -1;
+        o[1] = o[2] = o[3] = 0;
+        continue;
+      }
+      const sk::Segment sg = rg.at(p, k);
+      o[0] = sg.tile;
+      o[1] = sg.kb0;
+      o[2] = sg.nkb;
+      o[3] = sg.whole ? -1 : p.slot(c, sg.tile);
+    }
+  }
+  if (owners && w_query)
+    for (int i = 0; i < n_query; ++i) owners[i] = p.owner(w_query[i]);
+  return PF_OK;
+}

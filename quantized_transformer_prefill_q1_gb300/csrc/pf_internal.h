@@ -82,6 +82,12 @@ struct GemmArgs {
   int late_kb;
 };
 cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t stream);
+namespace sk {
+struct Plan;
+}
+// Applies a stream-K skew (GemmArgs::late_units / late_kb) to a plan whose tiles and units
+// are set: units [ctas - late_units, ctas) take up to late_kb k-blocks fewer each.
+void streamk_skew(sk::Plan& p, int late_units, int late_kb);
 // Whether GemmArgs::side_zero is available at this M (the persistent tcgen05 GEMM).
 bool gemm_side_zero_supported(int wfmt, int M);
 // M <= SMALL_M_MAX: the weight rows are the MMA's M side (gemm_small.cu); launch_gemm routes

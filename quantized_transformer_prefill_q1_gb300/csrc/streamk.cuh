@@ -16,12 +16,12 @@ struct Plan {
   long long total;
   int ctas;
   int late0, dk;  // dk <= total / ctas - 1 keeps every range non-empty
-  __device__ __forceinline__ long long begin(int c) const {
+  __host__ __device__ __forceinline__ long long begin(int c) const {
     const long long vt = total + static_cast<long long>(ctas - late0) * dk;
     return vt * c / ctas - static_cast<long long>(dk) * (c > late0 ? c - late0 : 0);
   }
   // unit whose range holds k-block w (the unskewed guess is off by a few units at most)
-  __device__ __forceinline__ int owner(long long w) const {
+  __host__ __device__ __forceinline__ int owner(long long w) const {
     int c = static_cast<int>(((w + 1) * ctas - 1) / total);
     while (c > 0 && begin(c) > w) --c;
     while (c + 1 < ctas && begin(c + 1) <= w) ++c;
@@ -29,7 +29,7 @@ struct Plan {
   }
   // scratch slot (0 or 1) of contributor c's partial for `tile`: 0 if c's range begins
   // inside the tile, 1 if it begins at or before the tile's start
-  __device__ __forceinline__ int slot(int c, int tile) const {
+  __host__ __device__ __forceinline__ int slot(int c, int tile) const {
     return begin(c) > static_cast<long long>(tile) * kbt ? 0 : 1;
   }
 };
@@ -46,7 +46,7 @@ struct Range {
   long long b, e;
   int t0, n, first_part, last_part;
   bool swap;  // the partial last segment runs first
-  __device__ __forceinline__ Range(const Plan& p, int c) {
+  __host__ __device__ __forceinline__ Range(const Plan& p, int c) {
     b = p.begin(c);
     e = p.begin(c + 1);
     t0 = static_cast<int>(b / p.kbt);
@@ -57,7 +57,7 @@ struct Range {
     last_part = (n > 1 && e != static_cast<long long>(t1 + 1) * p.kbt) ? 1 : 0;
     swap = first_part && last_part && e - static_cast<long long>(t1) * p.kbt < s0_end - b;
   }
-  __device__ __forceinline__ Segment at(const Plan& p, int k) const {
+  __host__ __device__ __forceinline__ Segment at(const Plan& p, int k) const {
     int i = k < first_part ? 0 : (k < first_part + last_part ? n - 1 : k - last_part);
     if (swap && k < 2) i = k == 0 ? n - 1 : 0;
     Segment s;

@@ -99,6 +99,7 @@ _SIGS = {
     "pf_op_gemm": ([_I32, _I32, _VP, _VP, _I32, _I32, _I32, _VP, _I32, _VP, _SZ, _VP, _VP], _I32),
     "pf_gemm_scratch_bytes": ([_I32, _I32, _I32], _SZ),
     "pf_op_gemm_static_scratch": ([_I32, _I32, _VP, _VP, _I32, _I32, _I32, _VP, _VP, _VP], _I32),
+    "pf_streamk_plan_host": ([_I32, _I32, _I32, _I32, _I32, _I32, _VP, _VP, _I32, _VP, _I32, _VP], _I32),
     "pf_op_qk_norm_rope_kv": ([ctypes.POINTER(pf_config), _VP, _VP, _VP, _VP, _I32, _I32, _I32,
                                _VP, _VP, _VP, _VP], _I32),
     "pf_op_attention": ([ctypes.POINTER(pf_config), _VP, _VP, _VP, _I32, _I32, _I32, _VP, _VP], _I32),
@@ -235,6 +236,19 @@ def pf_op_gemm_static_scratch(wfmt, epilogue, a, packed, m, n, k, out, status=No
     """pf_op_gemm with the library's fixed scratch: for callers that may not allocate."""
     check(lib().pf_op_gemm_static_scratch(wfmt, epilogue, _ptr(a), _ptr(packed), m, n, k, _ptr(out),
                                           _ptr(status), _stream(stream)))
+
+
+def pf_streamk_plan_host(n_mt, n_nt, kbt, ctas, late_units=0, late_kb=0, max_segs=8, w_query=None):
+    """The GEMMs' stream-K partition on the host: (begins [ctas + 1], segments [ctas, max_segs, 4]
+    as (tile, kb0, nkb, slot; -1 slot for a whole tile; tile -1 past the last), owners of
+    w_query or None)."""
+    begins = np.zeros(ctas + 1, np.int64)
+    segs = np.zeros((ctas, max_segs, 4), np.int32)
+    wq = None if w_query is None else np.ascontiguousarray(w_query, np.int64)
+    owners = None if wq is None else np.zeros(len(wq), np.int32)
+    check(lib().pf_streamk_plan_host(n_mt, n_nt, kbt, ctas, late_units, late_kb, _ptr(begins), _ptr(segs),
+                                     max_segs, _ptr(wq), 0 if wq is None else len(wq), _ptr(owners)))
+    return begins, segs, owners
 
 
 def pf_op_qk_norm_rope_kv(cfg, qkv, qn, kn, rope, layer, start, m, q, kc, vc, stream=None):
