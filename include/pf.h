@@ -123,7 +123,9 @@ typedef struct pf_session pf_session; /* opaque */
 /* ------------------------------------------------------------------ misc */
 const char* pf_last_error(void);      /* thread-local, never NULL */
 const char* pf_status_name(int status);
-int32_t pf_abi_version(void);         /* bumps on any ABI change (2: ring fields, 3: kv_block_pool) */
+int32_t pf_abi_version(void);         /* bumps on any ABI change (2: ring fields, 3: kv_block_pool,
+                                        4: split-KV counters in the attention scratch,
+                                        pf_streamk_plan_host) */
 
 /* ------------------------------------------------------------------ packing
  * Canonical host formats (the pages name "Q1 block bytes" and an "AoS -> SoA"

@@ -522,7 +522,7 @@ const char* pf_status_name(int st) {
   }
 }
 
-int32_t pf_abi_version(void) { return 3; }
+int32_t pf_abi_version(void) { return 4; }
 
 size_t pf_packed_bytes(int32_t wfmt, int64_t N, int64_t K) {
   if ((wfmt != PF_W_Q1_G128 && wfmt != PF_W_INT4_AFFINE_G128) || N <= 0 || K <= 0 || K % GROUP)

@@ -160,7 +160,7 @@ def test_ring_config_check_and_sizes(lib):
         assert lib.pf_config_check(ctypes.byref(bad)) == want, (R, S)
     f32 = pf.make_config(dataclasses.replace(s, kv_dtype="f32"), 512, ring_capacity=64, sink_count=0)
     assert lib.pf_config_check(ctypes.byref(f32)) == 8  # PF_ERR_UNSUPPORTED
-    assert lib.pf_abi_version() == 3
+    assert lib.pf_abi_version() == 4
 
 
 def test_paged_config_check_and_sizes(lib):
