@@ -639,16 +639,22 @@ __global__ void __launch_bounds__(512) lm_head_q1_kernel(const float* __restrict
   const int rr = threadIdx.x & (TILE_N - 1);
   const int part = threadIdx.x >> 8;
   const int g0 = part * (G / 2), g1 = part ? G : G / 2;
+  // one group's packed weights of this thread's row: two sign-word pairs and the scale
+  struct GroupW {
+    uint2 h0, h1;
+    unsigned short s;
+  };
   for (int tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
     const uint8_t* tw = W + static_cast<size_t>(tile) * G * Q1_CHUNK_BYTES;
-    float acc = 0.f;
-#pragma unroll 4
-    for (int g = g0; g < g1; ++g) {
+    auto load = [&](int g, GroupW& d) {
       const uint8_t* ch = tw + static_cast<size_t>(g) * Q1_CHUNK_BYTES;
-      const uint2 h0 = __ldg(reinterpret_cast<const uint2*>(ch + rr * 8));
-      const uint2 h1 = __ldg(reinterpret_cast<const uint2*>(ch + Q1_HALF_BYTES + rr * 8));
-      const float s = __half2float(__ushort_as_half(__ldg(reinterpret_cast<const unsigned short*>(ch + Q1_SCALE_OFF) + rr)));
-      const uint32_t words[4] = {h0.x, h0.y, h1.x, h1.y};
+      d.h0 = __ldg(reinterpret_cast<const uint2*>(ch + rr * 8));
+      d.h1 = __ldg(reinterpret_cast<const uint2*>(ch + Q1_HALF_BYTES + rr * 8));
+      d.s = __ldg(reinterpret_cast<const unsigned short*>(ch + Q1_SCALE_OFF) + rr);
+    };
+    float acc = 0.f;
+    auto add = [&](int g, const GroupW& d) {
+      const uint32_t words[4] = {d.h0.x, d.h0.y, d.h1.x, d.h1.y};
       float p[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int w = 0; w < 4; ++w) {
@@ -665,7 +671,22 @@ __global__ void __launch_bounds__(512) lm_head_q1_kernel(const float* __restrict
         p[2] += q1_lut_ld<6>(Z, base);
         p[3] += q1_lut_ld<7>(Z, base);
       }
-      acc = fmaf(s, (p[0] + p[1]) + (p[2] + p[3]), acc);
+      acc = fmaf(__half2float(__ushort_as_half(d.s)), (p[0] + p[1]) + (p[2] + p[3]), acc);
+    };
+    // four groups in flight while the previous four are added
+    GroupW cur[4], nxt[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      if (g0 + i < g1) load(g0 + i, cur[i]);
+    for (int g = g0; g < g1; g += 4) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        if (g + 4 + i < g1) load(g + 4 + i, nxt[i]);
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        if (g + i < g1) add(g + i, cur[i]);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) cur[i] = nxt[i];
     }
     if (part) half_sum[rr] = acc;
     __syncthreads();
