@@ -322,8 +322,8 @@ pf_status pf_op_dequant(int32_t wfmt, const void* packed_dev, int64_t N, int64_t
  * epilogue): its trailing per-tile counters must be zero before the first call, and each
  * call that completes leaves them zero; after PF_ERR_DEVICE_TIMEOUT zero them again.
  * Calls sharing one scratch must not overlap in time (same stream, or ordered).
- * The kernel depends on M: M > 64 the persistent tcgen05 GEMM described above; 8 < M <= 64
- * the same partition with the weight rows as the MMA's M side; M <= 8 a warp-level MMA
+ * The kernel depends on M: M > 64 the persistent tcgen05 GEMM described above; 16 < M <= 64
+ * the same partition with the weight rows as the MMA's M side; M <= 16 a warp-level MMA
  * GEMV that ignores max_ctas and the scratch (residual and store forms add with f32
  * atomics, the store form after zeroing out). The results agree to the GEMM tolerances:
  * all three use f16 operands with f32 accumulation. */

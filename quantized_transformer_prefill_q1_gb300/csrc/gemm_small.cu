@@ -1,10 +1,10 @@
-// gemm_small.cu — the quantised GEMM for chunks of a few tokens (M <= 64): the weight side
+// gemm_small.cu — the quantised GEMM for chunks of a few tokens (16 < M <= 64): the weight side
 // of a layer's projections (oxibonsai-kernels metal_prefill.rs `encode_layer_prefill`
 // sections 2, 4, 6 and 7) when the chunk is so short that streaming the packed weights from
 // HBM is the whole cost (the GEMV end of the small-M crossover).
 //
 // The MMA is turned around: weight rows are its M side (two MMAs of 128 rows cover one
-// 256-row packed tile) and the chunk's tokens (padded to NT = 16, 32 or 64) its N side,
+// 256-row packed tile) and the chunk's tokens (padded to NT = 32 or 64) its N side,
 // out^T[n, m] = sum_k w[n, k] a[m, k]. The dequantised f16 weights go from registers
 // straight into tensor memory (tcgen05.st) as the A operand, so shared memory carries only
 // the packed chunks and the small activation tiles. One stage is one 128-wide group: the
@@ -427,10 +427,8 @@ cudaError_t attr_fmt() {
 
 cudaError_t prepare_gemm_small_kernels() {
   cudaError_t e = cudaSuccess, r;
-  if ((r = attr_fmt<PF_W_Q1_G128, 16>()) != cudaSuccess) e = r;
   if ((r = attr_fmt<PF_W_Q1_G128, 32>()) != cudaSuccess) e = r;
   if ((r = attr_fmt<PF_W_Q1_G128, 64>()) != cudaSuccess) e = r;
-  if ((r = attr_fmt<PF_W_INT4_AFFINE_G128, 16>()) != cudaSuccess) e = r;
   if ((r = attr_fmt<PF_W_INT4_AFFINE_G128, 32>()) != cudaSuccess) e = r;
   if ((r = attr_fmt<PF_W_INT4_AFFINE_G128, 64>()) != cudaSuccess) e = r;
   return e;
@@ -449,13 +447,13 @@ cudaError_t launch_gemm_small(const GemmArgs& g, cudaStream_t stream) {
     r.epilogue = EPI_RESID_ADD;
     return launch_gemm_small(r, stream);
   }
-  const int nt = g.M <= 16 ? 16 : (g.M <= 32 ? 32 : 64);
+  // chunks of at most 16 tokens go to the GEMV (launch_gemm routes them there)
+  if (g.M <= GEMV_M_MAX_Q1 && g.M <= GEMV_M_MAX_I4) return cudaErrorInvalidValue;
+  const int nt = g.M <= 32 ? 32 : 64;
   if (g.wfmt == PF_W_Q1_G128) {
-    if (nt == 16) return launch_fmt<PF_W_Q1_G128, 16>(g, sms, stream);
     if (nt == 32) return launch_fmt<PF_W_Q1_G128, 32>(g, sms, stream);
     return launch_fmt<PF_W_Q1_G128, 64>(g, sms, stream);
   }
-  if (nt == 16) return launch_fmt<PF_W_INT4_AFFINE_G128, 16>(g, sms, stream);
   if (nt == 32) return launch_fmt<PF_W_INT4_AFFINE_G128, 32>(g, sms, stream);
   return launch_fmt<PF_W_INT4_AFFINE_G128, 64>(g, sms, stream);
 }

@@ -1,13 +1,16 @@
-// gemv.cu — the quantised projections for chunks of at most 8 tokens: the GEMV end of the
+// gemv.cu — the quantised projections for chunks of at most 16 tokens: the GEMV end of the
 // small-M crossover (oxibonsai-kernels metal_full_layer.rs `encode_layer_into`, the decode
-// layer, whose projections are one pass over the weights per token). At M <= 8 streaming the
-// packed weights from HBM is the whole cost; the tcgen05 path reads its A operand (the
-// weights) from tensor memory at a fixed ~22 weights per clock per SM whatever the token
-// count, so here the weights go from shared memory through registers into warp-level MMAs.
+// layer, whose projections are one pass over the weights per token). At M <= 16 streaming
+// the packed weights from HBM and dequantising them is the whole cost; the tcgen05 path reads
+// its A operand (the weights) from tensor memory at a fixed ~22 weights per clock per SM
+// whatever the token count, so here the weights go from shared memory through registers into
+// warp-level MMAs.
 //
 // A warp owns 16 weight rows (for SwiGLU 8 gate rows and their 8 up rows) and computes
-// out^T[16 rows, 8 tokens] with mma.sync m16n8k16 (f16 operands, f32 accumulation): the
-// dequantised codes are the A fragment, the activations (tokens >= M zero) the B fragment.
+// out^T[16 rows, 8 tokens] with mma.sync m16n8k16 (f16 operands, f32 accumulation) per block
+// of 8 tokens (one block for M <= 8, two for M <= 16, each dequantised A fragment feeding
+// both): the dequantised codes are the A fragment, the activations (tokens >= M zero) the B
+// fragment.
 // The (16-row tile, group) units are shared out in equal contiguous ranges, one per warp,
 // and warps never wait for one another; only SwiGLU pairs two warps of a CTA on one tile
 // (even and odd groups), which meet in shared memory to form silu(gate) * up. A warp streams its rows' slice of each packed chunk (16 rows x 128 weights: 1024 B of
@@ -19,7 +22,7 @@
 // taken from the packed word it reads (k permuted identically in A and B): lane (g, c) =
 // (lane / 4, lane % 4) reads, per 64-wide half of a group, 8 bytes (INT4: codes
 // 16c .. 16c+15 of the half) or one sign word (Q1: elements 32 (c / 2) .. +31) of MMA rows g
-// and g + 8, and the 16 activations 16c .. 16c+15 of the half for token g. Per group the
+// and g + 8, and the 16 activations 16c .. 16c+15 of the half for token g (+ 8 b). Per group the
 // accumulator is scaled by the row's scale (INT4: the codes enter as f16(q s - f16(z s)), whose
 // error against (q - z) s is of the order of the tcgen05 path's f16(f16(q - z) s): half an
 // ulp of z s against half an ulp of q - z, times s) and added to the row's total in f32.
@@ -213,24 +216,25 @@ __device__ __forceinline__ void tile_rows(int t, int& tile256, int& roA, int& ro
   }
 }
 
-template <int WFMT, int EPI, int GS>
+template <int WFMT, int EPI, int GS, int NB>
 __global__ void __launch_bounds__(THREADS_V)
     gemv_kernel(const __half* a, const uint8_t* __restrict__ wpk, int M, int N, int K,
                 void* __restrict__ out, long long units, int warps) {
   PF_TIMELINE(TL_GEMV + EPI);
+  // NB blocks of 8 token columns (M <= 8 NB): each dequantised A fragment feeds NB MMAs
   using S = ST<WFMT>;
   constexpr int DS = S::DS / GS;     // stages in flight per warp
   constexpr int SB = GS * S::BYTES;  // a stage: GS consecutive groups of one 16-row tile
   constexpr size_t P = WFMT == PF_W_Q1_G128 ? Q1_CHUNK_BYTES : I4_CHUNK_BYTES;
   static_assert(DS >= 2, "ring depth");
   extern __shared__ __align__(16) uint8_t gv_smem[];
-  __shared__ float part[WARPS_V / 2][32][4];  // SwiGLU: the odd-stage half of a tile's sums
+  __shared__ float part[WARPS_V / 2][32][4 * NB];  // SwiGLU: the odd-stage half of a tile's sums
   griddep_launch_dependents();
   const int G = K / GROUP;
   const int GG = G / GS;  // stages per tile
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gq = lane >> 2, c = lane & 3;
-  const bool tok = gq < M;  // this lane's B column (token gq) exists
+
   const int gw = blockIdx.x * WARPS_V + warp;
   // This warp's units (tile, stage) as a cursor (t, g) stepping by `gs`: SwiGLU tiles are
   // split between two warps of the CTA by stage parity (warp 2i + p takes stages p, p + 2, ...
@@ -278,17 +282,27 @@ __global__ void __launch_bounds__(THREADS_V)
   griddep_wait();  // the activations and the output do
 
   int tc = t0, gc = g0, sc = 0;  // compute cursor
-  const __half* xbase = a + static_cast<size_t>(tok ? gq : 0) * K + 16 * c;
-  uint4 xn[4] = {};  // the next group's 16 activations of each half (token gq)
-  auto load_x = [&](int g, uint4 (&x)[4]) {
+  // this lane's B columns: tokens gq + 8 b of the NB blocks (zero past M)
+  bool tok[NB];
+  const __half* xbase[NB];
 #pragma unroll
-    for (int e = 0; e < 4; ++e)
-      x[e] = tok ? ld_act16(xbase + g * GROUP + 64 * (e >> 1) + 8 * (e & 1)) : make_uint4(0u, 0u, 0u, 0u);
+  for (int b = 0; b < NB; ++b) {
+    tok[b] = gq + 8 * b < M;
+    xbase[b] = a + static_cast<size_t>(tok[b] ? gq + 8 * b : 0) * K + 16 * c;
+  }
+  uint4 xn[NB][4] = {};  // the next group's 16 activations of each half, per token block
+  auto load_x = [&](int g, uint4 (&x)[NB][4]) {
+#pragma unroll
+    for (int b = 0; b < NB; ++b)
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        x[b][e] = tok[b] ? ld_act16(xbase[b] + g * GROUP + 64 * (e >> 1) + 8 * (e & 1)) : make_uint4(0u, 0u, 0u, 0u);
   };
   if (n > 0) load_x(gc * GS, xn);
-  // four independent MMA chains (half, k-step parity), accumulated over a segment's groups
-  // (the scales are inside the A fragments): (row g, token 2c), (g, 2c+1), (g+8, 2c), (g+8, 2c+1)
-  float d[4][4] = {};
+  // four independent MMA chains per token block (half, k-step parity), accumulated over a
+  // segment's groups (the scales are inside the A fragments): (row g, token 2c), (g, 2c+1),
+  // (g+8, 2c), (g+8, 2c+1), tokens offset by 8 b
+  float d[NB][4][4] = {};
   bool seg_first = true;
   int seg_g0 = 0;
 #pragma unroll 1
@@ -308,9 +322,11 @@ __global__ void __launch_bounds__(THREADS_V)
     }
 #pragma unroll
     for (int q = 0; q < GS; ++q) {
-      uint4 xc[4];
+      uint4 xc[NB][4];
 #pragma unroll
-      for (int e = 0; e < 4; ++e) xc[e] = xn[e];
+      for (int b = 0; b < NB; ++b)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) xc[b][e] = xn[b][e];
       // the next group's activations: the next in this stage, else the next stage's first
       if (q + 1 < GS) load_x(gc * GS + q + 1, xn);
       else if (j + 1 < n) load_x(gn * GS, xn);
@@ -322,8 +338,11 @@ __global__ void __launch_bounds__(THREADS_V)
         for (int ks = 0; ks < 4; ++ks) {
           uint32_t af[4];
           fr.a(h, ks, c, af);
-          const uint4& xv = xc[2 * h + (ks >> 1)];
-          mma16816(af, (ks & 1) ? xv.z : xv.x, (ks & 1) ? xv.w : xv.y, d[2 * h + (ks & 1)]);
+#pragma unroll
+          for (int b = 0; b < NB; ++b) {
+            const uint4& xv = xc[b][2 * h + (ks >> 1)];
+            mma16816(af, (ks & 1) ? xv.z : xv.x, (ks & 1) ? xv.w : xv.y, d[b][2 * h + (ks & 1)]);
+          }
         }
       }
     }
@@ -335,65 +354,77 @@ __global__ void __launch_bounds__(THREADS_V)
     gc = gn;
     sc = sc + 1 == DS ? 0 : sc + 1;
     if (!tile_end || EPI == EPI_SWIGLU) continue;
-    // ---- end of a segment of tile t: its share (MMA row g + 8i, token 2c + e)
+    // ---- end of a segment of tile t: its share (MMA row g + 8i, token 8b + 2c + e)
     const bool whole = seg_g0 == 0 && g == GG - 1;
     float* o = reinterpret_cast<float*>(out);
 #pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      const int row = 16 * t + gq + 8 * i;
+    for (int b = 0; b < NB; ++b)
 #pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const int m = 2 * c + e;
-        const float v = (d[0][2 * i + e] + d[1][2 * i + e]) + (d[2][2 * i + e] + d[3][2 * i + e]);
-        if (row >= N || m >= M) continue;
-        float* p = o + static_cast<size_t>(m) * N + row;
-        if (whole) *p += v;  // no other warp has this tile
-        else atomicAdd(p, v);
+      for (int i = 0; i < 2; ++i) {
+        const int row = 16 * t + gq + 8 * i;
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int m = 8 * b + 2 * c + e;
+          const float v = (d[b][0][2 * i + e] + d[b][1][2 * i + e]) + (d[b][2][2 * i + e] + d[b][3][2 * i + e]);
+          if (row >= N || m >= M) continue;
+          float* p = o + static_cast<size_t>(m) * N + row;
+          if (whole) *p += v;  // no other warp has this tile
+          else atomicAdd(p, v);
+        }
       }
-    }
 #pragma unroll
-    for (int x = 0; x < 4; ++x)
+    for (int b = 0; b < NB; ++b)
 #pragma unroll
-      for (int y = 0; y < 4; ++y) d[x][y] = 0.f;
+      for (int x = 0; x < 4; ++x)
+#pragma unroll
+        for (int y = 0; y < 4; ++y) d[b][x][y] = 0.f;
     seg_first = true;
   }
   if (EPI == EPI_SWIGLU) {
     // the odd-stage warp hands its sums to the even-stage warp of the same tile, which forms
     // silu(gate) * up: MMA rows g are gate rows, g + 8 their up rows
-    float acc[4];
+    float acc[NB][4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) acc[i] = (d[0][i] + d[1][i]) + (d[2][i] + d[3][i]);
+    for (int b = 0; b < NB; ++b)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) acc[b][i] = (d[b][0][i] + d[b][1][i]) + (d[b][2][i] + d[b][3][i]);
     const int pair = warp >> 1;
     if (warp & 1) {
 #pragma unroll
-      for (int i = 0; i < 4; ++i) part[pair][lane][i] = acc[i];
+      for (int b = 0; b < NB; ++b)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) part[pair][lane][4 * b + i] = acc[b][i];
     }
     __syncthreads();
     if (!(warp & 1) && n > 0) {
       if (GG > 1) {
 #pragma unroll
-        for (int i = 0; i < 4; ++i) acc[i] += part[pair][lane][i];
+        for (int b = 0; b < NB; ++b)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) acc[b][i] += part[pair][lane][4 * b + i];
       }
       const int col = 8 * t0 + gq;
       __half* o = reinterpret_cast<__half*>(out);
 #pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const int m = 2 * c + e;
-        if (m < M && col < (N >> 1))
-          o[static_cast<size_t>(m) * (N >> 1) + col] = __float2half_rn(silu_mul_v(acc[e], acc[2 + e]));
-      }
+      for (int b = 0; b < NB; ++b)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int m = 8 * b + 2 * c + e;
+          if (m < M && col < (N >> 1))
+            o[static_cast<size_t>(m) * (N >> 1) + col] = __float2half_rn(silu_mul_v(acc[b][e], acc[b][2 + e]));
+        }
     }
   }
   cp_wait<0>();
 }
 
-template <int WFMT, int EPI, int GS>
+template <int WFMT, int EPI, int GS, int NB>
 cudaError_t launch_vg(const GemmArgs& g, cudaStream_t stream) {
   constexpr int smem = WARPS_V * (ST<WFMT>::DS / GS) * GS * ST<WFMT>::BYTES;
   static_assert(smem <= 48 * 1024, "GEMV stages");
   static const int warps_max = [] {
     int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gemv_kernel<WFMT, EPI, GS>, THREADS_V, smem) !=
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gemv_kernel<WFMT, EPI, GS, NB>, THREADS_V, smem) !=
             cudaSuccess ||
         per_sm < 1)
       per_sm = 1;
@@ -412,7 +443,7 @@ cudaError_t launch_vg(const GemmArgs& g, cudaStream_t stream) {
     warps = static_cast<int>(std::min<long long>(units, warps_max));
     ctas = (warps + WARPS_V - 1) / WARPS_V;
   }
-  return launch_pdl(gemv_kernel<WFMT, EPI, GS>, dim3(ctas), dim3(THREADS_V), smem, stream,
+  return launch_pdl(gemv_kernel<WFMT, EPI, GS, NB>, dim3(ctas), dim3(THREADS_V), smem, stream,
                     reinterpret_cast<const __half*>(g.a), g.w, g.M, g.N, g.K, g.out, units, warps);
 }
 
@@ -420,9 +451,14 @@ cudaError_t launch_vg(const GemmArgs& g, cudaStream_t stream) {
 template <int WFMT, int EPI>
 cudaError_t launch_v(const GemmArgs& g, cudaStream_t stream) {
   const int G = g.K / GROUP;
-  if (G % 4 == 0) return launch_vg<WFMT, EPI, 4>(g, stream);
-  if (G % 2 == 0) return launch_vg<WFMT, EPI, 2>(g, stream);
-  return launch_vg<WFMT, EPI, 1>(g, stream);
+  if (g.M > 8) {  // two 8-token column blocks
+    if (G % 4 == 0) return launch_vg<WFMT, EPI, 4, 2>(g, stream);
+    if (G % 2 == 0) return launch_vg<WFMT, EPI, 2, 2>(g, stream);
+    return launch_vg<WFMT, EPI, 1, 2>(g, stream);
+  }
+  if (G % 4 == 0) return launch_vg<WFMT, EPI, 4, 1>(g, stream);
+  if (G % 2 == 0) return launch_vg<WFMT, EPI, 2, 1>(g, stream);
+  return launch_vg<WFMT, EPI, 1, 1>(g, stream);
 }
 
 template <int WFMT>
@@ -436,7 +472,7 @@ cudaError_t launch_fmt_v(const GemmArgs& g, cudaStream_t stream) {
 int gemv_max_m(int wfmt) { return wfmt == PF_W_Q1_G128 ? GEMV_M_MAX_Q1 : GEMV_M_MAX_I4; }
 
 cudaError_t launch_gemv(const GemmArgs& g, cudaStream_t stream) {
-  if (g.M < 1 || g.M > 8 || g.K % GROUP) return cudaErrorInvalidValue;
+  if (g.M < 1 || g.M > 16 || g.K % GROUP) return cudaErrorInvalidValue;
   if (g.epilogue == EPI_SWIGLU && g.N % 256) return cudaErrorInvalidValue;
   if (g.epilogue == EPI_STORE_F32 && !g.out_zeroed) {
     // zero the M x N output (unless the caller has) and add every range's share, as the

@@ -96,8 +96,8 @@ cudaError_t prepare_gemm_small_kernels();
 constexpr int SMALL_M_MAX = 64;
 // M <= gemv_max_m(wfmt): the warp-MMA GEMV (gemv.cu), which needs no scratch; launch_gemm
 // routes there first
-constexpr int GEMV_M_MAX_Q1 = 8;
-constexpr int GEMV_M_MAX_I4 = 8;
+constexpr int GEMV_M_MAX_Q1 = 16;
+constexpr int GEMV_M_MAX_I4 = 16;
 int gemv_max_m(int wfmt);
 cudaError_t launch_gemv(const GemmArgs& g, cudaStream_t stream);
 bool encode_tmap_f16_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,

@@ -35,7 +35,7 @@ TOL = {"q1": 5e-5, "int4": 1e-3}
 @pytest.mark.parametrize("fmt", ["q1", "int4"])
 @pytest.mark.parametrize("epi", [pf.EPI_STORE_F32, pf.EPI_RESID_ADD, pf.EPI_SWIGLU])
 # (128, 512, 1024): 2 tiles on 16 CTAs, so the M > 64 kernel splits every SwiGLU tile and
-# passes the partials through the fixed array; (32, 768, 1024): the 8 < M <= 64 kernel, whose
+# passes the partials through the fixed array; (32, 768, 1024): the 16 < M <= 64 kernel, whose
 # SwiGLU splits use the array too; (1, 256, 128): the GEMV, which needs no scratch.
 @pytest.mark.parametrize("m,n,k", [(300, 768, 1024), (200, 1280, 512), (128, 512, 1024),
                                    (32, 768, 1024), (1, 256, 128)])
