@@ -620,17 +620,20 @@ __global__ void __launch_bounds__(512) lm_head_q1_kernel(const float* __restrict
   const float r = rsqrtf(ss / static_cast<float>(H) + eps);
   for (int i = threadIdx.x; i < H; i += blockDim.x) ys[i] = x_row[i] * r * nw[i];
   __syncthreads();
-  // table entry (u, n, v): sum over the nibble's four elements, negated where v's bit is set
-  for (int e = threadIdx.x; e < (H / 32) * 8 * 16; e += blockDim.x) {
-    const int v = e & 15, n = (e >> 4) & 7, u = e >> 7;
-    const float* yu = ys + 32 * u;
-    float t = 0.f;
+  // table entry (u, n, v): sum over the nibble's four elements, negated where v's bit is set.
+  // One thread fills one nibble's 16 entries: the signed sums of its elements (0, 1) and
+  // (2, 3) for the four sign patterns of each pair, then every entry is one pair sum plus
+  // the other.
+  for (int t = threadIdx.x; t < (H / 32) * 8; t += blockDim.x) {
+    const int n = t & 7;
+    const float* yu = ys + 32 * (t >> 3);
+    const float y0 = yu[q1_nibble_elem(n, 0)], y1 = yu[q1_nibble_elem(n, 1)];
+    const float y2 = yu[q1_nibble_elem(n, 2)], y3 = yu[q1_nibble_elem(n, 3)];
+    const float lo[4] = {y0 + y1, y1 - y0, y0 - y1, -y0 - y1};  // bits 0, 1 of v
+    const float hi[4] = {y2 + y3, y3 - y2, y2 - y3, -y2 - y3};  // bits 2, 3 of v
+    float4* dst = reinterpret_cast<float4*>(lut + 16 * t);
 #pragma unroll
-    for (int b = 0; b < 4; ++b) {
-      const float y = yu[q1_nibble_elem(n, b)];
-      t += (v >> b) & 1 ? -y : y;
-    }
-    lut[e] = t;
+    for (int q = 0; q < 4; ++q) dst[q] = make_float4(lo[0] + hi[q], lo[1] + hi[q], lo[2] + hi[q], lo[3] + hi[q]);
   }
   __syncthreads();
   // two threads per weight row, each over half of the groups (more loads in flight per SM)
