@@ -24,6 +24,12 @@
  *    says it synchronises. Kernels whose internal waits time out (a bounded wait on
  *    a barrier that never completed) record PF_ERR_DEVICE_TIMEOUT in a device status
  *    word; pf_session_sync() / pf_status_read() report it.
+ *  - Constant operands. Packed weights and norm weights are read as constants: a
+ *    kernel launched as a programmatic dependent of the previous kernel on the stream
+ *    may read them before that kernel has finished. Write them with a copy (or with a
+ *    kernel followed by a stream or event synchronisation), not with a kernel enqueued
+ *    directly before the call that reads them. Activations, caches and positions are
+ *    read only after every earlier kernel on the stream has completed.
  *  - Thread safety. Calls on distinct sessions may run concurrently; one session is
  *    used by one host thread at a time. pf_last_error() is thread-local.
  */
